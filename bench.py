@@ -1,0 +1,458 @@
+#!/usr/bin/env python
+"""Benchmark of the Q2_K weight-quantized matmul on GB300 (one JSON line).
+
+Headline workload (``--workload decode_gemv_4096``): the decode GEMV
+y = W x with M=1, N=K=4096 (5,505,024 bytes of Q2_K weights per matrix), x f32
+~ N(0,1).  One step streams L distinct seeded weight matrices of that shape
+(a stack of L projection layers, L chosen so the stack is at least 3x the L2
+cache, so no weight byte is served from L2) through one ``q2k_matmul`` launch
+each; the launches are captured once in a CUDA graph and replayed.
+
+``value``     weight bytes of all ranks / max-over-ranks step time (GB/s)
+``roofline``  the dominant kernel (the GEMV): algorithmic bytes per launch
+              (its weight bytes + x + y) / average launch time, against the
+              measured HBM copy bandwidth
+``e2e``       the same metric through the Python API, eager, with each step's
+              activations copied in from pinned host memory and its outputs
+              copied back inside the timed region (weights stay resident, as
+              model weights do)
+``secondary`` the other workloads: decode FFN pair, spec-verify M=16 with its
+              embedding gather, prefill M=512 (TFLOP/s against the bf16 peak)
+``cpu_baseline`` the CPU oracle (plain C, all host cores) on a bounded sample
+
+``--impl reference`` times the CPU oracle alone on the same workload.
+Under torchrun (N > 1) every rank runs an independent replica (weak scaling,
+no collective on the data path); rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import q2k_workloads as wl  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_gemv_4096")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ggml_q2_quantized_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_key: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernels are unchanged."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None, None
+    e = t.get(kernel_key, {}).get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None, None
+    return e.get("dram_bytes_per_launch"), e.get("note")
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                maxes.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# --------------------------------------------------------------------------- helpers
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def layers_for(weight_bytes: int, l2_bytes: int) -> int:
+    return max(2, math.ceil(3 * l2_bytes / weight_bytes))
+
+
+def stack_of_weights(w: wl.Workload, layers: int, first: np.ndarray):
+    """Layer 0 is the workload's own seeded matrix, layer l>0 draws from seed (w.seed, l)."""
+    out = [first]
+    nb = w.n * w.blocks_per_row
+    for l in range(1, layers):
+        out.append(wl.random_blocks(np.random.default_rng([w.seed, l]), nb))
+    return out
+
+
+def time_graph(torch, graph, stream, steps, warmup):
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / steps  # ms per step
+
+
+def capture(torch, stream, fn):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # warm the path (one-time per-device setup happens here, not in capture)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def bench_matmul(torch, q2k, w: wl.Workload, steps, warmup, l2_bytes, device, with_e2e=False):
+    """Time a stack of distinct weight matrices of workload ``w`` (one launch each)."""
+    inp = wl.make_inputs(w, with_gather=False)
+    layers = layers_for(w.weight_bytes, l2_bytes)
+    ws = [torch.from_numpy(a).to(device) for a in stack_of_weights(w, layers, inp.w)]
+    x = torch.from_numpy(inp.x).to(device)
+    ys = torch.empty((layers, w.m, w.n), dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def step():
+        for l in range(layers):
+            q2k.matmul(x, ws[l], w.n, out=ys[l])
+
+    g = capture(torch, stream, step)
+    ms = time_graph(torch, g, stream, steps, warmup)
+    res = {"layers": layers, "ms_per_step": ms, "us_per_call": ms * 1e3 / layers,
+           "launches_per_step": layers}
+    if with_e2e:
+        x_host = torch.from_numpy(inp.x).pin_memory()
+        y_host = torch.empty((layers, w.m, w.n), dtype=torch.float32).pin_memory()
+        with torch.cuda.stream(stream):
+            for _ in range(max(warmup, 3)):
+                x.copy_(x_host, non_blocking=True)
+                step()
+                y_host.copy_(ys, non_blocking=True)
+            stream.synchronize()
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            for _ in range(steps):
+                x.copy_(x_host, non_blocking=True)
+                step()
+                y_host.copy_(ys, non_blocking=True)
+            end.record(stream)
+            end.synchronize()
+        res["e2e_ms_per_step"] = start.elapsed_time(end) / steps
+        res["h2d_bytes_per_step"] = x_host.numel() * 4
+        res["d2h_bytes_per_step"] = y_host.numel() * 4
+    return res
+
+
+def bench_gather(torch, q2k, w: wl.Workload, steps, warmup, device):
+    inp = wl.make_inputs(w)
+    table = torch.from_numpy(inp.table).to(device)
+    ids = torch.from_numpy(inp.ids.astype(np.int32)).to(device)
+    out = torch.empty((w.gather_tokens, w.k), dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+    reps = 64
+
+    def step():
+        for _ in range(reps):
+            q2k.embedding_gather(table, ids, w.k, out=out, check=False)
+
+    g = capture(torch, stream, step)
+    ms = time_graph(torch, g, stream, steps, warmup)
+    return {"us_per_call": ms * 1e3 / reps, "n_tokens": w.gather_tokens,
+            "table": f"{w.gather_vocab}x{w.k}"}
+
+
+def cpu_baseline(w: wl.Workload, budget_s: float = 12.0):
+    import oracle
+    inp = wl.make_inputs(w, with_gather=False)
+    cores = os.cpu_count() or 1
+    # bounded sample: whole weight rows of the workload, all x rows
+    rows = w.n
+    if w.m * w.n * w.k > 2e9:
+        rows = max(1, int(2e9 // (w.m * w.k)))
+    row_bytes = w.blocks_per_row * wl.BLOCK_BYTES
+    wsub = inp.w[: rows * row_bytes]
+    oracle.matmul(inp.x, wsub, rows, threads=cores)  # warm (build + page-in)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.matmul(inp.x, wsub, rows, threads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el > budget_s or reps >= 1000:
+            break
+    sec = el / reps
+    return {"value": rows * row_bytes / sec / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x oracle matmul of {w.name} (M={w.m}, {rows} of {w.n} weight rows,"
+                      f" K={w.k}), {cores} threads, {el:.1f} s",
+            "flops_per_s": 2 * w.m * rows * w.k / sec}
+
+
+# --------------------------------------------------------------------------- arms
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    w = wl.by_name(args.workload)
+    if rank != 0:
+        return 0
+    import oracle
+    inp = wl.make_inputs(w, with_gather=False)
+    cores = os.cpu_count() or 1
+    rows = w.n if w.m * w.n * w.k <= 2e9 else max(1, int(2e9 // (w.m * w.k)))
+    row_bytes = w.blocks_per_row * wl.BLOCK_BYTES
+    wsub = inp.w[: rows * row_bytes]
+    for _ in range(args.warmup):
+        oracle.matmul(inp.x, wsub, rows, threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.matmul(inp.x, wsub, rows, threads=cores)
+    el = time.perf_counter() - t0
+    value = args.steps * rows * row_bytes / el / 1e9
+    sample = (f"each step: oracle matmul of {w.name} (M={w.m}, {rows} of {w.n} weight rows,"
+              f" K={w.k}) on {cores} host threads")
+    line = {"impl": "reference", "metric": "q2k_matmul_weight_GBps", "value": value,
+            "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "m": w.m, "n": w.n, "k": w.k},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from ggml_q2_quantized_gb300 import build as lib_build
+    import ggml_q2_quantized_gb300 as q2k
+    lib_build.build()
+    q2k.load()
+
+    peaks, peak_kind = load_peaks()
+    props = torch.cuda.get_device_properties(device)
+    l2_bytes = getattr(props, "L2_cache_size", 0) or 126 * 2**20
+    w = wl.by_name(args.workload)
+    steps, warmup = args.steps, max(3, args.warmup)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # ---- headline: the timed region
+    inp = wl.make_inputs(w, with_gather=False)
+    layers = layers_for(w.weight_bytes, l2_bytes)
+    ws = [torch.from_numpy(a).to(device) for a in stack_of_weights(w, layers, inp.w)]
+    x = torch.from_numpy(inp.x).to(device)
+    ys = torch.empty((layers, w.m, w.n), dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def step():
+        for l in range(layers):
+            q2k.matmul(x, ws[l], w.n, out=ys[l])
+
+    graph = capture(torch, stream, step)
+    for _ in range(warmup):
+        graph.replay()
+    barrier()
+    with ClockSampler(device.index) as clk:
+        barrier()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(steps):
+                graph.replay()
+            end.record(stream)
+        end.synchronize()
+        barrier()
+    ms = start.elapsed_time(end) / steps
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    assert q2k.device_error() == 0
+    bytes_per_step = layers * w.weight_bytes
+    value = world * bytes_per_step / (ms * 1e-3) / 1e9
+    launch_us = ms * 1e3 / layers
+    algo_bytes = w.weight_bytes + 4 * w.m * w.k + 4 * w.m * w.n
+    achieved = algo_bytes / (launch_us * 1e-6) / 1e9
+    kernel_key = "gemv" if w.m <= 8 else "tensor"
+    traffic, traffic_note = traffic_for(kernel_key, w.name)
+
+    line = {
+        "metric": "q2k_matmul_weight_GBps",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if w.m <= 8 else "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "m": w.m, "n": w.n, "k": w.k,
+                   "weight_bytes_per_matrix": w.weight_bytes, "matrices_per_step": layers,
+                   "l2_policy": f"inputs larger than L2: {layers} distinct weight matrices "
+                                f"({bytes_per_step / 2**20:.0f} MiB) per step vs "
+                                f"{l2_bytes / 2**20:.0f} MiB L2",
+                   "timing": "CUDA graph of the step's launches, CUDA events on the replay stream",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "us_per_call": launch_us,
+        "gpu_launches": steps * layers,
+        "roofline": {"bound": "hbm", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_source": f"{peak_kind} HBM copy bandwidth",
+                     "algorithmic_bytes_per_launch": algo_bytes,
+                     "kernel": "q2k gemv_kernel<1>" if w.m == 1 else f"q2k {kernel_key}",
+                     "frac_of_nominal_8TBps": achieved / 8000.0},
+    }
+    if traffic_note:
+        line["roofline"]["traffic_note"] = traffic_note
+    line["clocks"] = clk.summary()
+
+    # ---- e2e through the public API (eager), host buffers, copies inside the region
+    e2e = bench_matmul(torch, q2k, w, steps, warmup, l2_bytes, device, with_e2e=True)
+    line["e2e"] = {"value": world * bytes_per_step / (e2e["e2e_ms_per_step"] * 1e-3) / 1e9,
+                   "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                   "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+                   "ms_per_step": e2e["e2e_ms_per_step"],
+                   "how": "eager Python API calls (one q2k.matmul per weight matrix) with the "
+                          "activations copied from pinned host memory and all outputs copied "
+                          "back each step"}
+
+    # ---- secondary workloads (not the headline; reported for the metric's M=512 half)
+    if not args.no_secondary:
+        sec = {}
+        for name in ("ffn_pair", "ffn_pair_down", "spec_verify_m16", "prefill_m512"):
+            sw = wl.by_name(name)
+            r = bench_matmul(torch, q2k, sw, max(3, steps // 4), 3, l2_bytes, device)
+            us = r["us_per_call"]
+            entry = {"us_per_call": us, "weight_GBps": sw.weight_bytes / (us * 1e-6) / 1e9,
+                     "TFLOPs": sw.flops / (us * 1e-6) / 1e12, "m": sw.m, "n": sw.n, "k": sw.k,
+                     "path": "gemv" if sw.m <= 8 else "tensor", "matrices_per_step": r["layers"]}
+            entry["frac_hbm_measured"] = entry["weight_GBps"] / peaks["hbm_gbs"]
+            if sw.m > 8:
+                entry["frac_bf16_measured"] = entry["TFLOPs"] / peaks["bf16_tflops"]
+                entry["frac_bf16_nominal_2250"] = entry["TFLOPs"] / 2250.0
+            sec[name] = entry
+        sec["spec_verify_gather"] = bench_gather(torch, q2k, wl.by_name("spec_verify_m16"),
+                                                 max(3, steps // 4), 3, device)
+        line["secondary"] = sec
+        assert q2k.device_error() == 0
+
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

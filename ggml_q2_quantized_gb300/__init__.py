@@ -1,0 +1,214 @@
+"""GGML Q2_K weight-quantized matmul, dequantize and embedding gather on GB300.
+
+A thin ctypes binding over the C ABI of ``libq2k.so`` (declared in
+``include/q2k.h``).  It only marshals arguments: every step of the work runs in
+the library's CUDA kernels on the tensors' device, on PyTorch's current stream.
+PyTorch supplies device memory and streams, nothing else.  There is no CPU
+fallback: if the library has not been built (``ggml_q2_quantized_gb300.build``)
+or no sm_103 device is present, the calls raise.
+
+Names follow the mlx-native page "tests/deepseek_q2_k.rs": ``matmul`` is
+``quantized_matmul_ggml`` (with ``path=`` playing the role of
+``dispatch_mm_for_test``), ``embedding_gather`` is ``embedding_gather_q2_k`` and
+``dequantize`` is ``test_only_dequantize``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from . import build as _build
+
+QK_K = 256
+BLOCK_BYTES = 84
+GGML_TYPE_Q2_K = 10
+
+PATH_AUTO, PATH_GEMV, PATH_TENSOR = 0, 1, 2
+_PATHS = {"auto": PATH_AUTO, "gemv": PATH_GEMV, "tensor": PATH_TENSOR,
+          PATH_AUTO: PATH_AUTO, PATH_GEMV: PATH_GEMV, PATH_TENSOR: PATH_TENSOR}
+
+STATUS = {0: "Q2K_OK", 1: "Q2K_ERR_INVALID_ARGUMENT", 2: "Q2K_ERR_BAD_ID",
+          3: "Q2K_ERR_CUDA", 4: "Q2K_ERR_TIMEOUT", 5: "Q2K_ERR_NO_DEVICE"}
+
+HEADER = os.path.join(_build.INCLUDE, "q2k.h")
+LIB_PATH = _build.LIB_PATH
+
+
+class Q2KError(RuntimeError):
+    """A non-OK status from libq2k, with its message."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+class InvalidArgument(Q2KError, ValueError):
+    pass
+
+
+class MatmulParams(ctypes.Structure):
+    _fields_ = [("m", ctypes.c_uint32), ("n", ctypes.c_uint32), ("k", ctypes.c_uint32),
+                ("ggml_type", ctypes.c_uint32)]
+
+
+class EmbeddingParams(ctypes.Structure):
+    _fields_ = [("vocab_size", ctypes.c_uint32), ("embed_dim", ctypes.c_uint32),
+                ("n_tokens", ctypes.c_uint32), ("ggml_type", ctypes.c_uint32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def header_functions() -> list[str]:
+    """Names of the functions ``include/q2k.h`` declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(q2k_\w+)\s*\(", text, flags=re.M)
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the in-tree libq2k.so (built by ``build.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"libq2k is not built ({p} missing): run ggml_q2_quantized_gb300.build.build() "
+                "- there is no fallback implementation")
+        lib = ctypes.CDLL(p)
+        vp, sz, u32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(ctypes.c_uint32)
+        lib.q2k_dequantize.argtypes = [vp, sz, vp, sz, vp]
+        lib.q2k_embedding_gather.argtypes = [vp, sz, vp, vp, sz, ctypes.POINTER(EmbeddingParams),
+                                             vp, vp]
+        lib.q2k_matmul.argtypes = [vp, sz, vp, sz, vp, sz, ctypes.POINTER(MatmulParams), vp]
+        lib.q2k_matmul_path.argtypes = [ctypes.c_int, vp, sz, vp, sz, vp, sz,
+                                        ctypes.POINTER(MatmulParams), vp]
+        lib.q2k_device_error.argtypes = [u32p, vp]
+        for fn in ("q2k_dequantize", "q2k_embedding_gather", "q2k_matmul", "q2k_matmul_path",
+                   "q2k_device_error"):
+            getattr(lib, fn).restype = ctypes.c_int
+        lib.q2k_last_error.restype = ctypes.c_char_p
+        lib.q2k_last_error.argtypes = []
+        lib.q2k_abi_version.restype = ctypes.c_int
+        lib.q2k_abi_version.argtypes = []
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(lib, status: int):
+    if status != 0:
+        msg = lib.q2k_last_error().decode(errors="replace")
+        if status == 1:
+            raise InvalidArgument(status, msg)
+        raise Q2KError(status, msg)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(tensor) -> int:
+    torch = _torch()
+    return torch.cuda.current_stream(tensor.device).cuda_stream
+
+
+def _require_cuda(t, name, dtype):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def dequantize(blocks, out=None):
+    """Decode a uint8 CUDA tensor of whole Q2_K blocks to float32 (256 per block)."""
+    torch = _torch()
+    _require_cuda(blocks, "blocks", torch.uint8)
+    n_out = (blocks.numel() // BLOCK_BYTES) * QK_K
+    if out is None:
+        out = torch.empty(max(n_out, 1), dtype=torch.float32, device=blocks.device)[:n_out]
+    _require_cuda(out, "out", torch.float32)
+    lib = load()
+    with torch.cuda.device(blocks.device):
+        _check(lib, lib.q2k_dequantize(blocks.data_ptr(), blocks.numel(), out.data_ptr(),
+                                       out.numel(), _stream_handle(blocks)))
+    return out
+
+
+def embedding_gather(table, ids, embed_dim: int, vocab_size: int | None = None, out=None,
+                     check: bool = True):
+    """Rows ``ids`` of a Q2_K table ``[vocab, embed_dim]`` decoded to float32.
+
+    With ``check`` (the default) the call waits for the stream and raises
+    ``InvalidArgument`` if any id was >= vocab_size, as the pages' gather does;
+    with ``check=False`` it returns ``(out, bad_id_count)`` without waiting.
+    """
+    torch = _torch()
+    _require_cuda(table, "table", torch.uint8)
+    _require_cuda(ids, "ids", ids.dtype)
+    if ids.element_size() != 4 or ids.is_floating_point():
+        raise TypeError("ids must be a 32-bit integer tensor (read as uint32)")
+    row_bytes = (embed_dim // QK_K) * BLOCK_BYTES
+    if vocab_size is None:
+        vocab_size = table.numel() // row_bytes if row_bytes else 0
+    n_tokens = ids.numel()
+    if out is None:
+        out = torch.empty((n_tokens, embed_dim), dtype=torch.float32, device=table.device)
+    _require_cuda(out, "out", torch.float32)
+    bad = torch.zeros(1, dtype=torch.int32, device=table.device)
+    p = EmbeddingParams(vocab_size, embed_dim, n_tokens, GGML_TYPE_Q2_K)
+    lib = load()
+    with torch.cuda.device(table.device):
+        _check(lib, lib.q2k_embedding_gather(table.data_ptr(), table.numel(), ids.data_ptr(),
+                                             out.data_ptr(), out.numel(), ctypes.byref(p),
+                                             bad.data_ptr(), _stream_handle(table)))
+    if not check:
+        return out, bad
+    n_bad = int(bad.item())
+    if n_bad:
+        raise InvalidArgument(1, f"{n_bad} embedding id(s) >= vocab_size {vocab_size}")
+    return out
+
+
+def matmul(x, w, n: int, out=None, path="auto"):
+    """``y[m, r] = sum_k x[m, k] * W[r, k]`` with W = ``n`` rows of Q2_K blocks."""
+    torch = _torch()
+    _require_cuda(x, "x", torch.float32)
+    _require_cuda(w, "w", torch.uint8)
+    if x.dim() != 2:
+        raise ValueError("x must be [m, k]")
+    m, k = x.shape
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float32, device=x.device)
+    _require_cuda(out, "out", torch.float32)
+    p = MatmulParams(m, n, k, GGML_TYPE_Q2_K)
+    lib = load()
+    with torch.cuda.device(x.device):
+        _check(lib, lib.q2k_matmul_path(_PATHS[path], x.data_ptr(), x.numel(), w.data_ptr(),
+                                        w.numel(), out.data_ptr(), out.numel(), ctypes.byref(p),
+                                        _stream_handle(x)))
+    return out
+
+
+def device_error(device=None) -> int:
+    """Read and clear the device error word (nonzero: a kernel gave up waiting)."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    v = ctypes.c_uint32(0)
+    lib = load()
+    with torch.cuda.device(dev):
+        _check(lib, lib.q2k_device_error(ctypes.byref(v),
+                                         torch.cuda.current_stream(dev).cuda_stream))
+    return int(v.value)

@@ -1,0 +1,227 @@
+// C ABI of libq2k (declared in include/q2k.h): argument checks and dispatch.
+//
+// The checks follow the conventions of the mlx-native pages: exact byte
+// lengths with overflow-checked products (page "src/ops/dflash2_selector.rs",
+// fns product / require), outputs that may not alias inputs (fn
+// validate_disjoint), and InvalidArgument before anything is launched (page
+// "tests/deepseek_q2_k.rs", tests q2_k_host_decode_rejects_malformed_buffers
+// and ..._rejects_bad_ids).
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "q2k.h"
+#include "q2k_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+q2k_status fail(q2k_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+q2k_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(Q2K_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool mul_ok(size_t a, size_t b, size_t* out) {
+    if (a != 0 && b > SIZE_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlaps(const void* a, size_t a_bytes, const void* b, size_t b_bytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a_bytes != 0 && b_bytes != 0 && a0 < b0 + b_bytes && b0 < a0 + a_bytes;
+}
+
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+};
+
+// The current device must be a compute capability 10.3 part (the library is
+// built for sm_103a only).  The SM count is cached per device.
+q2k_status current_device(DeviceInfo* info) {
+    static int sm_cache[64];
+    static int cc_cache[64];
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(Q2K_ERR_NO_DEVICE, "device ordinal %d out of range", dev);
+    if (sm_cache[dev] == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        cc_cache[dev] = major * 10 + minor;
+        sm_cache[dev] = sms;
+    }
+    if (cc_cache[dev] != 103)
+        return fail(Q2K_ERR_NO_DEVICE, "device %d has compute capability %d.%d; libq2k is built for sm_103a",
+                    dev, cc_cache[dev] / 10, cc_cache[dev] % 10);
+    info->device = dev;
+    info->sm_count = sm_cache[dev];
+    return Q2K_OK;
+}
+
+q2k_status check_matmul(const float* x, size_t x_elems, const void* w, size_t w_bytes,
+                        const float* y, size_t y_elems, const q2k_matmul_params* p) {
+    if (p == nullptr) return fail(Q2K_ERR_INVALID_ARGUMENT, "params is NULL");
+    if (p->ggml_type != Q2K_GGML_TYPE_Q2_K)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "ggml_type %u is not Q2_K (10)", p->ggml_type);
+    if (p->m == 0 || p->n == 0 || p->k == 0)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "m, n, k must be >= 1 (got %u, %u, %u)", p->m, p->n, p->k);
+    if (p->k % Q2K_QK_K != 0)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "k = %u is not a multiple of 256", p->k);
+    if (p->m > INT_MAX || p->n > INT_MAX || p->k > INT_MAX)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "m, n, k must fit in a signed 32-bit int");
+    size_t want_x, want_w, want_y, blocks;
+    if (!mul_ok(p->m, p->k, &want_x) || !mul_ok(p->n, p->k / Q2K_QK_K, &blocks) ||
+        !mul_ok(blocks, Q2K_BLOCK_BYTES, &want_w) || !mul_ok(p->m, p->n, &want_y) ||
+        want_x > SIZE_MAX / 4 || want_y > SIZE_MAX / 4)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "matmul shape overflows size_t");
+    if (x == nullptr || w == nullptr || y == nullptr)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "x, w and y must be non-NULL");
+    if (x_elems != want_x)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "x has %zu elements, expected m*k = %zu", x_elems, want_x);
+    if (w_bytes != want_w)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "w has %zu bytes, expected n*k/256*84 = %zu", w_bytes, want_w);
+    if (y_elems != want_y)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "y has %zu elements, expected m*n = %zu", y_elems, want_y);
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(w, 4))
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "x and y must be 16-byte aligned and w 4-byte aligned");
+    if (overlaps(y, want_y * 4, x, want_x * 4) || overlaps(y, want_y * 4, w, want_w))
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "y must not alias x or w");
+    return Q2K_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* q2k_last_error(void) { return g_last_error; }
+
+int q2k_abi_version(void) { return Q2K_ABI_VERSION; }
+
+q2k_status q2k_dequantize(const void* blocks, size_t blocks_bytes, float* out, size_t out_elems,
+                          q2k_stream_t stream) {
+    g_last_error[0] = '\0';
+    if (blocks == nullptr || out == nullptr)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "blocks and out must be non-NULL");
+    if (blocks_bytes == 0 || blocks_bytes % Q2K_BLOCK_BYTES != 0)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "%zu bytes is not a positive whole number of 84-byte Q2_K blocks",
+                    blocks_bytes);
+    const size_t n_blocks = blocks_bytes / Q2K_BLOCK_BYTES;
+    size_t want;
+    if (!mul_ok(n_blocks, Q2K_QK_K, &want) || want > SIZE_MAX / 4)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "output size overflows size_t");
+    if (out_elems != want)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "out has %zu floats, expected %zu (256 per block)", out_elems, want);
+    if (!aligned(blocks, 4) || !aligned(out, 16))
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "blocks must be 4-byte and out 16-byte aligned");
+    if (overlaps(out, want * 4, blocks, blocks_bytes))
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "out must not alias blocks");
+    DeviceInfo dev;
+    q2k_status st = current_device(&dev);
+    if (st != Q2K_OK) return st;
+    cudaError_t e = q2k::launch_dequant(static_cast<const uint8_t*>(blocks), out, n_blocks,
+                                        dev.sm_count, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_dequantize launch");
+}
+
+q2k_status q2k_embedding_gather(const void* table, size_t table_bytes, const uint32_t* ids,
+                                float* out, size_t out_elems, const q2k_embedding_params* p,
+                                uint32_t* bad_id_count, q2k_stream_t stream) {
+    g_last_error[0] = '\0';
+    if (p == nullptr) return fail(Q2K_ERR_INVALID_ARGUMENT, "params is NULL");
+    if (p->ggml_type != Q2K_GGML_TYPE_Q2_K)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "ggml_type %u is not Q2_K (10)", p->ggml_type);
+    if (p->vocab_size == 0 || p->embed_dim == 0 || p->n_tokens == 0)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "vocab_size, embed_dim and n_tokens must be >= 1");
+    if (p->embed_dim % Q2K_QK_K != 0)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "embed_dim = %u is not a multiple of 256", p->embed_dim);
+    if (table == nullptr || ids == nullptr || out == nullptr)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "table, ids and out must be non-NULL");
+    size_t blocks, want_table, want_out;
+    if (!mul_ok(p->vocab_size, p->embed_dim / Q2K_QK_K, &blocks) ||
+        !mul_ok(blocks, Q2K_BLOCK_BYTES, &want_table) || !mul_ok(p->n_tokens, p->embed_dim, &want_out) ||
+        want_out > SIZE_MAX / 4)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "gather shape overflows size_t");
+    if (table_bytes != want_table)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "table has %zu bytes, expected vocab*embed_dim/256*84 = %zu",
+                    table_bytes, want_table);
+    if (out_elems != want_out)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "out has %zu floats, expected n_tokens*embed_dim = %zu",
+                    out_elems, want_out);
+    if (!aligned(table, 4) || !aligned(out, 16) || !aligned(ids, 4) ||
+        (bad_id_count != nullptr && !aligned(bad_id_count, 4)))
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "table, ids and bad_id_count must be 4-byte and out 16-byte aligned");
+    const size_t out_bytes = want_out * 4;
+    if (overlaps(out, out_bytes, table, want_table) || overlaps(out, out_bytes, ids, size_t(p->n_tokens) * 4) ||
+        (bad_id_count != nullptr &&
+         (overlaps(bad_id_count, 4, out, out_bytes) || overlaps(bad_id_count, 4, ids, size_t(p->n_tokens) * 4) ||
+          overlaps(bad_id_count, 4, table, want_table))))
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "writable buffers must not alias inputs or each other");
+    DeviceInfo dev;
+    q2k_status st = current_device(&dev);
+    if (st != Q2K_OK) return st;
+    cudaError_t e = q2k::launch_gather(static_cast<const uint8_t*>(table), ids, out, p->vocab_size,
+                                       p->embed_dim, p->n_tokens, bad_id_count, dev.sm_count,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_embedding_gather launch");
+}
+
+q2k_status q2k_matmul_path(q2k_path path, const float* x, size_t x_elems, const void* w,
+                           size_t w_bytes, float* y, size_t y_elems, const q2k_matmul_params* p,
+                           q2k_stream_t stream) {
+    g_last_error[0] = '\0';
+    q2k_status st = check_matmul(x, x_elems, w, w_bytes, y, y_elems, p);
+    if (st != Q2K_OK) return st;
+    if (path != Q2K_PATH_AUTO && path != Q2K_PATH_GEMV && path != Q2K_PATH_TENSOR)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "unknown path %d", static_cast<int>(path));
+    if (path == Q2K_PATH_AUTO) path = p->m <= 8 ? Q2K_PATH_GEMV : Q2K_PATH_TENSOR;
+    if (path == Q2K_PATH_GEMV && (p->m + 7u) / 8u > 65535u)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "GEMV path supports m <= 524280");
+    if (path == Q2K_PATH_TENSOR && (p->m + 127u) / 128u > 65535u)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "tensor-core path supports m <= 8388480");
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != Q2K_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint8_t* wb = static_cast<const uint8_t*>(w);
+    cudaError_t e;
+    if (path == Q2K_PATH_GEMV)
+        e = q2k::launch_gemv(x, wb, y, int(p->m), int(p->n), int(p->k), s);
+    else
+        e = q2k::launch_gemm_tc(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count, s);
+    return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul launch");
+}
+
+q2k_status q2k_matmul(const float* x, size_t x_elems, const void* w, size_t w_bytes, float* y,
+                      size_t y_elems, const q2k_matmul_params* p, q2k_stream_t stream) {
+    return q2k_matmul_path(Q2K_PATH_AUTO, x, x_elems, w, w_bytes, y, y_elems, p, stream);
+}
+
+q2k_status q2k_device_error(uint32_t* out, q2k_stream_t stream) {
+    g_last_error[0] = '\0';
+    if (out == nullptr) return fail(Q2K_ERR_INVALID_ARGUMENT, "out is NULL");
+    DeviceInfo dev;
+    q2k_status st = current_device(&dev);
+    if (st != Q2K_OK) return st;
+    cudaError_t e = q2k::read_and_clear_tc_error(out, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_device_error");
+}
+
+}  // extern "C"

@@ -1,0 +1,101 @@
+// Device-side helpers shared by the libq2k kernels (sm_103a only).
+//
+// Q2_K block layout (mlx-native page "tests/deepseek_q2_k.rs", fixture fn
+// block and fn reference_dequant): 84 bytes per 256 weights - scale bytes at
+// 0..15 (low nibble sc, high nibble m), 2-bit quants at 16..79, f16 d at
+// 80..81, f16 dmin at 82..83.  Weight k = 128 half + 32 j + 16 seg + lane is
+// dl*q - ml with q = (qs[32 half + 16 seg + lane] >> 2j) & 3 and
+// dl = d*(sc&15), ml = dmin*(sc>>4) taken from scale byte 8 half + 2 j + seg.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
+#error "libq2k is written for sm_103a (Blackwell) only"
+#endif
+
+namespace q2k {
+
+constexpr int kQK = 256;          // weights per super-block
+constexpr int kBlockBytes = 84;   // bytes per super-block
+constexpr int kWordsPerBlock = 21;
+
+// Bits of the device error word (see q2k_device_error in q2k.h).
+constexpr uint32_t kErrTimeoutFull = 1u;    // MMA issuer gave up waiting for a filled stage
+constexpr uint32_t kErrTimeoutEmpty = 2u;   // a producer gave up waiting for a free stage
+constexpr uint32_t kErrTimeoutAccum = 4u;   // epilogue gave up waiting for the accumulator
+constexpr uint32_t kErrTimeoutDrain = 8u;   // teardown gave up waiting for in-flight MMAs
+
+__device__ __forceinline__ float f16_bits_to_float(uint32_t bits16) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
+}
+
+__device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) {
+    return *reinterpret_cast<const uint32_t*>(p);
+}
+
+// Read-only, streamed once: do not keep it in L1.
+__device__ __forceinline__ uint32_t ldg_stream_u32(const uint8_t* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- mbarrier (shared::cta) -------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait until the phase with the given parity has completed, but never for
+// more than about `limit_ns`: on time-out (or when another thread of the CTA
+// already timed out and raised *abort) set `err_bit` in *err, raise *abort
+// and return false.  No wait in libq2k is unbounded.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort, unsigned int* err,
+                                                  uint32_t err_bit,
+                                                  uint64_t limit_ns = 1000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0u) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                atomicOr(err, err_bit);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+}  // namespace q2k

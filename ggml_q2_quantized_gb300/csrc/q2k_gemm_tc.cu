@@ -1,0 +1,488 @@
+// bf16 tensor-core Q2_K matmul for m > 8 (tcgen05 MMA, accumulator in TMEM).
+//
+// mlx-native page "tests/deepseek_q2_k.rs", fn run_dense with rows > 8 and
+// the forced mm paths (dispatch_mm_for_test, dispatch_mm_simd_for_test): the
+// pages run these in reduced precision (1e-2 absolute at n = 8, k = 256).
+// Here both operands are rounded to bf16 (round to nearest even) and the
+// products are summed in fp32 by the tensor cores.
+//
+// One CTA computes a 128 (x rows) x BN (weight rows) tile of y over the whole
+// K, in stages of 64 K-elements held in shared memory in the 128-byte-swizzled
+// K-major layout the MMA reads directly:
+//   warps 0-3    convert x rows (f32 -> bf16) into the A stage, then run the
+//                epilogue (TMEM -> registers -> y) for TMEM lanes 32w..32w+31;
+//   BN/32 warps  decode weight rows: raw 84-byte blocks are copied from global
+//                memory into a double-buffered shared slab with 4-byte
+//                cp.async (coalesced across rows), then each thread decodes its
+//                own row - per 16-weight segment a 4-entry bf16 table
+//                {-ml, dl-ml, 2dl-ml, 3dl-ml} is built and each pair of 2-bit
+//                quants picks two table entries with one byte permute;
+//   1 warp       allocates TMEM and issues tcgen05.mma (one thread), each
+//                stage released back to the producers by tcgen05.commit.
+// Every wait is bounded (about a second); on time-out the kernel records a bit
+// in the device error word, drains its MMAs, frees TMEM and returns.
+#include <cuda_runtime.h>
+
+#include "q2k_device.cuh"
+#include "q2k_internal.h"
+
+namespace q2k {
+
+__device__ unsigned int g_tc_error;
+
+namespace {
+
+constexpr int kBM = 128;                 // x rows per tile (MMA M)
+constexpr int kKS = 64;                  // K elements per stage: one 128-byte swizzle row
+constexpr int kAStage = kBM * kKS * 2;   // bytes of one A stage
+constexpr int kXWarps = 4;
+
+template <int BN>
+struct Cfg {
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
+    static constexpr int kStages = (BN <= 192) ? 4 : 3;
+    static constexpr int kBStage = BN * kKS * 2;
+    static constexpr int kRawBytes = BN * kBlockBytes;
+    static constexpr int kDecWarps = BN / 32;
+    static constexpr int kMmaWarp = kXWarps + kDecWarps;
+    static constexpr int kThreads = (kMmaWarp + 1) * 32;
+    static constexpr int kTmemCols = BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kStages * kAStage;
+    static constexpr int kOffRaw = kOffB + kStages * kBStage;
+    static constexpr int kOffBar = ((kOffRaw + 2 * kRawBytes) + 7) & ~7;
+    // bars: full[kStages], empty[kStages], accum, drain, raw_full[2]
+    static constexpr int kNumBars = 2 * kStages + 4;
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base
+    static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+// ---- tcgen05 / async-proxy wrappers ----------------------------------------
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (stride byte offset), version 1 (tcgen05).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);       // start address >> 4
+    d |= static_cast<uint64_t>(1u) << 16;                       // leading byte offset (unused here)
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;               // stride byte offset >> 4
+    d |= static_cast<uint64_t>(1u) << 46;                       // descriptor version
+    d |= static_cast<uint64_t>(2u) << 61;                       // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
+    return (1u << 4)                                  // D format: f32
+         | (1u << 7)                                  // A format: bf16
+         | (1u << 10)                                 // B format: bf16
+         | (static_cast<uint32_t>(n >> 3) << 17)      // N / 8
+         | (static_cast<uint32_t>(m >> 4) << 24);     // M / 16
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+          "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte offset of 16-byte chunk `c` (8 K-elements) of row `r` in a swizzled tile.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
+    return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// Copy the raw 84-byte blocks of column `b` for the tile's BN rows into `dst`
+// (row r at dst + 84 r).  Rows past N are zero-filled (d = dmin = 0 decode to 0).
+template <int BN>
+__device__ __forceinline__ void issue_raw_copy(const uint8_t* __restrict__ w, uint32_t dst,
+                                               int n0, int N, int blocks_per_row, int b,
+                                               int td) {
+    const size_t row_bytes = static_cast<size_t>(blocks_per_row) * kBlockBytes;
+#pragma unroll 3
+    for (int f = td; f < BN * kWordsPerBlock; f += BN) {
+        const int r = f / kWordsPerBlock;
+        const int wd = f - r * kWordsPerBlock;
+        const int n = n0 + r;
+        const bool ok = n < N;
+        const uint8_t* src = w + static_cast<size_t>(ok ? n : 0) * row_bytes +
+                             static_cast<size_t>(b) * kBlockBytes + 4 * wd;
+        cp_async_4(dst + r * kBlockBytes + 4 * wd, src, ok ? 4u : 0u);
+    }
+    cp_async_commit();
+}
+
+// Four bf16 weights of one quant word at shift 2j, picked from the table
+// (lo = {v0, v1}, hi = {v2, v3}).  Returns them as two bf16x2 words.
+template <int J>
+__device__ __forceinline__ void decode_word(uint32_t word, uint32_t lo, uint32_t hi,
+                                            uint32_t& p0, uint32_t& p1) {
+    uint32_t t2;  // byte i = 2 * q_i
+    if (J == 0)
+        t2 = (word << 1) & 0x06060606u;
+    else
+        t2 = (word >> (2 * J - 1)) & 0x06060606u;
+    const uint32_t sel = t2 | (t2 << 4) | 0x10101010u;  // nibbles 2q, 2q+1 per element
+    p0 = __byte_perm(lo, hi, sel);
+    p1 = __byte_perm(lo, hi, sel >> 16);
+}
+
+template <int C>
+__device__ __forceinline__ void decode_stage(const uint32_t (&sw)[4], float d, float dmin,
+                                             const uint32_t (&qw)[8], uint8_t* b_stage, int r) {
+    constexpr int H = C >> 1;
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        const int j = 2 * (C & 1) + jj;
+#pragma unroll
+        for (int seg = 0; seg < 2; ++seg) {
+            const int si = 8 * H + 2 * j + seg;
+            const uint32_t sc = (sw[si >> 2] >> (8 * (si & 3))) & 0xFFu;
+            const float dl = __fmul_rn(d, static_cast<float>(sc & 15u));
+            const float ml = __fmul_rn(dmin, static_cast<float>(sc >> 4));
+            const uint32_t lo = pack_bf16x2(-ml, __fsub_rn(dl, ml));
+            const uint32_t hi = pack_bf16x2(fmaf(2.f, dl, -ml), fmaf(3.f, dl, -ml));
+            uint32_t p[8];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const uint32_t word = qw[4 * seg + t];
+                if ((C & 1) == 0) {
+                    if (jj == 0) decode_word<0>(word, lo, hi, p[2 * t], p[2 * t + 1]);
+                    else decode_word<1>(word, lo, hi, p[2 * t], p[2 * t + 1]);
+                } else {
+                    if (jj == 0) decode_word<2>(word, lo, hi, p[2 * t], p[2 * t + 1]);
+                    else decode_word<3>(word, lo, hi, p[2 * t], p[2 * t + 1]);
+                }
+            }
+            const int chunk = 4 * jj + 2 * seg;
+            *reinterpret_cast<uint4*>(b_stage + sw128_offset(r, chunk)) =
+                make_uint4(p[0], p[1], p[2], p[3]);
+            *reinterpret_cast<uint4*>(b_stage + sw128_offset(r, chunk + 1)) =
+                make_uint4(p[4], p[5], p[6], p[7]);
+        }
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
+gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
+               int M, int N, int K) {
+    using C = Cfg<BN>;
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * BN;
+    const int m0 = blockIdx.y * kBM;
+    const int n_iters = K / kKS;
+    const int blocks_per_row = K / kQK;
+
+    const uint32_t bar_full = sbase + C::kOffBar;
+    const uint32_t bar_empty = bar_full + 8 * C::kStages;
+    const uint32_t bar_accum = bar_empty + 8 * C::kStages;
+    const uint32_t bar_drain = bar_accum + 8;
+    const uint32_t bar_raw = bar_drain + 8;  // two of them
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+    unsigned int* err = &g_tc_error;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar_full + 8 * s, (kXWarps + C::kDecWarps) * 32);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_accum, 1);
+        mbar_init(bar_drain, 1);
+        mbar_init(bar_raw, BN);
+        mbar_init(bar_raw + 8, BN);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == C::kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(C::kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_d = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+    if (warp < kXWarps) {
+        // ---------------- x producer: f32 rows -> bf16 A stages ----------------
+        const int t = threadIdx.x;
+        const int c = t & 7;
+        const int r0 = t >> 3;
+        for (int i = 0; i < n_iters; ++i) {
+            const int s = i % C::kStages;
+            if (i >= C::kStages &&
+                !mbar_wait_bounded(bar_empty + 8 * s, ((i / C::kStages) - 1) & 1, abort_flag, err,
+                                   kErrTimeoutEmpty))
+                break;
+            uint8_t* a_stage = smem + C::kOffA + s * kAStage;
+            float4 va[8], vb[8];
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int m = m0 + r0 + 16 * it;
+                if (m < M) {
+                    const float4* src = reinterpret_cast<const float4*>(
+                        x + static_cast<size_t>(m) * K + static_cast<size_t>(i) * kKS + 8 * c);
+                    va[it] = __ldg(src);
+                    vb[it] = __ldg(src + 1);
+                } else {
+                    va[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    vb[it] = va[it];
+                }
+            }
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int r = r0 + 16 * it;
+                *reinterpret_cast<uint4*>(a_stage + sw128_offset(r, c)) =
+                    make_uint4(pack_bf16x2(va[it].x, va[it].y), pack_bf16x2(va[it].z, va[it].w),
+                               pack_bf16x2(vb[it].x, vb[it].y), pack_bf16x2(vb[it].z, vb[it].w));
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar_full + 8 * s);
+        }
+        // ---------------- epilogue: TMEM -> y (lane quarter = warp) ----------------
+        const bool ok = mbar_wait_bounded(bar_accum, 0, abort_flag, err, kErrTimeoutAccum);
+        __syncwarp();
+        if (ok) {
+            tc_fence_after();
+            const int m = m0 + warp * 32 + lane;
+            const uint32_t taddr_row = tmem_d + (static_cast<uint32_t>(warp * 32) << 16);
+            const bool vec_ok = (N & 3) == 0;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(taddr_row + c0, v);
+                if (m < M) {
+                    float* dst = y + static_cast<size_t>(m) * N + n0 + c0;
+                    const int valid = N - (n0 + c0);
+                    if (vec_ok && valid >= 32) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            reinterpret_cast<float4*>(dst)[q] =
+                                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                            __uint_as_float(v[4 * q + 2]),
+                                            __uint_as_float(v[4 * q + 3]));
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q)
+                            if (q < valid) dst[q] = __uint_as_float(v[q]);
+                    }
+                }
+            }
+        }
+    } else if (warp < C::kMmaWarp) {
+        // ---------------- weight decoder: one tile row per thread ----------------
+        const int td = threadIdx.x - kXWarps * 32;  // 0 .. BN-1 = tile row
+        const uint32_t raw0 = sbase + C::kOffRaw;
+        issue_raw_copy<BN>(w, raw0, n0, N, blocks_per_row, 0, td);
+        bool ok = true;
+        for (int b = 0; b < blocks_per_row && ok; ++b) {
+            const int buf = b & 1;
+            cp_async_wait_all();
+            mbar_arrive(bar_raw + 8 * buf);
+            if (!mbar_wait_bounded(bar_raw + 8 * buf, (b >> 1) & 1, abort_flag, err,
+                                   kErrTimeoutEmpty)) {
+                ok = false;
+                break;
+            }
+            if (b + 1 < blocks_per_row)
+                issue_raw_copy<BN>(w, raw0 + (buf ^ 1) * C::kRawBytes, n0, N, blocks_per_row,
+                                   b + 1, td);
+            const uint8_t* mine = smem + C::kOffRaw + buf * C::kRawBytes + td * kBlockBytes;
+            uint32_t sw[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) sw[q] = ld_u32(mine + 4 * q);
+            const uint32_t dd = ld_u32(mine + 80);
+            const float d = f16_bits_to_float(dd);
+            const float dmin = f16_bits_to_float(dd >> 16);
+            uint32_t qw[8];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (c == 0 || c == 2) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) qw[q] = ld_u32(mine + 16 + 32 * (c >> 1) + 4 * q);
+                }
+                const int i = 4 * b + c;
+                const int s = i % C::kStages;
+                if (i >= C::kStages &&
+                    !mbar_wait_bounded(bar_empty + 8 * s, ((i / C::kStages) - 1) & 1, abort_flag,
+                                       err, kErrTimeoutEmpty)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* b_stage = smem + C::kOffB + s * C::kBStage;
+                if (c == 0) decode_stage<0>(sw, d, dmin, qw, b_stage, td);
+                else if (c == 1) decode_stage<1>(sw, d, dmin, qw, b_stage, td);
+                else if (c == 2) decode_stage<2>(sw, d, dmin, qw, b_stage, td);
+                else decode_stage<3>(sw, d, dmin, qw, b_stage, td);
+                fence_proxy_async_smem();
+                mbar_arrive(bar_full + 8 * s);
+            }
+        }
+        cp_async_wait_all();  // no copy may land after this CTA is gone
+    } else {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(kBM, BN);
+            bool ok = true;
+            for (int i = 0; i < n_iters; ++i) {
+                const int s = i % C::kStages;
+                if (!mbar_wait_bounded(bar_full + 8 * s, (i / C::kStages) & 1, abort_flag, err,
+                                       kErrTimeoutFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = sbase + C::kOffA + s * kAStage;
+                const uint32_t b_addr = sbase + C::kOffB + s * C::kBStage;
+#pragma unroll
+                for (int kk = 0; kk < kKS / 16; ++kk)
+                    mma_bf16(tmem_d, sw128_desc(a_addr + 32 * kk), sw128_desc(b_addr + 32 * kk),
+                             idesc, (i | kk) != 0 ? 1u : 0u);
+                mma_commit(bar_empty + 8 * s);
+            }
+            if (ok) {
+                mma_commit(bar_accum);
+            } else {
+                // Make sure no MMA is still writing TMEM before it is freed.
+                mma_commit(bar_drain);
+                volatile int no_abort = 0;
+                mbar_wait_bounded(bar_drain, 0, &no_abort, err, kErrTimeoutDrain);
+            }
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == C::kMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d),
+                     "r"(C::kTmemCols)
+                     : "memory");
+    }
+}
+
+template <int BN>
+cudaError_t launch_bn(const float* x, const uint8_t* w, float* y, int M, int N, int K, int device,
+                      cudaStream_t stream) {
+    using C = Cfg<BN>;
+    static bool attr_done[64] = {};
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    if (!attr_done[device]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done[device] = true;
+    }
+    dim3 grid((N + BN - 1) / BN, (M + kBM - 1) / kBM);
+    gemm_tc_kernel<BN><<<grid, C::kThreads, C::kSmemBytes, stream>>>(x, w, y, M, N, K);
+    return cudaGetLastError();
+}
+
+// Tile width: the smallest estimated time with tiles spread over the SMs; a
+// tile's time grows with BN (decode) plus a fixed share (x conversion, fill).
+int choose_bn(int M, int N, int sm_count) {
+    const int cands[4] = {256, 192, 128, 64};
+    int best = 128;
+    long best_cost = -1;
+    const long mt = (M + kBM - 1) / kBM;
+    for (int bn : cands) {
+        const long tiles = mt * ((N + bn - 1) / bn);
+        const long waves = (tiles + sm_count - 1) / sm_count;
+        const long cost = waves * (bn + 32);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, int N, int K,
+                           int device, int sm_count, cudaStream_t stream) {
+    switch (choose_bn(M, N, sm_count)) {
+        case 256: return launch_bn<256>(x, w, y, M, N, K, device, stream);
+        case 192: return launch_bn<192>(x, w, y, M, N, K, device, stream);
+        case 128: return launch_bn<128>(x, w, y, M, N, K, device, stream);
+        default: return launch_bn<64>(x, w, y, M, N, K, device, stream);
+    }
+}
+
+cudaError_t read_and_clear_tc_error(uint32_t* out, cudaStream_t stream) {
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_tc_error, sizeof(unsigned int), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyToSymbolAsync(g_tc_error, &zero, sizeof(unsigned int), 0,
+                                cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(stream);
+}
+
+}  // namespace q2k

@@ -1,0 +1,28 @@
+// Launchers shared between the libq2k translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace q2k {
+
+cudaError_t launch_dequant(const uint8_t* blocks, float* out, size_t n_blocks, int sm_count,
+                           cudaStream_t stream);
+
+cudaError_t launch_gather(const uint8_t* table, const uint32_t* ids, float* out, uint32_t vocab,
+                          uint32_t embed_dim, uint32_t n_tokens, uint32_t* bad_id_count,
+                          int sm_count, cudaStream_t stream);
+
+// M rows of x per launch slice are handled 8 at a time (grid.y = ceil(M/8)).
+cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N, int K,
+                        cudaStream_t stream);
+
+// bf16 tcgen05 GEMM; `device` selects per-device one-time setup.
+cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, int N, int K,
+                           int device, int sm_count, cudaStream_t stream);
+
+// Read and clear the tensor-core kernels' device error word (synchronises `stream`).
+cudaError_t read_and_clear_tc_error(uint32_t* out, cudaStream_t stream);
+
+}  // namespace q2k

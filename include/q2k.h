@@ -1,0 +1,159 @@
+/*
+ * q2k.h - C ABI of libq2k: GGML Q2_K dequantize, embedding gather and
+ * weight-quantized matmul on one NVIDIA GB300 (sm_103a).
+ *
+ * Q2_K storage (mlx-native page "tests/deepseek_q2_k.rs", consts QK_K and
+ * BLOCK_BYTES, fixture fn block, fn reference_dequant): a super-block of 256
+ * weights is 84 bytes -
+ *     bytes  0..15  scale byte per 16-weight group: low nibble sc, high nibble m
+ *     bytes 16..79  2-bit quants q, four per byte
+ *     bytes 80..81  f16 d      (little endian)
+ *     bytes 82..83  f16 dmin   (little endian)
+ * Weight k of a block (k = 128 half + 32 j + 16 segment + lane, shift = 2 j)
+ * is  dl*q - ml  with  q = (qs[32 half + 16 segment + lane] >> shift) & 3,
+ * dl = d * (sc & 15), ml = dmin * (sc >> 4) of scale byte 8 half + 2 j + segment.
+ * A matrix of n rows and k columns is n rows of k/256 consecutive blocks, row
+ * after row (block b of row r at byte (r * k/256 + b) * 84).
+ *
+ * Conventions shared by every call:
+ *  - Pointers are caller-owned DEVICE memory unless stated otherwise; the
+ *    library allocates no device memory in these calls and keeps no pointer
+ *    after returning.
+ *  - Sizes are exact: a buffer whose stated size differs from the size the
+ *    geometry implies is rejected (the pages' `require` check: exact byte
+ *    length, overflow-checked products).
+ *  - An output may not overlap any input (the pages' `validate_disjoint`).
+ *  - On any Q2K_ERR_INVALID_ARGUMENT nothing is launched; q2k_last_error()
+ *    returns a message (thread-local, valid until the next call on the thread).
+ *  - Work is enqueued on `stream` (NULL = the legacy default stream) and the
+ *    call returns without waiting, except where stated.  Launch failures map
+ *    to Q2K_ERR_CUDA.
+ *  - The device is the one current on the calling thread.
+ */
+#ifndef Q2K_H
+#define Q2K_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream, without pulling in the CUDA headers. */
+typedef struct CUstream_st *q2k_stream_t;
+
+typedef enum q2k_status {
+    Q2K_OK = 0,
+    Q2K_ERR_INVALID_ARGUMENT = 1, /* the pages' MlxError::InvalidArgument */
+    Q2K_ERR_BAD_ID = 2,           /* reserved: gather reports bad ids through bad_id_count */
+    Q2K_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed */
+    Q2K_ERR_TIMEOUT = 4,          /* a kernel gave up waiting (see q2k_device_error) */
+    Q2K_ERR_NO_DEVICE = 5         /* no sm_103 device is current */
+} q2k_status;
+
+enum {
+    Q2K_GGML_TYPE_Q2_K = 10, /* GGUF / GgmlType tag of Q2_K */
+    Q2K_QK_K = 256,          /* weights per super-block */
+    Q2K_BLOCK_BYTES = 84     /* bytes per super-block */
+};
+
+/* Geometry of y[m, n] = sum_k x[m, k] * W[n, k]; the pages'
+ * GgmlQuantizedMatmulParams {m, n, k, ggml_type} (page "tests/deepseek_q2_k.rs",
+ * fn run_dense).  16 bytes, fields in this order. */
+typedef struct q2k_matmul_params {
+    uint32_t m;          /* activation rows (tokens), >= 1 */
+    uint32_t n;          /* weight rows = output columns, >= 1 */
+    uint32_t k;          /* reduction length, a positive multiple of 256 */
+    uint32_t ggml_type;  /* must be Q2K_GGML_TYPE_Q2_K */
+} q2k_matmul_params;
+
+/* The pages' EmbeddingQ2KParams {vocab_size, embed_dim, n_tokens} (page
+ * "tests/deepseek_q2_k.rs", test q2_k_embedding_gather_...), plus the type tag. */
+typedef struct q2k_embedding_params {
+    uint32_t vocab_size; /* table rows, >= 1 */
+    uint32_t embed_dim;  /* table columns, a positive multiple of 256 */
+    uint32_t n_tokens;   /* ids to gather, >= 1 */
+    uint32_t ggml_type;  /* must be Q2K_GGML_TYPE_Q2_K */
+} q2k_embedding_params;
+
+/* Which kernel q2k_matmul_path runs (the pages' forced-path test hooks
+ * dispatch_mm_for_test / dispatch_mm_simd_for_test). */
+typedef enum q2k_path {
+    Q2K_PATH_AUTO = 0,   /* what q2k_matmul picks: GEMV for m <= 8, else tensor cores */
+    Q2K_PATH_GEMV = 1,   /* fp32 CUDA-core streaming GEMV, any m (fastest for m <= 8) */
+    Q2K_PATH_TENSOR = 2  /* bf16 tcgen05 tensor-core GEMM with fp32 accumulation */
+} q2k_path;
+
+/* q2k_dequantize - decode whole Q2_K blocks to f32.
+ * Page "tests/deepseek_q2_k.rs": fn test_only_dequantize and tests
+ * q2_k_host_decode_matches_all_256_canonical_values / ..._rejects_malformed_buffers.
+ *   blocks      device, blocks_bytes bytes, 4-byte aligned; blocks_bytes a
+ *               positive multiple of 84 (83 bytes is rejected)
+ *   out         device f32, out_elems = blocks_bytes / 84 * 256 exactly
+ *               (one float short is rejected); 16-byte aligned
+ * Results are bit-identical to the page's f32 loop (each product rounded on
+ * its own; all of them are exact in f32, so only the subtraction rounds). */
+q2k_status q2k_dequantize(const void *blocks, size_t blocks_bytes,
+                          float *out, size_t out_elems, q2k_stream_t stream);
+
+/* q2k_embedding_gather - out[t, :] = decoded table row ids[t].
+ * Page "tests/deepseek_q2_k.rs": fn embedding_gather_q2_k and test
+ * q2_k_embedding_gather_matches_canonical_rows_and_rejects_bad_ids.
+ *   table       device, table_bytes = vocab_size * embed_dim/256 * 84, 4-byte aligned
+ *   ids         device u32 [n_tokens]
+ *   out         device f32 [n_tokens, embed_dim], out_elems = n_tokens*embed_dim,
+ *               16-byte aligned
+ *   bad_id_count  device u32 or NULL.  The pages reject an id >= vocab_size.
+ *               Ids live on the device here, so the check runs in the kernel:
+ *               a row with a bad id is written as zeros and, when bad_id_count
+ *               is not NULL, the number of bad ids is stored there (the call
+ *               zeroes it first, stream-ordered).  Read it after the stream
+ *               completes; nonzero means the pages' error.
+ * Decoded values are bit-identical to q2k_dequantize of the same rows. */
+q2k_status q2k_embedding_gather(const void *table, size_t table_bytes,
+                                const uint32_t *ids, float *out, size_t out_elems,
+                                const q2k_embedding_params *params,
+                                uint32_t *bad_id_count, q2k_stream_t stream);
+
+/* q2k_matmul - y[m, n] = sum_k x[m, k] * W[n, k] with W in Q2_K, the
+ * dequantization fused into the product.
+ * Page "tests/deepseek_q2_k.rs": fn quantized_matmul_ggml, fn run_dense.
+ *   x           device f32 [m, k] row-major, x_elems = m*k, 16-byte aligned
+ *   w           device, w_bytes = n * k/256 * 84, 4-byte aligned
+ *   y           device f32 [m, n] row-major, y_elems = m*n, 16-byte aligned;
+ *               fully overwritten
+ * Path: m <= 8 runs the fp32 GEMV (error within 1e-5 * sum_k |x w| per
+ * output); m > 8 runs the bf16 tensor-core GEMM (x and W rounded to bf16,
+ * fp32 accumulation; error within 8e-3 * sum_k |x w|), mirroring the pages'
+ * switch of tolerance at rows > 8.  Repeated calls on the same inputs give
+ * bit-identical y (no floating-point atomics). */
+q2k_status q2k_matmul(const float *x, size_t x_elems, const void *w, size_t w_bytes,
+                      float *y, size_t y_elems, const q2k_matmul_params *params,
+                      q2k_stream_t stream);
+
+/* q2k_matmul_path - q2k_matmul with the kernel chosen by the caller (the
+ * pages' dispatch_mm_for_test); same arguments, sizes and errors. */
+q2k_status q2k_matmul_path(q2k_path path, const float *x, size_t x_elems,
+                           const void *w, size_t w_bytes, float *y, size_t y_elems,
+                           const q2k_matmul_params *params, q2k_stream_t stream);
+
+/* q2k_device_error - read and clear the library's device error word on the
+ * current device.  Kernels that wait on on-chip barriers give up after about a
+ * second, set a bit here and return instead of hanging.  Synchronises
+ * `stream`.  *out = 0 means no kernel gave up since the last read. */
+q2k_status q2k_device_error(uint32_t *out, q2k_stream_t stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char *q2k_last_error(void);
+
+/* ABI version of this header (bumped on any incompatible change). */
+int q2k_abi_version(void);
+
+#define Q2K_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q2K_H */

@@ -1,0 +1,117 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, lays out its structs as declared, and rejects malformed
+arguments before touching CUDA (page "tests/deepseek_q2_k.rs": malformed
+buffers and bad geometry are InvalidArgument, nothing is launched)."""
+
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import ggml_q2_quantized_gb300 as q2k
+from ggml_q2_quantized_gb300 import build as q2k_build
+
+INVALID = 1
+
+
+@pytest.fixture(scope="module")
+def lib():
+    q2k_build.build()
+    return q2k.load()
+
+
+def test_header_declares_the_calls():
+    names = q2k.header_functions()
+    for want in ("q2k_dequantize", "q2k_embedding_gather", "q2k_matmul", "q2k_matmul_path",
+                 "q2k_device_error", "q2k_last_error", "q2k_abi_version"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in q2k.header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_abi_version(lib):
+    assert lib.q2k_abi_version() == 1
+
+
+def test_struct_layout_matches_c(tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stddef.h>\n#include <stdio.h>\n#include "q2k.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu %zu\\n\", sizeof(q2k_matmul_params),"
+        " offsetof(q2k_matmul_params, ggml_type), sizeof(q2k_embedding_params),"
+        " offsetof(q2k_embedding_params, n_tokens), sizeof(q2k_status));return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", q2k_build.INCLUDE, str(src),
+                    "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert [int(v) for v in out] == [16, 12, 16, 8, 4]
+    assert ctypes.sizeof(q2k.MatmulParams) == 16
+    assert ctypes.sizeof(q2k.EmbeddingParams) == 16
+    assert q2k.MatmulParams.ggml_type.offset == 12
+
+
+def _mm(lib, params, x=0x10000, xe=None, w=0x100000, wb=None, y=0x1000000, ye=None, path=0):
+    m, n, k = params.m, params.n, params.k
+    xe = m * k if xe is None else xe
+    wb = n * (k // 256) * 84 if wb is None else wb
+    ye = m * n if ye is None else ye
+    return lib.q2k_matmul_path(path, x, xe, w, wb, y, ye, ctypes.byref(params), None)
+
+
+P = q2k.MatmulParams
+
+
+@pytest.mark.parametrize("params,kw,fragment", [
+    (P(1, 8, 255, 10), {}, "multiple of 256"),
+    (P(1, 8, 256, 11), {}, "not Q2_K"),
+    (P(0, 8, 256, 10), {}, ">= 1"),
+    (P(1, 0, 256, 10), {}, ">= 1"),
+    (P(1, 8, 256, 10), {"xe": 255}, "x has 255"),
+    (P(1, 8, 256, 10), {"wb": 8 * 84 - 1}, "w has 671"),
+    (P(1, 8, 256, 10), {"ye": 9}, "y has 9"),
+    (P(1, 8, 256, 10), {"x": 0}, "non-NULL"),
+    (P(1, 8, 256, 10), {"x": 0x10004}, "aligned"),
+    (P(1, 8, 256, 10), {"w": 0x100002}, "aligned"),
+    (P(1, 8, 256, 10), {"y": 0x10010}, "alias"),          # y inside x
+    (P(1, 8, 256, 10), {"y": 0x100000}, "alias"),         # y on top of w
+    (P(1, 8, 256, 10), {"path": 7}, "unknown path"),
+    (P(0xFFFFFFFF, 0xFFFFFFFF, 256, 10), {}, "signed 32-bit"),
+])
+def test_matmul_rejects(lib, params, kw, fragment):
+    assert _mm(lib, params, **kw) == INVALID
+    assert fragment in lib.q2k_last_error().decode()
+
+
+def test_dequantize_rejects_malformed(lib):
+    # page test q2_k_host_decode_rejects_malformed_buffers: 83 bytes, 255 floats
+    assert lib.q2k_dequantize(0x10000, 83, 0x100000, 256, None) == INVALID
+    assert lib.q2k_dequantize(0x10000, 84, 0x100000, 255, None) == INVALID
+    assert lib.q2k_dequantize(0x10000, 0, 0x100000, 0, None) == INVALID
+    assert lib.q2k_dequantize(0, 84, 0x100000, 256, None) == INVALID
+    assert lib.q2k_dequantize(0x10000, 84, 0x10000, 256, None) == INVALID  # aliasing
+
+
+def test_gather_rejects_malformed(lib):
+    E = q2k.EmbeddingParams
+    ok = dict(table=0x10000, tb=3 * 84, ids=0x20000, out=0x100000, oe=2 * 256)
+
+    def call(p, **kw):
+        a = dict(ok, **kw)
+        return lib.q2k_embedding_gather(a["table"], a["tb"], a["ids"], a["out"], a["oe"],
+                                        ctypes.byref(p), None, None)
+    assert call(E(3, 255, 2, 10)) == INVALID
+    assert call(E(3, 256, 2, 9)) == INVALID
+    assert call(E(3, 256, 2, 10), tb=3 * 84 + 1) == INVALID
+    assert call(E(3, 256, 2, 10), oe=511) == INVALID
+    assert call(E(3, 256, 2, 10), out=0x10000) == INVALID   # out over the table
+    assert call(E(0, 256, 2, 10)) == INVALID
+    assert "vocab_size" in lib.q2k_last_error().decode()
+
+
+def test_binding_refuses_missing_library(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        q2k.load(str(tmp_path / "nope.so"))
