@@ -203,7 +203,7 @@ q2k_status q2k_matmul_path(q2k_path path, const float* x, size_t x_elems, const 
     const uint8_t* wb = static_cast<const uint8_t*>(w);
     cudaError_t e;
     if (path == Q2K_PATH_GEMV)
-        e = q2k::launch_gemv(x, wb, y, int(p->m), int(p->n), int(p->k), s);
+        e = q2k::launch_gemv(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count, s);
     else
         e = q2k::launch_gemm_tc(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count, s);
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul launch");
@@ -220,7 +220,10 @@ q2k_status q2k_device_error(uint32_t* out, q2k_stream_t stream) {
     DeviceInfo dev;
     q2k_status st = current_device(&dev);
     if (st != Q2K_OK) return st;
-    cudaError_t e = q2k::read_and_clear_tc_error(out, reinterpret_cast<cudaStream_t>(stream));
+    uint32_t tc = 0, gemv = 0;
+    cudaError_t e = q2k::read_and_clear_tc_error(&tc, reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = q2k::read_and_clear_gemv_error(&gemv, reinterpret_cast<cudaStream_t>(stream));
+    *out = tc | gemv;
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_device_error");
 }
 

@@ -14,9 +14,13 @@ cudaError_t launch_gather(const uint8_t* table, const uint32_t* ids, float* out,
                           uint32_t embed_dim, uint32_t n_tokens, uint32_t* bad_id_count,
                           int sm_count, cudaStream_t stream);
 
-// M rows of x per launch slice are handled 8 at a time (grid.y = ceil(M/8)).
+// fp32 GEMV path: m = 1 uses the shared-memory streaming kernel when K <= 16384
+// and w is 16-byte aligned; otherwise x rows are handled 8 at a time.
 cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N, int K,
-                        cudaStream_t stream);
+                        int device, int sm_count, cudaStream_t stream);
+
+// Read and clear the GEMV kernels' device error word (synchronises `stream`).
+cudaError_t read_and_clear_gemv_error(uint32_t* out, cudaStream_t stream);
 
 // bf16 tcgen05 GEMM; `device` selects per-device one-time setup.
 cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, int N, int K,
