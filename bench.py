@@ -53,7 +53,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_gemv_4096")
@@ -111,11 +111,22 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
+            return self
+        # Let nvidia-smi finish starting up (its first query is slow) before the
+        # timed region begins: wait for the first sample line.
+        import select
+        deadline = time.time() + 5.0
+        self._first = ""
+        while time.time() < deadline:
+            r, _, _ = select.select([self.proc.stdout], [], [], 0.1)
+            if r:
+                self._first = self.proc.stdout.readline()
+                break
+        time.sleep(0.25)
         return self
 
     def __exit__(self, *exc):
@@ -126,6 +137,7 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
                 self.out, _ = self.proc.communicate()
+            self.out = (getattr(self, "_first", "") or "") + (self.out or "")
 
     def summary(self):
         if not self.out:

@@ -37,187 +37,186 @@ __device__ unsigned int g_gemv_error;
 
 namespace {
 
-#ifndef Q2K_GEMV_M1_VARIANT
-#define Q2K_GEMV_M1_VARIANT 0
-#endif
-
 constexpr int kGemvWarps = 8;
 constexpr int kPieceRows = 4;      // rows per bulk copy / mbarrier
-constexpr int kM1MaxThreads = 256;
 constexpr int kM1MaxSlices = 256;  // k <= 16384
+#ifndef Q2K_M1_THREADS
+#define Q2K_M1_THREADS 256
+#endif
+constexpr int kM1Threads = Q2K_M1_THREADS;  // 256 leaves room for the next grid's CTA
 
 // ------------------------------------------------------------------ m = 1
 
-struct SliceX {
-    float x[4][16];   // x at k = 256 b + 128 h + 32 j + 16 seg + l
-    float X[4];       // sum_l x[j][l]
-    uint32_t p0[4][4], p1[4][4], p2[4][4];  // byte planes (variant 2)
-    float inv_scale;  // 2^-e (variant 2)
+constexpr int kRowBatch = 4;  // rows reduced together by one transposed butterfly
+
+// x as exact integers: each 16-weight run r (k = 16 r .. 16 r + 15, one
+// (half, shift, segment) of a block) is scaled by 2^e_r so that its largest
+// |x| lies in [2^21, 2^22), rounded to nearest, and split into byte planes
+// x_int = p2 * 65536 + p1 * 256 + p0 (p2 signed, p1/p0 unsigned).  The plane
+// words of a run are 4 consecutive weights each.  Also kept per run: the f32
+// sum of its 16 x (for the -ml term) and 2^-e_r.
+struct RunPlanes {
+    uint32_t p0[4], p1[4], p2[4];
 };
 
-template <int kVariant>
-__device__ __forceinline__ void load_slice(const float* __restrict__ xs, SliceX& s) {
+__device__ __forceinline__ void convert_run(const float* __restrict__ xr, RunPlanes* planes,
+                                            float* run_sum, float* run_inv) {
+    float v[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 t = __ldg(reinterpret_cast<const float4*>(xr + 4 * q));
+        v[4 * q] = t.x;
+        v[4 * q + 1] = t.y;
+        v[4 * q + 2] = t.z;
+        v[4 * q + 3] = t.w;
+    }
+    float mx = 0.f, sum = 0.f;
+#pragma unroll
+    for (int l = 0; l < 16; ++l) {
+        mx = fmaxf(mx, fabsf(v[l]));
+        sum += v[l];
+    }
+    // e = 21 - floor(log2 max|x|), kept within the normal range; for max|x| = 0
+    // (or a subnormal max) any e gives zeros, so e = 0 then.
+    const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu);  // biased exponent
+    int e = (ex == 0 || ex == 255) ? 0 : 148 - ex;                            // 21 - (ex - 127)
+    e = max(-126, min(126, e));
+    const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);   // 2^e, exact
+    RunPlanes pl;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t b0 = 0, b1 = 0, b2 = 0;
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+            // |x 2^e| < 2^22: adding 1.5 * 2^23 rounds it to an integer (nearest,
+            // ties to even) held in the low mantissa bits.
+            const float biased = fmaf(v[4 * q + e4], up, 12582912.f);
+            const uint32_t xi = __float_as_uint(biased) - 0x4B400000u;  // two's complement
+            b0 |= (xi & 0xFFu) << (8 * e4);
+            b1 |= ((xi >> 8) & 0xFFu) << (8 * e4);
+            b2 |= ((xi >> 16) & 0xFFu) << (8 * e4);
+        }
+        pl.p0[q] = b0;
+        pl.p1[q] = b1;
+        pl.p2[q] = b2;
+    }
+    *planes = pl;
+    *run_sum = sum;
+    *run_inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
+}
+
+struct SlicePlanes {
+    RunPlanes r[4];  // shift j = 0..3
+    float X[4];      // sum of the run's x
+    float inv[4];    // 2^-e of the run
+};
+
+// The 7 words of one weight row a thread needs: its 16 quant bytes, the four
+// scale bytes of its segment (one per shift) and the packed f16 d, dmin.
+struct RowWords {
+    uint32_t q[4];
+    uint32_t sc4;
+    uint32_t dd;
+};
+
+__device__ __forceinline__ RowWords load_row_words(const uint8_t* __restrict__ rp, int h, int seg,
+                                                   uint32_t ssel) {
+    RowWords r;
+    const uint8_t* qp = rp + 16 + 32 * h + 16 * seg;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r.q[i] = ld_u32(qp + 4 * i);
+    r.sc4 = __byte_perm(ld_u32(rp + 8 * h), ld_u32(rp + 8 * h + 4), ssel);
+    r.dd = ld_u32(rp + 80);
+    return r;
+}
+
+// Partial dot product of one weight row with this thread's 64-weight slice:
+// sum_j (d sc_j 2^-e_j) S_j - (dmin m_j) X_j with S_j = sum_l q_l x_int_l exact.
+__device__ __forceinline__ float slice_dot(const RowWords& r, const SlicePlanes& s) {
+    const float d = f16_bits_to_float(r.dd);
+    const float dmin = f16_bits_to_float(r.dd >> 16);
+    const uint32_t lo = r.sc4 & 0x0F0F0F0Fu;
+    const uint32_t hi = (r.sc4 >> 4) & 0x0F0F0F0Fu;
+    float pa = 0.f, pb = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
+        int a2 = 0;
+        unsigned a1 = 0, a0 = 0;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(xs + 32 * j + 4 * q));
-            s.x[j][4 * q] = v.x;
-            s.x[j][4 * q + 1] = v.y;
-            s.x[j][4 * q + 2] = v.z;
-            s.x[j][4 * q + 3] = v.w;
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t t = (r.q[i] >> (2 * j)) & 0x03030303u;
+            a2 = __dp4a(static_cast<int>(s.r[j].p2[i]), static_cast<int>(t), a2);
+            a1 = __dp4a(s.r[j].p1[i], t, a1);
+            a0 = __dp4a(s.r[j].p0[i], t, a0);
         }
-        float acc = 0.f;
-#pragma unroll
-        for (int l = 0; l < 16; ++l) acc += s.x[j][l];
-        s.X[j] = acc;
+        const int sint = a2 * 65536 + static_cast<int>(a1 * 256u + a0);
+        // byte j of lo/hi -> exact float through the bits of 2^23 + v
+        const uint32_t sel = static_cast<uint32_t>(j) | (4u << 4) | (4u << 8) | (7u << 12);
+        const float scf = __uint_as_float(__byte_perm(lo, 0x4B000000u, sel)) - 8388608.f;
+        const float mf = __uint_as_float(__byte_perm(hi, 0x4B000000u, sel)) - 8388608.f;
+        pa = fmaf((d * s.inv[j]) * scf, static_cast<float>(sint), pa);
+        pb = fmaf(-(dmin * mf), s.X[j], pb);
     }
-    if (kVariant == 2) {
-        float mx = 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int l = 0; l < 16; ++l) mx = fmaxf(mx, fabsf(s.x[j][l]));
-        // e such that max|x| * 2^e < 2^22: every scaled value fits 23 bits with sign
-        int e = 0;
-        if (mx > 0.f) e = 21 - ilogbf(mx);
-        e = max(-126, min(e, 126));
-        s.inv_scale = ldexpf(1.f, -e);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t b0 = 0, b1 = 0, b2 = 0;
-#pragma unroll
-                for (int e4 = 0; e4 < 4; ++e4) {
-                    const int v = __float2int_rn(ldexpf(s.x[j][4 * q + e4], e));
-                    b0 |= (static_cast<uint32_t>(v) & 0xFFu) << (8 * e4);
-                    b1 |= ((static_cast<uint32_t>(v) >> 8) & 0xFFu) << (8 * e4);
-                    b2 |= ((static_cast<uint32_t>(v) >> 16) & 0xFFu) << (8 * e4);
-                }
-                s.p0[j][q] = b0;
-                s.p1[j][q] = b1;
-                s.p2[j][q] = b2;
-            }
-    }
+    return pa + pb;
 }
 
-__device__ __forceinline__ float small_uint_to_float(uint32_t byte_src, int which) {
-    // byte `which` of byte_src (a value < 256) -> float, exactly, via 2^23 + v - 2^23
-    const uint32_t sel = static_cast<uint32_t>(which) | (4u << 4) | (4u << 8) | (7u << 12);
-    return __uint_as_float(__byte_perm(byte_src, 0x4B000000u, sel)) - 8388608.f;
+// Sum v[0..kRowBatch) over the 32 lanes; afterwards lane L holds the total of
+// row (L >> 3) & (kRowBatch - 1) ... in a fixed order (deterministic).
+// Returns the row index this lane's value belongs to via *row.
+__device__ __forceinline__ float transpose_reduce4(float (&v)[kRowBatch], int lane, int* row) {
+    // xor 16: split rows {0,1} / {2,3}
+    const bool up16 = (lane & 16) != 0;
+    float a0 = up16 ? v[2] : v[0], a1 = up16 ? v[3] : v[1];
+    float s0 = up16 ? v[0] : v[2], s1 = up16 ? v[1] : v[3];
+    a0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 16);
+    a1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 16);
+    // xor 8: split the remaining pair
+    const bool up8 = (lane & 8) != 0;
+    float b = up8 ? a1 : a0;
+    const float t = up8 ? a0 : a1;
+    b += __shfl_xor_sync(0xFFFFFFFFu, t, 8);
+    b += __shfl_xor_sync(0xFFFFFFFFu, b, 4);
+    b += __shfl_xor_sync(0xFFFFFFFFu, b, 2);
+    b += __shfl_xor_sync(0xFFFFFFFFu, b, 1);
+    *row = (up16 ? 2 : 0) + (up8 ? 1 : 0);
+    return b;
 }
 
-// Partial dot product of one weight row with this thread's slice.
-template <int kVariant>
-__device__ __forceinline__ float slice_dot(const uint8_t* __restrict__ rp, int h, int seg,
-                                           uint32_t ssel, const SliceX& s) {
-    const uint8_t* qp = rp + 16 + 32 * h + 16 * seg;
-    uint32_t qw[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) qw[i] = ld_u32(qp + 4 * i);
-    const uint32_t sc4 = __byte_perm(ld_u32(rp + 8 * h), ld_u32(rp + 8 * h + 4), ssel);
-    const uint32_t dd = ld_u32(rp + 80);
-    const float d = f16_bits_to_float(dd);
-    const float dmin = f16_bits_to_float(dd >> 16);
-    const uint32_t lo = sc4 & 0x0F0F0F0Fu;
-    const uint32_t hi = (sc4 >> 4) & 0x0F0F0F0Fu;
-    float p = 0.f;
-    if (kVariant == 0) {
-        const float d4 = 4.f * d;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float c1 = d * small_uint_to_float(lo, j);      // dl
-            const float ml = dmin * small_uint_to_float(hi, j);   // ml
-            (void)d4;
-            float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t u = (j < 3) ? (qw[i] << (5 - 2 * j)) : (qw[i] >> 1);
-                const uint32_t v = (u & 0x60606060u) | 0x80808080u;  // byte = 0x80 | q << 5
-                float2 f01 = make_float2(__uint_as_float(__byte_perm(v, 0x3F000000u, 0x7054u)),
-                                         __uint_as_float(__byte_perm(v, 0x3F000000u, 0x7154u)));
-                float2 f23 = make_float2(__uint_as_float(__byte_perm(v, 0x3F000000u, 0x7254u)),
-                                         __uint_as_float(__byte_perm(v, 0x3F000000u, 0x7354u)));
-                // 1 + q/4 - 1 = q/4 exactly
-                f01 = fadd2(f01, make_float2(-1.f, -1.f));
-                f23 = fadd2(f23, make_float2(-1.f, -1.f));
-                acc = ffma2(make_float2(s.x[j][4 * i], s.x[j][4 * i + 1]), f01, acc);
-                acc = ffma2(make_float2(s.x[j][4 * i + 2], s.x[j][4 * i + 3]), f23, acc);
-            }
-            // acc = S_j / 4
-            p = fmaf(4.f * c1, acc.x + acc.y, p);
-            p = fmaf(-ml, s.X[j], p);
-        }
-    } else if (kVariant == 1) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float dl = d * static_cast<float>((lo >> (8 * j)) & 0xFFu);
-            const float ml = dmin * static_cast<float>((hi >> (8 * j)) & 0xFFu);
-            float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t t = (qw[i] >> (2 * j)) & 0x03030303u;
-                const float2 f01 = make_float2(static_cast<float>(t & 0xFFu),
-                                               static_cast<float>((t >> 8) & 0xFFu));
-                const float2 f23 = make_float2(static_cast<float>((t >> 16) & 0xFFu),
-                                               static_cast<float>(t >> 24));
-                acc = ffma2(make_float2(s.x[j][4 * i], s.x[j][4 * i + 1]), f01, acc);
-                acc = ffma2(make_float2(s.x[j][4 * i + 2], s.x[j][4 * i + 3]), f23, acc);
-            }
-            p = fmaf(dl, acc.x + acc.y, p);
-            p = fmaf(-ml, s.X[j], p);
-        }
-    } else {
-        const float dsc = d * s.inv_scale;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            int a2 = 0;
-            unsigned a1 = 0, a0 = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t t = (qw[i] >> (2 * j)) & 0x03030303u;
-                a2 = __dp4a(static_cast<int>(s.p2[j][i]), static_cast<int>(t), a2);
-                a1 = __dp4a(s.p1[j][i], t, a1);
-                a0 = __dp4a(s.p0[j][i], t, a0);
-            }
-            const int sint = a2 * 65536 + static_cast<int>(a1 * 256u + a0);
-            const float dl = dsc * static_cast<float>((lo >> (8 * j)) & 0xFFu);
-            const float ml = dmin * static_cast<float>((hi >> (8 * j)) & 0xFFu);
-            p = fmaf(dl, static_cast<float>(sint), p);
-            p = fmaf(-ml, s.X[j], p);
-        }
-    }
-    return p;
-}
-
-template <int kVariant>
-__global__ void __launch_bounds__(kM1MaxThreads, 2)
+__global__ void __launch_bounds__(512, 1)
 gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
                int N, int K, int rows_per_cta, int slices_pad, int groups) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
+    const int nthreads = blockDim.x;
     const int B = K >> 8;
     const int S = K >> 6;
+    const int n_runs = K >> 4;
     const size_t row_bytes = static_cast<size_t>(B) * kBlockBytes;
     const int r0 = blockIdx.x * rows_per_cta;
     const int rows = min(rows_per_cta, N - r0);
     const int n_pieces = (rows + kPieceRows - 1) / kPieceRows;
+    const int max_pieces = (rows_per_cta + kPieceRows - 1) / kPieceRows;
     const int warps_per_group = slices_pad >> 5;
+    // shared layout: W chunk | run planes | run sums | run scales | red | bars | flag
     const size_t w_smem = (static_cast<size_t>(rows_per_cta) * row_bytes + 15) & ~size_t(15);
-    float* red = reinterpret_cast<float*>(smem + w_smem);
-    const size_t red_bytes = (static_cast<size_t>(rows_per_cta) * warps_per_group * 4 + 7) & ~size_t(7);
-    const uint32_t bars = smem_u32(smem + w_smem + red_bytes);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + w_smem + red_bytes +
-                                                                8 * ((rows_per_cta + kPieceRows - 1) / kPieceRows));
+    RunPlanes* planes = reinterpret_cast<RunPlanes*>(smem + w_smem);
+    float* run_sum = reinterpret_cast<float*>(planes + n_runs);
+    float* run_inv = run_sum + n_runs;
+    float* red = run_inv + n_runs;
+    const size_t red_end = w_smem + static_cast<size_t>(n_runs) * (sizeof(RunPlanes) + 8) +
+                           static_cast<size_t>(rows_per_cta) * warps_per_group * 4;
+    const size_t bar_off = (red_end + 7) & ~size_t(7);
+    const uint32_t bars = smem_u32(smem + bar_off);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + bar_off + 8 * max_pieces);
     const uint8_t* gsrc = w + static_cast<size_t>(r0) * row_bytes;
     const size_t chunk = static_cast<size_t>(rows) * row_bytes;
 
     if (tid == 0) {
-        // The weights never depend on the previous grid's results being in
-        // shared memory, and an L2 prefetch is coherent with its writes.
-        for (size_t off = 0; off < (chunk & ~size_t(15)); off += (size_t(1) << 20)) {
-            const size_t left = (chunk & ~size_t(15)) - off;
+        // Weights never depend on the previous grid's results being in shared
+        // memory, and an L2 prefetch is coherent with that grid's writes.
+        const size_t pre = chunk & ~size_t(15);
+        for (size_t off = 0; off < pre; off += (size_t(1) << 20)) {
+            const size_t left = pre - off;
             bulk_prefetch_l2(gsrc + off, static_cast<uint32_t>(left < (size_t(1) << 20) ? left : (size_t(1) << 20)));
         }
         for (int p = 0; p < n_pieces; ++p) mbar_init(bars + 8 * p, 1);
@@ -242,47 +241,57 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
             bulk_copy_g2s(smem_u32(smem + off), gsrc + off, static_cast<uint32_t>(bulk), bars + 8 * p);
         }
     }
+    // x -> integer planes, once per CTA, while the weights stream in
+    for (int r = tid; r < n_runs; r += nthreads)
+        convert_run(x + 16 * r, &planes[r], &run_sum[r], &run_inv[r]);
+    __syncthreads();
 
     const int g = tid / slices_pad;
     const int sl = tid - g * slices_pad;
     const bool active = sl < S;
     const int b = sl >> 2, h = (sl >> 1) & 1, seg = sl & 1;
     const uint32_t ssel = seg | ((seg + 2) << 4) | ((seg + 4) << 8) | ((seg + 6) << 12);
-    SliceX s;
-    if (active) {
-        load_slice<kVariant>(x + 256 * b + 128 * h + 16 * seg, s);
-    } else {
+    SlicePlanes s;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            s.X[j] = 0.f;
-#pragma unroll
-            for (int l = 0; l < 16; ++l) s.x[j][l] = 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) s.p0[j][q] = s.p1[j][q] = s.p2[j][q] = 0u;
-        }
-        s.inv_scale = 0.f;
+    for (int j = 0; j < 4; ++j) {
+        // run of (block b, half h, shift j, segment seg)
+        const int run = active ? 16 * b + 8 * h + 2 * j + seg : 0;
+        s.r[j] = planes[run];
+        s.X[j] = active ? run_sum[run] : 0.f;
+        s.inv[j] = active ? run_inv[run] : 0.f;
     }
 
     const int lane = tid & 31;
     const int wig = sl >> 5;  // warp index within the group
+    const uint8_t* my_col = smem + b * kBlockBytes;
     int waited = -1;
     bool ok = true;
-    for (int lr = g; lr < rows; lr += groups) {
-        const int piece = lr / kPieceRows;
-        if (piece != waited) {
-            ok = ok && mbar_wait_bounded(bars + 8 * piece, 0, abort_flag, &g_gemv_error, kErrTimeoutGemv);
-            waited = piece;
-        }
-        float part = 0.f;
-        if (active && ok)
-            part = slice_dot<kVariant>(smem + static_cast<size_t>(lr) * row_bytes + b * kBlockBytes, h, seg,
-                                       ssel, s);
+    for (int base = g; base < rows; base += groups * kRowBatch) {
+        // Make sure every piece this batch touches has landed, then issue all
+        // shared-memory loads of the batch before any arithmetic.
+        const int last = min(rows - 1, base + (kRowBatch - 1) * groups);
+        for (int pw = waited + 1; pw <= last / kPieceRows; ++pw)
+            ok = ok && mbar_wait_bounded(bars + 8 * pw, 0, abort_flag, &g_gemv_error, kErrTimeoutGemv);
+        waited = max(waited, last / kPieceRows);
+        RowWords rw[kRowBatch];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, off);
-        if (lane == 0) red[lr * warps_per_group + wig] = part;
+        for (int u = 0; u < kRowBatch; ++u) {
+            const int lr = min(base + u * groups, last);
+            rw[u] = load_row_words(my_col + static_cast<size_t>(lr) * row_bytes, h, seg, ssel);
+        }
+        float part[kRowBatch];
+#pragma unroll
+        for (int u = 0; u < kRowBatch; ++u) {
+            const float v = slice_dot(rw[u], s);
+            part[u] = (active && ok && base + u * groups < rows) ? v : 0.f;
+        }
+        int which;
+        const float tot = transpose_reduce4(part, lane, &which);
+        const int lr = base + which * groups;
+        if ((lane & 7) == 0 && lr < rows) red[lr * warps_per_group + wig] = tot;
     }
     __syncthreads();
-    for (int lr = tid; lr < rows; lr += blockDim.x) {
+    for (int lr = tid; lr < rows; lr += nthreads) {
         float v = 0.f;
         for (int q = 0; q < warps_per_group; ++q) v += red[lr * warps_per_group + q];
         y[r0 + lr] = v;
@@ -300,43 +309,47 @@ struct M1Plan {
     size_t smem;
 };
 
+size_t m1_smem(int rows, int K, int slices_pad) {
+    const size_t row_bytes = static_cast<size_t>(K / 256) * kBlockBytes;
+    const int n_runs = K / 16;
+    const int pieces = (rows + kPieceRows - 1) / kPieceRows;
+    const size_t w_smem = (static_cast<size_t>(rows) * row_bytes + 15) & ~size_t(15);
+    const size_t red_end = w_smem + static_cast<size_t>(n_runs) * (sizeof(RunPlanes) + 8) +
+                           static_cast<size_t>(rows) * (slices_pad / 32) * 4;
+    return ((red_end + 7) & ~size_t(7)) + 8 * pieces + 16;
+}
+
 bool plan_m1(int N, int K, int sm_count, M1Plan* p) {
     const int B = K / 256;
     const int S = K / 64;
     if (S > kM1MaxSlices) return false;
-    const size_t row_bytes = static_cast<size_t>(B) * kBlockBytes;
     const int slices_pad = (S + 31) / 32 * 32;
-    const int groups = slices_pad >= kM1MaxThreads ? 1 : kM1MaxThreads / slices_pad;
-    const size_t smem_cap = 200 * 1024;
+    const int groups = slices_pad >= kM1Threads ? 1 : kM1Threads / slices_pad;
     int rows = 0;
     for (int waves = 1;; ++waves) {
         rows = (N + sm_count * waves - 1) / (sm_count * waves);
         if (B % 4) rows = (rows + 3) / 4 * 4;  // chunk starts stay 16-byte aligned
-        if (static_cast<size_t>(rows) * row_bytes <= smem_cap || rows <= kPieceRows) break;
+        if (m1_smem(rows, K, slices_pad) <= 200 * 1024 || rows <= kPieceRows) break;
     }
-    const int wpg = slices_pad / 32;
-    const int pieces = (rows + kPieceRows - 1) / kPieceRows;
     p->rows_per_cta = rows;
     p->ctas = (N + rows - 1) / rows;
     p->slices_pad = slices_pad;
     p->groups = groups;
     p->threads = slices_pad * groups;
-    p->smem = ((static_cast<size_t>(rows) * row_bytes + 15) & ~size_t(15)) +
-              ((static_cast<size_t>(rows) * wpg * 4 + 7) & ~size_t(7)) + 8 * pieces + 16;
+    p->smem = m1_smem(rows, K, slices_pad);
     return p->smem <= 227 * 1024;
 }
 
-template <int kVariant>
 cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, const M1Plan& p,
                       int device, cudaStream_t stream) {
-    static int smem_set[64] = {};
+    static bool smem_set[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-    if (smem_set[device] < static_cast<int>(p.smem)) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel<kVariant>,
+    if (!smem_set[device]) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              227 * 1024);
         if (e != cudaSuccess) return e;
-        smem_set[device] = 227 * 1024;
+        smem_set[device] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.ctas);
@@ -348,8 +361,8 @@ cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_m1_kernel<kVariant>, x, w, y, N, K, p.rows_per_cta,
-                              p.slices_pad, p.groups);
+    return cudaLaunchKernelEx(&cfg, gemv_m1_kernel, x, w, y, N, K, p.rows_per_cta, p.slices_pad,
+                              p.groups);
 }
 
 // ------------------------------------------------------------------ general m
@@ -448,7 +461,7 @@ cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N
                         int device, int sm_count, cudaStream_t stream) {
     M1Plan plan;
     if (M == 1 && (reinterpret_cast<uintptr_t>(w) & 15u) == 0 && plan_m1(N, K, sm_count, &plan))
-        return launch_m1<Q2K_GEMV_M1_VARIANT>(x, w, y, N, K, plan, device, stream);
+        return launch_m1(x, w, y, N, K, plan, device, stream);
     switch (M < 8 ? M : 8) {
         case 1: return launch_rows<1>(x, w, y, M, N, K, stream);
         case 2: return launch_rows<2>(x, w, y, M, N, K, stream);
