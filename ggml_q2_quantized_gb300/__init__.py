@@ -27,6 +27,7 @@ BLOCK_BYTES = 84
 GGML_TYPE_Q2_K = 10
 
 PATH_AUTO, PATH_GEMV, PATH_TENSOR = 0, 1, 2
+FLAG_CONST_WEIGHTS = 1
 _PATHS = {"auto": PATH_AUTO, "gemv": PATH_GEMV, "tensor": PATH_TENSOR,
           PATH_AUTO: PATH_AUTO, PATH_GEMV: PATH_GEMV, PATH_TENSOR: PATH_TENSOR}
 
@@ -91,9 +92,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q2k_matmul.argtypes = [vp, sz, vp, sz, vp, sz, ctypes.POINTER(MatmulParams), vp]
         lib.q2k_matmul_path.argtypes = [ctypes.c_int, vp, sz, vp, sz, vp, sz,
                                         ctypes.POINTER(MatmulParams), vp]
+        lib.q2k_matmul_ex.argtypes = [ctypes.c_int, ctypes.c_uint32, vp, sz, vp, sz, vp, sz,
+                                      ctypes.POINTER(MatmulParams), vp]
         lib.q2k_device_error.argtypes = [u32p, vp]
         for fn in ("q2k_dequantize", "q2k_embedding_gather", "q2k_matmul", "q2k_matmul_path",
-                   "q2k_device_error"):
+                   "q2k_matmul_ex", "q2k_device_error"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.q2k_last_error.restype = ctypes.c_char_p
         lib.q2k_last_error.argtypes = []
@@ -182,8 +185,12 @@ def embedding_gather(table, ids, embed_dim: int, vocab_size: int | None = None, 
     return out
 
 
-def matmul(x, w, n: int, out=None, path="auto"):
-    """``y[m, r] = sum_k x[m, k] * W[r, k]`` with W = ``n`` rows of Q2_K blocks."""
+def matmul(x, w, n: int, out=None, path="auto", const_weights: bool = False):
+    """``y[m, r] = sum_k x[m, k] * W[r, k]`` with W = ``n`` rows of Q2_K blocks.
+
+    ``const_weights=True`` passes Q2K_FLAG_CONST_WEIGHTS: the caller promises
+    that the kernel enqueued just before on the stream does not write ``w``.
+    """
     torch = _torch()
     _require_cuda(x, "x", torch.float32)
     _require_cuda(w, "w", torch.uint8)
@@ -196,9 +203,10 @@ def matmul(x, w, n: int, out=None, path="auto"):
     p = MatmulParams(m, n, k, GGML_TYPE_Q2_K)
     lib = load()
     with torch.cuda.device(x.device):
-        _check(lib, lib.q2k_matmul_path(_PATHS[path], x.data_ptr(), x.numel(), w.data_ptr(),
-                                        w.numel(), out.data_ptr(), out.numel(), ctypes.byref(p),
-                                        _stream_handle(x)))
+        _check(lib, lib.q2k_matmul_ex(_PATHS[path], FLAG_CONST_WEIGHTS if const_weights else 0,
+                                      x.data_ptr(), x.numel(), w.data_ptr(), w.numel(),
+                                      out.data_ptr(), out.numel(), ctypes.byref(p),
+                                      _stream_handle(x)))
     return out
 
 

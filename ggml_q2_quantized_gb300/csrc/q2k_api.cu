@@ -183,12 +183,14 @@ q2k_status q2k_embedding_gather(const void* table, size_t table_bytes, const uin
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_embedding_gather launch");
 }
 
-q2k_status q2k_matmul_path(q2k_path path, const float* x, size_t x_elems, const void* w,
-                           size_t w_bytes, float* y, size_t y_elems, const q2k_matmul_params* p,
-                           q2k_stream_t stream) {
+q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float* x, size_t x_elems,
+                         const void* w, size_t w_bytes, float* y, size_t y_elems,
+                         const q2k_matmul_params* p, q2k_stream_t stream) {
     g_last_error[0] = '\0';
     q2k_status st = check_matmul(x, x_elems, w, w_bytes, y, y_elems, p);
     if (st != Q2K_OK) return st;
+    if ((flags & ~static_cast<uint32_t>(Q2K_FLAG_CONST_WEIGHTS)) != 0)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "unknown flag bits 0x%x", flags);
     if (path != Q2K_PATH_AUTO && path != Q2K_PATH_GEMV && path != Q2K_PATH_TENSOR)
         return fail(Q2K_ERR_INVALID_ARGUMENT, "unknown path %d", static_cast<int>(path));
     if (path == Q2K_PATH_AUTO) path = p->m <= 8 ? Q2K_PATH_GEMV : Q2K_PATH_TENSOR;
@@ -203,10 +205,17 @@ q2k_status q2k_matmul_path(q2k_path path, const float* x, size_t x_elems, const 
     const uint8_t* wb = static_cast<const uint8_t*>(w);
     cudaError_t e;
     if (path == Q2K_PATH_GEMV)
-        e = q2k::launch_gemv(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count, s);
+        e = q2k::launch_gemv(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count,
+                             (flags & Q2K_FLAG_CONST_WEIGHTS) != 0, s);
     else
         e = q2k::launch_gemm_tc(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count, s);
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul launch");
+}
+
+q2k_status q2k_matmul_path(q2k_path path, const float* x, size_t x_elems, const void* w,
+                           size_t w_bytes, float* y, size_t y_elems, const q2k_matmul_params* p,
+                           q2k_stream_t stream) {
+    return q2k_matmul_ex(path, 0u, x, x_elems, w, w_bytes, y, y_elems, p, stream);
 }
 
 q2k_status q2k_matmul(const float* x, size_t x_elems, const void* w, size_t w_bytes, float* y,

@@ -182,9 +182,31 @@ __device__ __forceinline__ float transpose_reduce4(float (&v)[kRowBatch], int la
     return b;
 }
 
+// Bulk copies of the CTA's weight rows into shared memory, kPieceRows rows per
+// mbarrier (each completes when its bytes have landed).  Piece starts are
+// 16-byte aligned (the host plan keeps chunk starts aligned); the ragged end of
+// the last piece (a multiple of 4 bytes below 16) is copied with plain loads
+// before the barrier's arrival.
+__device__ __forceinline__ void issue_weight_copies(uint8_t* smem, const uint8_t* gsrc,
+                                                    uint32_t bars, int rows, size_t row_bytes) {
+    const int n_pieces = (rows + kPieceRows - 1) / kPieceRows;
+    for (int p = 0; p < n_pieces; ++p) {
+        const int ra = p * kPieceRows;
+        const int rb = min(rows, ra + kPieceRows);
+        const size_t off = static_cast<size_t>(ra) * row_bytes;
+        const size_t bytes = static_cast<size_t>(rb - ra) * row_bytes;
+        const size_t bulk = bytes & ~size_t(15);
+        for (size_t t = bulk; t < bytes; t += 4)
+            *reinterpret_cast<uint32_t*>(smem + off + t) =
+                *reinterpret_cast<const uint32_t*>(gsrc + off + t);
+        mbar_arrive_expect_tx(bars + 8 * p, static_cast<uint32_t>(bulk));
+        bulk_copy_g2s(smem_u32(smem + off), gsrc + off, static_cast<uint32_t>(bulk), bars + 8 * p);
+    }
+}
+
 __global__ void __launch_bounds__(512, 1)
 gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
-               int N, int K, int rows_per_cta, int slices_pad, int groups) {
+               int N, int K, int rows_per_cta, int slices_pad, int groups, int const_weights) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
     const int nthreads = blockDim.x;
@@ -211,36 +233,30 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     const uint8_t* gsrc = w + static_cast<size_t>(r0) * row_bytes;
     const size_t chunk = static_cast<size_t>(rows) * row_bytes;
 
+    // Let the next grid in the stream start now: its prologue (barrier set-up,
+    // weight prefetch or copy) then overlaps this grid; it still waits for this
+    // grid to complete before it reads x or writes y.
+    pdl_allow_dependents();
     if (tid == 0) {
-        // Weights never depend on the previous grid's results being in shared
-        // memory, and an L2 prefetch is coherent with that grid's writes.
-        const size_t pre = chunk & ~size_t(15);
-        for (size_t off = 0; off < pre; off += (size_t(1) << 20)) {
-            const size_t left = pre - off;
-            bulk_prefetch_l2(gsrc + off, static_cast<uint32_t>(left < (size_t(1) << 20) ? left : (size_t(1) << 20)));
-        }
         for (int p = 0; p < n_pieces; ++p) mbar_init(bars + 8 * p, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    pdl_wait_prerequisites();
-    pdl_allow_dependents();
-    __syncthreads();
-
-    if (tid == 0) {
-        for (int p = 0; p < n_pieces; ++p) {
-            const int ra = p * kPieceRows;
-            const int rb = min(rows, ra + kPieceRows);
-            const size_t off = static_cast<size_t>(ra) * row_bytes;
-            const size_t bytes = static_cast<size_t>(rb - ra) * row_bytes;
-            const size_t bulk = bytes & ~size_t(15);
-            for (size_t t = bulk; t < bytes; t += 4)  // ragged end of the last piece
-                *reinterpret_cast<uint32_t*>(smem + off + t) =
-                    *reinterpret_cast<const uint32_t*>(gsrc + off + t);
-            mbar_arrive_expect_tx(bars + 8 * p, static_cast<uint32_t>(bulk));
-            bulk_copy_g2s(smem_u32(smem + off), gsrc + off, static_cast<uint32_t>(bulk), bars + 8 * p);
+        if (const_weights) {
+            // The caller guarantees the grid before this one does not write W,
+            // so the weight copies may start before the dependency wait.
+            issue_weight_copies(smem, gsrc, bars, rows, row_bytes);
+        } else {
+            // An L2 prefetch is coherent with the previous grid's writes.
+            const size_t pre = chunk & ~size_t(15);
+            for (size_t off = 0; off < pre; off += (size_t(1) << 20)) {
+                const size_t left = pre - off;
+                bulk_prefetch_l2(gsrc + off, static_cast<uint32_t>(left < (size_t(1) << 20) ? left : (size_t(1) << 20)));
+            }
         }
     }
+    pdl_wait_prerequisites();
+    __syncthreads();
+    if (tid == 0 && !const_weights) issue_weight_copies(smem, gsrc, bars, rows, row_bytes);
     // x -> integer planes, once per CTA, while the weights stream in
     for (int r = tid; r < n_runs; r += nthreads)
         convert_run(x + 16 * r, &planes[r], &run_sum[r], &run_inv[r]);
@@ -341,7 +357,7 @@ bool plan_m1(int N, int K, int sm_count, M1Plan* p) {
 }
 
 cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, const M1Plan& p,
-                      int device, cudaStream_t stream) {
+                      int device, bool const_weights, cudaStream_t stream) {
     static bool smem_set[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!smem_set[device]) {
@@ -362,7 +378,7 @@ cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, gemv_m1_kernel, x, w, y, N, K, p.rows_per_cta, p.slices_pad,
-                              p.groups);
+                              p.groups, const_weights ? 1 : 0);
 }
 
 // ------------------------------------------------------------------ general m
@@ -458,10 +474,10 @@ cudaError_t launch_rows(const float* x, const uint8_t* w, float* y, int M, int N
 }  // namespace
 
 cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N, int K,
-                        int device, int sm_count, cudaStream_t stream) {
+                        int device, int sm_count, bool const_weights, cudaStream_t stream) {
     M1Plan plan;
     if (M == 1 && (reinterpret_cast<uintptr_t>(w) & 15u) == 0 && plan_m1(N, K, sm_count, &plan))
-        return launch_m1(x, w, y, N, K, plan, device, stream);
+        return launch_m1(x, w, y, N, K, plan, device, const_weights, stream);
     switch (M < 8 ? M : 8) {
         case 1: return launch_rows<1>(x, w, y, M, N, K, stream);
         case 2: return launch_rows<2>(x, w, y, M, N, K, stream);

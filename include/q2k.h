@@ -138,6 +138,22 @@ q2k_status q2k_matmul_path(q2k_path path, const float *x, size_t x_elems,
                            const void *w, size_t w_bytes, float *y, size_t y_elems,
                            const q2k_matmul_params *params, q2k_stream_t stream);
 
+/* Flags of q2k_matmul_ex. */
+enum {
+    /* The caller guarantees that the kernel enqueued on `stream` immediately
+     * before this call does not write W (model weights that are only read).
+     * The m = 1 GEMV then starts copying W before it waits for that kernel,
+     * overlapping the weight stream with it.  Without the flag it only
+     * prefetches W into L2 (always safe) and copies after the wait. */
+    Q2K_FLAG_CONST_WEIGHTS = 1
+};
+
+/* q2k_matmul_ex - q2k_matmul_path plus `flags` (a mask of Q2K_FLAG_*; unknown
+ * bits are rejected).  Same arguments, sizes, errors and results otherwise. */
+q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float *x, size_t x_elems,
+                         const void *w, size_t w_bytes, float *y, size_t y_elems,
+                         const q2k_matmul_params *params, q2k_stream_t stream);
+
 /* q2k_device_error - read and clear the library's device error word on the
  * current device.  Kernels that wait on on-chip barriers give up after about a
  * second, set a bit here and return instead of hanging.  Synchronises

@@ -24,7 +24,7 @@ def lib():
 def test_header_declares_the_calls():
     names = q2k.header_functions()
     for want in ("q2k_dequantize", "q2k_embedding_gather", "q2k_matmul", "q2k_matmul_path",
-                 "q2k_device_error", "q2k_last_error", "q2k_abi_version"):
+                 "q2k_matmul_ex", "q2k_device_error", "q2k_last_error", "q2k_abi_version"):
         assert want in names
 
 
@@ -115,3 +115,10 @@ def test_gather_rejects_malformed(lib):
 def test_binding_refuses_missing_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         q2k.load(str(tmp_path / "nope.so"))
+
+
+def test_matmul_ex_rejects_unknown_flags(lib):
+    p = q2k.MatmulParams(1, 8, 256, 10)
+    assert lib.q2k_matmul_ex(0, 2, 0x10000, 256, 0x100000, 672, 0x1000000, 8,
+                             ctypes.byref(p), None) == INVALID
+    assert "flag" in lib.q2k_last_error().decode()

@@ -302,3 +302,16 @@ def test_invalid_arguments_launch_nothing():
     p = q2k.MatmulParams(1, 8, 256, 10)
     assert lib.q2k_matmul(x.data_ptr(), 256, w.data_ptr(), 672, x.data_ptr(), 8,
                           ctypes.byref(p), None) == 1  # y aliases x
+
+
+@pytest.mark.parametrize("n,k", [(4096, 4096), (333, 4096), (1000, 1280), (77, 14336)])
+def test_const_weights_flag_same_bits(n, k):
+    """Q2K_FLAG_CONST_WEIGHTS only moves the weight copies earlier: same bits."""
+    x, w = wl.make_matmul_inputs(91 + n, 1, n, k)
+    xd, wd = dev(x), dev(w)
+    a = q2k.matmul(xd, wd, n)
+    b = q2k.matmul(xd, wd, n, const_weights=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    yref, s = oracle.matmul(x, w, n, threads=ORACLE_THREADS)
+    assert_close(b.cpu().numpy().astype(np.float64), yref, s, TOL_GEMV, f"const n={n} k={k}")
