@@ -93,7 +93,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q2k_matmul_path.argtypes = [ctypes.c_int, vp, sz, vp, sz, vp, sz,
                                         ctypes.POINTER(MatmulParams), vp]
         lib.q2k_matmul_ex.argtypes = [ctypes.c_int, ctypes.c_uint32, vp, sz, vp, sz, vp, sz,
-                                      ctypes.POINTER(MatmulParams), vp]
+                                      ctypes.POINTER(MatmulParams), vp, sz, vp]
+        lib.q2k_matmul_workspace_bytes.argtypes = [ctypes.POINTER(MatmulParams), ctypes.c_int]
+        lib.q2k_matmul_workspace_bytes.restype = ctypes.c_size_t
         lib.q2k_device_error.argtypes = [u32p, vp]
         for fn in ("q2k_dequantize", "q2k_embedding_gather", "q2k_matmul", "q2k_matmul_path",
                    "q2k_matmul_ex", "q2k_device_error"):
@@ -185,11 +187,14 @@ def embedding_gather(table, ids, embed_dim: int, vocab_size: int | None = None, 
     return out
 
 
-def matmul(x, w, n: int, out=None, path="auto", const_weights: bool = False):
+def matmul(x, w, n: int, out=None, path="auto", const_weights: bool = False,
+           workspace="auto"):
     """``y[m, r] = sum_k x[m, k] * W[r, k]`` with W = ``n`` rows of Q2_K blocks.
 
     ``const_weights=True`` passes Q2K_FLAG_CONST_WEIGHTS: the caller promises
     that the kernel enqueued just before on the stream does not write ``w``.
+    ``workspace``: "auto" allocates the tensor-core path's workspace from
+    PyTorch's caching allocator; None runs without one; or a uint8 CUDA tensor.
     """
     torch = _torch()
     _require_cuda(x, "x", torch.float32)
@@ -202,11 +207,21 @@ def matmul(x, w, n: int, out=None, path="auto", const_weights: bool = False):
     _require_cuda(out, "out", torch.float32)
     p = MatmulParams(m, n, k, GGML_TYPE_Q2_K)
     lib = load()
+    ws_ptr, ws_bytes = None, 0
+    if isinstance(workspace, str):
+        need = lib.q2k_matmul_workspace_bytes(ctypes.byref(p), _PATHS[path])
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        else:
+            workspace = None
+    if workspace is not None:
+        _require_cuda(workspace, "workspace", torch.uint8)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
     with torch.cuda.device(x.device):
         _check(lib, lib.q2k_matmul_ex(_PATHS[path], FLAG_CONST_WEIGHTS if const_weights else 0,
                                       x.data_ptr(), x.numel(), w.data_ptr(), w.numel(),
                                       out.data_ptr(), out.numel(), ctypes.byref(p),
-                                      _stream_handle(x)))
+                                      ws_ptr, ws_bytes, _stream_handle(x)))
     return out
 
 

@@ -183,9 +183,21 @@ q2k_status q2k_embedding_gather(const void* table, size_t table_bytes, const uin
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_embedding_gather launch");
 }
 
+size_t q2k_matmul_workspace_bytes(const q2k_matmul_params* p, q2k_path path) {
+    if (p == nullptr || p->ggml_type != Q2K_GGML_TYPE_Q2_K || p->m == 0 || p->n == 0 || p->k == 0 ||
+        p->k % Q2K_QK_K != 0 || p->m > INT_MAX || p->n > INT_MAX || p->k > INT_MAX)
+        return 0;
+    if (path == Q2K_PATH_AUTO) path = p->m <= 8 ? Q2K_PATH_GEMV : Q2K_PATH_TENSOR;
+    if (path != Q2K_PATH_TENSOR) return 0;
+    const size_t m_pad = (static_cast<size_t>(p->m) + 127) / 128 * 128;
+    if (m_pad > SIZE_MAX / 2 / p->k) return 0;
+    return q2k::gemm_tc_workspace_bytes(int(p->m), int(p->k));
+}
+
 q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float* x, size_t x_elems,
                          const void* w, size_t w_bytes, float* y, size_t y_elems,
-                         const q2k_matmul_params* p, q2k_stream_t stream) {
+                         const q2k_matmul_params* p, void* workspace, size_t workspace_bytes,
+                         q2k_stream_t stream) {
     g_last_error[0] = '\0';
     q2k_status st = check_matmul(x, x_elems, w, w_bytes, y, y_elems, p);
     if (st != Q2K_OK) return st;
@@ -194,6 +206,18 @@ q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float* x, size_t x
     if (path != Q2K_PATH_AUTO && path != Q2K_PATH_GEMV && path != Q2K_PATH_TENSOR)
         return fail(Q2K_ERR_INVALID_ARGUMENT, "unknown path %d", static_cast<int>(path));
     if (path == Q2K_PATH_AUTO) path = p->m <= 8 ? Q2K_PATH_GEMV : Q2K_PATH_TENSOR;
+    void* ws = nullptr;
+    if (workspace != nullptr && path == Q2K_PATH_TENSOR) {
+        const size_t need = q2k::gemm_tc_workspace_bytes(int(p->m), int(p->k));
+        if (workspace_bytes < need)
+            return fail(Q2K_ERR_INVALID_ARGUMENT, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+        if (!aligned(workspace, 16))
+            return fail(Q2K_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+        if (overlaps(workspace, need, x, size_t(p->m) * p->k * 4) ||
+            overlaps(workspace, need, w, w_bytes) || overlaps(workspace, need, y, size_t(p->m) * p->n * 4))
+            return fail(Q2K_ERR_INVALID_ARGUMENT, "workspace must not alias x, w or y");
+        ws = workspace;
+    }
     if (path == Q2K_PATH_GEMV && (p->m + 7u) / 8u > 65535u)
         return fail(Q2K_ERR_INVALID_ARGUMENT, "GEMV path supports m <= 524280");
     if (path == Q2K_PATH_TENSOR && (p->m + 127u) / 128u > 65535u)
@@ -208,14 +232,14 @@ q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float* x, size_t x
         e = q2k::launch_gemv(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count,
                              (flags & Q2K_FLAG_CONST_WEIGHTS) != 0, s);
     else
-        e = q2k::launch_gemm_tc(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count, s);
+        e = q2k::launch_gemm_tc(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count, ws, s);
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul launch");
 }
 
 q2k_status q2k_matmul_path(q2k_path path, const float* x, size_t x_elems, const void* w,
                            size_t w_bytes, float* y, size_t y_elems, const q2k_matmul_params* p,
                            q2k_stream_t stream) {
-    return q2k_matmul_ex(path, 0u, x, x_elems, w, w_bytes, y, y_elems, p, stream);
+    return q2k_matmul_ex(path, 0u, x, x_elems, w, w_bytes, y, y_elems, p, nullptr, 0, stream);
 }
 
 q2k_status q2k_matmul(const float* x, size_t x_elems, const void* w, size_t w_bytes, float* y,

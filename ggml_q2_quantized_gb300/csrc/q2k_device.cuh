@@ -132,6 +132,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the hardware may suspend the thread for up to
+// `suspend_ns` until the phase completes (no instructions issued meanwhile).
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed, but never for
 // more than about `limit_ns`: on time-out (or when another thread of the CTA
 // already timed out and raised *abort) set `err_bit` in *err, raise *abort
@@ -143,8 +158,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0u) {
+        if (mbar_try_wait_suspend(bar, parity, 1000u)) return true;
+        if ((it & 7u) == 0u) {
             if (*abort) return false;
             if (global_timer_ns() - t0 > limit_ns) {
                 atomicOr(err, err_bit);
@@ -153,6 +168,44 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
             }
         }
     }
+}
+
+// As mbar_wait_bounded (kept as a separate entry for waiters off the critical
+// path); both suspend in hardware between polls instead of spinning, so
+// waiting threads take no issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort, unsigned int* err,
+                                                  uint32_t err_bit, uint32_t max_sleep_ns,
+                                                  uint64_t limit_ns = 1000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_suspend(bar, parity, max_sleep_ns < 1000u ? 1000u : max_sleep_ns))
+            return true;
+        if ((it & 7u) == 0u) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                atomicOr(err, err_bit);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// ---- explicit shared-memory accesses (addresses from smem_u32) -------------
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
 }
 
 }  // namespace q2k

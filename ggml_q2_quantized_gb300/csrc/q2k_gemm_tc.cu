@@ -37,22 +37,33 @@ constexpr int kKS = 64;                  // K elements per stage: one 128-byte s
 constexpr int kAStage = kBM * kKS * 2;   // bytes of one A stage
 constexpr int kXWarps = 4;
 
-template <int BN>
+// Warp roles.  Without a workspace: warps 0-3 convert x into the A stages, then
+// BN/32 decoder warps (one weight row per thread), then the MMA warp.  With a
+// workspace (A stages arrive by bulk copy): every warp before the MMA warp
+// decodes weights, two threads per row (each half a stage) when BN <= 192.
+// Warps 0-3 also run the epilogue (TMEM lane quarter = warp).
+template <int BN, bool kBulkA>
 struct Cfg {
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
+    static constexpr int kTPR = (kBulkA && BN <= 192) ? 2 : 1;  // decoder threads per row
+    static constexpr int kDecThreads = kTPR * BN;
+    static constexpr int kDecWarp0 = kBulkA ? 0 : kXWarps;
     static constexpr int kStages = (BN <= 192) ? 4 : 3;
+    // raw 84-byte block slabs in flight: the decoders run kRaw - 1 blocks
+    // (4 (kRaw - 1) stages) ahead of their own use to hide the weight fetch
+    static constexpr int kRaw = (BN <= 192) ? 4 : 3;
     static constexpr int kBStage = BN * kKS * 2;
     static constexpr int kRawBytes = BN * kBlockBytes;
-    static constexpr int kDecWarps = BN / 32;
-    static constexpr int kMmaWarp = kXWarps + kDecWarps;
-    static constexpr int kThreads = (kMmaWarp + 1) * 32;
+    static constexpr int kDecWarps = kDecThreads / 32;
+    static constexpr int kMmaWarp = kDecWarp0 + kDecWarps;
+    static constexpr int kThreads = (kMmaWarp + (kBulkA ? 2 : 1)) * 32;  // + A producer warp
     static constexpr int kTmemCols = BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kStages * kAStage;
     static constexpr int kOffRaw = kOffB + kStages * kBStage;
-    static constexpr int kOffBar = ((kOffRaw + 2 * kRawBytes) + 7) & ~7;
-    // bars: full[kStages], empty[kStages], accum, drain, raw_full[2]
-    static constexpr int kNumBars = 2 * kStages + 4;
+    static constexpr int kOffBar = ((kOffRaw + kRaw * kRawBytes) + 7) & ~7;
+    // bars: full[kStages], empty[kStages], accum, drain, raw_full[kRaw]
+    static constexpr int kNumBars = 2 * kStages + 2 + kRaw;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base
     static_assert(kSmemBytes <= 232448, "shared memory");
@@ -130,6 +141,10 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -146,13 +161,13 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
 
 // Copy the raw 84-byte blocks of column `b` for the tile's BN rows into `dst`
 // (row r at dst + 84 r).  Rows past N are zero-filled (d = dmin = 0 decode to 0).
-template <int BN>
+template <int BN, int kThreadsDec>
 __device__ __forceinline__ void issue_raw_copy(const uint8_t* __restrict__ w, uint32_t dst,
                                                int n0, int N, int blocks_per_row, int b,
                                                int td) {
     const size_t row_bytes = static_cast<size_t>(blocks_per_row) * kBlockBytes;
 #pragma unroll 3
-    for (int f = td; f < BN * kWordsPerBlock; f += BN) {
+    for (int f = td; f < BN * kWordsPerBlock; f += kThreadsDec) {
         const int r = f / kWordsPerBlock;
         const int wd = f - r * kWordsPerBlock;
         const int n = n0 + r;
@@ -169,23 +184,32 @@ __device__ __forceinline__ void issue_raw_copy(const uint8_t* __restrict__ w, ui
 template <int J>
 __device__ __forceinline__ void decode_word(uint32_t word, uint32_t lo, uint32_t hi,
                                             uint32_t& p0, uint32_t& p1) {
-    uint32_t t2;  // byte i = 2 * q_i
+    // byte i of t2 = 2 q_i for the four lanes of this word at shift 2J
+    uint32_t t2;
     if (J == 0)
-        t2 = (word << 1) & 0x06060606u;
+        t2 = (word * 2u) & 0x06060606u;
     else
         t2 = (word >> (2 * J - 1)) & 0x06060606u;
-    const uint32_t sel = t2 | (t2 << 4) | 0x10101010u;  // nibbles 2q, 2q+1 per element
+    // byte i -> nibbles (2 q_i, 2 q_i + 1); 17 * 6 + 16 < 256, so no carries.
+    // Multiply-adds run on the FMA pipe and leave the integer ALU pipe (which
+    // the masks and byte permutes need) less loaded.
+    const uint32_t sel = t2 * 0x11u + 0x10101010u;
     p0 = __byte_perm(lo, hi, sel);
-    p1 = __byte_perm(lo, hi, sel >> 16);
+    p1 = __byte_perm(lo, hi, __umulhi(sel, 0x10000u));  // sel >> 16
 }
 
-template <int C>
-__device__ __forceinline__ void decode_stage(const uint32_t (&sw)[4], float d, float dmin,
-                                             const uint32_t (&qw)[8], uint8_t* b_stage, int r) {
+// Stage C (0..3) of a block for one weight row, decoded into registers: for
+// kJJ < 0 both 32-K halves (out[32], chunks 0..7), else half kJJ (out[16],
+// chunks 4 kJJ .. 4 kJJ + 3).  Word 4 q + e of a chunk is bf16 pair e of it.
+template <int C, int kJJ, int NW>
+__device__ __forceinline__ void decode_stage_regs(const uint32_t (&sw)[4], float d, float dmin,
+                                                  const uint32_t (&qw)[8], uint32_t (&out)[NW]) {
     constexpr int H = C >> 1;
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
+        if (kJJ >= 0 && jj != kJJ) continue;
         const int j = 2 * (C & 1) + jj;
+        const int base_jj = kJJ >= 0 ? 0 : jj;
 #pragma unroll
         for (int seg = 0; seg < 2; ++seg) {
             const int si = 8 * H + 2 * j + seg;
@@ -194,7 +218,7 @@ __device__ __forceinline__ void decode_stage(const uint32_t (&sw)[4], float d, f
             const float ml = __fmul_rn(dmin, static_cast<float>(sc >> 4));
             const uint32_t lo = pack_bf16x2(-ml, __fsub_rn(dl, ml));
             const uint32_t hi = pack_bf16x2(fmaf(2.f, dl, -ml), fmaf(3.f, dl, -ml));
-            uint32_t p[8];
+            uint32_t* p = out + (base_jj * 2 + seg) * 8;
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 const uint32_t word = qw[4 * seg + t];
@@ -206,20 +230,36 @@ __device__ __forceinline__ void decode_stage(const uint32_t (&sw)[4], float d, f
                     else decode_word<3>(word, lo, hi, p[2 * t], p[2 * t + 1]);
                 }
             }
-            const int chunk = 4 * jj + 2 * seg;
-            *reinterpret_cast<uint4*>(b_stage + sw128_offset(r, chunk)) =
-                make_uint4(p[0], p[1], p[2], p[3]);
-            *reinterpret_cast<uint4*>(b_stage + sw128_offset(r, chunk + 1)) =
-                make_uint4(p[4], p[5], p[6], p[7]);
         }
     }
 }
 
-template <int BN>
-__global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
-gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
-               int M, int N, int K) {
-    using C = Cfg<BN>;
+template <int kJJ, int NW>
+__device__ __forceinline__ void decode_regs(int c, const uint32_t (&sw)[4], float d, float dmin,
+                                            const uint32_t (&qw)[8], uint32_t (&out)[NW]) {
+    if (c == 0) decode_stage_regs<0, kJJ>(sw, d, dmin, qw, out);
+    else if (c == 1) decode_stage_regs<1, kJJ>(sw, d, dmin, qw, out);
+    else if (c == 2) decode_stage_regs<2, kJJ>(sw, d, dmin, qw, out);
+    else decode_stage_regs<3, kJJ>(sw, d, dmin, qw, out);
+}
+
+// Store decoded words of row r into a swizzled B stage (chunks 0..7, or the
+// four chunks of half kJJ).
+template <int kJJ, int NW>
+__device__ __forceinline__ void store_stage(const uint32_t (&in)[NW], uint32_t b_stage, int r) {
+#pragma unroll
+    for (int q = 0; q < NW / 4; ++q) {
+        const int chunk = (kJJ >= 0 ? 4 * kJJ : 0) + q;
+        st_shared_v4(b_stage + sw128_offset(r, chunk), in[4 * q], in[4 * q + 1], in[4 * q + 2],
+                     in[4 * q + 3]);
+    }
+}
+
+template <int BN, bool kBulkA>
+__global__ void __launch_bounds__(Cfg<BN, kBulkA>::kThreads, 1)
+gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ xa,
+               const uint8_t* __restrict__ w, float* __restrict__ y, int M, int N, int K) {
+    using C = Cfg<BN, kBulkA>;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -235,20 +275,22 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     const uint32_t bar_empty = bar_full + 8 * C::kStages;
     const uint32_t bar_accum = bar_empty + 8 * C::kStages;
     const uint32_t bar_drain = bar_accum + 8;
-    const uint32_t bar_raw = bar_drain + 8;  // two of them
+    const uint32_t bar_raw = bar_drain + 8;  // kRaw of them
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
     unsigned int* err = &g_tc_error;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(bar_full + 8 * s, (kXWarps + C::kDecWarps) * 32);
+            // one arrival per decoder warp, plus per x-producer warp without a
+            // workspace, or with one the A producer's expect-tx arrival (the
+            // stage completes when its bulk copy has landed too)
+            mbar_init(bar_full + 8 * s, kBulkA ? C::kDecWarps + 1 : kXWarps + C::kDecWarps);
             mbar_init(bar_empty + 8 * s, 1);
         }
         mbar_init(bar_accum, 1);
         mbar_init(bar_drain, 1);
-        mbar_init(bar_raw, BN);
-        mbar_init(bar_raw + 8, BN);
+        for (int r = 0; r < C::kRaw; ++r) mbar_init(bar_raw + 8 * r, C::kDecWarps);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -264,7 +306,8 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     tc_fence_after();
     const uint32_t tmem_d = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-    if (warp < kXWarps) {
+    if (!kBulkA && warp < kXWarps) {
+        {
         // ---------------- x producer: f32 rows -> bf16 A stages ----------------
         const int t = threadIdx.x;
         const int c = t & 7;
@@ -272,8 +315,8 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
         for (int i = 0; i < n_iters; ++i) {
             const int s = i % C::kStages;
             if (i >= C::kStages &&
-                !mbar_wait_bounded(bar_empty + 8 * s, ((i / C::kStages) - 1) & 1, abort_flag, err,
-                                   kErrTimeoutEmpty))
+                !__all_sync(0xFFFFFFFFu, mbar_wait_backoff(bar_empty + 8 * s, ((i / C::kStages) - 1) & 1,
+                                                           abort_flag, err, kErrTimeoutEmpty, 128)))
                 break;
             uint8_t* a_stage = smem + C::kOffA + s * kAStage;
             float4 va[8], vb[8];
@@ -297,62 +340,59 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
                     make_uint4(pack_bf16x2(va[it].x, va[it].y), pack_bf16x2(va[it].z, va[it].w),
                                pack_bf16x2(vb[it].x, vb[it].y), pack_bf16x2(vb[it].z, vb[it].w));
             }
-            fence_proxy_async_smem();
-            mbar_arrive(bar_full + 8 * s);
+            fence_proxy_async_smem();  // this thread's stores -> visible to the MMA
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_full + 8 * s);
         }
-        // ---------------- epilogue: TMEM -> y (lane quarter = warp) ----------------
-        const bool ok = mbar_wait_bounded(bar_accum, 0, abort_flag, err, kErrTimeoutAccum);
-        __syncwarp();
-        if (ok) {
-            tc_fence_after();
-            const int m = m0 + warp * 32 + lane;
-            const uint32_t taddr_row = tmem_d + (static_cast<uint32_t>(warp * 32) << 16);
-            const bool vec_ok = (N & 3) == 0;
-#pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(taddr_row + c0, v);
-                if (m < M) {
-                    float* dst = y + static_cast<size_t>(m) * N + n0 + c0;
-                    const int valid = N - (n0 + c0);
-                    if (vec_ok && valid >= 32) {
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            reinterpret_cast<float4*>(dst)[q] =
-                                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                            __uint_as_float(v[4 * q + 2]),
-                                            __uint_as_float(v[4 * q + 3]));
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 32; ++q)
-                            if (q < valid) dst[q] = __uint_as_float(v[q]);
-                    }
-                }
-            }
         }
-    } else if (warp < C::kMmaWarp) {
-        // ---------------- weight decoder: one tile row per thread ----------------
-        const int td = threadIdx.x - kXWarps * 32;  // 0 .. BN-1 = tile row
+    } else if (warp >= C::kDecWarp0 && warp < C::kMmaWarp) {
+        // ---------------- weight decoders ----------------
+        const int td = threadIdx.x - C::kDecWarp0 * 32;  // 0 .. kDecThreads - 1
+        const int row = td % BN;                         // tile row
+        const int half_sel = td / BN;                    // which 32-K half (two threads per row)
         const uint32_t raw0 = sbase + C::kOffRaw;
-        issue_raw_copy<BN>(w, raw0, n0, N, blocks_per_row, 0, td);
+        // Start pulling this tile's weight rows into L2 now (one bulk prefetch
+        // per row, all K) so the 84-byte block gathers below hit L2.
+        if (td < BN && n0 + td < N) {
+            const size_t row_bytes = static_cast<size_t>(blocks_per_row) * kBlockBytes;
+            const uint8_t* rp = w + static_cast<size_t>(n0 + td) * row_bytes;
+            const uintptr_t a = (reinterpret_cast<uintptr_t>(rp) + 15) & ~uintptr_t(15);
+            const uintptr_t e = (reinterpret_cast<uintptr_t>(rp) + row_bytes) & ~uintptr_t(15);
+            if (e > a) bulk_prefetch_l2(reinterpret_cast<const void*>(a), static_cast<uint32_t>(e - a));
+        }
+        // One cp.async group per block (an empty one past the last block), so
+        // "all but the newest kRaw - 2 groups done" always means block b landed.
+        for (int pb = 0; pb < C::kRaw - 1; ++pb) {
+            if (pb < blocks_per_row)
+                issue_raw_copy<BN, C::kDecThreads>(w, raw0 + pb * C::kRawBytes, n0, N, blocks_per_row,
+                                                   pb, td);
+            else
+                cp_async_commit();
+        }
         bool ok = true;
         for (int b = 0; b < blocks_per_row && ok; ++b) {
-            const int buf = b & 1;
-            cp_async_wait_all();
-            mbar_arrive(bar_raw + 8 * buf);
-            if (!mbar_wait_bounded(bar_raw + 8 * buf, (b >> 1) & 1, abort_flag, err,
-                                   kErrTimeoutEmpty)) {
+            const int buf = b % C::kRaw;
+            cp_async_wait_group<C::kRaw - 2>();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_raw + 8 * buf);
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_backoff(bar_raw + 8 * buf, (b / C::kRaw) & 1,
+                                                           abort_flag, err, kErrTimeoutEmpty, 128))) {
                 ok = false;
                 break;
             }
-            if (b + 1 < blocks_per_row)
-                issue_raw_copy<BN>(w, raw0 + (buf ^ 1) * C::kRawBytes, n0, N, blocks_per_row,
-                                   b + 1, td);
-            const uint8_t* mine = smem + C::kOffRaw + buf * C::kRawBytes + td * kBlockBytes;
+            // Every thread has finished with block b - 1's slab (it arrived for
+            // block b above), which is where block b + kRaw - 1 goes.
+            const int nb = b + C::kRaw - 1;
+            if (nb < blocks_per_row)
+                issue_raw_copy<BN, C::kDecThreads>(w, raw0 + (nb % C::kRaw) * C::kRawBytes, n0, N,
+                                                   blocks_per_row, nb, td);
+            else
+                cp_async_commit();
+            const uint32_t mine = raw0 + buf * C::kRawBytes + row * kBlockBytes;
             uint32_t sw[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) sw[q] = ld_u32(mine + 4 * q);
-            const uint32_t dd = ld_u32(mine + 80);
+            for (int q = 0; q < 4; ++q) sw[q] = ld_shared_u32(mine + 4 * q);
+            const uint32_t dd = ld_shared_u32(mine + 80);
             const float d = f16_bits_to_float(dd);
             const float dmin = f16_bits_to_float(dd >> 16);
             uint32_t qw[8];
@@ -360,27 +400,60 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
             for (int c = 0; c < 4; ++c) {
                 if (c == 0 || c == 2) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) qw[q] = ld_u32(mine + 16 + 32 * (c >> 1) + 4 * q);
+                    for (int q = 0; q < 8; ++q) qw[q] = ld_shared_u32(mine + 16 + 32 * (c >> 1) + 4 * q);
                 }
                 const int i = 4 * b + c;
                 const int s = i % C::kStages;
+                // Decode first (registers only), then wait for the slot: the
+                // decode latency overlaps the MMAs still reading this slot.
+                constexpr int NW = C::kTPR == 1 ? 32 : 16;
+                uint32_t pw[NW];
+                if (C::kTPR == 1) decode_regs<-1>(c, sw, d, dmin, qw, pw);
+                else if (half_sel == 0) decode_regs<0>(c, sw, d, dmin, qw, pw);
+                else decode_regs<1>(c, sw, d, dmin, qw, pw);
                 if (i >= C::kStages &&
-                    !mbar_wait_bounded(bar_empty + 8 * s, ((i / C::kStages) - 1) & 1, abort_flag,
-                                       err, kErrTimeoutEmpty)) {
+                    !__all_sync(0xFFFFFFFFu,
+                                mbar_wait_backoff(bar_empty + 8 * s, ((i / C::kStages) - 1) & 1,
+                                                  abort_flag, err, kErrTimeoutEmpty, 32))) {
                     ok = false;
                     break;
                 }
-                uint8_t* b_stage = smem + C::kOffB + s * C::kBStage;
-                if (c == 0) decode_stage<0>(sw, d, dmin, qw, b_stage, td);
-                else if (c == 1) decode_stage<1>(sw, d, dmin, qw, b_stage, td);
-                else if (c == 2) decode_stage<2>(sw, d, dmin, qw, b_stage, td);
-                else decode_stage<3>(sw, d, dmin, qw, b_stage, td);
-                fence_proxy_async_smem();
-                mbar_arrive(bar_full + 8 * s);
+                const uint32_t b_stage = sbase + C::kOffB + s * C::kBStage;
+                if (C::kTPR == 1) store_stage<-1>(pw, b_stage, row);
+                else if (half_sel == 0) store_stage<0>(pw, b_stage, row);
+                else store_stage<1>(pw, b_stage, row);
+                fence_proxy_async_smem();  // this thread's stores -> visible to the MMA
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_full + 8 * s);
             }
         }
         cp_async_wait_all();  // no copy may land after this CTA is gone
-    } else {
+
+    } else if (kBulkA && warp == C::kMmaWarp + 1) {
+        // ---------------- A producer: one 16 KB bulk copy per stage ----------------
+        // The prepass wrote x as bf16 in exactly this swizzled tile layout, tile
+        // (m tile, K stage) at xa + (m_tile * n_iters + stage) * 16 KB.
+        if (lane == 0) {
+            const uint8_t* src = xa + static_cast<size_t>(blockIdx.y) * n_iters * kAStage;
+            for (int i = 0; i < n_iters; ++i) {
+                const int s = i % C::kStages;
+                if (i >= C::kStages &&
+                    !mbar_wait_backoff(bar_empty + 8 * s, ((i / C::kStages) - 1) & 1, abort_flag,
+                                       err, kErrTimeoutEmpty, 32))
+                    break;
+                mbar_arrive_expect_tx(bar_full + 8 * s, kAStage);
+                bulk_copy_g2s(sbase + C::kOffA + s * kAStage, src + static_cast<size_t>(i) * kAStage,
+                              kAStage, bar_full + 8 * s);
+            }
+            if (*abort_flag) {
+                // A copy may still be in flight and its barrier can no longer
+                // complete: give it a bounded 50 us to land before leaving.
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 50000ull) __nanosleep(1000);
+            }
+        }
+        __syncwarp();
+    } else if (warp == C::kMmaWarp) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idesc = make_idesc(kBM, BN);
@@ -413,6 +486,39 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
         __syncwarp();
     }
 
+    if (warp < 4) {
+        // ---------------- epilogue: TMEM -> y (lane quarter = warp) ----------------
+        const bool ok = __all_sync(0xFFFFFFFFu,
+                                   mbar_wait_backoff(bar_accum, 0, abort_flag, err, kErrTimeoutAccum, 512));
+        if (ok) {
+            tc_fence_after();
+            const int m = m0 + warp * 32 + lane;
+            const uint32_t taddr_row = tmem_d + (static_cast<uint32_t>(warp * 32) << 16);
+            const bool vec_ok = (N & 3) == 0;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(taddr_row + c0, v);
+                if (m < M) {
+                    float* dst = y + static_cast<size_t>(m) * N + n0 + c0;
+                    const int valid = N - (n0 + c0);
+                    if (vec_ok && valid >= 32) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            reinterpret_cast<float4*>(dst)[q] =
+                                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                            __uint_as_float(v[4 * q + 2]),
+                                            __uint_as_float(v[4 * q + 3]));
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q)
+                            if (q < valid) dst[q] = __uint_as_float(v[q]);
+                    }
+                }
+            }
+        }
+    }
+
     tc_fence_before();
     __syncthreads();
     if (warp == C::kMmaWarp) {
@@ -423,22 +529,58 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     }
 }
 
-template <int BN>
-cudaError_t launch_bn(const float* x, const uint8_t* w, float* y, int M, int N, int K, int device,
-                      cudaStream_t stream) {
-    using C = Cfg<BN>;
+// x (f32 [M, K]) -> bf16 in the tile image the GEMM copies into shared memory:
+// tile (m tile t, K stage s) is 16 KB at xa + (t * K/64 + s) * 16384 and holds
+// rows 128 t .. 128 t + 127 (zeros past M) x K 64 s .. 64 s + 63 in the
+// 128-byte-swizzled K-major layout.  One thread writes one 16-byte chunk.
+__global__ void __launch_bounds__(256)
+x_to_bf16_tiles_kernel(const float* __restrict__ x, uint8_t* __restrict__ xa, int M, int K,
+                       size_t n_chunks) {
+    const int chunks_per_row = K >> 3;
+    const int stages = K / kKS;
+    for (size_t id = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; id < n_chunks;
+         id += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int m = static_cast<int>(id / chunks_per_row);
+        const int j = static_cast<int>(id - static_cast<size_t>(m) * chunks_per_row);
+        uint4 packed = make_uint4(0u, 0u, 0u, 0u);
+        if (m < M) {
+            const float4* src = reinterpret_cast<const float4*>(x + static_cast<size_t>(m) * K + 8 * j);
+            const float4 a = __ldg(src), b = __ldg(src + 1);
+            packed = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                                pack_bf16x2(b.z, b.w));
+        }
+        const size_t tile = static_cast<size_t>(m / kBM) * stages + (j >> 3);
+        *reinterpret_cast<uint4*>(xa + tile * kAStage + sw128_offset(m % kBM, j & 7)) = packed;
+    }
+}
+
+template <int BN, bool kBulkA>
+cudaError_t launch_bn(const float* x, const uint8_t* xa, const uint8_t* w, float* y, int M, int N,
+                      int K, int device, cudaStream_t stream) {
+    using C = Cfg<BN, kBulkA>;
     static bool attr_done[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!attr_done[device]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, kBulkA>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_done[device] = true;
     }
     dim3 grid((N + BN - 1) / BN, (M + kBM - 1) / kBM);
-    gemm_tc_kernel<BN><<<grid, C::kThreads, C::kSmemBytes, stream>>>(x, w, y, M, N, K);
+    gemm_tc_kernel<BN, kBulkA><<<grid, C::kThreads, C::kSmemBytes, stream>>>(x, xa, w, y, M, N, K);
     return cudaGetLastError();
+}
+
+template <bool kBulkA>
+cudaError_t launch_width(int bn, const float* x, const uint8_t* xa, const uint8_t* w, float* y,
+                         int M, int N, int K, int device, cudaStream_t stream) {
+    switch (bn) {
+        case 256: return launch_bn<256, kBulkA>(x, xa, w, y, M, N, K, device, stream);
+        case 192: return launch_bn<192, kBulkA>(x, xa, w, y, M, N, K, device, stream);
+        case 128: return launch_bn<128, kBulkA>(x, xa, w, y, M, N, K, device, stream);
+        default: return launch_bn<64, kBulkA>(x, xa, w, y, M, N, K, device, stream);
+    }
 }
 
 // Tile width: the smallest estimated time with tiles spread over the SMs; a
@@ -462,14 +604,25 @@ int choose_bn(int M, int N, int sm_count) {
 
 }  // namespace
 
+size_t gemm_tc_workspace_bytes(int M, int K) {
+    const size_t m_pad = static_cast<size_t>((M + kBM - 1) / kBM) * kBM;
+    return m_pad * static_cast<size_t>(K) * 2;
+}
+
 cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, int N, int K,
-                           int device, int sm_count, cudaStream_t stream) {
-    switch (choose_bn(M, N, sm_count)) {
-        case 256: return launch_bn<256>(x, w, y, M, N, K, device, stream);
-        case 192: return launch_bn<192>(x, w, y, M, N, K, device, stream);
-        case 128: return launch_bn<128>(x, w, y, M, N, K, device, stream);
-        default: return launch_bn<64>(x, w, y, M, N, K, device, stream);
-    }
+                           int device, int sm_count, void* workspace, cudaStream_t stream) {
+    const int bn = choose_bn(M, N, sm_count);
+    if (workspace == nullptr)
+        return launch_width<false>(bn, x, nullptr, w, y, M, N, K, device, stream);
+    uint8_t* xa = static_cast<uint8_t*>(workspace);
+    const size_t n_chunks = gemm_tc_workspace_bytes(M, K) / 16;
+    size_t blocks = (n_chunks + 255) / 256;
+    const size_t cap = static_cast<size_t>(sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    x_to_bf16_tiles_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, xa, M, K, n_chunks);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_width<true>(bn, x, xa, w, y, M, N, K, device, stream);
 }
 
 cudaError_t read_and_clear_tc_error(uint32_t* out, cudaStream_t stream) {

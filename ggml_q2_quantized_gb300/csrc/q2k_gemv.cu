@@ -287,7 +287,7 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
         // shared-memory loads of the batch before any arithmetic.
         const int last = min(rows - 1, base + (kRowBatch - 1) * groups);
         for (int pw = waited + 1; pw <= last / kPieceRows; ++pw)
-            ok = ok && mbar_wait_bounded(bars + 8 * pw, 0, abort_flag, &g_gemv_error, kErrTimeoutGemv);
+            ok = ok && mbar_wait_backoff(bars + 8 * pw, 0, abort_flag, &g_gemv_error, kErrTimeoutGemv, 64);
         waited = max(waited, last / kPieceRows);
         RowWords rw[kRowBatch];
 #pragma unroll

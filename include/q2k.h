@@ -148,11 +148,27 @@ enum {
     Q2K_FLAG_CONST_WEIGHTS = 1
 };
 
+/* q2k_matmul_workspace_bytes - device bytes of workspace q2k_matmul_ex can use
+ * for this geometry and path (0: the path takes none).  The tensor-core path
+ * stores x there as bf16 in the tile layout its shared memory uses:
+ * ceil(m / 128) * 128 * k * 2 bytes.  Returns 0 for invalid params. */
+size_t q2k_matmul_workspace_bytes(const q2k_matmul_params *params, q2k_path path);
+
 /* q2k_matmul_ex - q2k_matmul_path plus `flags` (a mask of Q2K_FLAG_*; unknown
- * bits are rejected).  Same arguments, sizes, errors and results otherwise. */
+ * bits are rejected) and an optional caller-owned workspace.
+ *   workspace        device, NULL or at least q2k_matmul_workspace_bytes(params,
+ *                    path) bytes, 16-byte aligned, not overlapping x, w or y.
+ *                    Its contents on entry do not matter and are clobbered.
+ *                    With it the tensor-core path converts x once in a prepass
+ *                    and streams it into the GEMM by bulk copies (faster for
+ *                    large m); without it the GEMM converts x itself.
+ *   workspace_bytes  its size (ignored when workspace is NULL).
+ * Same arguments, sizes, errors and tolerances otherwise.  Calls on different
+ * streams must not share a workspace while both may run. */
 q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float *x, size_t x_elems,
                          const void *w, size_t w_bytes, float *y, size_t y_elems,
-                         const q2k_matmul_params *params, q2k_stream_t stream);
+                         const q2k_matmul_params *params, void *workspace,
+                         size_t workspace_bytes, q2k_stream_t stream);
 
 /* q2k_device_error - read and clear the library's device error word on the
  * current device.  Kernels that wait on on-chip barriers give up after about a

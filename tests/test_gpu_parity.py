@@ -315,3 +315,17 @@ def test_const_weights_flag_same_bits(n, k):
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
     yref, s = oracle.matmul(x, w, n, threads=ORACLE_THREADS)
     assert_close(b.cpu().numpy().astype(np.float64), yref, s, TOL_GEMV, f"const n={n} k={k}")
+
+
+@pytest.mark.parametrize("m,n,k", [(9, 8, 256), (130, 10000, 256), (300, 1000, 512), (16, 4096, 1024)])
+def test_tensor_workspace_and_in_kernel_conversion_agree(m, n, k):
+    """With a workspace x is converted by the prepass; without, inside the GEMM.
+    Both round x to bf16 the same way and run the same MMAs: same bits."""
+    x, w = wl.make_matmul_inputs(3000 + m + n, m, n, k)
+    xd, wd = dev(x), dev(w)
+    a = q2k.matmul(xd, wd, n, path="tensor", workspace=None)
+    b = q2k.matmul(xd, wd, n, path="tensor")
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    yref, s = oracle.matmul(x, w, n, threads=ORACLE_THREADS)
+    assert_close(a.cpu().numpy().astype(np.float64), yref, s, TOL_TC, f"no-ws m={m} n={n} k={k}")
