@@ -16,6 +16,9 @@
 #include "q2k.h"
 #include "q2k_internal.h"
 
+static_assert(Q2K_STATIC_WORKSPACE_BYTES == q2k::kStaticWorkspaceBytes,
+              "header and library disagree on the fixed scratch size");
+
 namespace {
 
 thread_local char g_last_error[512] = "";
@@ -245,6 +248,27 @@ q2k_status q2k_matmul_path(q2k_path path, const float* x, size_t x_elems, const 
 q2k_status q2k_matmul(const float* x, size_t x_elems, const void* w, size_t w_bytes, float* y,
                       size_t y_elems, const q2k_matmul_params* p, q2k_stream_t stream) {
     return q2k_matmul_path(Q2K_PATH_AUTO, x, x_elems, w, w_bytes, y, y_elems, p, stream);
+}
+
+q2k_status q2k_matmul_static_workspace(const float* x, size_t x_elems, const void* w,
+                                       size_t w_bytes, float* y, size_t y_elems,
+                                       const q2k_matmul_params* p, q2k_stream_t stream) {
+    g_last_error[0] = '\0';
+    q2k_status st = check_matmul(x, x_elems, w, w_bytes, y, y_elems, p);
+    if (st != Q2K_OK) return st;
+    const size_t need = q2k::gemm_tc_workspace_bytes(int(p->m), int(p->k));
+    if (need > q2k::kStaticWorkspaceBytes)
+        return fail(Q2K_ERR_INVALID_ARGUMENT,
+                    "m = %u, k = %u needs %zu bytes of scratch; the library's fixed scratch holds %zu "
+                    "(ceil(m/128)*128 * k <= %zu)",
+                    p->m, p->k, need, q2k::kStaticWorkspaceBytes, q2k::kStaticWorkspaceBytes / 2);
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != Q2K_OK) return st;
+    cudaError_t e = q2k::launch_gemm_tc_static(x, static_cast<const uint8_t*>(w), y, int(p->m),
+                                               int(p->n), int(p->k), dev.device, dev.sm_count,
+                                               reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul_static_workspace launch");
 }
 
 q2k_status q2k_device_error(uint32_t* out, q2k_stream_t stream) {

@@ -23,12 +23,19 @@
 // in the device error word, drains its MMAs, frees TMEM and returns.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "q2k_device.cuh"
 #include "q2k_internal.h"
 
 namespace q2k {
 
 __device__ unsigned int g_tc_error;
+
+// Fixed scratch for callers that cannot allocate device memory: it holds the
+// bf16 x tile image of the tensor-core path (ceil(m/128)*128 * k * 2 bytes).
+// Every GPU that loads the library keeps these bytes until the process exits.
+static __device__ __align__(256) uint8_t g_static_x_image[kStaticWorkspaceBytes];
 
 namespace {
 
@@ -623,6 +630,23 @@ cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, in
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_width<true>(bn, x, xa, w, y, M, N, K, device, stream);
+}
+
+cudaError_t launch_gemm_tc_static(const float* x, const uint8_t* w, float* y, int M, int N, int K,
+                                  int device, int sm_count, cudaStream_t stream) {
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    if (gemm_tc_workspace_bytes(M, K) > kStaticWorkspaceBytes) return cudaErrorInvalidValue;
+    // In host code the array's name is only a stand-in: its device address is
+    // looked up once per device, with that device current (the caller's).
+    static std::once_flag once[64];
+    static void* addr[64] = {};
+    static cudaError_t status[64] = {};
+    std::call_once(once[device], [device]() {
+        status[device] = cudaGetSymbolAddress(&addr[device], g_static_x_image);
+    });
+    if (status[device] != cudaSuccess) return status[device];
+    if (addr[device] == nullptr) return cudaErrorInvalidSymbol;
+    return launch_gemm_tc(x, w, y, M, N, K, device, sm_count, addr[device], stream);
 }
 
 cudaError_t read_and_clear_tc_error(uint32_t* out, cudaStream_t stream) {

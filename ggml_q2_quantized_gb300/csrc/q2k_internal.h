@@ -34,6 +34,17 @@ size_t gemm_tc_workspace_bytes(int M, int K);
 cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, int N, int K,
                            int device, int sm_count, void* workspace, cudaStream_t stream);
 
+// Size of the library's own fixed scratch for the tensor-core path (the x tile
+// image), used by q2k_matmul_static_workspace.
+constexpr size_t kStaticWorkspaceBytes = size_t(8) << 20;
+
+// The tensor-core path with its x tile image in the library's fixed device
+// scratch instead of a caller workspace.  cudaErrorInvalidValue when the
+// image would not fit; the first call on a device looks up the scratch's
+// device address (cudaGetSymbolAddress) with that device current.
+cudaError_t launch_gemm_tc_static(const float* x, const uint8_t* w, float* y, int M, int N, int K,
+                                  int device, int sm_count, cudaStream_t stream);
+
 // Read and clear the tensor-core kernels' device error word (synchronises `stream`).
 cudaError_t read_and_clear_tc_error(uint32_t* out, cudaStream_t stream);
 

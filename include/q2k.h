@@ -170,6 +170,32 @@ q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float *x, size_t x
                          const q2k_matmul_params *params, void *workspace,
                          size_t workspace_bytes, q2k_stream_t stream);
 
+/* q2k_matmul_static_workspace - the tensor-core matmul (as q2k_matmul_path
+ * with Q2K_PATH_TENSOR and a workspace) for callers that cannot allocate
+ * device memory at the point of the call: code being captured into a CUDA
+ * graph, where an allocation would break or serialise the capture; hosts or
+ * plugin interfaces that hand over only the input and output buffers and own
+ * the device memory budget; real-time loops that must not call the allocator.
+ * The pages have no counterpart of this call; it is this library's own.
+ *   The x tile image normally kept in a caller workspace goes into a fixed
+ *   array inside the library instead, Q2K_STATIC_WORKSPACE_BYTES (8 MiB) on
+ *   every GPU that loads the library, held until the process exits.  It fits
+ *   ceil(m / 128) * 128 * k <= 4194304 (e.g. m = 512, k = 7168); larger
+ *   geometries are rejected with Q2K_ERR_INVALID_ARGUMENT.
+ *   Nothing is allocated by the call.  The first call on a device looks up the
+ *   array's device address (with that device current); make that first call
+ *   before any stream capture.
+ *   All calls share the one array: calls whose work may overlap on the GPU
+ *   (different streams, different host threads without ordering) race on it
+ *   and give wrong results; serialise them, e.g. on one stream.  Each call
+ *   rewrites every byte of the array it reads, so leftovers of earlier calls
+ *   do not matter.
+ * Arguments, sizes, errors and tolerance (8e-3 * sum_k |x w|) as q2k_matmul. */
+enum { Q2K_STATIC_WORKSPACE_BYTES = 8388608 };
+q2k_status q2k_matmul_static_workspace(const float *x, size_t x_elems, const void *w,
+                                       size_t w_bytes, float *y, size_t y_elems,
+                                       const q2k_matmul_params *params, q2k_stream_t stream);
+
 /* q2k_device_error - read and clear the library's device error word on the
  * current device.  Kernels that wait on on-chip barriers give up after about a
  * second, set a bit here and return instead of hanging.  Synchronises
