@@ -210,7 +210,8 @@ def capture(torch, stream, fn):
     return g
 
 
-def bench_matmul(torch, q2k, w: wl.Workload, steps, warmup, l2_bytes, device, with_e2e=False):
+def bench_matmul(torch, q2k, w: wl.Workload, steps, warmup, l2_bytes, device, with_e2e=False,
+                 path="auto"):
     """Time a stack of distinct weight matrices of workload ``w`` (one launch each)."""
     inp = wl.make_inputs(w, with_gather=False)
     layers = layers_for(w.weight_bytes, l2_bytes)
@@ -221,7 +222,7 @@ def bench_matmul(torch, q2k, w: wl.Workload, steps, warmup, l2_bytes, device, wi
 
     def step():
         for l in range(layers):
-            q2k.matmul(x, ws[l], w.n, out=ys[l])
+            q2k.matmul(x, ws[l], w.n, out=ys[l], path=path)
 
     g = capture(torch, stream, step)
     ms = time_graph(torch, g, stream, steps, warmup)
@@ -285,7 +286,7 @@ def cpu_baseline(w: wl.Workload, budget_s: float = 12.0):
         oracle.matmul(inp.x, wsub, rows, threads=cores)
         reps += 1
         el = time.perf_counter() - t0
-        if el > budget_s or reps >= 1000:
+        if el > budget_s or reps >= 100000:
             break
     sec = el / reps
     return {"value": rows * row_bytes / sec / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
@@ -445,6 +446,14 @@ def run_ours(args):
                 entry["frac_bf16_measured"] = entry["TFLOPs"] / peaks["bf16_tflops"]
                 entry["frac_bf16_nominal_2250"] = entry["TFLOPs"] / 2250.0
             sec[name] = entry
+        # the M=16 workload through the fp32 GEMV path as well (forced)
+        sw = wl.by_name("spec_verify_m16")
+        r = bench_matmul(torch, q2k, sw, max(3, steps // 4), 3, l2_bytes, device, path="gemv")
+        us = r["us_per_call"]
+        sec["spec_verify_m16_gemv_path"] = {
+            "us_per_call": us, "weight_GBps": sw.weight_bytes / (us * 1e-6) / 1e9,
+            "TFLOPs": sw.flops / (us * 1e-6) / 1e12, "m": sw.m, "n": sw.n, "k": sw.k,
+            "path": "gemv", "matrices_per_step": r["layers"]}
         sec["spec_verify_gather"] = bench_gather(torch, q2k, wl.by_name("spec_verify_m16"),
                                                  max(3, steps // 4), 3, device)
         line["secondary"] = sec
