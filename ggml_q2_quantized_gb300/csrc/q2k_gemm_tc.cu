@@ -55,10 +55,14 @@ struct Cfg {
     static constexpr int kTPR = (kBulkA && BN <= 192) ? 2 : 1;  // decoder threads per row
     static constexpr int kDecThreads = kTPR * BN;
     static constexpr int kDecWarp0 = kBulkA ? 0 : kXWarps;
-    static constexpr int kStages = (BN <= 192) ? 4 : 3;
+    // A (x) and B (decoded weights) have separate rings: A stages arrive by
+    // copies whose latency the ring must cover, B stages are refilled by the
+    // decoders a few hundred cycles ahead, so A gets the deeper ring.
+    static constexpr int kAStages = (BN <= 128) ? 6 : (BN <= 192 ? 6 : 5);
+    static constexpr int kBStages = (BN <= 128) ? 4 : 3;
     // raw 84-byte block slabs in flight: the decoders run kRaw - 1 blocks
     // (4 (kRaw - 1) stages) ahead of their own use to hide the weight fetch
-    static constexpr int kRaw = (BN <= 192) ? 4 : 3;
+    static constexpr int kRaw = (BN <= 128) ? 4 : (BN <= 192 ? 3 : 2);
     static constexpr int kBStage = BN * kKS * 2;
     static constexpr int kRawBytes = BN * kBlockBytes;
     static constexpr int kDecWarps = kDecThreads / 32;
@@ -66,11 +70,12 @@ struct Cfg {
     static constexpr int kThreads = (kMmaWarp + (kBulkA ? 2 : 1)) * 32;  // + A producer warp
     static constexpr int kTmemCols = BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
     static constexpr int kOffA = 0;
-    static constexpr int kOffB = kStages * kAStage;
-    static constexpr int kOffRaw = kOffB + kStages * kBStage;
+    static constexpr int kOffB = kAStages * kAStage;
+    static constexpr int kOffRaw = kOffB + kBStages * kBStage;
     static constexpr int kOffBar = ((kOffRaw + kRaw * kRawBytes) + 7) & ~7;
-    // bars: full[kStages], empty[kStages], accum, drain, raw_full[kRaw]
-    static constexpr int kNumBars = 2 * kStages + 2 + kRaw;
+    // bars: a_full[kAStages], a_empty[kAStages], b_full[kBStages], b_empty[kBStages],
+    //       accum, drain, raw_full[kRaw]
+    static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 + kRaw;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base
     static_assert(kSmemBytes <= 232448, "shared memory");
@@ -278,9 +283,11 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ xa,
     const int n_iters = K / kKS;
     const int blocks_per_row = K / kQK;
 
-    const uint32_t bar_full = sbase + C::kOffBar;
-    const uint32_t bar_empty = bar_full + 8 * C::kStages;
-    const uint32_t bar_accum = bar_empty + 8 * C::kStages;
+    const uint32_t bar_afull = sbase + C::kOffBar;
+    const uint32_t bar_aempty = bar_afull + 8 * C::kAStages;
+    const uint32_t bar_bfull = bar_aempty + 8 * C::kAStages;
+    const uint32_t bar_bempty = bar_bfull + 8 * C::kBStages;
+    const uint32_t bar_accum = bar_bempty + 8 * C::kBStages;
     const uint32_t bar_drain = bar_accum + 8;
     const uint32_t bar_raw = bar_drain + 8;  // kRaw of them
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -288,12 +295,15 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ xa,
     unsigned int* err = &g_tc_error;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            // one arrival per decoder warp, plus per x-producer warp without a
-            // workspace, or with one the A producer's expect-tx arrival (the
-            // stage completes when its bulk copy has landed too)
-            mbar_init(bar_full + 8 * s, kBulkA ? C::kDecWarps + 1 : kXWarps + C::kDecWarps);
-            mbar_init(bar_empty + 8 * s, 1);
+        for (int s = 0; s < C::kAStages; ++s) {
+            // A: the producer's expect-tx arrival plus the copy's bytes, or one
+            // arrival per x-producer warp without a workspace
+            mbar_init(bar_afull + 8 * s, kBulkA ? 1 : kXWarps);
+            mbar_init(bar_aempty + 8 * s, 1);
+        }
+        for (int s = 0; s < C::kBStages; ++s) {
+            mbar_init(bar_bfull + 8 * s, C::kDecWarps);  // one arrival per decoder warp
+            mbar_init(bar_bempty + 8 * s, 1);
         }
         mbar_init(bar_accum, 1);
         mbar_init(bar_drain, 1);
@@ -320,9 +330,9 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ xa,
         const int c = t & 7;
         const int r0 = t >> 3;
         for (int i = 0; i < n_iters; ++i) {
-            const int s = i % C::kStages;
-            if (i >= C::kStages &&
-                !__all_sync(0xFFFFFFFFu, mbar_wait_backoff(bar_empty + 8 * s, ((i / C::kStages) - 1) & 1,
+            const int s = i % C::kAStages;
+            if (i >= C::kAStages &&
+                !__all_sync(0xFFFFFFFFu, mbar_wait_backoff(bar_aempty + 8 * s, ((i / C::kAStages) - 1) & 1,
                                                            abort_flag, err, kErrTimeoutEmpty, 128)))
                 break;
             uint8_t* a_stage = smem + C::kOffA + s * kAStage;
@@ -349,7 +359,7 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ xa,
             }
             fence_proxy_async_smem();  // this thread's stores -> visible to the MMA
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_full + 8 * s);
+            if (lane == 0) mbar_arrive(bar_afull + 8 * s);
         }
         }
     } else if (warp >= C::kDecWarp0 && warp < C::kMmaWarp) {
@@ -410,7 +420,7 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ xa,
                     for (int q = 0; q < 8; ++q) qw[q] = ld_shared_u32(mine + 16 + 32 * (c >> 1) + 4 * q);
                 }
                 const int i = 4 * b + c;
-                const int s = i % C::kStages;
+                const int s = i % C::kBStages;
                 // Decode first (registers only), then wait for the slot: the
                 // decode latency overlaps the MMAs still reading this slot.
                 constexpr int NW = C::kTPR == 1 ? 32 : 16;
@@ -418,9 +428,9 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ xa,
                 if (C::kTPR == 1) decode_regs<-1>(c, sw, d, dmin, qw, pw);
                 else if (half_sel == 0) decode_regs<0>(c, sw, d, dmin, qw, pw);
                 else decode_regs<1>(c, sw, d, dmin, qw, pw);
-                if (i >= C::kStages &&
+                if (i >= C::kBStages &&
                     !__all_sync(0xFFFFFFFFu,
-                                mbar_wait_backoff(bar_empty + 8 * s, ((i / C::kStages) - 1) & 1,
+                                mbar_wait_backoff(bar_bempty + 8 * s, ((i / C::kBStages) - 1) & 1,
                                                   abort_flag, err, kErrTimeoutEmpty, 32))) {
                     ok = false;
                     break;
@@ -431,7 +441,7 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ xa,
                 else store_stage<1>(pw, b_stage, row);
                 fence_proxy_async_smem();  // this thread's stores -> visible to the MMA
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_full + 8 * s);
+                if (lane == 0) mbar_arrive(bar_bfull + 8 * s);
             }
         }
         cp_async_wait_all();  // no copy may land after this CTA is gone
@@ -443,14 +453,14 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ xa,
         if (lane == 0) {
             const uint8_t* src = xa + static_cast<size_t>(blockIdx.y) * n_iters * kAStage;
             for (int i = 0; i < n_iters; ++i) {
-                const int s = i % C::kStages;
-                if (i >= C::kStages &&
-                    !mbar_wait_backoff(bar_empty + 8 * s, ((i / C::kStages) - 1) & 1, abort_flag,
+                const int s = i % C::kAStages;
+                if (i >= C::kAStages &&
+                    !mbar_wait_backoff(bar_aempty + 8 * s, ((i / C::kAStages) - 1) & 1, abort_flag,
                                        err, kErrTimeoutEmpty, 32))
                     break;
-                mbar_arrive_expect_tx(bar_full + 8 * s, kAStage);
+                mbar_arrive_expect_tx(bar_afull + 8 * s, kAStage);
                 bulk_copy_g2s(sbase + C::kOffA + s * kAStage, src + static_cast<size_t>(i) * kAStage,
-                              kAStage, bar_full + 8 * s);
+                              kAStage, bar_afull + 8 * s);
             }
             if (*abort_flag) {
                 // A copy may still be in flight and its barrier can no longer
@@ -466,20 +476,25 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ xa,
             constexpr uint32_t idesc = make_idesc(kBM, BN);
             bool ok = true;
             for (int i = 0; i < n_iters; ++i) {
-                const int s = i % C::kStages;
-                if (!mbar_wait_bounded(bar_full + 8 * s, (i / C::kStages) & 1, abort_flag, err,
+                const int sa = i % C::kAStages;
+                const int sb = i % C::kBStages;
+                if (!mbar_wait_bounded(bar_afull + 8 * sa, (i / C::kAStages) & 1, abort_flag, err,
+                                       kErrTimeoutFull) ||
+                    !mbar_wait_bounded(bar_bfull + 8 * sb, (i / C::kBStages) & 1, abort_flag, err,
                                        kErrTimeoutFull)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a_addr = sbase + C::kOffA + s * kAStage;
-                const uint32_t b_addr = sbase + C::kOffB + s * C::kBStage;
+                const uint32_t a_addr = sbase + C::kOffA + sa * kAStage;
+                const uint32_t b_addr = sbase + C::kOffB + sb * C::kBStage;
 #pragma unroll
                 for (int kk = 0; kk < kKS / 16; ++kk)
                     mma_bf16(tmem_d, sw128_desc(a_addr + 32 * kk), sw128_desc(b_addr + 32 * kk),
                              idesc, (i | kk) != 0 ? 1u : 0u);
-                mma_commit(bar_empty + 8 * s);
+                // both slots are free once these MMAs have read them
+                mma_commit(bar_aempty + 8 * sa);
+                mma_commit(bar_bempty + 8 * sb);
             }
             if (ok) {
                 mma_commit(bar_accum);
