@@ -21,8 +21,11 @@
 //                stage released back to the producers by tcgen05.commit.
 // Every wait is bounded (about a second); on time-out the kernel records a bit
 // in the device error word, drains its MMAs, frees TMEM and returns.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "q2k_device.cuh"
@@ -551,6 +554,491 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ xa,
     }
 }
 
+// ============================================================================
+// Weights-as-A variant (needs the x tile image).  The decoded weights go from
+// registers straight into tensor memory (tcgen05.st) and are the MMA's A
+// operand there; x stages, copied in bulk from the tile image, are the B
+// operand in shared memory.  Per MMA-clock this moves about half the shared-
+// memory bytes of the variant above (no decoded-weight stores or reads, and
+// one x stage feeds kHalves weight halves), which is what bounds that one.
+//
+// One CTA: kHalves * 128 weight rows x NX x rows (NX <= 128, a multiple of 16,
+// the MMA's N).  Half h is an M = 128 MMA accumulating into TMEM columns
+// [128 h, 128 h + NX); its decoded stage s sits at columns kColA + 32 kHalves s
+// + 32 h, K-step t (16 weights, 8 bf16x2 columns) at + 8 t.
+//   warps 0 .. 8 kHalves - 1   decoders, then the epilogue.  Warp w stores to
+//                              TMEM lanes 32 (w % 4) .. + 31; g = w / 4 picks
+//                              the half (g / 2) and the 16-weight segment of a
+//                              32-weight quant group (g % 2): per block the
+//                              thread reads 16 of its row's 64 quant bytes per
+//                              half and decodes all four 2-bit planes of them
+//   next warp                  TMEM allocation, MMA issue (one thread)
+//   next warp                  x stage bulk copies (one thread)
+//   last warp                  waits for the next kPair stages to be filled and
+//                              hands them to the MMA warp at a named barrier
+//                              both warps pass once per hand-over; the MMA
+//                              thread itself never polls an mbarrier, so
+//                              nothing but MMAs and commits sits between its
+//                              MMAs (the MMA pipe runs dry while the issuing
+//                              thread is busy elsewhere)
+// Raw 84-byte blocks reach shared memory as in the kernel above (4-byte
+// cp.async, rows 84 bytes apart so one-word-per-lane reads hit 32 banks).
+// ============================================================================
+
+// Bytes per row of the raw-weight TMA box: an 84-byte block starts 0, 4, 8 or
+// 12 bytes past a 16-byte boundary, so 96 would do; 112 (28 words) puts rows
+// 8 banks apart instead of 24, halving the bank conflicts of the row reads.
+constexpr int kTmaBoxBytes = 112;
+
+template <int kHalves, bool kTmaW>
+struct WtCfg {
+    static constexpr int kRows = 128 * kHalves;            // weight rows per CTA
+    static constexpr int kDecWarps = 8 * kHalves;
+    static constexpr int kDecThreads = 32 * kDecWarps;
+    static constexpr int kMmaWarp = kDecWarps;
+    static constexpr int kXWarp = kDecWarps + 1;
+    static constexpr int kWaitWarp = kDecWarps + 2;
+    static constexpr int kWWarp = kDecWarps + 3;            // raw weight TMA (kTmaW only)
+    static constexpr int kThreads = 32 * (kDecWarps + (kTmaW ? 4 : 3));
+    static constexpr int kPair = 2;                         // K stages per MMA hand-over
+    static constexpr int kXStages = 8;
+    static constexpr int kAStages = 4;                      // decoded stages in TMEM
+    static constexpr int kRaw = 3;
+    // Raw slab row pitch: 84 (one block per row, rows copied by cp.async), or
+    // the 112-byte TMA box that holds the block at byte 4 (b % 4) (the box
+    // starts at the 16-byte boundary at or below the block).
+    static constexpr int kRawPitch = kTmaW ? kTmaBoxBytes : kBlockBytes;
+    static constexpr int kRawBytes = kRows * kRawPitch;
+    static constexpr uint32_t kColA = 128u * kHalves;       // first A column
+    static constexpr int kTmemCols = 256 * kHalves;         // D + A ring, a power of two
+    static constexpr int kOffX = 0;
+    static constexpr int kOffRaw = kXStages * kAStage;
+    // bars: x_full[kXStages], x_empty[kXStages], a_full[kAStages], a_empty[kAStages],
+    //       raw_full[kRaw], accum, drain, raw_empty[kRaw]
+    static constexpr int kNumBars = 2 * kXStages + 2 * kAStages + 2 * kRaw + 2;
+    static constexpr int kOffBar = ((kOffRaw + kRaw * kRawBytes) + 7) & ~7;
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(kColA + 32u * kHalves * kAStages <= static_cast<uint32_t>(kTmemCols), "TMEM");
+};
+
+// D[tmem_d] (+)= A[tmem_a] * B[bdesc]^T with A in tensor memory.
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Eight consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+          "r"(v[6]), "r"(v[7])
+        : "memory");
+}
+// 2-D tiled TMA load of the box at (x, y) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Stage C (0..3) of a block for one thread: the two 16-weight K-steps of
+// quant segment `seg` at the two 2-bit planes J = 2 (C & 1) + {0, 1} of half
+// H = C / 2.  qw = the thread's four quant words of each half, sws = the 16
+// scale bytes shifted right by 8 seg (so the segment's byte sits at the low
+// byte of each 16-bit lane).  o0 gets K-step seg, o1 K-step 2 + seg; word 2e
+// (2e + 1) holds the weights of quant byte lanes 4e, 4e + 1 (4e + 2, 4e + 3).
+template <int C>
+__device__ __forceinline__ void wt_decode_stage(const uint32_t (&qw)[8], const uint32_t (&sws)[4],
+                                                float d, float dmin, uint32_t (&o0)[8],
+                                                uint32_t (&o1)[8]) {
+    constexpr int H = C >> 1;
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        constexpr int kJ0 = 2 * (C & 1);
+        const int j = kJ0 + jj;
+        // scale index 8 H + 2 j + seg -> word 2 H + j / 2, byte 2 (j % 2) + seg
+        const uint32_t sc = (sws[2 * H + (j >> 1)] >> (16 * (j & 1))) & 0xFFu;
+        const float dl = __fmul_rn(d, static_cast<float>(sc & 15u));
+        const float ml = __fmul_rn(dmin, static_cast<float>(sc >> 4));
+        const uint32_t lo = pack_bf16x2(-ml, __fsub_rn(dl, ml));
+        const uint32_t hi = pack_bf16x2(fmaf(2.f, dl, -ml), fmaf(3.f, dl, -ml));
+        uint32_t* o = jj == 0 ? o0 : o1;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t word = qw[4 * H + e];
+            if (kJ0 + jj == 0) decode_word<0>(word, lo, hi, o[2 * e], o[2 * e + 1]);
+            else if (kJ0 + jj == 1) decode_word<1>(word, lo, hi, o[2 * e], o[2 * e + 1]);
+            else if (kJ0 + jj == 2) decode_word<2>(word, lo, hi, o[2 * e], o[2 * e + 1]);
+            else decode_word<3>(word, lo, hi, o[2 * e], o[2 * e + 1]);
+        }
+    }
+}
+
+// Copy block b (84 bytes per row) of the CTA's kRows weight rows into a raw
+// slab, row r at dst + 84 r; rows past N are zero-filled (they decode to 0).
+template <int kRows, int kThreadsDec>
+__device__ __forceinline__ void wt_issue_raw(const uint8_t* __restrict__ w, uint32_t dst, int n0,
+                                             int N, size_t row_bytes, int b, int td) {
+    constexpr int kWords = kRows * kWordsPerBlock;
+#pragma unroll 4
+    for (int f = td; f < kWords; f += kThreadsDec) {
+        const int r = f / kWordsPerBlock;
+        const int wd = f - r * kWordsPerBlock;
+        const bool ok = n0 + r < N;
+        const uint8_t* src = w + (ok ? static_cast<size_t>(n0 + r) * row_bytes +
+                                           static_cast<size_t>(b) * kBlockBytes + 4 * wd
+                                     : 0);
+        cp_async_4(dst + r * kBlockBytes + 4 * wd, src, ok ? 4u : 0u);
+    }
+    cp_async_commit();
+}
+
+template <int kHalves, bool kTmaW>
+__global__ void __launch_bounds__(WtCfg<kHalves, kTmaW>::kThreads, 1)
+gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
+               float* __restrict__ y, int M, int N, int K, const __grid_constant__ CUtensorMap tmap_w) {
+    using C = WtCfg<kHalves, kTmaW>;
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * C::kRows;
+    const int m0 = blockIdx.y * kBM;
+    const int nx = min(kBM, (M - m0 + 15) & ~15);  // MMA N: this tile's x rows, padded to 16
+    const int n_iters = K / kKS;
+    const int blocks_per_row = K / kQK;
+    const size_t row_bytes = static_cast<size_t>(blocks_per_row) * kBlockBytes;
+
+    const uint32_t bar_xfull = sbase + C::kOffBar;
+    const uint32_t bar_xempty = bar_xfull + 8 * C::kXStages;
+    const uint32_t bar_afull = bar_xempty + 8 * C::kXStages;
+    const uint32_t bar_aempty = bar_afull + 8 * C::kAStages;
+    const uint32_t bar_raw = bar_aempty + 8 * C::kAStages;
+    const uint32_t bar_accum = bar_raw + 8 * C::kRaw;
+    const uint32_t bar_drain = bar_accum + 8;
+    const uint32_t bar_rawempty = bar_drain + 8;  // kRaw of them (kTmaW)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+    unsigned int* err = &g_tc_error;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kXStages; ++s) {
+            mbar_init(bar_xfull + 8 * s, 1);   // producer's expect-tx arrival + the copy's bytes
+            mbar_init(bar_xempty + 8 * s, 1);  // MMA commit
+        }
+        for (int s = 0; s < C::kAStages; ++s) {
+            mbar_init(bar_afull + 8 * s, C::kDecWarps);  // one arrival per decoder warp
+            mbar_init(bar_aempty + 8 * s, 1);            // MMA commit
+        }
+        for (int r = 0; r < C::kRaw; ++r) {
+            // TMA: the producer's expect-tx arrival + the box bytes; else one
+            // arrival per decoder warp once its cp.async groups landed
+            mbar_init(bar_raw + 8 * r, kTmaW ? 1 : C::kDecWarps);
+            mbar_init(bar_rawempty + 8 * r, C::kDecWarps);  // decoders done reading (kTmaW)
+        }
+        mbar_init(bar_accum, 1);
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == C::kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(C::kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+    if (warp < C::kDecWarps) {
+        // ---------------- weight decoders ----------------
+        const int td = threadIdx.x;
+        const int quarter = warp & 3;
+        const int g = warp >> 2;
+        const int h = g >> 1;
+        const int seg = g & 1;
+        const int row = 128 * h + 32 * quarter + lane;  // weight row within the tile
+        const uint32_t raw0 = sbase + C::kOffRaw;
+        const uint32_t t_lane = static_cast<uint32_t>(32 * quarter) << 16;
+        // A columns of K-steps seg and 2 + seg of this thread's half, stage 0
+        const uint32_t a_col0 = tmem_base + t_lane + C::kColA + 32u * h + 8u * seg;
+        if constexpr (!kTmaW) {
+            // Pull the tile's weight rows into L2 now (one bulk prefetch per row).
+            if (td < C::kRows && n0 + td < N) {
+                const uint8_t* rp = w + static_cast<size_t>(n0 + td) * row_bytes;
+                const uintptr_t a = (reinterpret_cast<uintptr_t>(rp) + 15) & ~uintptr_t(15);
+                const uintptr_t e = (reinterpret_cast<uintptr_t>(rp) + row_bytes) & ~uintptr_t(15);
+                if (e > a)
+                    bulk_prefetch_l2(reinterpret_cast<const void*>(a), static_cast<uint32_t>(e - a));
+            }
+            for (int pb = 0; pb < C::kRaw - 1; ++pb) {
+                if (pb < blocks_per_row)
+                    wt_issue_raw<C::kRows, C::kDecThreads>(w, raw0 + pb * C::kRawBytes, n0, N,
+                                                           row_bytes, pb, td);
+                else
+                    cp_async_commit();
+            }
+        }
+        bool ok = true;
+        for (int b = 0; b < blocks_per_row && ok; ++b) {
+            const int buf = b % C::kRaw;
+            uint32_t mine;
+            if constexpr (kTmaW) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait_backoff(bar_raw + 8 * buf, (b / C::kRaw) & 1,
+                                                               abort_flag, err, kErrTimeoutEmpty, 128))) {
+                    ok = false;
+                    break;
+                }
+                mine = raw0 + buf * C::kRawBytes + row * C::kRawPitch + 4 * (b & 3);
+            } else {
+                cp_async_wait_group<C::kRaw - 2>();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_raw + 8 * buf);
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait_backoff(bar_raw + 8 * buf, (b / C::kRaw) & 1,
+                                                               abort_flag, err, kErrTimeoutEmpty, 128))) {
+                    ok = false;
+                    break;
+                }
+                // Every decoder has read block b - 1's slab (it arrived for block
+                // b above): block b + kRaw - 1 goes there.
+                const int nb = b + C::kRaw - 1;
+                if (nb < blocks_per_row)
+                    wt_issue_raw<C::kRows, C::kDecThreads>(w, raw0 + (nb % C::kRaw) * C::kRawBytes,
+                                                           n0, N, row_bytes, nb, td);
+                else
+                    cp_async_commit();
+                mine = raw0 + buf * C::kRawBytes + row * kBlockBytes;
+            }
+            uint32_t sws[4], qw[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) sws[q] = ld_shared_u32(mine + 4 * q) >> (8 * seg);
+#pragma unroll
+            for (int H = 0; H < 2; ++H)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    qw[4 * H + e] = ld_shared_u32(mine + 16 + 32 * H + 16 * seg + 4 * e);
+            const uint32_t dd = ld_shared_u32(mine + 80);
+            if constexpr (kTmaW) {
+                // this warp has its block in registers: the slab may be refilled
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_rawempty + 8 * buf);
+            }
+            const float d = f16_bits_to_float(dd);
+            const float dmin = f16_bits_to_float(dd >> 16);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = 4 * b + c;
+                const int s = i % C::kAStages;
+                uint32_t o0[8], o1[8];
+                if (c == 0) wt_decode_stage<0>(qw, sws, d, dmin, o0, o1);
+                else if (c == 1) wt_decode_stage<1>(qw, sws, d, dmin, o0, o1);
+                else if (c == 2) wt_decode_stage<2>(qw, sws, d, dmin, o0, o1);
+                else wt_decode_stage<3>(qw, sws, d, dmin, o0, o1);
+                // The previous stage's TMEM stores had this decode to land:
+                // publish that stage now.
+                if (i > 0) {
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_afull + 8 * ((i - 1) % C::kAStages));
+                }
+                if (i >= C::kAStages &&
+                    !__all_sync(0xFFFFFFFFu,
+                                mbar_wait_backoff(bar_aempty + 8 * s, ((i / C::kAStages) - 1) & 1,
+                                                  abort_flag, err, kErrTimeoutEmpty, 32))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();  // the MMAs that read this stage are done
+                const uint32_t a_col = a_col0 + 32u * kHalves * s;
+                tmem_st8(a_col, o0);
+                tmem_st8(a_col + 16u, o1);
+            }
+        }
+        if (ok) {
+            // publish the last stage
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_afull + 8 * ((n_iters - 1) % C::kAStages));
+        }
+        if constexpr (!kTmaW) cp_async_wait_all();  // no copy may land after this CTA is gone
+
+        // ---------------- epilogue: TMEM -> y ----------------
+        const bool acc_ok = __all_sync(
+            0xFFFFFFFFu, mbar_wait_backoff(bar_accum, 0, abort_flag, err, kErrTimeoutAccum, 512));
+        if (acc_ok) {
+            tc_fence_after();
+            const int n = n0 + row;
+            // this warp's columns: [64 seg, 64 seg + 64) of half h, within nx
+            const uint32_t t_row = tmem_base + t_lane + 128u * h;
+#pragma unroll 1
+            for (int c0 = 64 * seg; c0 < min(64 * seg + 64, nx); c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(t_row + c0, v);
+                if (n < N) {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int m = m0 + c0 + q;
+                        if (m < M) y[static_cast<size_t>(m) * N + n] = __uint_as_float(v[q]);
+                    }
+                }
+            }
+        }
+    } else if (warp == C::kMmaWarp) {
+        // ---------------- MMA issuer ----------------
+        // Both this warp and the waiter pass named barrier 1 exactly
+        // n_iters / kPair times, whatever happens, so neither can be left
+        // waiting there; after an abort the MMAs are skipped.
+        // Everything but the MMAs is worked out per stage, so the issuing
+        // thread (which shares its scheduler with decoder warps) spends about
+        // one instruction per MMA: stage s of the x ring starts 16 KB (1024
+        // descriptor units) after stage s - 1, each K-step 32 bytes (2 units).
+        const uint32_t idesc = make_idesc(kBM, nx);
+        const uint64_t xdesc0 = sw128_desc(sbase + C::kOffX);
+        const uint32_t a_base0 = tmem_base + C::kColA;
+        uint32_t acc = 0u;  // 0 only for each half's first MMA
+        for (int i0 = 0; i0 < n_iters; i0 += C::kPair) {
+            asm volatile("bar.sync 1, 64;" ::: "memory");
+            if (lane == 0 && !*abort_flag) {
+                tc_fence_after();
+#pragma unroll
+                for (int u = 0; u < C::kPair; ++u) {
+                    const int i = i0 + u;
+                    const int sx = i % C::kXStages;
+                    const int sa = i % C::kAStages;
+                    const uint64_t xdesc = xdesc0 + static_cast<uint64_t>(sx * (kAStage >> 4));
+                    const uint32_t a_s = a_base0 + 32u * kHalves * sa;
+#pragma unroll
+                    for (int hh = 0; hh < kHalves; ++hh)
+#pragma unroll
+                        for (int kk = 0; kk < kKS / 16; ++kk) {
+                            mma_bf16_tmem_a(tmem_base + 128u * hh, a_s + 32u * hh + 8u * kk,
+                                            xdesc + 2u * kk, idesc, acc | static_cast<uint32_t>(kk));
+                        }
+                    acc = 1u;
+                    mma_commit(bar_aempty + 8 * sa);
+                    mma_commit(bar_xempty + 8 * sx);
+                }
+            }
+            __syncwarp();
+        }
+        if (lane == 0) {
+            if (!*abort_flag) {
+                mma_commit(bar_accum);
+            } else {
+                // Make sure no MMA is still writing TMEM before it is freed.
+                mma_commit(bar_drain);
+                volatile int no_abort = 0;
+                mbar_wait_bounded(bar_drain, 0, &no_abort, err, kErrTimeoutDrain);
+            }
+        }
+        __syncwarp();
+    } else if (warp == C::kWaitWarp) {
+        // ---------------- stage waiter: hands filled stages to the MMA warp ----------------
+        for (int i0 = 0; i0 < n_iters; i0 += C::kPair) {
+            if (lane == 0 && !*abort_flag) {
+#pragma unroll
+                for (int u = 0; u < C::kPair; ++u) {
+                    const int i = i0 + u;
+                    if (!mbar_wait_bounded(bar_xfull + 8 * (i % C::kXStages), (i / C::kXStages) & 1,
+                                           abort_flag, err, kErrTimeoutFull) ||
+                        !mbar_wait_bounded(bar_afull + 8 * (i % C::kAStages), (i / C::kAStages) & 1,
+                                           abort_flag, err, kErrTimeoutFull))
+                        break;
+                }
+            }
+            __syncwarp();
+            asm volatile("bar.sync 1, 64;" ::: "memory");
+        }
+    } else if (kTmaW && warp == C::kWWarp) {
+        // ---------------- raw weight blocks: one TMA box per block ----------------
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w))
+                         : "memory");
+            const uint32_t raw0 = sbase + C::kOffRaw;
+            for (int b = 0; b < blocks_per_row; ++b) {
+                const int buf = b % C::kRaw;
+                if (b >= C::kRaw &&
+                    !mbar_wait_backoff(bar_rawempty + 8 * buf, ((b / C::kRaw) - 1) & 1, abort_flag,
+                                       err, kErrTimeoutEmpty, 32))
+                    break;
+                mbar_arrive_expect_tx(bar_raw + 8 * buf, C::kRawBytes);
+                // x: the 16-byte boundary at or below block b (84 b - 4 (b % 4))
+                tma_load_2d(raw0 + buf * C::kRawBytes, &tmap_w, (kBlockBytes * b) & ~15, n0,
+                            bar_raw + 8 * buf);
+            }
+            if (*abort_flag) {
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 50000ull) __nanosleep(1000);
+            }
+        }
+        __syncwarp();
+    } else if (warp == C::kXWarp) {
+        // ---------------- x stages: one bulk copy each ----------------
+        if (lane == 0) {
+            const uint8_t* src = xa + static_cast<size_t>(blockIdx.y) * n_iters * kAStage;
+            const uint32_t bytes = static_cast<uint32_t>(nx) * 128u;
+            for (int i = 0; i < n_iters; ++i) {
+                const int s = i % C::kXStages;
+                if (i >= C::kXStages &&
+                    !mbar_wait_backoff(bar_xempty + 8 * s, ((i / C::kXStages) - 1) & 1, abort_flag,
+                                       err, kErrTimeoutEmpty, 32))
+                    break;
+                mbar_arrive_expect_tx(bar_xfull + 8 * s, bytes);
+                bulk_copy_g2s(sbase + C::kOffX + s * kAStage, src + static_cast<size_t>(i) * kAStage,
+                              bytes, bar_xfull + 8 * s);
+            }
+            if (*abort_flag) {
+                // a copy may still be in flight: give it a bounded 50 us to land
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 50000ull) __nanosleep(1000);
+            }
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == C::kMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(C::kTmemCols)
+                     : "memory");
+    }
+}
+
 // x (f32 [M, K]) -> bf16 in the tile image the GEMM copies into shared memory:
 // tile (m tile t, K stage s) is 16 KB at xa + (t * K/64 + s) * 16384 and holds
 // rows 128 t .. 128 t + 127 (zeros past M) x K 64 s .. 64 s + 63 in the
@@ -605,6 +1093,84 @@ cudaError_t launch_width(int bn, const float* x, const uint8_t* xa, const uint8_
     }
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The raw weights as a 2-D byte tensor (N rows of K/256 * 84 bytes) with a
+// box of kRows rows x 112 bytes.  Needs 16-byte rows (K a multiple of 1024)
+// and a 16-byte aligned base; false when that or the encoder is unavailable.
+bool make_weight_map(CUtensorMap* map, const uint8_t* w, int N, int K, int rows) {
+    const uint64_t row_bytes = static_cast<uint64_t>(K / kQK) * kBlockBytes;
+    if (row_bytes % 16 != 0 || (reinterpret_cast<uintptr_t>(w) & 15) != 0) return false;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    const cuuint64_t dims[2] = {row_bytes, static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTmaBoxBytes), static_cast<cuuint32_t>(rows)};
+    const cuuint32_t elem[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w), dims, strides, box,
+                  elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int kHalves, bool kTmaW>
+cudaError_t launch_wt_kernel(const uint8_t* xa, const uint8_t* w, float* y, int M, int N, int K,
+                             int device, const CUtensorMap& map, cudaStream_t stream) {
+    using C = WtCfg<kHalves, kTmaW>;
+    static bool attr_done[64] = {};
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    if (!attr_done[device]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_wt_kernel<kHalves, kTmaW>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done[device] = true;
+    }
+    dim3 grid((N + C::kRows - 1) / C::kRows, (M + kBM - 1) / kBM);
+    gemm_wt_kernel<kHalves, kTmaW><<<grid, C::kThreads, C::kSmemBytes, stream>>>(xa, w, y, M, N, K, map);
+    return cudaGetLastError();
+}
+
+template <int kHalves>
+cudaError_t launch_wt(const uint8_t* xa, const uint8_t* w, float* y, int M, int N, int K,
+                      int device, cudaStream_t stream) {
+    alignas(64) CUtensorMap map;
+    if (make_weight_map(&map, w, N, K, 128 * kHalves))
+        return launch_wt_kernel<kHalves, true>(xa, w, y, M, N, K, device, map, stream);
+    memset(&map, 0, sizeof(map));
+    return launch_wt_kernel<kHalves, false>(xa, w, y, M, N, K, device, map, stream);
+}
+
+// Weight rows per CTA of the weights-as-A kernel (128 or 256): the fewer
+// waves of CTAs times the rows each decodes; ties go to 256, which reads each
+// x stage into shared memory once for both halves.
+int choose_wt_halves(int M, int N, int sm_count) {
+    const long mt = (M + kBM - 1) / kBM;
+    long best_cost = -1;
+    int best = 2;
+    for (int kh = 2; kh >= 1; --kh) {
+        const long ctas = mt * ((N + 128 * kh - 1) / (128 * kh));
+        const long cost = ((ctas + sm_count - 1) / sm_count) * kh;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = kh;
+        }
+    }
+    return best;
+}
+
 // Tile width: the smallest estimated time with tiles spread over the SMs; a
 // tile's time grows with BN (decode) plus a fixed share (x conversion, fill).
 int choose_bn(int M, int N, int sm_count) {
@@ -644,7 +1210,8 @@ cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, in
     x_to_bf16_tiles_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, xa, M, K, n_chunks);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_width<true>(bn, x, xa, w, y, M, N, K, device, stream);
+    if (choose_wt_halves(M, N, sm_count) == 2) return launch_wt<2>(xa, w, y, M, N, K, device, stream);
+    return launch_wt<1>(xa, w, y, M, N, K, device, stream);
 }
 
 cudaError_t launch_gemm_tc_static(const float* x, const uint8_t* w, float* y, int M, int N, int K,
