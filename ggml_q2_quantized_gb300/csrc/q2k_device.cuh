@@ -193,6 +193,43 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity,
     }
 }
 
+// Non-blocking test of a phase (one instruction, never suspends).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for warps that share their scheduler with busy warps: one
+// test per poll and a short sleep between polls, so a waiting warp spends a
+// handful of instructions per poll (the suspending try_wait form expands to
+// a longer retry loop).  Same abort / time-out contract as mbar_wait_bounded.
+__device__ __forceinline__ bool mbar_wait_lean(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               unsigned int* err, uint32_t err_bit,
+                                               uint32_t sleep_ns,
+                                               uint64_t limit_ns = 1000000000ull) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(sleep_ns);
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((it & 15u) == 0u) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                atomicOr(err, err_bit);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
 // ---- explicit shared-memory accesses (addresses from smem_u32) -------------
 
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {

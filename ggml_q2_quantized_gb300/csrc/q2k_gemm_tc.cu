@@ -558,69 +558,75 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ xa,
 // Weights-as-A variant (needs the x tile image).  The decoded weights go from
 // registers straight into tensor memory (tcgen05.st) and are the MMA's A
 // operand there; x stages, copied in bulk from the tile image, are the B
-// operand in shared memory.  Per MMA-clock this moves about half the shared-
-// memory bytes of the variant above (no decoded-weight stores or reads, and
-// one x stage feeds kHalves weight halves), which is what bounds that one.
+// operand in shared memory.  Per MMA-clock this moves far fewer shared-memory
+// bytes than the variant above (no decoded-weight stores or reads), and each
+// decoded weight feeds up to 256 x rows instead of 128.
 //
-// One CTA: kHalves * 128 weight rows x NX x rows (NX <= 128, a multiple of 16,
-// the MMA's N).  Half h is an M = 128 MMA accumulating into TMEM columns
-// [128 h, 128 h + NX); its decoded stage s sits at columns kColA + 32 kHalves s
-// + 32 h, K-step t (16 weights, 8 bf16x2 columns) at + 8 t.
-//   warps 0 .. 8 kHalves - 1   decoders, then the epilogue.  Warp w stores to
-//                              TMEM lanes 32 (w % 4) .. + 31; g = w / 4 picks
-//                              the half (g / 2) and the 16-weight segment of a
-//                              32-weight quant group (g % 2): per block the
-//                              thread reads 16 of its row's 64 quant bytes per
-//                              half and decodes all four 2-bit planes of them
-//   next warp                  TMEM allocation, MMA issue (one thread)
-//   next warp                  x stage bulk copies (one thread)
-//   last warp                  waits for the next kPair stages to be filled and
-//                              hands them to the MMA warp at a named barrier
-//                              both warps pass once per hand-over; the MMA
-//                              thread itself never polls an mbarrier, so
-//                              nothing but MMAs and commits sits between its
-//                              MMAs (the MMA pipe runs dry while the issuing
-//                              thread is busy elsewhere)
-// Raw 84-byte blocks reach shared memory as in the kernel above (4-byte
-// cp.async, rows 84 bytes apart so one-word-per-lane reads hit 32 banks).
+// One CTA: 128 weight rows x up to kXRows x rows (kXRows 128 or 256).  The
+// MMA is M = 128 (weight rows, TMEM lanes) x N = this tile's x rows padded to
+// 16, accumulating into TMEM columns [0, N); decoded stage s (64 K) sits at
+// columns kColA + 32 s, K-step t (16 weights, 8 bf16x2 columns) at + 8 t.
+//   warps 0-7   decoders, then the epilogue.  Warp w stores to TMEM lanes
+//               32 (w % 4) .. + 31; w / 4 picks the 16-weight segment of a
+//               32-weight quant group: per block the thread reads 16 of its
+//               row's 32 quant bytes per half and decodes all four 2-bit
+//               planes of them
+//   warp 8      TMEM allocation, MMA issue (one thread)
+//   warp 9      waits for the next kPair stages to be filled and hands them to
+//               the MMA warp at a named barrier both warps pass once per
+//               hand-over: the MMA thread never polls an mbarrier, so nothing
+//               but MMAs and commits sits between its MMAs (the MMA pipe runs
+//               dry while the issuing thread is busy elsewhere)
+//   warp 10     raw weight blocks: one 2-D TMA box (128 rows x 112 bytes) per
+//               block (without TMA the decoders copy them with 4-byte cp.async)
+//   warps 11-12 x stages, even and odd: one bulk copy each (a thread's bulk
+//               copies complete one after another, so two issuers double the
+//               rate a single one gets)
 // ============================================================================
 
 // Bytes per row of the raw-weight TMA box: an 84-byte block starts 0, 4, 8 or
 // 12 bytes past a 16-byte boundary, so 96 would do; 112 (28 words) puts rows
 // 8 banks apart instead of 24, halving the bank conflicts of the row reads.
 constexpr int kTmaBoxBytes = 112;
+// x tile image: super-tiles of 256 rows x 64 K (32 KB, 128-byte swizzled,
+// K-major), super-tile (t, stage s) at (t * K/64 + s) * 32 KB.
+constexpr int kXSuperRows = 256;
+constexpr int kXSuperBytes = kXSuperRows * kKS * 2;
 
-template <int kHalves, bool kTmaW>
+template <int kXRows, bool kTmaW>
 struct WtCfg {
-    static constexpr int kRows = 128 * kHalves;            // weight rows per CTA
-    static constexpr int kDecWarps = 8 * kHalves;
+    static_assert(kXRows == 128 || kXRows == 256, "x rows per CTA");
+    static constexpr int kRows = 128;                       // weight rows per CTA
+    static constexpr int kDecWarps = 8;
     static constexpr int kDecThreads = 32 * kDecWarps;
-    static constexpr int kMmaWarp = kDecWarps;
-    static constexpr int kXWarp = kDecWarps + 1;
-    static constexpr int kWaitWarp = kDecWarps + 2;
-    static constexpr int kWWarp = kDecWarps + 3;            // raw weight TMA (kTmaW only)
-    static constexpr int kThreads = 32 * (kDecWarps + (kTmaW ? 4 : 3));
+    static constexpr int kMmaWarp = 8;
+    static constexpr int kWaitWarp = 9;
+    static constexpr int kWWarp = 10;
+    static constexpr int kXWarp0 = 11;
+    static constexpr int kThreads = 32 * 13;
     static constexpr int kPair = 2;                         // K stages per MMA hand-over
-    static constexpr int kXStages = 8;
-    static constexpr int kAStages = 4;                      // decoded stages in TMEM
+    static constexpr int kXStage = kXRows * kKS * 2;        // bytes of one x stage
+    static constexpr int kXStages = kXRows == 256 ? 5 : 8;
+    static constexpr int kAStages = 8;                      // decoded stages in TMEM
     static constexpr int kRaw = 3;
     // Raw slab row pitch: 84 (one block per row, rows copied by cp.async), or
-    // the 112-byte TMA box that holds the block at byte 4 (b % 4) (the box
+    // the 112-byte TMA box that holds block b at byte 4 (b % 4) (the box
     // starts at the 16-byte boundary at or below the block).
     static constexpr int kRawPitch = kTmaW ? kTmaBoxBytes : kBlockBytes;
     static constexpr int kRawBytes = kRows * kRawPitch;
-    static constexpr uint32_t kColA = 128u * kHalves;       // first A column
-    static constexpr int kTmemCols = 256 * kHalves;         // D + A ring, a power of two
+    static constexpr uint32_t kColA = kXRows;               // A ring after the accumulator
+    static constexpr int kTmemCols = 512;
     static constexpr int kOffX = 0;
-    static constexpr int kOffRaw = kXStages * kAStage;
+    static constexpr int kOffRaw = kXStages * kXStage;
     // bars: x_full[kXStages], x_empty[kXStages], a_full[kAStages], a_empty[kAStages],
-    //       raw_full[kRaw], accum, drain, raw_empty[kRaw]
+    //       raw_full[kRaw], raw_empty[kRaw], accum, drain
     static constexpr int kNumBars = 2 * kXStages + 2 * kAStages + 2 * kRaw + 2;
     static constexpr int kOffBar = ((kOffRaw + kRaw * kRawBytes) + 7) & ~7;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory");
-    static_assert(kColA + 32u * kHalves * kAStages <= static_cast<uint32_t>(kTmemCols), "TMEM");
+    static_assert(kColA + 32u * kAStages <= static_cast<uint32_t>(kTmemCols), "TMEM");
+    static_assert(kRawBytes % 128 == 0 && kOffRaw % 1024 == 0, "TMA destination alignment");
 };
 
 // D[tmem_d] (+)= A[tmem_a] * B[bdesc]^T with A in tensor memory.
@@ -642,6 +648,7 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8])
           "r"(v[6]), "r"(v[7])
         : "memory");
 }
+
 // 2-D tiled TMA load of the box at (x, y) into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
@@ -719,11 +726,11 @@ __device__ __forceinline__ void wt_issue_raw(const uint8_t* __restrict__ w, uint
     cp_async_commit();
 }
 
-template <int kHalves, bool kTmaW>
-__global__ void __launch_bounds__(WtCfg<kHalves, kTmaW>::kThreads, 1)
+template <int kXRows, bool kTmaW>
+__global__ void __launch_bounds__(WtCfg<kXRows, kTmaW>::kThreads, 1)
 gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
                float* __restrict__ y, int M, int N, int K, const __grid_constant__ CUtensorMap tmap_w) {
-    using C = WtCfg<kHalves, kTmaW>;
+    using C = WtCfg<kXRows, kTmaW>;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -731,8 +738,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * C::kRows;
-    const int m0 = blockIdx.y * kBM;
-    const int nx = min(kBM, (M - m0 + 15) & ~15);  // MMA N: this tile's x rows, padded to 16
+    const int m0 = blockIdx.y * kXRows;
+    const int nx = min(kXRows, (M - m0 + 15) & ~15);  // MMA N: this tile's x rows, padded to 16
     const int n_iters = K / kKS;
     const int blocks_per_row = K / kQK;
     const size_t row_bytes = static_cast<size_t>(blocks_per_row) * kBlockBytes;
@@ -742,9 +749,9 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
     const uint32_t bar_afull = bar_xempty + 8 * C::kXStages;
     const uint32_t bar_aempty = bar_afull + 8 * C::kAStages;
     const uint32_t bar_raw = bar_aempty + 8 * C::kAStages;
-    const uint32_t bar_accum = bar_raw + 8 * C::kRaw;
+    const uint32_t bar_rawempty = bar_raw + 8 * C::kRaw;
+    const uint32_t bar_accum = bar_rawempty + 8 * C::kRaw;
     const uint32_t bar_drain = bar_accum + 8;
-    const uint32_t bar_rawempty = bar_drain + 8;  // kRaw of them (kTmaW)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
     unsigned int* err = &g_tc_error;
@@ -785,14 +792,12 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
         // ---------------- weight decoders ----------------
         const int td = threadIdx.x;
         const int quarter = warp & 3;
-        const int g = warp >> 2;
-        const int h = g >> 1;
-        const int seg = g & 1;
-        const int row = 128 * h + 32 * quarter + lane;  // weight row within the tile
+        const int seg = warp >> 2;
+        const int row = 32 * quarter + lane;  // weight row within the tile = TMEM lane
         const uint32_t raw0 = sbase + C::kOffRaw;
         const uint32_t t_lane = static_cast<uint32_t>(32 * quarter) << 16;
-        // A columns of K-steps seg and 2 + seg of this thread's half, stage 0
-        const uint32_t a_col0 = tmem_base + t_lane + C::kColA + 32u * h + 8u * seg;
+        // A columns of K-steps seg and 2 + seg, stage 0
+        const uint32_t a_col0 = tmem_base + t_lane + C::kColA + 8u * seg;
         if constexpr (!kTmaW) {
             // Pull the tile's weight rows into L2 now (one bulk prefetch per row).
             if (td < C::kRows && n0 + td < N) {
@@ -815,8 +820,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
             const int buf = b % C::kRaw;
             uint32_t mine;
             if constexpr (kTmaW) {
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait_backoff(bar_raw + 8 * buf, (b / C::kRaw) & 1,
-                                                               abort_flag, err, kErrTimeoutEmpty, 128))) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait_lean(bar_raw + 8 * buf, (b / C::kRaw) & 1,
+                                                            abort_flag, err, kErrTimeoutEmpty, 64))) {
                     ok = false;
                     break;
                 }
@@ -825,8 +830,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
                 cp_async_wait_group<C::kRaw - 2>();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_raw + 8 * buf);
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait_backoff(bar_raw + 8 * buf, (b / C::kRaw) & 1,
-                                                               abort_flag, err, kErrTimeoutEmpty, 128))) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait_lean(bar_raw + 8 * buf, (b / C::kRaw) & 1,
+                                                            abort_flag, err, kErrTimeoutEmpty, 64))) {
                     ok = false;
                     break;
                 }
@@ -875,13 +880,13 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
                 }
                 if (i >= C::kAStages &&
                     !__all_sync(0xFFFFFFFFu,
-                                mbar_wait_backoff(bar_aempty + 8 * s, ((i / C::kAStages) - 1) & 1,
-                                                  abort_flag, err, kErrTimeoutEmpty, 32))) {
+                                mbar_wait_lean(bar_aempty + 8 * s, ((i / C::kAStages) - 1) & 1,
+                                               abort_flag, err, kErrTimeoutEmpty, 64))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();  // the MMAs that read this stage are done
-                const uint32_t a_col = a_col0 + 32u * kHalves * s;
+                const uint32_t a_col = a_col0 + 32u * s;
                 tmem_st8(a_col, o0);
                 tmem_st8(a_col + 16u, o1);
             }
@@ -901,10 +906,10 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
         if (acc_ok) {
             tc_fence_after();
             const int n = n0 + row;
-            // this warp's columns: [64 seg, 64 seg + 64) of half h, within nx
-            const uint32_t t_row = tmem_base + t_lane + 128u * h;
+            const uint32_t t_row = tmem_base + t_lane;
+            // 16-column groups alternate between the two warps of a lane quarter
 #pragma unroll 1
-            for (int c0 = 64 * seg; c0 < min(64 * seg + 64, nx); c0 += 16) {
+            for (int c0 = 16 * seg; c0 < nx; c0 += 32) {
                 uint32_t v[16];
                 tmem_ld16(t_row + c0, v);
                 if (n < N) {
@@ -920,15 +925,14 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
         // ---------------- MMA issuer ----------------
         // Both this warp and the waiter pass named barrier 1 exactly
         // n_iters / kPair times, whatever happens, so neither can be left
-        // waiting there; after an abort the MMAs are skipped.
-        // Everything but the MMAs is worked out per stage, so the issuing
-        // thread (which shares its scheduler with decoder warps) spends about
-        // one instruction per MMA: stage s of the x ring starts 16 KB (1024
-        // descriptor units) after stage s - 1, each K-step 32 bytes (2 units).
+        // waiting there; after an abort the MMAs are skipped.  Everything but
+        // the MMAs is worked out per stage: x stage s starts kXStage bytes
+        // (kXStage / 16 descriptor units) after stage s - 1, each K-step 32
+        // bytes (2 units) after the previous one.
         const uint32_t idesc = make_idesc(kBM, nx);
         const uint64_t xdesc0 = sw128_desc(sbase + C::kOffX);
         const uint32_t a_base0 = tmem_base + C::kColA;
-        uint32_t acc = 0u;  // 0 only for each half's first MMA
+        uint32_t acc = 0u;  // 0 only for the very first MMA
         for (int i0 = 0; i0 < n_iters; i0 += C::kPair) {
             asm volatile("bar.sync 1, 64;" ::: "memory");
             if (lane == 0 && !*abort_flag) {
@@ -938,15 +942,13 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
                     const int i = i0 + u;
                     const int sx = i % C::kXStages;
                     const int sa = i % C::kAStages;
-                    const uint64_t xdesc = xdesc0 + static_cast<uint64_t>(sx * (kAStage >> 4));
-                    const uint32_t a_s = a_base0 + 32u * kHalves * sa;
+                    const uint64_t xdesc = xdesc0 + static_cast<uint64_t>(sx * (C::kXStage >> 4));
+                    const uint32_t a_s = a_base0 + 32u * sa;
 #pragma unroll
-                    for (int hh = 0; hh < kHalves; ++hh)
-#pragma unroll
-                        for (int kk = 0; kk < kKS / 16; ++kk) {
-                            mma_bf16_tmem_a(tmem_base + 128u * hh, a_s + 32u * hh + 8u * kk,
-                                            xdesc + 2u * kk, idesc, acc | static_cast<uint32_t>(kk));
-                        }
+                    for (int kk = 0; kk < kKS / 16; ++kk) {
+                        mma_bf16_tmem_a(tmem_base, a_s + 8u * kk, xdesc + 2u * kk, idesc,
+                                        acc | static_cast<uint32_t>(kk));
+                    }
                     acc = 1u;
                     mma_commit(bar_aempty + 8 * sa);
                     mma_commit(bar_xempty + 8 * sx);
@@ -972,27 +974,27 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
 #pragma unroll
                 for (int u = 0; u < C::kPair; ++u) {
                     const int i = i0 + u;
-                    if (!mbar_wait_bounded(bar_xfull + 8 * (i % C::kXStages), (i / C::kXStages) & 1,
-                                           abort_flag, err, kErrTimeoutFull) ||
-                        !mbar_wait_bounded(bar_afull + 8 * (i % C::kAStages), (i / C::kAStages) & 1,
-                                           abort_flag, err, kErrTimeoutFull))
+                    if (!mbar_wait_lean(bar_xfull + 8 * (i % C::kXStages), (i / C::kXStages) & 1,
+                                        abort_flag, err, kErrTimeoutFull, 32) ||
+                        !mbar_wait_lean(bar_afull + 8 * (i % C::kAStages), (i / C::kAStages) & 1,
+                                        abort_flag, err, kErrTimeoutFull, 32))
                         break;
                 }
             }
             __syncwarp();
             asm volatile("bar.sync 1, 64;" ::: "memory");
         }
-    } else if (kTmaW && warp == C::kWWarp) {
+    } else if (warp == C::kWWarp) {
         // ---------------- raw weight blocks: one TMA box per block ----------------
-        if (lane == 0) {
+        if (kTmaW && lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w))
                          : "memory");
             const uint32_t raw0 = sbase + C::kOffRaw;
             for (int b = 0; b < blocks_per_row; ++b) {
                 const int buf = b % C::kRaw;
                 if (b >= C::kRaw &&
-                    !mbar_wait_backoff(bar_rawempty + 8 * buf, ((b / C::kRaw) - 1) & 1, abort_flag,
-                                       err, kErrTimeoutEmpty, 32))
+                    !mbar_wait_lean(bar_rawempty + 8 * buf, ((b / C::kRaw) - 1) & 1, abort_flag,
+                                    err, kErrTimeoutEmpty, 128))
                     break;
                 mbar_arrive_expect_tx(bar_raw + 8 * buf, C::kRawBytes);
                 // x: the 16-byte boundary at or below block b (84 b - 4 (b % 4))
@@ -1000,28 +1002,33 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
                             bar_raw + 8 * buf);
             }
             if (*abort_flag) {
+                // a copy may still be in flight: give it a bounded 50 us to land
                 const uint64_t t0 = global_timer_ns();
                 while (global_timer_ns() - t0 < 50000ull) __nanosleep(1000);
             }
         }
         __syncwarp();
-    } else if (warp == C::kXWarp) {
-        // ---------------- x stages: one bulk copy each ----------------
+    } else {
+        // ---------------- x stages: one bulk copy each, even / odd stages ----------------
         if (lane == 0) {
-            const uint8_t* src = xa + static_cast<size_t>(blockIdx.y) * n_iters * kAStage;
-            const uint32_t bytes = static_cast<uint32_t>(nx) * 128u;
-            for (int i = 0; i < n_iters; ++i) {
+            // This tile's rows of super-tile m0 / 256 (the second 128 of them when
+            // the tile starts half-way into it); a whole super-tile stage when
+            // kXRows is 256 (the rows past M are zeros in the image).
+            const uint8_t* src = xa + static_cast<size_t>(m0 / kXSuperRows) * n_iters * kXSuperBytes +
+                                 static_cast<size_t>(m0 % kXSuperRows) * (kKS * 2);
+            const uint32_t bytes = kXRows == kXSuperRows ? static_cast<uint32_t>(kXSuperBytes)
+                                                         : static_cast<uint32_t>(nx) * (kKS * 2);
+            for (int i = warp - C::kXWarp0; i < n_iters; i += 2) {
                 const int s = i % C::kXStages;
                 if (i >= C::kXStages &&
-                    !mbar_wait_backoff(bar_xempty + 8 * s, ((i / C::kXStages) - 1) & 1, abort_flag,
-                                       err, kErrTimeoutEmpty, 32))
+                    !mbar_wait_lean(bar_xempty + 8 * s, ((i / C::kXStages) - 1) & 1, abort_flag,
+                                    err, kErrTimeoutEmpty, 128))
                     break;
                 mbar_arrive_expect_tx(bar_xfull + 8 * s, bytes);
-                bulk_copy_g2s(sbase + C::kOffX + s * kAStage, src + static_cast<size_t>(i) * kAStage,
-                              bytes, bar_xfull + 8 * s);
+                bulk_copy_g2s(sbase + C::kOffX + s * C::kXStage,
+                              src + static_cast<size_t>(i) * kXSuperBytes, bytes, bar_xfull + 8 * s);
             }
             if (*abort_flag) {
-                // a copy may still be in flight: give it a bounded 50 us to land
                 const uint64_t t0 = global_timer_ns();
                 while (global_timer_ns() - t0 < 50000ull) __nanosleep(1000);
             }
@@ -1040,9 +1047,10 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
 }
 
 // x (f32 [M, K]) -> bf16 in the tile image the GEMM copies into shared memory:
-// tile (m tile t, K stage s) is 16 KB at xa + (t * K/64 + s) * 16384 and holds
-// rows 128 t .. 128 t + 127 (zeros past M) x K 64 s .. 64 s + 63 in the
-// 128-byte-swizzled K-major layout.  One thread writes one 16-byte chunk.
+// super-tile (t, K stage s) is 32 KB at xa + (t * K/64 + s) * 32768 and holds
+// rows 256 t .. 256 t + 255 (zeros past M) x K 64 s .. 64 s + 63 in the
+// 128-byte-swizzled K-major layout (8-row groups 1024 bytes apart).  One
+// thread writes one 16-byte chunk.
 __global__ void __launch_bounds__(256)
 x_to_bf16_tiles_kernel(const float* __restrict__ x, uint8_t* __restrict__ xa, int M, int K,
                        size_t n_chunks) {
@@ -1059,8 +1067,9 @@ x_to_bf16_tiles_kernel(const float* __restrict__ x, uint8_t* __restrict__ xa, in
             packed = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
                                 pack_bf16x2(b.z, b.w));
         }
-        const size_t tile = static_cast<size_t>(m / kBM) * stages + (j >> 3);
-        *reinterpret_cast<uint4*>(xa + tile * kAStage + sw128_offset(m % kBM, j & 7)) = packed;
+        const size_t tile = static_cast<size_t>(m / kXSuperRows) * stages + (j >> 3);
+        *reinterpret_cast<uint4*>(xa + tile * kXSuperBytes + sw128_offset(m % kXSuperRows, j & 7)) =
+            packed;
     }
 }
 
@@ -1125,50 +1134,40 @@ bool make_weight_map(CUtensorMap* map, const uint8_t* w, int N, int K, int rows)
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int kHalves, bool kTmaW>
+template <int kXRows, bool kTmaW>
 cudaError_t launch_wt_kernel(const uint8_t* xa, const uint8_t* w, float* y, int M, int N, int K,
                              int device, const CUtensorMap& map, cudaStream_t stream) {
-    using C = WtCfg<kHalves, kTmaW>;
+    using C = WtCfg<kXRows, kTmaW>;
     static bool attr_done[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!attr_done[device]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_wt_kernel<kHalves, kTmaW>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_wt_kernel<kXRows, kTmaW>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_done[device] = true;
     }
-    dim3 grid((N + C::kRows - 1) / C::kRows, (M + kBM - 1) / kBM);
-    gemm_wt_kernel<kHalves, kTmaW><<<grid, C::kThreads, C::kSmemBytes, stream>>>(xa, w, y, M, N, K, map);
+    dim3 grid((N + C::kRows - 1) / C::kRows, (M + kXRows - 1) / kXRows);
+    gemm_wt_kernel<kXRows, kTmaW><<<grid, C::kThreads, C::kSmemBytes, stream>>>(xa, w, y, M, N, K, map);
     return cudaGetLastError();
 }
 
-template <int kHalves>
+template <int kXRows>
 cudaError_t launch_wt(const uint8_t* xa, const uint8_t* w, float* y, int M, int N, int K,
                       int device, cudaStream_t stream) {
     alignas(64) CUtensorMap map;
-    if (make_weight_map(&map, w, N, K, 128 * kHalves))
-        return launch_wt_kernel<kHalves, true>(xa, w, y, M, N, K, device, map, stream);
+    if (make_weight_map(&map, w, N, K, 128))
+        return launch_wt_kernel<kXRows, true>(xa, w, y, M, N, K, device, map, stream);
     memset(&map, 0, sizeof(map));
-    return launch_wt_kernel<kHalves, false>(xa, w, y, M, N, K, device, map, stream);
+    return launch_wt_kernel<kXRows, false>(xa, w, y, M, N, K, device, map, stream);
 }
 
-// Weight rows per CTA of the weights-as-A kernel (128 or 256): the fewer
-// waves of CTAs times the rows each decodes; ties go to 256, which reads each
-// x stage into shared memory once for both halves.
-int choose_wt_halves(int M, int N, int sm_count) {
-    const long mt = (M + kBM - 1) / kBM;
-    long best_cost = -1;
-    int best = 2;
-    for (int kh = 2; kh >= 1; --kh) {
-        const long ctas = mt * ((N + 128 * kh - 1) / (128 * kh));
-        const long cost = ((ctas + sm_count - 1) / sm_count) * kh;
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best = kh;
-        }
-    }
-    return best;
+// x rows per CTA of the weights-as-A kernel: 256 (each decoded weight feeds
+// twice the MMA work) once 128-row x tiles would need more than one wave of
+// CTAs, else 128 (twice the CTAs).
+int choose_wt_xrows(int M, int N, int sm_count) {
+    const long ctas128 = static_cast<long>((N + 127) / 128) * ((M + 127) / 128);
+    return ctas128 > sm_count ? 256 : 128;
 }
 
 // Tile width: the smallest estimated time with tiles spread over the SMs; a
@@ -1193,7 +1192,7 @@ int choose_bn(int M, int N, int sm_count) {
 }  // namespace
 
 size_t gemm_tc_workspace_bytes(int M, int K) {
-    const size_t m_pad = static_cast<size_t>((M + kBM - 1) / kBM) * kBM;
+    const size_t m_pad = static_cast<size_t>((M + kXSuperRows - 1) / kXSuperRows) * kXSuperRows;
     return m_pad * static_cast<size_t>(K) * 2;
 }
 
@@ -1210,8 +1209,8 @@ cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, in
     x_to_bf16_tiles_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, xa, M, K, n_chunks);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (choose_wt_halves(M, N, sm_count) == 2) return launch_wt<2>(xa, w, y, M, N, K, device, stream);
-    return launch_wt<1>(xa, w, y, M, N, K, device, stream);
+    if (choose_wt_xrows(M, N, sm_count) == 256) return launch_wt<256>(xa, w, y, M, N, K, device, stream);
+    return launch_wt<128>(xa, w, y, M, N, K, device, stream);
 }
 
 cudaError_t launch_gemm_tc_static(const float* x, const uint8_t* w, float* y, int M, int N, int K,

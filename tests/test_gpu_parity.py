@@ -207,6 +207,7 @@ def test_gemv_workloads_full(name):
     (200, 300, 512),    # ragged x tile (72 rows) and weight tile
     (257, 520, 1024),   # 1-row last x tile, 256-row weight tiles with a ragged one
     (384, 2000, 768),   # several waves of 128-row weight tiles
+    (300, 20000, 1024), # 256-row x tiles (one ragged: 48 rows), TMA weight boxes, ragged N
 ])
 def test_tensor_parity(m, n, k):
     check_matmul(2000 + m + n + k, m, n, k, "tensor", TOL_TC)
