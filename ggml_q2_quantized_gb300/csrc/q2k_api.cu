@@ -260,7 +260,7 @@ q2k_status q2k_matmul_static_workspace(const float* x, size_t x_elems, const voi
     if (need > q2k::kStaticWorkspaceBytes)
         return fail(Q2K_ERR_INVALID_ARGUMENT,
                     "m = %u, k = %u needs %zu bytes of scratch; the library's fixed scratch holds %zu "
-                    "(ceil(m/128)*128 * k <= %zu)",
+                    "(ceil(m/256)*256 * k <= %zu)",
                     p->m, p->k, need, q2k::kStaticWorkspaceBytes, q2k::kStaticWorkspaceBytes / 2);
     DeviceInfo dev;
     st = current_device(&dev);

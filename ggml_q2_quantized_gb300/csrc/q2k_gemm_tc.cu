@@ -36,7 +36,7 @@ namespace q2k {
 __device__ unsigned int g_tc_error;
 
 // Fixed scratch for callers that cannot allocate device memory: it holds the
-// bf16 x tile image of the tensor-core path (ceil(m/128)*128 * k * 2 bytes).
+// bf16 x tile image of the tensor-core path (ceil(m/256)*256 * k * 2 bytes).
 // Every GPU that loads the library keeps these bytes until the process exits.
 static __device__ __align__(256) uint8_t g_static_x_image[kStaticWorkspaceBytes];
 

@@ -151,7 +151,7 @@ enum {
 /* q2k_matmul_workspace_bytes - device bytes of workspace q2k_matmul_ex can use
  * for this geometry and path (0: the path takes none).  The tensor-core path
  * stores x there as bf16 in the tile layout its shared memory uses:
- * ceil(m / 128) * 128 * k * 2 bytes.  Returns 0 for invalid params. */
+ * ceil(m / 256) * 256 * k * 2 bytes.  Returns 0 for invalid params. */
 size_t q2k_matmul_workspace_bytes(const q2k_matmul_params *params, q2k_path path);
 
 /* q2k_matmul_ex - q2k_matmul_path plus `flags` (a mask of Q2K_FLAG_*; unknown
@@ -180,7 +180,7 @@ q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float *x, size_t x
  *   The x tile image normally kept in a caller workspace goes into a fixed
  *   array inside the library instead, Q2K_STATIC_WORKSPACE_BYTES (8 MiB) on
  *   every GPU that loads the library, held until the process exits.  It fits
- *   ceil(m / 128) * 128 * k <= 4194304 (e.g. m = 512, k = 7168); larger
+ *   ceil(m / 256) * 256 * k <= 4194304 (e.g. m = 512, k = 7168); larger
  *   geometries are rejected with Q2K_ERR_INVALID_ARGUMENT.
  *   Nothing is allocated by the call.  The first call on a device looks up the
  *   array's device address (with that device current); make that first call

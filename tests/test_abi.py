@@ -127,8 +127,8 @@ def test_matmul_ex_rejects_unknown_flags(lib):
 def test_workspace_bytes(lib):
     P = q2k.MatmulParams
     assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(1, 8, 256, 10)), 0) == 0      # GEMV
-    assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(9, 8, 256, 10)), 0) == 128 * 256 * 2
-    assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(1, 8, 256, 10)), 2) == 128 * 256 * 2
+    assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(9, 8, 256, 10)), 0) == 256 * 256 * 2
+    assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(1, 8, 256, 10)), 2) == 256 * 256 * 2
     assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(512, 7168, 7168, 10)), 0) == 512 * 7168 * 2
     assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(129, 8, 512, 10)), 0) == 256 * 512 * 2
     assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(9, 8, 255, 10)), 0) == 0      # invalid
@@ -136,7 +136,7 @@ def test_workspace_bytes(lib):
 
 def test_workspace_rejected_when_small_or_aliasing(lib):
     p = q2k.MatmulParams(9, 8, 256, 10)
-    need = 128 * 256 * 2
+    need = 256 * 256 * 2
     args = (0x10000, 9 * 256, 0x100000, 8 * 84, 0x1000000, 9 * 8, ctypes.byref(p))
     assert lib.q2k_matmul_ex(2, 0, *args, 0x2000000, need - 1, None) == INVALID
     assert "workspace" in lib.q2k_last_error().decode()

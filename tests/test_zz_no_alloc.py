@@ -31,7 +31,7 @@ def _bind(lib):
 
 
 def test_static_workspace_rejects_oversize_geometry():
-    """Beyond the fixed scratch (ceil(m/128)*128 * k * 2 > 8 MiB): a clear error, no launch."""
+    """Beyond the fixed scratch (ceil(m/256)*256 * k * 2 > 8 MiB): a clear error, no launch."""
     q2k_build.build()
     lib = q2k.load()
     f = _bind(lib)
