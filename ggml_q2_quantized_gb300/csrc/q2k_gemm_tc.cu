@@ -606,9 +606,11 @@ struct WtCfg {
     static constexpr int kThreads = 32 * 13;
     static constexpr int kPair = 2;                         // K stages per MMA hand-over
     static constexpr int kXStage = kXRows * kKS * 2;        // bytes of one x stage
-    static constexpr int kXStages = kXRows == 256 ? 5 : 8;
+    static constexpr int kXStages = kXRows == 256 ? 6 : 8;
     static constexpr int kAStages = 8;                      // decoded stages in TMEM
-    static constexpr int kRaw = 3;
+    // Raw weight slabs: the decoders take a block into registers as soon as it
+    // lands, so two slabs keep the next block's copy a whole block ahead.
+    static constexpr int kRaw = kTmaW ? 2 : 3;
     // Raw slab row pitch: 84 (one block per row, rows copied by cp.async), or
     // the 112-byte TMA box that holds block b at byte 4 (b % 4) (the box
     // starts at the 16-byte boundary at or below the block).
@@ -1018,6 +1020,7 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
                                  static_cast<size_t>(m0 % kXSuperRows) * (kKS * 2);
             const uint32_t bytes = kXRows == kXSuperRows ? static_cast<uint32_t>(kXSuperBytes)
                                                          : static_cast<uint32_t>(nx) * (kKS * 2);
+            pdl_wait_prerequisites();  // the image is written by the grid before this one
             for (int i = warp - C::kXWarp0; i < n_iters; i += 2) {
                 const int s = i % C::kXStages;
                 if (i >= C::kXStages &&
@@ -1051,26 +1054,39 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
 // rows 256 t .. 256 t + 255 (zeros past M) x K 64 s .. 64 s + 63 in the
 // 128-byte-swizzled K-major layout (8-row groups 1024 bytes apart).  One
 // thread writes one 16-byte chunk.
+__device__ __forceinline__ void x_chunk_to_image(const float* __restrict__ x, uint8_t* __restrict__ xa,
+                                                 int M, int K, size_t id) {
+    const int chunks_per_row = K >> 3;
+    const int stages = K / kKS;
+    const int m = static_cast<int>(id / chunks_per_row);
+    const int j = static_cast<int>(id - static_cast<size_t>(m) * chunks_per_row);
+    uint4 packed = make_uint4(0u, 0u, 0u, 0u);
+    if (m < M) {
+        const float4* src = reinterpret_cast<const float4*>(x + static_cast<size_t>(m) * K + 8 * j);
+        const float4 a = __ldg(src), b = __ldg(src + 1);
+        packed = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                            pack_bf16x2(b.z, b.w));
+    }
+    const size_t tile = static_cast<size_t>(m / kXSuperRows) * stages + (j >> 3);
+    *reinterpret_cast<uint4*>(xa + tile * kXSuperBytes + sw128_offset(m % kXSuperRows, j & 7)) =
+        packed;
+}
+
+// The GEMM after this kernel is launched as its programmatic dependent: it may
+// start (TMEM, barriers, weight decode) as soon as every block here has begun,
+// and waits for this grid to finish only before it copies the image.  Few
+// blocks per SM leave room for it.
 __global__ void __launch_bounds__(256)
 x_to_bf16_tiles_kernel(const float* __restrict__ x, uint8_t* __restrict__ xa, int M, int K,
                        size_t n_chunks) {
-    const int chunks_per_row = K >> 3;
-    const int stages = K / kKS;
-    for (size_t id = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; id < n_chunks;
-         id += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const int m = static_cast<int>(id / chunks_per_row);
-        const int j = static_cast<int>(id - static_cast<size_t>(m) * chunks_per_row);
-        uint4 packed = make_uint4(0u, 0u, 0u, 0u);
-        if (m < M) {
-            const float4* src = reinterpret_cast<const float4*>(x + static_cast<size_t>(m) * K + 8 * j);
-            const float4 a = __ldg(src), b = __ldg(src + 1);
-            packed = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
-                                pack_bf16x2(b.z, b.w));
-        }
-        const size_t tile = static_cast<size_t>(m / kXSuperRows) * stages + (j >> 3);
-        *reinterpret_cast<uint4*>(xa + tile * kXSuperBytes + sw128_offset(m % kXSuperRows, j & 7)) =
-            packed;
+    pdl_allow_dependents();
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    size_t id = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; id + stride < n_chunks; id += 2 * stride) {
+        x_chunk_to_image(x, xa, M, K, id);
+        x_chunk_to_image(x, xa, M, K, id + stride);
     }
+    if (id < n_chunks) x_chunk_to_image(x, xa, M, K, id);
 }
 
 template <int BN, bool kBulkA>
@@ -1147,9 +1163,17 @@ cudaError_t launch_wt_kernel(const uint8_t* xa, const uint8_t* w, float* y, int 
         if (e != cudaSuccess) return e;
         attr_done[device] = true;
     }
-    dim3 grid((N + C::kRows - 1) / C::kRows, (M + kXRows - 1) / kXRows);
-    gemm_wt_kernel<kXRows, kTmaW><<<grid, C::kThreads, C::kSmemBytes, stream>>>(xa, w, y, M, N, K, map);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((N + C::kRows - 1) / C::kRows, (M + kXRows - 1) / kXRows);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_wt_kernel<kXRows, kTmaW>, xa, w, y, M, N, K, map);
 }
 
 template <int kXRows>
@@ -1204,7 +1228,7 @@ cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, in
     uint8_t* xa = static_cast<uint8_t*>(workspace);
     const size_t n_chunks = gemm_tc_workspace_bytes(M, K) / 16;
     size_t blocks = (n_chunks + 255) / 256;
-    const size_t cap = static_cast<size_t>(sm_count) * 8;
+    const size_t cap = static_cast<size_t>(sm_count) * 4;
     if (blocks > cap) blocks = cap;
     x_to_bf16_tiles_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, xa, M, K, n_chunks);
     cudaError_t e = cudaGetLastError();
