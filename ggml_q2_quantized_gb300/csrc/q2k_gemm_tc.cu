@@ -566,20 +566,24 @@ gemm_tc_kernel(const float* __restrict__ x, const uint8_t* __restrict__ xa,
 // MMA is M = 128 (weight rows, TMEM lanes) x N = this tile's x rows padded to
 // 16, accumulating into TMEM columns [0, N); decoded stage s (64 K) sits at
 // columns kColA + 32 s, K-step t (16 weights, 8 bf16x2 columns) at + 8 t.
-//   warps 0-7   decoders, then the epilogue.  Warp w stores to TMEM lanes
-//               32 (w % 4) .. + 31; w / 4 picks the 16-weight segment of a
-//               32-weight quant group: per block the thread reads 16 of its
-//               row's 32 quant bytes per half and decodes all four 2-bit
-//               planes of them
-//   warp 8      TMEM allocation, MMA issue (one thread)
-//   warp 9      waits for the next kPair stages to be filled and hands them to
+//   warps 0-15  decoders, then the epilogue.  Warp w stores to TMEM lanes
+//               32 (w % 4) .. + 31; (w / 4) % 2 picks the 16-weight segment of
+//               a 32-weight quant group and w / 8 the half of each block (its
+//               two 64-K stages) the warp decodes: per block the thread reads
+//               16 of its row's 32 quant bytes of that half and the half's
+//               scales, and decodes all four 2-bit planes of them, two per
+//               stage.  Two groups on alternate stage pairs give each warp
+//               twice the time per stage (the decode is latency-bound: a scale
+//               table then byte permutes, plus a barrier test per stage)
+//   warp 16     TMEM allocation, MMA issue (one thread)
+//   warp 17     waits for the next kPair stages to be filled and hands them to
 //               the MMA warp at a named barrier both warps pass once per
 //               hand-over: the MMA thread never polls an mbarrier, so nothing
 //               but MMAs and commits sits between its MMAs (the MMA pipe runs
 //               dry while the issuing thread is busy elsewhere)
-//   warp 10     raw weight blocks: one 2-D TMA box (128 rows x 112 bytes) per
+//   warp 18     raw weight blocks: one 2-D TMA box (128 rows x 112 bytes) per
 //               block (without TMA the decoders copy them with 4-byte cp.async)
-//   warps 11-12 x stages, even and odd: one bulk copy each (a thread's bulk
+//   warps 19-20 x stages, even and odd: one bulk copy each (a thread's bulk
 //               copies complete one after another, so two issuers double the
 //               rate a single one gets)
 // ============================================================================
@@ -597,13 +601,14 @@ template <int kXRows, bool kTmaW>
 struct WtCfg {
     static_assert(kXRows == 128 || kXRows == 256, "x rows per CTA");
     static constexpr int kRows = 128;                       // weight rows per CTA
-    static constexpr int kDecWarps = 8;
+    static constexpr int kDecWarps = 16;                    // two groups of 8, one per block half
+    static constexpr int kGroupWarps = 8;                   // decoders of one stage
     static constexpr int kDecThreads = 32 * kDecWarps;
-    static constexpr int kMmaWarp = 8;
-    static constexpr int kWaitWarp = 9;
-    static constexpr int kWWarp = 10;
-    static constexpr int kXWarp0 = 11;
-    static constexpr int kThreads = 32 * 13;
+    static constexpr int kMmaWarp = kDecWarps;
+    static constexpr int kWaitWarp = kDecWarps + 1;
+    static constexpr int kWWarp = kDecWarps + 2;
+    static constexpr int kXWarp0 = kDecWarps + 3;
+    static constexpr int kThreads = 32 * (kDecWarps + 5);
     static constexpr int kPair = 2;                         // K stages per MMA hand-over
     static constexpr int kXStage = kXRows * kKS * 2;        // bytes of one x stage
     static constexpr int kXStages = kXRows == 256 ? 6 : 8;
@@ -676,23 +681,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Stage C (0..3) of a block for one thread: the two 16-weight K-steps of
-// quant segment `seg` at the two 2-bit planes J = 2 (C & 1) + {0, 1} of half
-// H = C / 2.  qw = the thread's four quant words of each half, sws = the 16
-// scale bytes shifted right by 8 seg (so the segment's byte sits at the low
-// byte of each 16-bit lane).  o0 gets K-step seg, o1 K-step 2 + seg; word 2e
-// (2e + 1) holds the weights of quant byte lanes 4e, 4e + 1 (4e + 2, 4e + 3).
-template <int C>
-__device__ __forceinline__ void wt_decode_stage(const uint32_t (&qw)[8], const uint32_t (&sws)[4],
-                                                float d, float dmin, uint32_t (&o0)[8],
-                                                uint32_t (&o1)[8]) {
-    constexpr int H = C >> 1;
+// Stage Cp (0 or 1) of one half of a block for one thread: the two 16-weight
+// K-steps of quant segment `seg` at the 2-bit planes J = 2 Cp + {0, 1}.  qh =
+// the thread's four quant words of the half, sh = the half's two scale words
+// shifted right by 8 seg (the segment's byte at the low byte of each 16-bit
+// lane).  o0 gets K-step seg, o1 K-step 2 + seg; word 2e (2e + 1) holds the
+// weights of quant byte lanes 4e, 4e + 1 (4e + 2, 4e + 3).
+template <int Cp>
+__device__ __forceinline__ void wt_decode_half_stage(const uint32_t* qh, const uint32_t* sh, float d,
+                                                     float dmin, uint32_t (&o0)[8],
+                                                     uint32_t (&o1)[8]) {
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
-        constexpr int kJ0 = 2 * (C & 1);
+        constexpr int kJ0 = 2 * Cp;
         const int j = kJ0 + jj;
-        // scale index 8 H + 2 j + seg -> word 2 H + j / 2, byte 2 (j % 2) + seg
-        const uint32_t sc = (sws[2 * H + (j >> 1)] >> (16 * (j & 1))) & 0xFFu;
+        // scale index 8 H + 2 j + seg -> word j / 2 of the half, byte 2 (j % 2) + seg
+        const uint32_t sc = (sh[j >> 1] >> (16 * (j & 1))) & 0xFFu;
         const float dl = __fmul_rn(d, static_cast<float>(sc & 15u));
         const float ml = __fmul_rn(dmin, static_cast<float>(sc >> 4));
         const uint32_t lo = pack_bf16x2(-ml, __fsub_rn(dl, ml));
@@ -700,11 +704,10 @@ __device__ __forceinline__ void wt_decode_stage(const uint32_t (&qw)[8], const u
         uint32_t* o = jj == 0 ? o0 : o1;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const uint32_t word = qw[4 * H + e];
-            if (kJ0 + jj == 0) decode_word<0>(word, lo, hi, o[2 * e], o[2 * e + 1]);
-            else if (kJ0 + jj == 1) decode_word<1>(word, lo, hi, o[2 * e], o[2 * e + 1]);
-            else if (kJ0 + jj == 2) decode_word<2>(word, lo, hi, o[2 * e], o[2 * e + 1]);
-            else decode_word<3>(word, lo, hi, o[2 * e], o[2 * e + 1]);
+            if (kJ0 + jj == 0) decode_word<0>(qh[e], lo, hi, o[2 * e], o[2 * e + 1]);
+            else if (kJ0 + jj == 1) decode_word<1>(qh[e], lo, hi, o[2 * e], o[2 * e + 1]);
+            else if (kJ0 + jj == 2) decode_word<2>(qh[e], lo, hi, o[2 * e], o[2 * e + 1]);
+            else decode_word<3>(qh[e], lo, hi, o[2 * e], o[2 * e + 1]);
         }
     }
 }
@@ -764,7 +767,7 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
             mbar_init(bar_xempty + 8 * s, 1);  // MMA commit
         }
         for (int s = 0; s < C::kAStages; ++s) {
-            mbar_init(bar_afull + 8 * s, C::kDecWarps);  // one arrival per decoder warp
+            mbar_init(bar_afull + 8 * s, C::kGroupWarps);  // one arrival per warp of its group
             mbar_init(bar_aempty + 8 * s, 1);            // MMA commit
         }
         for (int r = 0; r < C::kRaw; ++r) {
@@ -794,7 +797,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
         // ---------------- weight decoders ----------------
         const int td = threadIdx.x;
         const int quarter = warp & 3;
-        const int seg = warp >> 2;
+        const int seg = (warp >> 2) & 1;
+        const int half = warp >> 3;           // block half = stages 2 half, 2 half + 1
         const int row = 32 * quarter + lane;  // weight row within the tile = TMEM lane
         const uint32_t raw0 = sbase + C::kOffRaw;
         const uint32_t t_lane = static_cast<uint32_t>(32 * quarter) << 16;
@@ -847,14 +851,12 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
                     cp_async_commit();
                 mine = raw0 + buf * C::kRawBytes + row * kBlockBytes;
             }
-            uint32_t sws[4], qw[8];
+            uint32_t sh[2], qh[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) sws[q] = ld_shared_u32(mine + 4 * q) >> (8 * seg);
+            for (int q = 0; q < 2; ++q) sh[q] = ld_shared_u32(mine + 8 * half + 4 * q) >> (8 * seg);
 #pragma unroll
-            for (int H = 0; H < 2; ++H)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    qw[4 * H + e] = ld_shared_u32(mine + 16 + 32 * H + 16 * seg + 4 * e);
+            for (int e = 0; e < 4; ++e)
+                qh[e] = ld_shared_u32(mine + 16 + 32 * half + 16 * seg + 4 * e);
             const uint32_t dd = ld_shared_u32(mine + 80);
             if constexpr (kTmaW) {
                 // this warp has its block in registers: the slab may be refilled
@@ -864,21 +866,20 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
             const float d = f16_bits_to_float(dd);
             const float dmin = f16_bits_to_float(dd >> 16);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int i = 4 * b + c;
+            for (int cp = 0; cp < 2; ++cp) {
+                const int i = 4 * b + 2 * half + cp;
                 const int s = i % C::kAStages;
                 uint32_t o0[8], o1[8];
-                if (c == 0) wt_decode_stage<0>(qw, sws, d, dmin, o0, o1);
-                else if (c == 1) wt_decode_stage<1>(qw, sws, d, dmin, o0, o1);
-                else if (c == 2) wt_decode_stage<2>(qw, sws, d, dmin, o0, o1);
-                else wt_decode_stage<3>(qw, sws, d, dmin, o0, o1);
-                // The previous stage's TMEM stores had this decode to land:
-                // publish that stage now.
-                if (i > 0) {
+                if (cp == 0) wt_decode_half_stage<0>(qh, sh, d, dmin, o0, o1);
+                else wt_decode_half_stage<1>(qh, sh, d, dmin, o0, o1);
+                // This warp's previous stage (i - 1, or i - 3 across a block):
+                // its TMEM stores had this decode to land; publish it now.
+                if (b > 0 || cp > 0) {
+                    const int prev = cp > 0 ? i - 1 : i - 3;
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_afull + 8 * ((i - 1) % C::kAStages));
+                    if (lane == 0) mbar_arrive(bar_afull + 8 * (prev % C::kAStages));
                 }
                 if (i >= C::kAStages &&
                     !__all_sync(0xFFFFFFFFu,
@@ -894,11 +895,11 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
             }
         }
         if (ok) {
-            // publish the last stage
+            // publish this warp's last stage
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_afull + 8 * ((n_iters - 1) % C::kAStages));
+            if (lane == 0) mbar_arrive(bar_afull + 8 * ((n_iters - 3 + 2 * half) % C::kAStages));
         }
         if constexpr (!kTmaW) cp_async_wait_all();  // no copy may land after this CTA is gone
 
@@ -909,9 +910,9 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
             tc_fence_after();
             const int n = n0 + row;
             const uint32_t t_row = tmem_base + t_lane;
-            // 16-column groups alternate between the two warps of a lane quarter
+            // 16-column groups rotate over the four warps of a lane quarter
 #pragma unroll 1
-            for (int c0 = 16 * seg; c0 < nx; c0 += 32) {
+            for (int c0 = 16 * (warp >> 2); c0 < nx; c0 += 64) {
                 uint32_t v[16];
                 tmem_ld16(t_row + c0, v);
                 if (n < N) {
