@@ -28,6 +28,7 @@ GGML_TYPE_Q2_K = 10
 
 PATH_AUTO, PATH_GEMV, PATH_TENSOR = 0, 1, 2
 FLAG_CONST_WEIGHTS = 1
+FLAG_INDEPENDENT = 2
 _PATHS = {"auto": PATH_AUTO, "gemv": PATH_GEMV, "tensor": PATH_TENSOR,
           PATH_AUTO: PATH_AUTO, PATH_GEMV: PATH_GEMV, PATH_TENSOR: PATH_TENSOR}
 
@@ -188,11 +189,15 @@ def embedding_gather(table, ids, embed_dim: int, vocab_size: int | None = None, 
 
 
 def matmul(x, w, n: int, out=None, path="auto", const_weights: bool = False,
-           workspace="auto"):
+           workspace="auto", independent: bool = False):
     """``y[m, r] = sum_k x[m, k] * W[r, k]`` with W = ``n`` rows of Q2_K blocks.
 
     ``const_weights=True`` passes Q2K_FLAG_CONST_WEIGHTS: the caller promises
     that the kernel enqueued just before on the stream does not write ``w``.
+    ``independent=True`` passes Q2K_FLAG_INDEPENDENT: no kernel still running
+    on the stream writes ``x`` or ``w`` or touches ``out`` (e.g. several
+    projections of one activation enqueued back to back), so consecutive
+    m = 1 calls overlap.
     ``workspace``: "auto" allocates the tensor-core path's workspace from
     PyTorch's caching allocator; None runs without one; or a uint8 CUDA tensor.
     """
@@ -218,7 +223,8 @@ def matmul(x, w, n: int, out=None, path="auto", const_weights: bool = False,
         _require_cuda(workspace, "workspace", torch.uint8)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
     with torch.cuda.device(x.device):
-        _check(lib, lib.q2k_matmul_ex(_PATHS[path], FLAG_CONST_WEIGHTS if const_weights else 0,
+        flags = (FLAG_CONST_WEIGHTS if const_weights else 0) | (FLAG_INDEPENDENT if independent else 0)
+        _check(lib, lib.q2k_matmul_ex(_PATHS[path], flags,
                                       x.data_ptr(), x.numel(), w.data_ptr(), w.numel(),
                                       out.data_ptr(), out.numel(), ctypes.byref(p),
                                       ws_ptr, ws_bytes, _stream_handle(x)))

@@ -204,7 +204,7 @@ q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float* x, size_t x
     g_last_error[0] = '\0';
     q2k_status st = check_matmul(x, x_elems, w, w_bytes, y, y_elems, p);
     if (st != Q2K_OK) return st;
-    if ((flags & ~static_cast<uint32_t>(Q2K_FLAG_CONST_WEIGHTS)) != 0)
+    if ((flags & ~static_cast<uint32_t>(Q2K_FLAG_CONST_WEIGHTS | Q2K_FLAG_INDEPENDENT)) != 0)
         return fail(Q2K_ERR_INVALID_ARGUMENT, "unknown flag bits 0x%x", flags);
     if (path != Q2K_PATH_AUTO && path != Q2K_PATH_GEMV && path != Q2K_PATH_TENSOR)
         return fail(Q2K_ERR_INVALID_ARGUMENT, "unknown path %d", static_cast<int>(path));
@@ -233,7 +233,9 @@ q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float* x, size_t x
     cudaError_t e;
     if (path == Q2K_PATH_GEMV)
         e = q2k::launch_gemv(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count,
-                             (flags & Q2K_FLAG_CONST_WEIGHTS) != 0, s);
+                             ((flags & Q2K_FLAG_CONST_WEIGHTS) ? q2k::kGemvConstWeights : 0u) |
+                                 ((flags & Q2K_FLAG_INDEPENDENT) ? q2k::kGemvIndependent : 0u),
+                             s);
     else
         e = q2k::launch_gemm_tc(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count, ws, s);
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul launch");

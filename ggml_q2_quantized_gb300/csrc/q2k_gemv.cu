@@ -40,10 +40,12 @@ namespace {
 constexpr int kGemvWarps = 8;
 constexpr int kPieceRows = 4;      // rows per bulk copy / mbarrier
 constexpr int kM1MaxSlices = 256;  // k <= 16384
-#ifndef Q2K_M1_THREADS
-#define Q2K_M1_THREADS 256
-#endif
-constexpr int kM1Threads = Q2K_M1_THREADS;  // 256 leaves room for the next grid's CTA
+// Threads per CTA of the m = 1 kernel.  A dependent call runs alone once its
+// predecessor completes, so it takes more threads per CTA (shorter critical
+// path); independent calls overlap, so smaller CTAs let more calls share an SM
+// (up to four at 116 registers a thread).
+constexpr int kM1ThreadsDependent = 256;
+constexpr int kM1ThreadsIndependent = 128;
 
 // ------------------------------------------------------------------ m = 1
 
@@ -186,11 +188,14 @@ __device__ __forceinline__ float transpose_reduce4(float (&v)[kRowBatch], int la
 // mbarrier (each completes when its bytes have landed).  Piece starts are
 // 16-byte aligned (the host plan keeps chunk starts aligned); the ragged end of
 // the last piece (a multiple of 4 bytes below 16) is copied with plain loads
-// before the barrier's arrival.
+// before the barrier's arrival.  Lane 0 of warp w issues pieces w, w + nwarps,
+// ...: one thread's bulk copies complete one after another, so spreading them
+// over the warps multiplies the rate at which the chunk lands.
 __device__ __forceinline__ void issue_weight_copies(uint8_t* smem, const uint8_t* gsrc,
-                                                    uint32_t bars, int rows, size_t row_bytes) {
+                                                    uint32_t bars, int rows, size_t row_bytes,
+                                                    int first, int step) {
     const int n_pieces = (rows + kPieceRows - 1) / kPieceRows;
-    for (int p = 0; p < n_pieces; ++p) {
+    for (int p = first; p < n_pieces; p += step) {
         const int ra = p * kPieceRows;
         const int rb = min(rows, ra + kPieceRows);
         const size_t off = static_cast<size_t>(ra) * row_bytes;
@@ -206,7 +211,9 @@ __device__ __forceinline__ void issue_weight_copies(uint8_t* smem, const uint8_t
 
 __global__ void __launch_bounds__(512, 1)
 gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
-               int N, int K, int rows_per_cta, int slices_pad, int groups, int const_weights) {
+               int N, int K, int rows_per_cta, int slices_pad, int groups, uint32_t flags) {
+    const bool independent = (flags & kGemvIndependent) != 0;
+    const bool const_weights = independent || (flags & kGemvConstWeights) != 0;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
     const int nthreads = blockDim.x;
@@ -237,26 +244,30 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     // weight prefetch or copy) then overlaps this grid; it still waits for this
     // grid to complete before it reads x or writes y.
     pdl_allow_dependents();
+    const int nwarps = nthreads >> 5;
+    const bool issuer = (tid & 31) == 0;
     if (tid == 0) {
         for (int p = 0; p < n_pieces; ++p) mbar_init(bars + 8 * p, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        if (const_weights) {
-            // The caller guarantees the grid before this one does not write W,
-            // so the weight copies may start before the dependency wait.
-            issue_weight_copies(smem, gsrc, bars, rows, row_bytes);
-        } else {
-            // An L2 prefetch is coherent with the previous grid's writes.
-            const size_t pre = chunk & ~size_t(15);
-            for (size_t off = 0; off < pre; off += (size_t(1) << 20)) {
-                const size_t left = pre - off;
-                bulk_prefetch_l2(gsrc + off, static_cast<uint32_t>(left < (size_t(1) << 20) ? left : (size_t(1) << 20)));
-            }
+    }
+    __syncthreads();
+    if (const_weights) {
+        // The caller guarantees the grids that may still run do not write W,
+        // so the weight copies may start before the dependency wait.
+        if (issuer) issue_weight_copies(smem, gsrc, bars, rows, row_bytes, tid >> 5, nwarps);
+    } else if (tid == 0) {
+        // An L2 prefetch is coherent with the previous grid's writes.
+        const size_t pre = chunk & ~size_t(15);
+        for (size_t off = 0; off < pre; off += (size_t(1) << 20)) {
+            const size_t left = pre - off;
+            bulk_prefetch_l2(gsrc + off, static_cast<uint32_t>(left < (size_t(1) << 20) ? left : (size_t(1) << 20)));
         }
     }
-    pdl_wait_prerequisites();
+    if (!independent) pdl_wait_prerequisites();
     __syncthreads();
-    if (tid == 0 && !const_weights) issue_weight_copies(smem, gsrc, bars, rows, row_bytes);
+    if (issuer && !const_weights)
+        issue_weight_copies(smem, gsrc, bars, rows, row_bytes, tid >> 5, nwarps);
     // x -> integer planes, once per CTA, while the weights stream in
     for (int r = tid; r < n_runs; r += nthreads)
         convert_run(x + 16 * r, &planes[r], &run_sum[r], &run_inv[r]);
@@ -318,6 +329,11 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
         for (int p = 0; p < n_pieces; ++p)
             mbar_wait_bounded(bars + 8 * p, 0, &no_abort, &g_gemv_error, kErrTimeoutGemv);
     }
+    // Independent calls finish only after the grid before them, so work
+    // enqueued later on the stream sees every earlier call complete.  One CTA
+    // waiting keeps the grid from completing early; the others leave and free
+    // their SM for the calls after this one.
+    if (independent && blockIdx.x == 0) pdl_wait_prerequisites();
 }
 
 struct M1Plan {
@@ -335,12 +351,12 @@ size_t m1_smem(int rows, int K, int slices_pad) {
     return ((red_end + 7) & ~size_t(7)) + 8 * pieces + 16;
 }
 
-bool plan_m1(int N, int K, int sm_count, M1Plan* p) {
+bool plan_m1(int N, int K, int sm_count, int threads, M1Plan* p) {
     const int B = K / 256;
     const int S = K / 64;
     if (S > kM1MaxSlices) return false;
     const int slices_pad = (S + 31) / 32 * 32;
-    const int groups = slices_pad >= kM1Threads ? 1 : kM1Threads / slices_pad;
+    const int groups = slices_pad >= threads ? 1 : threads / slices_pad;
     int rows = 0;
     for (int waves = 1;; ++waves) {
         rows = (N + sm_count * waves - 1) / (sm_count * waves);
@@ -357,7 +373,7 @@ bool plan_m1(int N, int K, int sm_count, M1Plan* p) {
 }
 
 cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, const M1Plan& p,
-                      int device, bool const_weights, cudaStream_t stream) {
+                      int device, uint32_t flags, cudaStream_t stream) {
     static bool smem_set[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!smem_set[device]) {
@@ -378,7 +394,7 @@ cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, gemv_m1_kernel, x, w, y, N, K, p.rows_per_cta, p.slices_pad,
-                              p.groups, const_weights ? 1 : 0);
+                              p.groups, flags);
 }
 
 // ------------------------------------------------------------------ general m
@@ -474,10 +490,12 @@ cudaError_t launch_rows(const float* x, const uint8_t* w, float* y, int M, int N
 }  // namespace
 
 cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N, int K,
-                        int device, int sm_count, bool const_weights, cudaStream_t stream) {
+                        int device, int sm_count, uint32_t flags, cudaStream_t stream) {
     M1Plan plan;
-    if (M == 1 && (reinterpret_cast<uintptr_t>(w) & 15u) == 0 && plan_m1(N, K, sm_count, &plan))
-        return launch_m1(x, w, y, N, K, plan, device, const_weights, stream);
+    const int threads = (flags & kGemvIndependent) ? kM1ThreadsIndependent : kM1ThreadsDependent;
+    if (M == 1 && (reinterpret_cast<uintptr_t>(w) & 15u) == 0 &&
+        plan_m1(N, K, sm_count, threads, &plan))
+        return launch_m1(x, w, y, N, K, plan, device, flags, stream);
     switch (M < 8 ? M : 8) {
         case 1: return launch_rows<1>(x, w, y, M, N, K, stream);
         case 2: return launch_rows<2>(x, w, y, M, N, K, stream);

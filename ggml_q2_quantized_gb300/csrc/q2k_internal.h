@@ -16,10 +16,15 @@ cudaError_t launch_gather(const uint8_t* table, const uint32_t* ids, float* out,
 
 // fp32 GEMV path: m = 1 uses the shared-memory streaming kernel when K <= 16384
 // and w is 16-byte aligned; otherwise x rows are handled 8 at a time.
-// const_weights: the caller guarantees the kernel enqueued just before does not
-// write w, so weight loads may start before the programmatic-launch wait.
+// flags (m = 1 kernel only):
+//   kGemvConstWeights  the kernels that may still run do not write w: weight
+//                      loads may start before the programmatic-launch wait;
+//   kGemvIndependent   they touch neither x, w nor y: the kernel waits for the
+//                      grid before it only at its very end (completion order).
+constexpr uint32_t kGemvConstWeights = 1u;
+constexpr uint32_t kGemvIndependent = 2u;
 cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N, int K,
-                        int device, int sm_count, bool const_weights, cudaStream_t stream);
+                        int device, int sm_count, uint32_t flags, cudaStream_t stream);
 
 // Read and clear the GEMV kernels' device error word (synchronises `stream`).
 cudaError_t read_and_clear_gemv_error(uint32_t* out, cudaStream_t stream);

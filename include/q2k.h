@@ -145,7 +145,15 @@ enum {
      * The m = 1 GEMV then starts copying W before it waits for that kernel,
      * overlapping the weight stream with it.  Without the flag it only
      * prefetches W into L2 (always safe) and copies after the wait. */
-    Q2K_FLAG_CONST_WEIGHTS = 1
+    Q2K_FLAG_CONST_WEIGHTS = 1,
+    /* The caller guarantees that no kernel enqueued on `stream` before this
+     * call that may still be running writes x or W, or reads or writes y
+     * (e.g. several projections of one activation, each with its own W and
+     * y, enqueued back to back).  The m = 1 GEMV then reads x and writes y
+     * without waiting for the kernel before it, so consecutive calls overlap;
+     * it still waits for that kernel before it finishes, so calls complete in
+     * stream order.  Implies Q2K_FLAG_CONST_WEIGHTS.  Other paths ignore it. */
+    Q2K_FLAG_INDEPENDENT = 2
 };
 
 /* q2k_matmul_workspace_bytes - device bytes of workspace q2k_matmul_ex can use

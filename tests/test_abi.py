@@ -119,7 +119,7 @@ def test_binding_refuses_missing_library(tmp_path):
 
 def test_matmul_ex_rejects_unknown_flags(lib):
     p = q2k.MatmulParams(1, 8, 256, 10)
-    assert lib.q2k_matmul_ex(0, 2, 0x10000, 256, 0x100000, 672, 0x1000000, 8,
+    assert lib.q2k_matmul_ex(0, 4, 0x10000, 256, 0x100000, 672, 0x1000000, 8,
                              ctypes.byref(p), None, 0, None) == INVALID
     assert "flag" in lib.q2k_last_error().decode()
 

@@ -339,3 +339,42 @@ def test_tensor_workspace_and_in_kernel_conversion_agree(m, n, k):
     assert_close(yb, yref, s, TOL_TC, f"ws m={m} n={n} k={k}")
     # same bf16 operands, fp32 sums of k exact products in two orders
     assert np.all(np.abs(ya - yb) <= 1e-5 * s + 1e-30)
+
+
+@pytest.mark.parametrize("n,k", [(4096, 4096), (333, 4096), (14336, 4096), (77, 14336)])
+def test_independent_flag_same_bits(n, k):
+    """Q2K_FLAG_INDEPENDENT only drops the wait before x is read: same bits."""
+    x, w = wl.make_matmul_inputs(191 + n, 1, n, k)
+    xd, wd = dev(x), dev(w)
+    a = q2k.matmul(xd, wd, n)
+    b = q2k.matmul(xd, wd, n, independent=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    yref, s = oracle.matmul(x, w, n, threads=ORACLE_THREADS)
+    assert_close(b.cpu().numpy().astype(np.float64), yref, s, TOL_GEMV, f"indep n={n} k={k}")
+
+
+def test_independent_calls_complete_in_order_before_a_dependent_one():
+    """Back-to-back independent projections of one x, then a dependent call that
+    reads all their outputs at once (their concatenation is its x): it must see
+    every projection finished, as must the host after a plain synchronize."""
+    n_proj, n, k = 6, 1024, 4096
+    x, _ = wl.make_matmul_inputs(501, 1, 1, k)
+    ws = [wl.make_matmul_inputs(510 + i, 1, n, k)[1] for i in range(n_proj)]
+    w_next = wl.make_matmul_inputs(530, 1, 256, n_proj * n)[1]
+    xd = dev(x)
+    wds = [dev(w) for w in ws]
+    wnd = dev(w_next)
+    cat = torch.full((1, n_proj * n), float("nan"), device="cuda")
+    for rep in range(3):
+        cat.fill_(float("nan"))
+        for i in range(n_proj):
+            q2k.matmul(xd, wds[i], n, out=cat[:, i * n:(i + 1) * n], independent=True)
+        z = q2k.matmul(cat, wnd, 256, const_weights=True)
+        torch.cuda.synchronize()
+        got = cat.cpu().numpy().astype(np.float64)
+        for i in range(n_proj):
+            yref, s = oracle.matmul(x, ws[i], n, threads=ORACLE_THREADS)
+            assert_close(got[:, i * n:(i + 1) * n], yref, s, TOL_GEMV, f"projection {i}")
+        zref, s = oracle.matmul(got.astype(np.float32), w_next, 256, threads=ORACLE_THREADS)
+        assert_close(z.cpu().numpy().astype(np.float64), zref, s, TOL_GEMV, f"consumer rep {rep}")
