@@ -51,12 +51,14 @@ constexpr int kM1ThreadsIndependent = 128;
 
 constexpr int kRowBatch = 4;  // rows reduced together by one transposed butterfly
 
-// x as exact integers: each 16-weight run r (k = 16 r .. 16 r + 15, one
-// (half, shift, segment) of a block) is scaled by 2^e_r so that its largest
-// |x| lies in [2^21, 2^22), rounded to nearest, and split into byte planes
-// x_int = p2 * 65536 + p1 * 256 + p0 (p2 signed, p1/p0 unsigned).  The plane
-// words of a run are 4 consecutive weights each.  Also kept per run: the f32
-// sum of its 16 x (for the -ml term) and 2^-e_r.
+// x as integers: each 16-weight run r (k = 16 r .. 16 r + 15, one (half,
+// shift, segment) of a block) is scaled by 2^e_r so that its largest |x| lies
+// in [2^18, 2^19), rounded to nearest (relative error <= 2^-19 of the run's
+// largest |x|), and split into byte planes x_int = p2 * 65536 + p1 * 256 + p0
+// (p2 signed, p1/p0 unsigned).  19 bits keep every integer product of the
+// dot below 2^31 (16 * 12 * 15 * 2^19 < 2^31), so the scale multiplies stay
+// in integers.  The plane words of a run are 4 consecutive weights each.
+// Also kept per run: the f32 sum of its 16 x (for the -ml term) and 2^-e_r.
 struct RunPlanes {
     uint32_t p0[4], p1[4], p2[4];
 };
@@ -78,10 +80,10 @@ __device__ __forceinline__ void convert_run(const float* __restrict__ xr, RunPla
         mx = fmaxf(mx, fabsf(v[l]));
         sum += v[l];
     }
-    // e = 21 - floor(log2 max|x|), kept within the normal range; for max|x| = 0
+    // e = 18 - floor(log2 max|x|), kept within the normal range; for max|x| = 0
     // (or a subnormal max) any e gives zeros, so e = 0 then.
     const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu);  // biased exponent
-    int e = (ex == 0 || ex == 255) ? 0 : 148 - ex;                            // 21 - (ex - 127)
+    int e = (ex == 0 || ex == 255) ? 0 : 145 - ex;                            // 18 - (ex - 127)
     e = max(-126, min(126, e));
     const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);   // 2^e, exact
     RunPlanes pl;
@@ -90,7 +92,7 @@ __device__ __forceinline__ void convert_run(const float* __restrict__ xr, RunPla
         uint32_t b0 = 0, b1 = 0, b2 = 0;
 #pragma unroll
         for (int e4 = 0; e4 < 4; ++e4) {
-            // |x 2^e| < 2^22: adding 1.5 * 2^23 rounds it to an integer (nearest,
+            // |x 2^e| < 2^19: adding 1.5 * 2^23 rounds it to an integer (nearest,
             // ties to even) held in the low mantissa bits.
             const float biased = fmaf(v[4 * q + e4], up, 12582912.f);
             const uint32_t xi = __float_as_uint(biased) - 0x4B400000u;  // two's complement
@@ -109,9 +111,35 @@ __device__ __forceinline__ void convert_run(const float* __restrict__ xr, RunPla
 
 struct SlicePlanes {
     RunPlanes r[4];  // shift j = 0..3
-    float X[4];      // sum of the run's x
-    float inv[4];    // 2^-e of the run
+    float inv[4];    // 2^-e of the run, times 1/4 for odd j (see slice_dot)
+    // The four run sums X_j as integers with one scale 2^eX for the slice
+    // (largest |X_j| in [2^21, 2^22)), byte j of each word = run j's byte.
+    uint32_t xq0, xq1, xq2;
+    float xinv;      // 2^-eX
 };
+
+// X_j -> the slice's integer byte planes (same rounding as convert_run).
+__device__ __forceinline__ void quantize_run_sums(const float (&X)[4], SlicePlanes& s) {
+    float mx = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(X[j]));
+    const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu);
+    int e = (ex == 0 || ex == 255) ? 0 : 148 - ex;  // 21 - (ex - 127)
+    e = max(-126, min(126, e));
+    const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+    uint32_t b0 = 0, b1 = 0, b2 = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t xi = __float_as_uint(fmaf(X[j], up, 12582912.f)) - 0x4B400000u;
+        b0 |= (xi & 0xFFu) << (8 * j);
+        b1 |= ((xi >> 8) & 0xFFu) << (8 * j);
+        b2 |= ((xi >> 16) & 0xFFu) << (8 * j);
+    }
+    s.xq0 = b0;
+    s.xq1 = b1;
+    s.xq2 = b2;
+    s.xinv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+}
 
 // The 7 words of one weight row a thread needs: its 16 quant bytes, the four
 // scale bytes of its segment (one per shift) and the packed f16 d, dmin.
@@ -133,33 +161,41 @@ __device__ __forceinline__ RowWords load_row_words(const uint8_t* __restrict__ r
 }
 
 // Partial dot product of one weight row with this thread's 64-weight slice:
-// sum_j (d sc_j 2^-e_j) S_j - (dmin m_j) X_j with S_j = sum_l q_l x_int_l exact.
+// d sum_j sc_j 2^-e_j S_j - dmin sum_j m_j X_j with S_j = sum_l q_l x_int_l.
+// The 2-bit codes of shift j sit at bits 2 j of each quant byte; the odd
+// shifts are masked in place (the code times 4, no shift needed) and s.inv
+// carries the compensating 1/4.  sc_j S_j is formed in integers (below 2^31,
+// see convert_run) and the min term is one integer dot of the four 4-bit
+// mins with the slice's quantized run sums.
 __device__ __forceinline__ float slice_dot(const RowWords& r, const SlicePlanes& s) {
-    const float d = f16_bits_to_float(r.dd);
-    const float dmin = f16_bits_to_float(r.dd >> 16);
     const uint32_t lo = r.sc4 & 0x0F0F0F0Fu;
     const uint32_t hi = (r.sc4 >> 4) & 0x0F0F0F0Fu;
-    float pa = 0.f, pb = 0.f;
+    uint32_t q4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q4[i] = r.q[i] >> 4;
+    float acc = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
+        const uint32_t mask = (j & 1) ? 0x0C0C0C0Cu : 0x03030303u;
         int a2 = 0;
         unsigned a1 = 0, a0 = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t t = (r.q[i] >> (2 * j)) & 0x03030303u;
+            const uint32_t t = (j < 2 ? r.q[i] : q4[i]) & mask;
             a2 = __dp4a(static_cast<int>(s.r[j].p2[i]), static_cast<int>(t), a2);
             a1 = __dp4a(s.r[j].p1[i], t, a1);
             a0 = __dp4a(s.r[j].p0[i], t, a0);
         }
         const int sint = a2 * 65536 + static_cast<int>(a1 * 256u + a0);
-        // byte j of lo/hi -> exact float through the bits of 2^23 + v
-        const uint32_t sel = static_cast<uint32_t>(j) | (4u << 4) | (4u << 8) | (7u << 12);
-        const float scf = __uint_as_float(__byte_perm(lo, 0x4B000000u, sel)) - 8388608.f;
-        const float mf = __uint_as_float(__byte_perm(hi, 0x4B000000u, sel)) - 8388608.f;
-        pa = fmaf((d * s.inv[j]) * scf, static_cast<float>(sint), pa);
-        pb = fmaf(-(dmin * mf), s.X[j], pb);
+        const int sc = static_cast<int>(__byte_perm(lo, 0u, static_cast<uint32_t>(j) | 0x4440u));
+        acc = fmaf(static_cast<float>(sint * sc), s.inv[j], acc);
     }
-    return pa + pb;
+    int m2 = __dp4a(static_cast<int>(s.xq2), static_cast<int>(hi), 0);
+    unsigned m1 = __dp4a(s.xq1, hi, 0u), m0 = __dp4a(s.xq0, hi, 0u);
+    const int mint = m2 * 65536 + static_cast<int>(m1 * 256u + m0);
+    const float d = f16_bits_to_float(r.dd);
+    const float dmin = f16_bits_to_float(r.dd >> 16);
+    return fmaf(d, acc, -(dmin * (static_cast<float>(mint) * s.xinv)));
 }
 
 // Sum v[0..kRowBatch) over the 32 lanes; afterwards lane L holds the total of
@@ -279,13 +315,17 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     const int b = sl >> 2, h = (sl >> 1) & 1, seg = sl & 1;
     const uint32_t ssel = seg | ((seg + 2) << 4) | ((seg + 4) << 8) | ((seg + 6) << 12);
     SlicePlanes s;
+    {
+        float X[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        // run of (block b, half h, shift j, segment seg)
-        const int run = active ? 16 * b + 8 * h + 2 * j + seg : 0;
-        s.r[j] = planes[run];
-        s.X[j] = active ? run_sum[run] : 0.f;
-        s.inv[j] = active ? run_inv[run] : 0.f;
+        for (int j = 0; j < 4; ++j) {
+            // run of (block b, half h, shift j, segment seg)
+            const int run = active ? 16 * b + 8 * h + 2 * j + seg : 0;
+            s.r[j] = planes[run];
+            X[j] = active ? run_sum[run] : 0.f;
+            s.inv[j] = active ? run_inv[run] * ((j & 1) ? 0.25f : 1.f) : 0.f;
+        }
+        quantize_run_sums(X, s);
     }
 
     const int lane = tid & 31;
