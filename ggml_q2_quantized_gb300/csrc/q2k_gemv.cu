@@ -63,7 +63,12 @@ struct RunPlanes {
     uint32_t p0[4], p1[4], p2[4];
 };
 
-__device__ __forceinline__ void convert_run(const float* __restrict__ xr, RunPlanes* planes,
+// Shared-memory home of the planes: the 4 runs of slice sl (its 48 words,
+// run j's planes at 12 j) start at word kSlicePitch * sl; the odd pitch puts
+// the 32 slices a warp reads at once in 32 different banks.
+constexpr int kSlicePitch = 49;
+
+__device__ __forceinline__ void convert_run(const float* __restrict__ xr, uint32_t* planes,
                                             float* run_sum, float* run_inv) {
     float v[16];
 #pragma unroll
@@ -104,7 +109,12 @@ __device__ __forceinline__ void convert_run(const float* __restrict__ xr, RunPla
         pl.p1[q] = b1;
         pl.p2[q] = b2;
     }
-    *planes = pl;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        planes[q] = pl.p0[q];
+        planes[4 + q] = pl.p1[q];
+        planes[8 + q] = pl.p2[q];
+    }
     *run_sum = sum;
     *run_inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
 }
@@ -264,11 +274,12 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     const int warps_per_group = slices_pad >> 5;
     // shared layout: W chunk | run planes | run sums | run scales | red | bars | flag
     const size_t w_smem = (static_cast<size_t>(rows_per_cta) * row_bytes + 15) & ~size_t(15);
-    RunPlanes* planes = reinterpret_cast<RunPlanes*>(smem + w_smem);
-    float* run_sum = reinterpret_cast<float*>(planes + n_runs);
+    uint32_t* planes = reinterpret_cast<uint32_t*>(smem + w_smem);
+    float* run_sum = reinterpret_cast<float*>(planes + (n_runs >> 2) * kSlicePitch);
     float* run_inv = run_sum + n_runs;
     float* red = run_inv + n_runs;
-    const size_t red_end = w_smem + static_cast<size_t>(n_runs) * (sizeof(RunPlanes) + 8) +
+    const size_t red_end = w_smem + static_cast<size_t>(n_runs >> 2) * kSlicePitch * 4 +
+                           static_cast<size_t>(n_runs) * 8 +
                            static_cast<size_t>(rows_per_cta) * warps_per_group * 4;
     const size_t bar_off = (red_end + 7) & ~size_t(7);
     const uint32_t bars = smem_u32(smem + bar_off);
@@ -305,8 +316,12 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     if (issuer && !const_weights)
         issue_weight_copies(smem, gsrc, bars, rows, row_bytes, tid >> 5, nwarps);
     // x -> integer planes, once per CTA, while the weights stream in
-    for (int r = tid; r < n_runs; r += nthreads)
-        convert_run(x + 16 * r, &planes[r], &run_sum[r], &run_inv[r]);
+    for (int r = tid; r < n_runs; r += nthreads) {
+        // run r = (block, half, shift j, segment): slice 4 block + 2 half + segment
+        const int slr = ((r >> 4) << 2) | (((r >> 3) & 1) << 1) | (r & 1);
+        convert_run(x + 16 * r, planes + slr * kSlicePitch + 12 * ((r >> 1) & 3), &run_sum[r],
+                    &run_inv[r]);
+    }
     __syncthreads();
 
     const int g = tid / slices_pad;
@@ -321,7 +336,13 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
         for (int j = 0; j < 4; ++j) {
             // run of (block b, half h, shift j, segment seg)
             const int run = active ? 16 * b + 8 * h + 2 * j + seg : 0;
-            s.r[j] = planes[run];
+            const uint32_t* pj = planes + (active ? sl : 0) * kSlicePitch + 12 * j;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                s.r[j].p0[q] = pj[q];
+                s.r[j].p1[q] = pj[4 + q];
+                s.r[j].p2[q] = pj[8 + q];
+            }
             X[j] = active ? run_sum[run] : 0.f;
             s.inv[j] = active ? run_inv[run] * ((j & 1) ? 0.25f : 1.f) : 0.f;
         }
@@ -386,8 +407,8 @@ size_t m1_smem(int rows, int K, int slices_pad) {
     const int n_runs = K / 16;
     const int pieces = (rows + kPieceRows - 1) / kPieceRows;
     const size_t w_smem = (static_cast<size_t>(rows) * row_bytes + 15) & ~size_t(15);
-    const size_t red_end = w_smem + static_cast<size_t>(n_runs) * (sizeof(RunPlanes) + 8) +
-                           static_cast<size_t>(rows) * (slices_pad / 32) * 4;
+    const size_t red_end = w_smem + static_cast<size_t>(n_runs / 4) * kSlicePitch * 4 +
+                           static_cast<size_t>(n_runs) * 8 + static_cast<size_t>(rows) * (slices_pad / 32) * 4;
     return ((red_end + 7) & ~size_t(7)) + 8 * pieces + 16;
 }
 
