@@ -255,7 +255,7 @@ __device__ __forceinline__ void issue_weight_copies(uint8_t* smem, const uint8_t
     }
 }
 
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(256, 1)
 gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
                int N, int K, int rows_per_cta, int slices_pad, int groups, uint32_t flags) {
     const bool independent = (flags & kGemvIndependent) != 0;
@@ -322,6 +322,15 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
         convert_run(x + 16 * r, planes + slr * kSlicePitch + 12 * ((r >> 1) & 3), &run_sum[r],
                     &run_inv[r]);
     }
+    // With the copies issued before the dependency wait they have (nearly)
+    // landed by now: one thread waits for all of them, and the barrier below
+    // publishes that, so the row loop needs no barrier polls of its own.
+    bool all_ok = true;
+    if (const_weights && tid == 0) {
+        for (int p = 0; p < n_pieces; ++p)
+            all_ok = all_ok && mbar_wait_backoff(bars + 8 * p, 0, abort_flag, &g_gemv_error,
+                                                 kErrTimeoutGemv, 64);
+    }
     __syncthreads();
 
     const int g = tid / slices_pad;
@@ -352,31 +361,38 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     const int lane = tid & 31;
     const int wig = sl >> 5;  // warp index within the group
     const uint8_t* my_col = smem + b * kBlockBytes;
-    int waited = -1;
-    bool ok = true;
-    for (int base = g; base < rows; base += groups * kRowBatch) {
+    int waited = const_weights ? n_pieces - 1 : -1;
+    bool ok = !(const_weights && *abort_flag);
+    constexpr int kLoad = 2 * kRowBatch;  // rows loaded and decoded together
+    for (int base = g; base < rows; base += groups * kLoad) {
         // Make sure every piece this batch touches has landed, then issue all
         // shared-memory loads of the batch before any arithmetic.
-        const int last = min(rows - 1, base + (kRowBatch - 1) * groups);
+        const int last = min(rows - 1, base + (kLoad - 1) * groups);
         for (int pw = waited + 1; pw <= last / kPieceRows; ++pw)
             ok = ok && mbar_wait_backoff(bars + 8 * pw, 0, abort_flag, &g_gemv_error, kErrTimeoutGemv, 64);
         waited = max(waited, last / kPieceRows);
-        RowWords rw[kRowBatch];
+        RowWords rw[kLoad];
 #pragma unroll
-        for (int u = 0; u < kRowBatch; ++u) {
+        for (int u = 0; u < kLoad; ++u) {
             const int lr = min(base + u * groups, last);
             rw[u] = load_row_words(my_col + static_cast<size_t>(lr) * row_bytes, h, seg, ssel);
         }
-        float part[kRowBatch];
+        float part[kLoad];
 #pragma unroll
-        for (int u = 0; u < kRowBatch; ++u) {
+        for (int u = 0; u < kLoad; ++u) {
             const float v = slice_dot(rw[u], s);
             part[u] = (active && ok && base + u * groups < rows) ? v : 0.f;
         }
-        int which;
-        const float tot = transpose_reduce4(part, lane, &which);
-        const int lr = base + which * groups;
-        if ((lane & 7) == 0 && lr < rows) red[lr * warps_per_group + wig] = tot;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            float p4[kRowBatch];
+#pragma unroll
+            for (int u = 0; u < kRowBatch; ++u) p4[u] = part[hb * kRowBatch + u];
+            int which;
+            const float tot = transpose_reduce4(p4, lane, &which);
+            const int lr = base + (hb * kRowBatch + which) * groups;
+            if ((lane & 7) == 0 && lr < rows) red[lr * warps_per_group + wig] = tot;
+        }
     }
     __syncthreads();
     for (int lr = tid; lr < rows; lr += nthreads) {
