@@ -4,9 +4,14 @@
 Headline workload (``--workload decode_gemv_4096``): the decode GEMV
 y = W x with M=1, N=K=4096 (5,505,024 bytes of Q2_K weights per matrix), x f32
 ~ N(0,1).  One step streams L distinct seeded weight matrices of that shape
-(a stack of L projection layers, L chosen so the stack is at least 3x the L2
-cache, so no weight byte is served from L2) through one ``q2k_matmul`` launch
-each; the launches are captured once in a CUDA graph and replayed.
+(L chosen so they are at least 3x the L2 cache, so no weight byte is served
+from L2) through one ``q2k_matmul`` launch each: L projections of one
+activation x, each with its own W and y, so every call carries
+Q2K_FLAG_INDEPENDENT (no call reads or writes what another writes) and
+consecutive launches overlap.  The launches are captured once in a CUDA graph
+and replayed.  ``secondary.decode_gemv_4096_dependent_chain`` times the same
+matrices as a chain (each call's x is the previous call's y), where every
+launch waits for the one before it.
 
 ``value``     weight bytes of all ranks / max-over-ranks step time (GB/s)
 ``roofline``  the dominant kernel (the GEMV): algorithmic bytes per launch
@@ -211,8 +216,9 @@ def capture(torch, stream, fn):
 
 
 def bench_matmul(torch, q2k, w: wl.Workload, steps, warmup, l2_bytes, device, with_e2e=False,
-                 path="auto"):
-    """Time a stack of distinct weight matrices of workload ``w`` (one launch each)."""
+                 path="auto", independent=False):
+    """Time a stack of distinct weight matrices of workload ``w`` (one launch each),
+    all applied to the same x (independent projections when ``independent``)."""
     inp = wl.make_inputs(w, with_gather=False)
     layers = layers_for(w.weight_bytes, l2_bytes)
     ws = [torch.from_numpy(a).to(device) for a in stack_of_weights(w, layers, inp.w)]
@@ -222,7 +228,7 @@ def bench_matmul(torch, q2k, w: wl.Workload, steps, warmup, l2_bytes, device, wi
 
     def step():
         for l in range(layers):
-            q2k.matmul(x, ws[l], w.n, out=ys[l], path=path)
+            q2k.matmul(x, ws[l], w.n, out=ys[l], path=path, independent=independent)
 
     g = capture(torch, stream, step)
     ms = time_graph(torch, g, stream, steps, warmup)
@@ -250,6 +256,28 @@ def bench_matmul(torch, q2k, w: wl.Workload, steps, warmup, l2_bytes, device, wi
         res["h2d_bytes_per_step"] = x_host.numel() * 4
         res["d2h_bytes_per_step"] = y_host.numel() * 4
     return res
+
+
+def bench_chain(torch, q2k, w: wl.Workload, steps, warmup, l2_bytes, device):
+    """The stack as a dependent chain (N = K): x of call l + 1 is y of call l."""
+    assert w.m == 1 and w.n == w.k
+    inp = wl.make_inputs(w, with_gather=False)
+    layers = layers_for(w.weight_bytes, l2_bytes)
+    ws = [torch.from_numpy(a).to(device) for a in stack_of_weights(w, layers, inp.w)]
+    acts = torch.empty((layers + 1, 1, w.k), dtype=torch.float32, device=device)
+    acts[0].copy_(torch.from_numpy(inp.x))
+    stream = torch.cuda.Stream(device)
+
+    def step():
+        for l in range(layers):
+            q2k.matmul(acts[l], ws[l], w.n, out=acts[l + 1], const_weights=True)
+
+    g = capture(torch, stream, step)
+    ms = time_graph(torch, g, stream, steps, warmup)
+    us = ms * 1e3 / layers
+    return {"us_per_call": us, "weight_GBps": w.weight_bytes / (us * 1e-6) / 1e9,
+            "m": 1, "n": w.n, "k": w.k, "path": "gemv", "matrices_per_step": layers,
+            "calls": "each call's x is the previous call's y (Q2K_FLAG_CONST_WEIGHTS)"}
 
 
 def bench_gather(torch, q2k, w: wl.Workload, steps, warmup, device):
@@ -362,9 +390,11 @@ def run_ours(args):
     ys = torch.empty((layers, w.m, w.n), dtype=torch.float32, device=device)
     stream = torch.cuda.Stream(device)
 
+    indep = w.m == 1
+
     def step():
         for l in range(layers):
-            q2k.matmul(x, ws[l], w.n, out=ys[l])
+            q2k.matmul(x, ws[l], w.n, out=ys[l], independent=indep)
 
     graph = capture(torch, stream, step)
     for _ in range(warmup):
@@ -406,6 +436,8 @@ def run_ours(args):
                                 f"({bytes_per_step / 2**20:.0f} MiB) per step vs "
                                 f"{l2_bytes / 2**20:.0f} MiB L2",
                    "timing": "CUDA graph of the step's launches, CUDA events on the replay stream",
+                   "calls": ("independent projections of one x (Q2K_FLAG_INDEPENDENT)" if indep
+                             else "one launch per matrix"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "us_per_call": launch_us,
         "gpu_launches": steps * layers,
@@ -422,21 +454,23 @@ def run_ours(args):
     line["clocks"] = clk.summary()
 
     # ---- e2e through the public API (eager), host buffers, copies inside the region
-    e2e = bench_matmul(torch, q2k, w, steps, warmup, l2_bytes, device, with_e2e=True)
+    e2e = bench_matmul(torch, q2k, w, steps, warmup, l2_bytes, device, with_e2e=True,
+                       independent=indep)
     line["e2e"] = {"value": world * bytes_per_step / (e2e["e2e_ms_per_step"] * 1e-3) / 1e9,
                    "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
                    "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
                    "ms_per_step": e2e["e2e_ms_per_step"],
-                   "how": "eager Python API calls (one q2k.matmul per weight matrix) with the "
-                          "activations copied from pinned host memory and all outputs copied "
-                          "back each step"}
+                   "how": "eager Python API calls (one q2k.matmul per weight matrix, as the "
+                          "headline) with the activations copied from pinned host memory and "
+                          "all outputs copied back each step"}
 
     # ---- secondary workloads (not the headline; reported for the metric's M=512 half)
     if not args.no_secondary:
         sec = {}
         for name in ("ffn_pair", "ffn_pair_down", "spec_verify_m16", "prefill_m512"):
             sw = wl.by_name(name)
-            r = bench_matmul(torch, q2k, sw, max(3, steps // 4), 3, l2_bytes, device)
+            r = bench_matmul(torch, q2k, sw, max(3, steps // 4), 3, l2_bytes, device,
+                             independent=sw.m == 1)
             us = r["us_per_call"]
             entry = {"us_per_call": us, "weight_GBps": sw.weight_bytes / (us * 1e-6) / 1e9,
                      "TFLOPs": sw.flops / (us * 1e-6) / 1e12, "m": sw.m, "n": sw.n, "k": sw.k,
@@ -454,6 +488,9 @@ def run_ours(args):
             "us_per_call": us, "weight_GBps": sw.weight_bytes / (us * 1e-6) / 1e9,
             "TFLOPs": sw.flops / (us * 1e-6) / 1e12, "m": sw.m, "n": sw.n, "k": sw.k,
             "path": "gemv", "matrices_per_step": r["layers"]}
+        if w.m == 1 and w.n == w.k:
+            sec[f"{w.name}_dependent_chain"] = bench_chain(torch, q2k, w, max(3, steps // 4), 3,
+                                                           l2_bytes, device)
         sec["spec_verify_gather"] = bench_gather(torch, q2k, wl.by_name("spec_verify_m16"),
                                                  max(3, steps // 4), 3, device)
         line["secondary"] = sec
