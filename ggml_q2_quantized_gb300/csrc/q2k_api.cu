@@ -192,9 +192,9 @@ size_t q2k_matmul_workspace_bytes(const q2k_matmul_params* p, q2k_path path) {
         return 0;
     if (path == Q2K_PATH_AUTO) path = p->m <= 8 ? Q2K_PATH_GEMV : Q2K_PATH_TENSOR;
     if (path != Q2K_PATH_TENSOR) return 0;
-    const size_t m_pad = (static_cast<size_t>(p->m) + 127) / 128 * 128;
+    const size_t m_pad = (static_cast<size_t>(p->m) + 255) / 256 * 256;
     if (m_pad > SIZE_MAX / 2 / p->k) return 0;
-    return q2k::gemm_tc_workspace_bytes(int(p->m), int(p->k));
+    return q2k::gemm_tc_workspace_bytes(int(p->m), int(p->n), int(p->k));
 }
 
 q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float* x, size_t x_elems,
@@ -211,7 +211,7 @@ q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float* x, size_t x
     if (path == Q2K_PATH_AUTO) path = p->m <= 8 ? Q2K_PATH_GEMV : Q2K_PATH_TENSOR;
     void* ws = nullptr;
     if (workspace != nullptr && path == Q2K_PATH_TENSOR) {
-        const size_t need = q2k::gemm_tc_workspace_bytes(int(p->m), int(p->k));
+        const size_t need = q2k::gemm_tc_workspace_bytes(int(p->m), int(p->n), int(p->k));
         if (workspace_bytes < need)
             return fail(Q2K_ERR_INVALID_ARGUMENT, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
         if (!aligned(workspace, 16))
@@ -258,12 +258,12 @@ q2k_status q2k_matmul_static_workspace(const float* x, size_t x_elems, const voi
     g_last_error[0] = '\0';
     q2k_status st = check_matmul(x, x_elems, w, w_bytes, y, y_elems, p);
     if (st != Q2K_OK) return st;
-    const size_t need = q2k::gemm_tc_workspace_bytes(int(p->m), int(p->k));
+    const size_t need = q2k::gemm_tc_workspace_bytes(int(p->m), int(p->n), int(p->k));
     if (need > q2k::kStaticWorkspaceBytes)
         return fail(Q2K_ERR_INVALID_ARGUMENT,
-                    "m = %u, k = %u needs %zu bytes of scratch; the library's fixed scratch holds %zu "
-                    "(ceil(m/256)*256 * k <= %zu)",
-                    p->m, p->k, need, q2k::kStaticWorkspaceBytes, q2k::kStaticWorkspaceBytes / 2);
+                    "m = %u, n = %u, k = %u needs %zu bytes of scratch; the library's fixed scratch "
+                    "holds %zu",
+                    p->m, p->n, p->k, need, q2k::kStaticWorkspaceBytes);
     DeviceInfo dev;
     st = current_device(&dev);
     if (st != Q2K_OK) return st;

@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -734,7 +735,8 @@ __device__ __forceinline__ void wt_issue_raw(const uint8_t* __restrict__ w, uint
 template <int kXRows, bool kTmaW>
 __global__ void __launch_bounds__(WtCfg<kXRows, kTmaW>::kThreads, 1)
 gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
-               float* __restrict__ y, int M, int N, int K, const __grid_constant__ CUtensorMap tmap_w) {
+               float* __restrict__ y, float* __restrict__ partial, int M, int N, int K,
+               const __grid_constant__ CUtensorMap tmap_w) {
     using C = WtCfg<kXRows, kTmaW>;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -745,9 +747,15 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
     const int n0 = blockIdx.x * C::kRows;
     const int m0 = blockIdx.y * kXRows;
     const int nx = min(kXRows, (M - m0 + 15) & ~15);  // MMA N: this tile's x rows, padded to 16
-    const int n_iters = K / kKS;
     const int blocks_per_row = K / kQK;
     const size_t row_bytes = static_cast<size_t>(blocks_per_row) * kBlockBytes;
+    // K split (gridDim.z parts): this CTA's blocks [kb0, kb0 + n_blocks) of each
+    // row; loop indices below are relative to kb0 unless named otherwise
+    const int kb0 = static_cast<int>(static_cast<long>(blockIdx.z) * blocks_per_row / gridDim.z);
+    const int n_blocks =
+        static_cast<int>(static_cast<long>(blockIdx.z + 1) * blocks_per_row / gridDim.z) - kb0;
+    const int n_iters = 4 * n_blocks;  // 64-K stages
+    const int n_stages_row = K / kKS;  // stages of a whole row (x image layout)
 
     const uint32_t bar_xfull = sbase + C::kOffBar;
     const uint32_t bar_xempty = bar_xfull + 8 * C::kXStages;
@@ -814,15 +822,15 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
                     bulk_prefetch_l2(reinterpret_cast<const void*>(a), static_cast<uint32_t>(e - a));
             }
             for (int pb = 0; pb < C::kRaw - 1; ++pb) {
-                if (pb < blocks_per_row)
+                if (pb < n_blocks)
                     wt_issue_raw<C::kRows, C::kDecThreads>(w, raw0 + pb * C::kRawBytes, n0, N,
-                                                           row_bytes, pb, td);
+                                                           row_bytes, kb0 + pb, td);
                 else
                     cp_async_commit();
             }
         }
         bool ok = true;
-        for (int b = 0; b < blocks_per_row && ok; ++b) {
+        for (int b = 0; b < n_blocks && ok; ++b) {
             const int buf = b % C::kRaw;
             uint32_t mine;
             if constexpr (kTmaW) {
@@ -831,7 +839,7 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
                     ok = false;
                     break;
                 }
-                mine = raw0 + buf * C::kRawBytes + row * C::kRawPitch + 4 * (b & 3);
+                mine = raw0 + buf * C::kRawBytes + row * C::kRawPitch + 4 * ((kb0 + b) & 3);
             } else {
                 cp_async_wait_group<C::kRaw - 2>();
                 __syncwarp();
@@ -844,9 +852,9 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
                 // Every decoder has read block b - 1's slab (it arrived for block
                 // b above): block b + kRaw - 1 goes there.
                 const int nb = b + C::kRaw - 1;
-                if (nb < blocks_per_row)
+                if (nb < n_blocks)
                     wt_issue_raw<C::kRows, C::kDecThreads>(w, raw0 + (nb % C::kRaw) * C::kRawBytes,
-                                                           n0, N, row_bytes, nb, td);
+                                                           n0, N, row_bytes, kb0 + nb, td);
                 else
                     cp_async_commit();
                 mine = raw0 + buf * C::kRawBytes + row * kBlockBytes;
@@ -915,11 +923,14 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
             for (int c0 = 16 * (warp >> 2); c0 < nx; c0 += 64) {
                 uint32_t v[16];
                 tmem_ld16(t_row + c0, v);
+                // one K part alone goes to y; parts of a split go to their own
+                // slice of the partial buffer, summed in order afterwards
+                float* out = gridDim.z == 1 ? y : partial + static_cast<size_t>(blockIdx.z) * M * N;
                 if (n < N) {
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
                         const int m = m0 + c0 + q;
-                        if (m < M) y[static_cast<size_t>(m) * N + n] = __uint_as_float(v[q]);
+                        if (m < M) out[static_cast<size_t>(m) * N + n] = __uint_as_float(v[q]);
                     }
                 }
             }
@@ -993,15 +1004,16 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w))
                          : "memory");
             const uint32_t raw0 = sbase + C::kOffRaw;
-            for (int b = 0; b < blocks_per_row; ++b) {
+            for (int b = 0; b < n_blocks; ++b) {
                 const int buf = b % C::kRaw;
                 if (b >= C::kRaw &&
                     !mbar_wait_lean(bar_rawempty + 8 * buf, ((b / C::kRaw) - 1) & 1, abort_flag,
                                     err, kErrTimeoutEmpty, 128))
                     break;
                 mbar_arrive_expect_tx(bar_raw + 8 * buf, C::kRawBytes);
-                // x: the 16-byte boundary at or below block b (84 b - 4 (b % 4))
-                tma_load_2d(raw0 + buf * C::kRawBytes, &tmap_w, (kBlockBytes * b) & ~15, n0,
+                // x: the 16-byte boundary at or below row block kb0 + b
+                // (84 (kb0 + b) - 4 ((kb0 + b) % 4))
+                tma_load_2d(raw0 + buf * C::kRawBytes, &tmap_w, (kBlockBytes * (kb0 + b)) & ~15, n0,
                             bar_raw + 8 * buf);
             }
             if (*abort_flag) {
@@ -1016,8 +1028,11 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
         if (lane == 0) {
             // This tile's rows of super-tile m0 / 256 (the second 128 of them when
             // the tile starts half-way into it); a whole super-tile stage when
-            // kXRows is 256 (the rows past M are zeros in the image).
-            const uint8_t* src = xa + static_cast<size_t>(m0 / kXSuperRows) * n_iters * kXSuperBytes +
+            // kXRows is 256.  Image rows past M are never written: they feed only
+            // the accumulator columns of x rows >= M, which the epilogue drops.
+            const uint8_t* src = xa +
+                                 (static_cast<size_t>(m0 / kXSuperRows) * n_stages_row + 4 * kb0) *
+                                     kXSuperBytes +
                                  static_cast<size_t>(m0 % kXSuperRows) * (kKS * 2);
             const uint32_t bytes = kXRows == kXSuperRows ? static_cast<uint32_t>(kXSuperBytes)
                                                          : static_cast<uint32_t>(nx) * (kKS * 2);
@@ -1152,8 +1167,9 @@ bool make_weight_map(CUtensorMap* map, const uint8_t* w, int N, int K, int rows)
 }
 
 template <int kXRows, bool kTmaW>
-cudaError_t launch_wt_kernel(const uint8_t* xa, const uint8_t* w, float* y, int M, int N, int K,
-                             int device, const CUtensorMap& map, cudaStream_t stream) {
+cudaError_t launch_wt_kernel(const uint8_t* xa, const uint8_t* w, float* y, float* partial,
+                             int splits, int M, int N, int K, int device, const CUtensorMap& map,
+                             cudaStream_t stream) {
     using C = WtCfg<kXRows, kTmaW>;
     static bool attr_done[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
@@ -1165,7 +1181,7 @@ cudaError_t launch_wt_kernel(const uint8_t* xa, const uint8_t* w, float* y, int 
         attr_done[device] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((N + C::kRows - 1) / C::kRows, (M + kXRows - 1) / kXRows);
+    cfg.gridDim = dim3((N + C::kRows - 1) / C::kRows, (M + kXRows - 1) / kXRows, splits);
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
@@ -1174,17 +1190,42 @@ cudaError_t launch_wt_kernel(const uint8_t* xa, const uint8_t* w, float* y, int 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_wt_kernel<kXRows, kTmaW>, xa, w, y, M, N, K, map);
+    return cudaLaunchKernelEx(&cfg, gemm_wt_kernel<kXRows, kTmaW>, xa, w, y, partial, M, N, K, map);
 }
 
 template <int kXRows>
-cudaError_t launch_wt(const uint8_t* xa, const uint8_t* w, float* y, int M, int N, int K,
-                      int device, cudaStream_t stream) {
+cudaError_t launch_wt(const uint8_t* xa, const uint8_t* w, float* y, float* partial, int splits,
+                      int M, int N, int K, int device, cudaStream_t stream) {
     alignas(64) CUtensorMap map;
     if (make_weight_map(&map, w, N, K, 128))
-        return launch_wt_kernel<kXRows, true>(xa, w, y, M, N, K, device, map, stream);
+        return launch_wt_kernel<kXRows, true>(xa, w, y, partial, splits, M, N, K, device, map,
+                                              stream);
     memset(&map, 0, sizeof(map));
-    return launch_wt_kernel<kXRows, false>(xa, w, y, M, N, K, device, map, stream);
+    return launch_wt_kernel<kXRows, false>(xa, w, y, partial, splits, M, N, K, device, map, stream);
+}
+
+// y = the K parts summed in a fixed order (bit-reproducible).
+__global__ void __launch_bounds__(256)
+sum_k_parts_kernel(const float* __restrict__ partial, float* __restrict__ y, size_t mn, int parts) {
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < mn;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        float v = partial[i];
+        for (int p = 1; p < parts; ++p) v += partial[static_cast<size_t>(p) * mn + i];
+        y[i] = v;
+    }
+}
+
+// K parts of the weights-as-A kernel: with fewer than 64 weight tiles (small m
+// and n) the GPU would sit mostly idle, so each row's K blocks are split into
+// up to 8 parts (about 128 CTAs), each part's accumulator written to its own
+// slice of a partial buffer and the parts summed afterwards.  Depends only on
+// the geometry, so a workspace sized for it fits every device.
+int wt_splits(int M, int N, int K) {
+    if (M > 128) return 1;
+    const long tiles = (N + 127) / 128;
+    const int bpr = K / kQK;
+    if (tiles >= 64 || bpr < 2) return 1;
+    return static_cast<int>(std::max(1L, std::min<long>(128 / tiles, std::min(8, bpr))));
 }
 
 // x rows per CTA of the weights-as-A kernel: 256 (each decoded weight feeds
@@ -1216,9 +1257,17 @@ int choose_bn(int M, int N, int sm_count) {
 
 }  // namespace
 
-size_t gemm_tc_workspace_bytes(int M, int K) {
+// x image (m rows padded to 256-row super-tiles) then, when K is split, the
+// partial buffer (parts x m x n f32) at the next 256-byte boundary.
+static size_t image_bytes(int M, int K) {
     const size_t m_pad = static_cast<size_t>((M + kXSuperRows - 1) / kXSuperRows) * kXSuperRows;
     return m_pad * static_cast<size_t>(K) * 2;
+}
+
+size_t gemm_tc_workspace_bytes(int M, int N, int K) {
+    const int splits = wt_splits(M, N, K);
+    const size_t img = (image_bytes(M, K) + 255) & ~size_t(255);
+    return splits > 1 ? img + static_cast<size_t>(splits) * M * N * 4 : image_bytes(M, K);
 }
 
 cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, int N, int K,
@@ -1227,21 +1276,34 @@ cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, in
     if (workspace == nullptr)
         return launch_width<false>(bn, x, nullptr, w, y, M, N, K, device, stream);
     uint8_t* xa = static_cast<uint8_t*>(workspace);
-    const size_t n_chunks = gemm_tc_workspace_bytes(M, K) / 16;
+    // only x's own rows: the image's padding rows are never read into a kept output
+    const size_t n_chunks = static_cast<size_t>(M) * (K / 8);
     size_t blocks = (n_chunks + 255) / 256;
     const size_t cap = static_cast<size_t>(sm_count) * 4;
     if (blocks > cap) blocks = cap;
     x_to_bf16_tiles_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, xa, M, K, n_chunks);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (choose_wt_xrows(M, N, sm_count) == 256) return launch_wt<256>(xa, w, y, M, N, K, device, stream);
-    return launch_wt<128>(xa, w, y, M, N, K, device, stream);
+    const int splits = wt_splits(M, N, K);
+    float* partial = splits > 1 ? reinterpret_cast<float*>(
+                                      xa + ((image_bytes(M, K) + 255) & ~size_t(255)))
+                                : nullptr;
+    if (choose_wt_xrows(M, N, sm_count) == 256)
+        e = launch_wt<256>(xa, w, y, partial, splits, M, N, K, device, stream);
+    else
+        e = launch_wt<128>(xa, w, y, partial, splits, M, N, K, device, stream);
+    if (e != cudaSuccess || splits == 1) return e;
+    const size_t mn = static_cast<size_t>(M) * N;
+    size_t sb = (mn + 255) / 256;
+    if (sb > static_cast<size_t>(sm_count) * 4) sb = static_cast<size_t>(sm_count) * 4;
+    sum_k_parts_kernel<<<static_cast<unsigned>(sb), 256, 0, stream>>>(partial, y, mn, splits);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_tc_static(const float* x, const uint8_t* w, float* y, int M, int N, int K,
                                   int device, int sm_count, cudaStream_t stream) {
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-    if (gemm_tc_workspace_bytes(M, K) > kStaticWorkspaceBytes) return cudaErrorInvalidValue;
+    if (gemm_tc_workspace_bytes(M, N, K) > kStaticWorkspaceBytes) return cudaErrorInvalidValue;
     // In host code the array's name is only a stand-in: its device address is
     // looked up once per device, with that device current (the caller's).
     static std::once_flag once[64];

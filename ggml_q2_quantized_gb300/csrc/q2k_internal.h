@@ -29,11 +29,12 @@ cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N
 // Read and clear the GEMV kernels' device error word (synchronises `stream`).
 cudaError_t read_and_clear_gemv_error(uint32_t* out, cudaStream_t stream);
 
-// Bytes of the x bf16 tile image the tensor-core path uses when given a workspace.
-size_t gemm_tc_workspace_bytes(int M, int K);
+// Bytes of workspace the tensor-core path uses when given one: the x bf16 tile
+// image, plus a buffer of per-part results when K is split (small m and n).
+size_t gemm_tc_workspace_bytes(int M, int N, int K);
 
 // bf16 tcgen05 GEMM; `device` selects per-device one-time setup.  With a
-// workspace of gemm_tc_workspace_bytes(M, K) bytes (16-byte aligned), x is first
+// workspace of gemm_tc_workspace_bytes(M, N, K) bytes (16-byte aligned), x is first
 // converted to the bf16 tile image there and the GEMM copies A stages in bulk;
 // with workspace == nullptr the GEMM converts x itself.
 cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, int N, int K,

@@ -158,8 +158,12 @@ enum {
 
 /* q2k_matmul_workspace_bytes - device bytes of workspace q2k_matmul_ex can use
  * for this geometry and path (0: the path takes none).  The tensor-core path
- * stores x there as bf16 in the tile layout its shared memory uses:
- * ceil(m / 256) * 256 * k * 2 bytes.  Returns 0 for invalid params. */
+ * stores x there as bf16 in the tile layout its shared memory uses,
+ * ceil(m / 256) * 256 * k * 2 bytes; when m <= 128 and n is small (fewer than
+ * 64 tiles of 128 weight rows) it splits K into P parts (P <= 8, fixed by m, n
+ * and k) and adds P * m * n * 4 bytes (after 256-byte alignment) for the
+ * parts' results, which are then summed in a fixed order.  Returns 0 for
+ * invalid params. */
 size_t q2k_matmul_workspace_bytes(const q2k_matmul_params *params, q2k_path path);
 
 /* q2k_matmul_ex - q2k_matmul_path plus `flags` (a mask of Q2K_FLAG_*; unknown
@@ -188,16 +192,16 @@ q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float *x, size_t x
  *   The x tile image normally kept in a caller workspace goes into a fixed
  *   array inside the library instead, Q2K_STATIC_WORKSPACE_BYTES (8 MiB) on
  *   every GPU that loads the library, held until the process exits.  It fits
- *   ceil(m / 256) * 256 * k <= 4194304 (e.g. m = 512, k = 7168); larger
- *   geometries are rejected with Q2K_ERR_INVALID_ARGUMENT.
+ *   q2k_matmul_workspace_bytes(params, Q2K_PATH_TENSOR) <= 8 MiB (e.g. m = 512,
+ *   k = 7168); larger geometries are rejected with Q2K_ERR_INVALID_ARGUMENT.
  *   Nothing is allocated by the call.  The first call on a device looks up the
  *   array's device address (with that device current); make that first call
  *   before any stream capture.
  *   All calls share the one array: calls whose work may overlap on the GPU
  *   (different streams, different host threads without ordering) race on it
- *   and give wrong results; serialise them, e.g. on one stream.  Each call
- *   rewrites every byte of the array it reads, so leftovers of earlier calls
- *   do not matter.
+ *   and give wrong results; serialise them, e.g. on one stream.  Leftovers
+ *   of earlier calls do not matter: each call rewrites every byte whose value
+ *   reaches y (image rows past m are read but feed only dropped outputs).
  * Arguments, sizes, errors and tolerance (8e-3 * sum_k |x w|) as q2k_matmul. */
 enum { Q2K_STATIC_WORKSPACE_BYTES = 8388608 };
 q2k_status q2k_matmul_static_workspace(const float *x, size_t x_elems, const void *w,
