@@ -118,14 +118,48 @@ def _check(lib, status: int):
         raise Q2KError(status, msg)
 
 
+_torch_mod = None
+_raw_stream = None
+
+
 def _torch():
-    import torch
-    return torch
+    global _torch_mod, _raw_stream
+    if _torch_mod is None:
+        import torch
+        # the raw handle of a device's current stream without building a
+        # torch.cuda.Stream object (the per-call cost of the public accessor)
+        _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        _torch_mod = torch
+    return _torch_mod
 
 
 def _stream_handle(tensor) -> int:
     torch = _torch()
+    if _raw_stream is not None:
+        return _raw_stream(tensor.device.index)
     return torch.cuda.current_stream(tensor.device).cuda_stream
+
+
+class _on_device:
+    """``torch.cuda.device(t.device)`` only when it is not already current."""
+
+    __slots__ = ("idx", "prev")
+
+    def __init__(self, tensor):
+        self.idx = tensor.device.index
+        self.prev = None
+
+    def __enter__(self):
+        torch = _torch()
+        cur = torch.cuda.current_device()
+        if cur != self.idx:
+            self.prev = cur
+            torch.cuda.set_device(self.idx)
+        return self
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            _torch().cuda.set_device(self.prev)
 
 
 def _require_cuda(t, name, dtype):
@@ -147,7 +181,7 @@ def dequantize(blocks, out=None):
         out = torch.empty(max(n_out, 1), dtype=torch.float32, device=blocks.device)[:n_out]
     _require_cuda(out, "out", torch.float32)
     lib = load()
-    with torch.cuda.device(blocks.device):
+    with _on_device(blocks):
         _check(lib, lib.q2k_dequantize(blocks.data_ptr(), blocks.numel(), out.data_ptr(),
                                        out.numel(), _stream_handle(blocks)))
     return out
@@ -176,7 +210,7 @@ def embedding_gather(table, ids, embed_dim: int, vocab_size: int | None = None, 
     bad = torch.zeros(1, dtype=torch.int32, device=table.device)
     p = EmbeddingParams(vocab_size, embed_dim, n_tokens, GGML_TYPE_Q2_K)
     lib = load()
-    with torch.cuda.device(table.device):
+    with _on_device(table):
         _check(lib, lib.q2k_embedding_gather(table.data_ptr(), table.numel(), ids.data_ptr(),
                                              out.data_ptr(), out.numel(), ctypes.byref(p),
                                              bad.data_ptr(), _stream_handle(table)))
@@ -186,6 +220,9 @@ def embedding_gather(table, ids, embed_dim: int, vocab_size: int | None = None, 
     if n_bad:
         raise InvalidArgument(1, f"{n_bad} embedding id(s) >= vocab_size {vocab_size}")
     return out
+
+
+_ws_bytes_cache: dict = {}
 
 
 def matmul(x, w, n: int, out=None, path="auto", const_weights: bool = False,
@@ -211,22 +248,27 @@ def matmul(x, w, n: int, out=None, path="auto", const_weights: bool = False,
         out = torch.empty((m, n), dtype=torch.float32, device=x.device)
     _require_cuda(out, "out", torch.float32)
     p = MatmulParams(m, n, k, GGML_TYPE_Q2_K)
-    lib = load()
+    lib = _lib if _lib is not None else load()
+    pcode = _PATHS[path]
     ws_ptr, ws_bytes = None, 0
     if isinstance(workspace, str):
-        need = lib.q2k_matmul_workspace_bytes(ctypes.byref(p), _PATHS[path])
-        if need:
-            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
-        else:
+        # the GEMV path takes no workspace: skip the query for it
+        if pcode == PATH_GEMV or (pcode == PATH_AUTO and m <= 8):
             workspace = None
+        else:
+            key = (m, n, k, pcode)
+            need = _ws_bytes_cache.get(key)
+            if need is None:
+                need = lib.q2k_matmul_workspace_bytes(ctypes.byref(p), pcode)
+                _ws_bytes_cache[key] = need
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device) if need else None
     if workspace is not None:
         _require_cuda(workspace, "workspace", torch.uint8)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
-    with torch.cuda.device(x.device):
-        flags = (FLAG_CONST_WEIGHTS if const_weights else 0) | (FLAG_INDEPENDENT if independent else 0)
-        _check(lib, lib.q2k_matmul_ex(_PATHS[path], flags,
-                                      x.data_ptr(), x.numel(), w.data_ptr(), w.numel(),
-                                      out.data_ptr(), out.numel(), ctypes.byref(p),
+    flags = (FLAG_CONST_WEIGHTS if const_weights else 0) | (FLAG_INDEPENDENT if independent else 0)
+    with _on_device(x):
+        _check(lib, lib.q2k_matmul_ex(pcode, flags, x.data_ptr(), x.numel(), w.data_ptr(),
+                                      w.numel(), out.data_ptr(), out.numel(), ctypes.byref(p),
                                       ws_ptr, ws_bytes, _stream_handle(x)))
     return out
 
