@@ -428,15 +428,20 @@ size_t m1_smem(int rows, int K, int slices_pad) {
     return ((red_end + 7) & ~size_t(7)) + 8 * pieces + 16;
 }
 
-bool plan_m1(int N, int K, int sm_count, int threads, M1Plan* p) {
+bool plan_m1(int N, int K, int sm_count, int threads, bool whole_batches, M1Plan* p) {
     const int B = K / 256;
     const int S = K / 64;
     if (S > kM1MaxSlices) return false;
     const int slices_pad = (S + 31) / 32 * 32;
     const int groups = slices_pad >= threads ? 1 : threads / slices_pad;
+    // Rows per CTA a multiple of what one pass of the row loop covers (groups x
+    // 8 rows) when asked: the loop then never decodes a row twice at the end.
+    // Independent calls share the SMs, so fewer CTAs than SMs costs nothing there.
+    const int quantum = whole_batches ? groups * 2 * kRowBatch : 1;
     int rows = 0;
     for (int waves = 1;; ++waves) {
         rows = (N + sm_count * waves - 1) / (sm_count * waves);
+        rows = (rows + quantum - 1) / quantum * quantum;
         if (B % 4) rows = (rows + 3) / 4 * 4;  // chunk starts stay 16-byte aligned
         if (m1_smem(rows, K, slices_pad) <= 200 * 1024 || rows <= kPieceRows) break;
     }
@@ -571,7 +576,7 @@ cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N
     M1Plan plan;
     const int threads = (flags & kGemvIndependent) ? kM1ThreadsIndependent : kM1ThreadsDependent;
     if (M == 1 && (reinterpret_cast<uintptr_t>(w) & 15u) == 0 &&
-        plan_m1(N, K, sm_count, threads, &plan))
+        plan_m1(N, K, sm_count, threads, (flags & kGemvIndependent) != 0, &plan))
         return launch_m1(x, w, y, N, K, plan, device, flags, stream);
     switch (M < 8 ? M : 8) {
         case 1: return launch_rows<1>(x, w, y, M, N, K, stream);
