@@ -98,8 +98,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q2k_matmul_workspace_bytes.argtypes = [ctypes.POINTER(MatmulParams), ctypes.c_int]
         lib.q2k_matmul_workspace_bytes.restype = ctypes.c_size_t
         lib.q2k_device_error.argtypes = [u32p, vp]
+        lib.q2k_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         for fn in ("q2k_dequantize", "q2k_embedding_gather", "q2k_matmul", "q2k_matmul_path",
-                   "q2k_matmul_ex", "q2k_device_error"):
+                   "q2k_matmul_ex", "q2k_device_error", "q2k_selftest_wait_timeout"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.q2k_last_error.restype = ctypes.c_char_p
         lib.q2k_last_error.argtypes = []
@@ -271,6 +272,18 @@ def matmul(x, w, n: int, out=None, path="auto", const_weights: bool = False,
                                       w.numel(), out.data_ptr(), out.numel(), ctypes.byref(p),
                                       ws_ptr, ws_bytes, _stream_handle(x)))
     return out
+
+
+def selftest_wait_timeout(limit_us: int = 2000, device=None) -> None:
+    """Enqueue the library's bounded-wait self-test on the current stream: a kernel
+    waits ~limit_us on a barrier nothing completes, gives up and sets the time-out
+    bit that ``device_error()`` then returns."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    lib = load()
+    with torch.cuda.device(dev):
+        _check(lib, lib.q2k_selftest_wait_timeout(int(limit_us),
+                                                  torch.cuda.current_stream(dev).cuda_stream))
 
 
 def device_error(device=None) -> int:

@@ -273,6 +273,18 @@ q2k_status q2k_matmul_static_workspace(const float* x, size_t x_elems, const voi
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul_static_workspace launch");
 }
 
+q2k_status q2k_selftest_wait_timeout(uint32_t limit_us, q2k_stream_t stream) {
+    g_last_error[0] = '\0';
+    if (limit_us == 0 || limit_us > 100000)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "limit_us must be in 1..100000, got %u", limit_us);
+    DeviceInfo dev;
+    q2k_status st = current_device(&dev);
+    if (st != Q2K_OK) return st;
+    cudaError_t e = q2k::launch_wait_timeout_selftest(uint64_t(limit_us) * 1000u,
+                                                      reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_selftest_wait_timeout launch");
+}
+
 q2k_status q2k_device_error(uint32_t* out, q2k_stream_t stream) {
     g_last_error[0] = '\0';
     if (out == nullptr) return fail(Q2K_ERR_INVALID_ARGUMENT, "out is NULL");

@@ -590,6 +590,32 @@ cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N
     }
 }
 
+namespace {
+
+// One CTA waits on an mbarrier that nothing ever arrives at, with the bounded
+// wait every kernel of the library uses but a short limit: the wait must give
+// up, record kErrTimeoutGemv and return (no hang, no fault).
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ volatile int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        mbar_wait_lean(smem_u32(&bar), 0, &abort_flag, &g_gemv_error, kErrTimeoutGemv, 256, limit_ns);
+    __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_gemv_error(uint32_t* out, cudaStream_t stream) {
     unsigned int zero = 0;
     cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_gemv_error, sizeof(unsigned int), 0,

@@ -26,6 +26,10 @@ constexpr uint32_t kGemvIndependent = 2u;
 cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N, int K,
                         int device, int sm_count, uint32_t flags, cudaStream_t stream);
 
+// Self-test of the bounded wait: one CTA waits for about limit_ns on a barrier
+// nothing completes, then sets the GEMV error word's time-out bit.
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
+
 // Read and clear the GEMV kernels' device error word (synchronises `stream`).
 cudaError_t read_and_clear_gemv_error(uint32_t* out, cudaStream_t stream);
 

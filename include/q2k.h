@@ -208,6 +208,15 @@ q2k_status q2k_matmul_static_workspace(const float *x, size_t x_elems, const voi
                                        size_t w_bytes, float *y, size_t y_elems,
                                        const q2k_matmul_params *params, q2k_stream_t stream);
 
+/* q2k_selftest_wait_timeout - exercise the library's bounded on-chip wait
+ * (the pages have no counterpart: this library's own failure detection).
+ * Enqueues on `stream` one small kernel that waits on a barrier nothing
+ * completes, giving up after about limit_us microseconds (1..100000): it then
+ * sets the time-out bit of the device error word and returns, without
+ * faulting or hanging.  A following q2k_device_error reports that bit (and
+ * clears it).  Q2K_ERR_INVALID_ARGUMENT for a limit out of range. */
+q2k_status q2k_selftest_wait_timeout(uint32_t limit_us, q2k_stream_t stream);
+
 /* q2k_device_error - read and clear the library's device error word on the
  * current device.  Kernels that wait on on-chip barriers give up after about a
  * second, set a bit here and return instead of hanging.  Synchronises

@@ -142,3 +142,10 @@ def test_workspace_rejected_when_small_or_aliasing(lib):
     assert "workspace" in lib.q2k_last_error().decode()
     assert lib.q2k_matmul_ex(2, 0, *args, 0x2000008, need, None) == INVALID
     assert lib.q2k_matmul_ex(2, 0, *args, 0x10000, need, None) == INVALID   # over x
+
+
+def test_selftest_wait_timeout_rejects_out_of_range_limits(lib):
+    """Checked before any device work: 0 and > 100 ms are refused."""
+    for bad in (0, 100001):
+        assert lib.q2k_selftest_wait_timeout(bad, None) == INVALID
+        assert "limit_us" in lib.q2k_last_error().decode()

@@ -378,3 +378,24 @@ def test_independent_calls_complete_in_order_before_a_dependent_one():
             assert_close(got[:, i * n:(i + 1) * n], yref, s, TOL_GEMV, f"projection {i}")
         zref, s = oracle.matmul(got.astype(np.float32), w_next, 256, threads=ORACLE_THREADS)
         assert_close(z.cpu().numpy().astype(np.float64), zref, s, TOL_GEMV, f"consumer rep {rep}")
+
+
+def test_bounded_wait_times_out_and_reports_without_fault():
+    """The bounded wait every kernel uses, run against a barrier nothing completes:
+    it gives up after the limit, the host reads the time-out bit, the read clears
+    it, and the context keeps working (a matmul right after is still correct)."""
+    assert q2k.device_error() == 0
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    q2k.selftest_wait_timeout(2000)
+    t1.record()
+    torch.cuda.synchronize()
+    waited_ms = t0.elapsed_time(t1)
+    assert 1.5 <= waited_ms < 1000.0, waited_ms
+    assert q2k.device_error() == 16  # the GEMV time-out bit
+    assert q2k.device_error() == 0
+    x, w = wl.make_matmul_inputs(77, 1, 256, 1024)
+    y = q2k.matmul(dev(x), dev(w), 256)
+    yref, s = oracle.matmul(x, w, 256)
+    assert_close(y.cpu().numpy().astype(np.float64), yref, s, TOL_GEMV, "after time-out")
