@@ -597,6 +597,8 @@ constexpr int kTmaBoxBytes = 112;
 // K-major), super-tile (t, stage s) at (t * K/64 + s) * 32 KB.
 constexpr int kXSuperRows = 256;
 constexpr int kXSuperBytes = kXSuperRows * kKS * 2;
+// most K parts one weights-as-A grid splits a row's blocks into
+constexpr int kMaxKParts = 8;
 
 template <int kXRows, bool kTmaW>
 struct WtCfg {
@@ -735,7 +737,8 @@ __device__ __forceinline__ void wt_issue_raw(const uint8_t* __restrict__ w, uint
 template <int kXRows, bool kTmaW>
 __global__ void __launch_bounds__(WtCfg<kXRows, kTmaW>::kThreads, 1)
 gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
-               float* __restrict__ y, float* __restrict__ partial, int M, int N, int K,
+               float* __restrict__ y, float* __restrict__ partial,
+               unsigned int* __restrict__ tile_count, int M, int N, int K,
                const __grid_constant__ CUtensorMap tmap_w) {
     using C = WtCfg<kXRows, kTmaW>;
     extern __shared__ uint8_t smem_dyn[];
@@ -924,13 +927,66 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
                 uint32_t v[16];
                 tmem_ld16(t_row + c0, v);
                 // one K part alone goes to y; parts of a split go to their own
-                // slice of the partial buffer, summed in order afterwards
+                // slice of the partial buffer, summed in part order below
                 float* out = gridDim.z == 1 ? y : partial + static_cast<size_t>(blockIdx.z) * M * N;
                 if (n < N) {
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
                         const int m = m0 + c0 + q;
                         if (m < M) out[static_cast<size_t>(m) * N + n] = __uint_as_float(v[q]);
+                    }
+                }
+            }
+        }
+        if (gridDim.z > 1) {
+            // K split: every part has stored its slice; the part that arrives last
+            // at this tile's counter sums the slices in part order into y (no CTA
+            // ever waits for another).  The counter was zeroed by the grid before.
+            // The barrier orders every decoder thread's slice stores before one
+            // thread's device-scope fence and count (the release); that thread
+            // fences again after the count (the acquire) before the barrier that
+            // lets the others read.
+            volatile int* last = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+            asm volatile("bar.sync 2, %0;" ::"n"(C::kDecThreads) : "memory");
+            if (td == 0) {
+                __threadfence();
+                pdl_wait_prerequisites();
+                const unsigned prev = atomicAdd(&tile_count[blockIdx.y * gridDim.x + blockIdx.x], 1u);
+                __threadfence();
+                *last = prev == gridDim.z - 1 ? 1 : 0;
+            }
+            asm volatile("bar.sync 2, %0;" ::"n"(C::kDecThreads) : "memory");
+            if (*last) {
+                // all the loads of a pass are issued before any sum: one L2
+                // round trip per pass instead of one per part and element
+                constexpr int kMaxParts = kMaxKParts;
+                constexpr int kPer = 4;
+                const int parts = static_cast<int>(gridDim.z);
+                const size_t mn = static_cast<size_t>(M) * N;
+                const int total = C::kRows * nx;
+                for (int base = td; base < total; base += kPer * C::kDecThreads) {
+                    float v[kPer][kMaxParts];
+                    size_t off[kPer];
+                    bool ok[kPer];
+#pragma unroll
+                    for (int j = 0; j < kPer; ++j) {
+                        const int idx = base + j * C::kDecThreads;
+                        const int nn = n0 + (idx & (C::kRows - 1));
+                        const int mm = m0 + idx / C::kRows;
+                        ok[j] = idx < total && nn < N && mm < M;
+                        off[j] = ok[j] ? static_cast<size_t>(mm) * N + nn : 0;
+#pragma unroll
+                        for (int p = 0; p < kMaxParts; ++p)
+                            v[j][p] = ok[j] && p < parts ? __ldcg(partial + p * mn + off[j]) : 0.f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < kPer; ++j) {
+                        if (!ok[j]) continue;
+                        float sum = v[j][0];
+#pragma unroll
+                        for (int p = 1; p < kMaxParts; ++p)
+                            if (p < parts) sum += v[j][p];
+                        y[off[j]] = sum;
                     }
                 }
             }
@@ -1094,8 +1150,11 @@ __device__ __forceinline__ void x_chunk_to_image(const float* __restrict__ x, ui
 // blocks per SM leave room for it.
 __global__ void __launch_bounds__(256)
 x_to_bf16_tiles_kernel(const float* __restrict__ x, uint8_t* __restrict__ xa, int M, int K,
-                       size_t n_chunks) {
+                       size_t n_chunks, unsigned int* __restrict__ tile_count, int n_tiles) {
     pdl_allow_dependents();
+    // the GEMM's per-tile arrival counters of a split K start at zero each call
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < n_tiles; t += gridDim.x * blockDim.x)
+        tile_count[t] = 0u;
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     size_t id = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     for (; id + stride < n_chunks; id += 2 * stride) {
@@ -1168,8 +1227,8 @@ bool make_weight_map(CUtensorMap* map, const uint8_t* w, int N, int K, int rows)
 
 template <int kXRows, bool kTmaW>
 cudaError_t launch_wt_kernel(const uint8_t* xa, const uint8_t* w, float* y, float* partial,
-                             int splits, int M, int N, int K, int device, const CUtensorMap& map,
-                             cudaStream_t stream) {
+                             unsigned int* tile_count, int splits, int M, int N, int K, int device,
+                             const CUtensorMap& map, cudaStream_t stream) {
     using C = WtCfg<kXRows, kTmaW>;
     static bool attr_done[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
@@ -1190,42 +1249,35 @@ cudaError_t launch_wt_kernel(const uint8_t* xa, const uint8_t* w, float* y, floa
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_wt_kernel<kXRows, kTmaW>, xa, w, y, partial, M, N, K, map);
+    return cudaLaunchKernelEx(&cfg, gemm_wt_kernel<kXRows, kTmaW>, xa, w, y, partial, tile_count, M,
+                              N, K, map);
 }
 
 template <int kXRows>
-cudaError_t launch_wt(const uint8_t* xa, const uint8_t* w, float* y, float* partial, int splits,
-                      int M, int N, int K, int device, cudaStream_t stream) {
+cudaError_t launch_wt(const uint8_t* xa, const uint8_t* w, float* y, float* partial,
+                      unsigned int* tile_count, int splits, int M, int N, int K, int device,
+                      cudaStream_t stream) {
     alignas(64) CUtensorMap map;
     if (make_weight_map(&map, w, N, K, 128))
-        return launch_wt_kernel<kXRows, true>(xa, w, y, partial, splits, M, N, K, device, map,
-                                              stream);
+        return launch_wt_kernel<kXRows, true>(xa, w, y, partial, tile_count, splits, M, N, K,
+                                              device, map, stream);
     memset(&map, 0, sizeof(map));
-    return launch_wt_kernel<kXRows, false>(xa, w, y, partial, splits, M, N, K, device, map, stream);
-}
-
-// y = the K parts summed in a fixed order (bit-reproducible).
-__global__ void __launch_bounds__(256)
-sum_k_parts_kernel(const float* __restrict__ partial, float* __restrict__ y, size_t mn, int parts) {
-    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < mn;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        float v = partial[i];
-        for (int p = 1; p < parts; ++p) v += partial[static_cast<size_t>(p) * mn + i];
-        y[i] = v;
-    }
+    return launch_wt_kernel<kXRows, false>(xa, w, y, partial, tile_count, splits, M, N, K, device,
+                                           map, stream);
 }
 
 // K parts of the weights-as-A kernel: with fewer than 64 weight tiles (small m
 // and n) the GPU would sit mostly idle, so each row's K blocks are split into
 // up to 8 parts (about 128 CTAs), each part's accumulator written to its own
-// slice of a partial buffer and the parts summed afterwards.  Depends only on
+// slice of a partial buffer; the last part to finish on a tile sums them in
+// part order, so the result does not depend on which part ends first.  Depends only on
 // the geometry, so a workspace sized for it fits every device.
 int wt_splits(int M, int N, int K) {
     if (M > 128) return 1;
     const long tiles = (N + 127) / 128;
     const int bpr = K / kQK;
     if (tiles >= 64 || bpr < 2) return 1;
-    return static_cast<int>(std::max(1L, std::min<long>(128 / tiles, std::min(8, bpr))));
+    return static_cast<int>(std::max(1L, std::min<long>(128 / tiles, std::min(kMaxKParts, bpr))));
 }
 
 // x rows per CTA of the weights-as-A kernel: 256 (each decoded weight feeds
@@ -1264,10 +1316,17 @@ static size_t image_bytes(int M, int K) {
     return m_pad * static_cast<size_t>(K) * 2;
 }
 
+// With a split K: the parts' buffer, then one arrival counter per output tile.
+static size_t parts_bytes(int M, int N, int splits) {
+    return (static_cast<size_t>(splits) * M * N * 4 + 255) & ~size_t(255);
+}
+
 size_t gemm_tc_workspace_bytes(int M, int N, int K) {
     const int splits = wt_splits(M, N, K);
+    if (splits == 1) return image_bytes(M, K);
     const size_t img = (image_bytes(M, K) + 255) & ~size_t(255);
-    return splits > 1 ? img + static_cast<size_t>(splits) * M * N * 4 : image_bytes(M, K);
+    const size_t tiles = static_cast<size_t>((N + 127) / 128) * ((M + 127) / 128);
+    return img + parts_bytes(M, N, splits) + tiles * 4;
 }
 
 cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, int N, int K,
@@ -1276,28 +1335,28 @@ cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, in
     if (workspace == nullptr)
         return launch_width<false>(bn, x, nullptr, w, y, M, N, K, device, stream);
     uint8_t* xa = static_cast<uint8_t*>(workspace);
+    const int splits = wt_splits(M, N, K);
+    float* partial = nullptr;
+    unsigned int* tile_count = nullptr;
+    int n_tiles = 0;
+    if (splits > 1) {
+        uint8_t* p = xa + ((image_bytes(M, K) + 255) & ~size_t(255));
+        partial = reinterpret_cast<float*>(p);
+        tile_count = reinterpret_cast<unsigned int*>(p + parts_bytes(M, N, splits));
+        n_tiles = ((N + 127) / 128) * ((M + 127) / 128);
+    }
     // only x's own rows: the image's padding rows are never read into a kept output
     const size_t n_chunks = static_cast<size_t>(M) * (K / 8);
     size_t blocks = (n_chunks + 255) / 256;
     const size_t cap = static_cast<size_t>(sm_count) * 4;
     if (blocks > cap) blocks = cap;
-    x_to_bf16_tiles_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, xa, M, K, n_chunks);
+    x_to_bf16_tiles_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, xa, M, K, n_chunks,
+                                                                             tile_count, n_tiles);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int splits = wt_splits(M, N, K);
-    float* partial = splits > 1 ? reinterpret_cast<float*>(
-                                      xa + ((image_bytes(M, K) + 255) & ~size_t(255)))
-                                : nullptr;
     if (choose_wt_xrows(M, N, sm_count) == 256)
-        e = launch_wt<256>(xa, w, y, partial, splits, M, N, K, device, stream);
-    else
-        e = launch_wt<128>(xa, w, y, partial, splits, M, N, K, device, stream);
-    if (e != cudaSuccess || splits == 1) return e;
-    const size_t mn = static_cast<size_t>(M) * N;
-    size_t sb = (mn + 255) / 256;
-    if (sb > static_cast<size_t>(sm_count) * 4) sb = static_cast<size_t>(sm_count) * 4;
-    sum_k_parts_kernel<<<static_cast<unsigned>(sb), 256, 0, stream>>>(partial, y, mn, splits);
-    return cudaGetLastError();
+        return launch_wt<256>(xa, w, y, partial, tile_count, splits, M, N, K, device, stream);
+    return launch_wt<128>(xa, w, y, partial, tile_count, splits, M, N, K, device, stream);
 }
 
 cudaError_t launch_gemm_tc_static(const float* x, const uint8_t* w, float* y, int M, int N, int K,

@@ -162,8 +162,9 @@ enum {
  * ceil(m / 256) * 256 * k * 2 bytes; when m <= 128 and n is small (fewer than
  * 64 tiles of 128 weight rows) it splits K into P parts (P <= 8, fixed by m, n
  * and k) and adds P * m * n * 4 bytes (after 256-byte alignment) for the
- * parts' results, which are then summed in a fixed order.  Returns 0 for
- * invalid params. */
+ * parts' results plus one 4-byte arrival counter per 128 x 128 output tile;
+ * the last part to finish a tile sums the parts in part order, so y does not
+ * depend on their timing.  Returns 0 for invalid params. */
 size_t q2k_matmul_workspace_bytes(const q2k_matmul_params *params, q2k_path path);
 
 /* q2k_matmul_ex - q2k_matmul_path plus `flags` (a mask of Q2K_FLAG_*; unknown
