@@ -597,12 +597,21 @@ constexpr int kTmaBoxBytes = 112;
 // K-major), super-tile (t, stage s) at (t * K/64 + s) * 32 KB.
 constexpr int kXSuperRows = 256;
 constexpr int kXSuperBytes = kXSuperRows * kKS * 2;
-// most K parts one weights-as-A grid splits a row's blocks into
+// most K parts one weights-as-A grid splits a row's blocks into (also the
+// largest portable cluster: the parts of a small-m tile form one cluster)
 constexpr int kMaxKParts = 8;
+// Small m (x tiles of at most 64 rows): every K stage of the CTA's x rows is
+// converted to bf16 by the kernel itself and stays in shared memory, in this
+// many bytes.
+constexpr int kSmallXBytes = 160 * 1024;
 
 template <int kXRows, bool kTmaW>
 struct WtCfg {
-    static_assert(kXRows == 128 || kXRows == 256, "x rows per CTA");
+    static_assert(kXRows == 16 || kXRows == 32 || kXRows == 64 || kXRows == 128 || kXRows == 256,
+                  "x rows per CTA");
+    // small m: x converted in the kernel, all of the CTA's K stages resident,
+    // K parts summed through the cluster's shared memory
+    static constexpr bool kSmall = kXRows <= 64;
     static constexpr int kRows = 128;                       // weight rows per CTA
     static constexpr int kDecWarps = 16;                    // two groups of 8, one per block half
     static constexpr int kGroupWarps = 8;                   // decoders of one stage
@@ -614,30 +623,67 @@ struct WtCfg {
     static constexpr int kThreads = 32 * (kDecWarps + 5);
     static constexpr int kPair = 2;                         // K stages per MMA hand-over
     static constexpr int kXStage = kXRows * kKS * 2;        // bytes of one x stage
-    static constexpr int kXStages = kXRows == 256 ? 6 : 8;
+    static constexpr int kXStages = kSmall ? kSmallXBytes / kXStage : (kXRows == 256 ? 6 : 8);
+    // x barriers: a full / empty pair per ring stage; small m has one "all of
+    // x converted" barrier (one arrival per decoder warp)
+    static constexpr int kXBars = kSmall ? 1 : kXStages;
     static constexpr int kAStages = 8;                      // decoded stages in TMEM
     // Raw weight slabs: the decoders take a block into registers as soon as it
-    // lands, so two slabs keep the next block's copy a whole block ahead.
-    static constexpr int kRaw = kTmaW ? 2 : 3;
+    // lands, so two slabs keep the next block's copy a whole block ahead.  A
+    // small-m CTA has few blocks and little else to hide their latency behind:
+    // four slabs keep four blocks in flight.
+    static constexpr int kRaw = kSmall ? 4 : (kTmaW ? 2 : 3);
     // Raw slab row pitch: 84 (one block per row, rows copied by cp.async), or
     // the 112-byte TMA box that holds block b at byte 4 (b % 4) (the box
     // starts at the 16-byte boundary at or below the block).
     static constexpr int kRawPitch = kTmaW ? kTmaBoxBytes : kBlockBytes;
     static constexpr int kRawBytes = kRows * kRawPitch;
-    static constexpr uint32_t kColA = kXRows;               // A ring after the accumulator
+    // Accumulators.  Consecutive MMAs into one accumulator wait for each other;
+    // a narrow MMA (16 to 64 x rows) is over long before that latency, so small
+    // m rotates its MMAs over several accumulators (summed in the epilogue,
+    // in order) to keep the tensor pipe busy.
+    static constexpr int kAcc = kSmall ? (kXRows <= 32 ? 8 : 4) : 1;
+    static constexpr uint32_t kColA = kXRows * kAcc;        // A ring after the accumulators
     static constexpr int kTmemCols = 512;
     static constexpr int kOffX = 0;
     static constexpr int kOffRaw = kXStages * kXStage;
-    // bars: x_full[kXStages], x_empty[kXStages], a_full[kAStages], a_empty[kAStages],
+    // bars: x_full[kXBars], x_empty[kXBars], a_full[kAStages], a_empty[kAStages],
     //       raw_full[kRaw], raw_empty[kRaw], accum, drain
-    static constexpr int kNumBars = 2 * kXStages + 2 * kAStages + 2 * kRaw + 2;
+    static constexpr int kNumBars = 2 * kXBars + 2 * kAStages + 2 * kRaw + 2;
     static constexpr int kOffBar = ((kOffRaw + kRaw * kRawBytes) + 7) & ~7;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory");
     static_assert(kColA + 32u * kAStages <= static_cast<uint32_t>(kTmemCols), "TMEM");
     static_assert(kRawBytes % 128 == 0 && kOffRaw % 1024 == 0, "TMA destination alignment");
+    // the small-m epilogue reuses the x region for the 128 x kXRows f32 slice
+    static_assert(!kSmall || kOffRaw >= kRows * kXRows * 4, "reduction slice");
 };
+
+// ---- thread-block cluster: barrier and distributed shared memory -----------
+
+// Every thread of every CTA in the cluster arrives (release) and waits
+// (acquire): shared-memory writes before it are visible to the whole cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_cta_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// The address of this CTA's shared-memory word `saddr` in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
 
 // D[tmem_d] (+)= A[tmem_a] * B[bdesc]^T with A in tensor memory.
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
@@ -736,8 +782,8 @@ __device__ __forceinline__ void wt_issue_raw(const uint8_t* __restrict__ w, uint
 
 template <int kXRows, bool kTmaW>
 __global__ void __launch_bounds__(WtCfg<kXRows, kTmaW>::kThreads, 1)
-gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
-               float* __restrict__ y, float* __restrict__ partial,
+gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
+               const uint8_t* __restrict__ w, float* __restrict__ y, float* __restrict__ partial,
                unsigned int* __restrict__ tile_count, int M, int N, int K,
                const __grid_constant__ CUtensorMap tmap_w) {
     using C = WtCfg<kXRows, kTmaW>;
@@ -761,8 +807,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
     const int n_stages_row = K / kKS;  // stages of a whole row (x image layout)
 
     const uint32_t bar_xfull = sbase + C::kOffBar;
-    const uint32_t bar_xempty = bar_xfull + 8 * C::kXStages;
-    const uint32_t bar_afull = bar_xempty + 8 * C::kXStages;
+    const uint32_t bar_xempty = bar_xfull + 8 * C::kXBars;
+    const uint32_t bar_afull = bar_xempty + 8 * C::kXBars;
     const uint32_t bar_aempty = bar_afull + 8 * C::kAStages;
     const uint32_t bar_raw = bar_aempty + 8 * C::kAStages;
     const uint32_t bar_rawempty = bar_raw + 8 * C::kRaw;
@@ -772,9 +818,16 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
     unsigned int* err = &g_tc_error;
 
+    if constexpr (C::kSmall) {
+        // The grid before this one may still run (programmatic launch): set up
+        // now, read x and W and write y only after waiting for it.
+        pdl_allow_dependents();
+    }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kXStages; ++s) {
-            mbar_init(bar_xfull + 8 * s, 1);   // producer's expect-tx arrival + the copy's bytes
+        for (int s = 0; s < C::kXBars; ++s) {
+            // producer's expect-tx arrival + the copy's bytes; small m: one
+            // arrival per decoder warp once its share of x is converted
+            mbar_init(bar_xfull + 8 * s, C::kSmall ? C::kDecWarps : 1);
             mbar_init(bar_xempty + 8 * s, 1);  // MMA commit
         }
         for (int s = 0; s < C::kAStages; ++s) {
@@ -815,6 +868,45 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
         const uint32_t t_lane = static_cast<uint32_t>(32 * quarter) << 16;
         // A columns of K-steps seg and 2 + seg, stage 0
         const uint32_t a_col0 = tmem_base + t_lane + C::kColA + 8u * seg;
+        if constexpr (C::kSmall) {
+            pdl_wait_prerequisites();  // x (and W) may be written by the grid before this one
+            // x rows m0 .. m0 + nx - 1 over the CTA's K stages -> bf16, stage i
+            // at kOffX + i kXStage in the swizzled K-major layout the MMA reads
+            // (rows past M as zeros).  One 16-byte chunk (8 K-elements) per
+            // thread and pass, four passes' loads issued before any store.
+            const int chunks = n_iters * nx * 8;
+            const float* xk = xf + static_cast<size_t>(kb0) * kQK;
+            for (int c0 = td; c0 < chunks; c0 += 4 * C::kDecThreads) {
+                float4 lo[4], hi[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = c0 + u * C::kDecThreads;
+                    const int r = (c >> 3) % nx;
+                    const int i = (c >> 3) / nx;
+                    lo[u] = hi[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (c < chunks && m0 + r < M) {
+                        const float4* src = reinterpret_cast<const float4*>(
+                            xk + static_cast<size_t>(m0 + r) * K + kKS * i + 8 * (c & 7));
+                        lo[u] = __ldg(src);
+                        hi[u] = __ldg(src + 1);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = c0 + u * C::kDecThreads;
+                    if (c < chunks) {
+                        const int r = (c >> 3) % nx;
+                        const int i = (c >> 3) / nx;
+                        st_shared_v4(sbase + C::kOffX + i * C::kXStage + sw128_offset(r, c & 7),
+                                     pack_bf16x2(lo[u].x, lo[u].y), pack_bf16x2(lo[u].z, lo[u].w),
+                                     pack_bf16x2(hi[u].x, hi[u].y), pack_bf16x2(hi[u].z, hi[u].w));
+                    }
+                }
+            }
+            fence_proxy_async_smem();  // this thread's stores -> visible to the MMA
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_xfull);
+        }
         if constexpr (!kTmaW) {
             // Pull the tile's weight rows into L2 now (one bulk prefetch per row).
             if (td < C::kRows && n0 + td < N) {
@@ -926,6 +1018,24 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
             for (int c0 = 16 * (warp >> 2); c0 < nx; c0 += 64) {
                 uint32_t v[16];
                 tmem_ld16(t_row + c0, v);
+#pragma unroll 1
+                for (int a = 1; a < C::kAcc; ++a) {  // the accumulators, summed in order
+                    uint32_t u[16];
+                    tmem_ld16(t_row + static_cast<uint32_t>(a * kXRows) + c0, u);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        v[q] = __float_as_uint(__uint_as_float(v[q]) + __uint_as_float(u[q]));
+                }
+                if (C::kSmall && gridDim.z > 1) {
+                    // this part's slice, column-major (x row c, weight row
+                    // `row` at word 128 c + row), in the x region the MMAs
+                    // are done with; the cluster sums the parts below
+                    float* red = reinterpret_cast<float*>(smem + C::kOffX);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        if (c0 + q < nx) red[(c0 + q) * C::kRows + row] = __uint_as_float(v[q]);
+                    continue;
+                }
                 // one K part alone goes to y; parts of a split go to their own
                 // slice of the partial buffer, summed in part order below
                 float* out = gridDim.z == 1 ? y : partial + static_cast<size_t>(blockIdx.z) * M * N;
@@ -938,7 +1048,7 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
                 }
             }
         }
-        if (gridDim.z > 1) {
+        if (!C::kSmall && gridDim.z > 1) {
             // K split: every part has stored its slice; the part that arrives last
             // at this tile's counter sums the slices in part order into y (no CTA
             // ever waits for another).  The counter was zeroed by the grid before.
@@ -1002,7 +1112,6 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
         const uint32_t idesc = make_idesc(kBM, nx);
         const uint64_t xdesc0 = sw128_desc(sbase + C::kOffX);
         const uint32_t a_base0 = tmem_base + C::kColA;
-        uint32_t acc = 0u;  // 0 only for the very first MMA
         for (int i0 = 0; i0 < n_iters; i0 += C::kPair) {
             asm volatile("bar.sync 1, 64;" ::: "memory");
             if (lane == 0 && !*abort_flag) {
@@ -1016,12 +1125,15 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
                     const uint32_t a_s = a_base0 + 32u * sa;
 #pragma unroll
                     for (int kk = 0; kk < kKS / 16; ++kk) {
-                        mma_bf16_tmem_a(tmem_base, a_s + 8u * kk, xdesc + 2u * kk, idesc,
-                                        acc | static_cast<uint32_t>(kk));
+                        // MMA g = 4 i + kk goes to accumulator g % kAcc; the
+                        // first one into each starts it from zero
+                        const int g = 4 * i + kk;
+                        const uint32_t d = tmem_base + static_cast<uint32_t>((g % C::kAcc) * kXRows);
+                        mma_bf16_tmem_a(d, a_s + 8u * kk, xdesc + 2u * kk, idesc,
+                                        g >= C::kAcc ? 1u : 0u);
                     }
-                    acc = 1u;
                     mma_commit(bar_aempty + 8 * sa);
-                    mma_commit(bar_xempty + 8 * sx);
+                    if (!C::kSmall) mma_commit(bar_xempty + 8 * sx);
                 }
             }
             __syncwarp();
@@ -1039,13 +1151,16 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
         __syncwarp();
     } else if (warp == C::kWaitWarp) {
         // ---------------- stage waiter: hands filled stages to the MMA warp ----------------
+        if (C::kSmall && lane == 0)  // all of x, once
+            mbar_wait_lean(bar_xfull, 0, abort_flag, err, kErrTimeoutFull, 32);
         for (int i0 = 0; i0 < n_iters; i0 += C::kPair) {
             if (lane == 0 && !*abort_flag) {
 #pragma unroll
                 for (int u = 0; u < C::kPair; ++u) {
                     const int i = i0 + u;
-                    if (!mbar_wait_lean(bar_xfull + 8 * (i % C::kXStages), (i / C::kXStages) & 1,
-                                        abort_flag, err, kErrTimeoutFull, 32) ||
+                    if ((!C::kSmall &&
+                         !mbar_wait_lean(bar_xfull + 8 * (i % C::kXStages), (i / C::kXStages) & 1,
+                                         abort_flag, err, kErrTimeoutFull, 32)) ||
                         !mbar_wait_lean(bar_afull + 8 * (i % C::kAStages), (i / C::kAStages) & 1,
                                         abort_flag, err, kErrTimeoutFull, 32))
                         break;
@@ -1059,6 +1174,7 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
         if (kTmaW && lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w))
                          : "memory");
+            if constexpr (C::kSmall) pdl_wait_prerequisites();  // W may be written by it
             const uint32_t raw0 = sbase + C::kOffRaw;
             for (int b = 0; b < n_blocks; ++b) {
                 const int buf = b % C::kRaw;
@@ -1081,7 +1197,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
         __syncwarp();
     } else {
         // ---------------- x stages: one bulk copy each, even / odd stages ----------------
-        if (lane == 0) {
+        // (small m: the decoders converted x already)
+        if (!C::kSmall && lane == 0) {
             // This tile's rows of super-tile m0 / 256 (the second 128 of them when
             // the tile starts half-way into it); a whole super-tile stage when
             // kXRows is 256.  Image rows past M are never written: they feed only
@@ -1109,6 +1226,46 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const uint8_t* __restrict__ w,
             }
         }
         __syncwarp();
+    }
+
+    if constexpr (C::kSmall) {
+        if (gridDim.z > 1) {
+            // The K parts of this tile are the CTAs of one cluster, each with
+            // its slice in shared memory.  Every thread of the cluster passes
+            // both barriers whatever happened before (no role returns early),
+            // so neither can be left waiting.  Part r sums its share of the
+            // tile's elements over the parts in part order (deterministic);
+            // the second barrier keeps every slice alive until all are read.
+            __syncwarp();
+            cluster_sync_all();
+            if (warp < C::kDecWarps) {
+                const int parts = static_cast<int>(gridDim.z);
+                const int rank = static_cast<int>(cluster_cta_rank());
+                const int total = C::kRows * nx;
+                const int e0 = rank * total / parts;
+                const int e1 = (rank + 1) * total / parts;
+                const uint32_t red = sbase + C::kOffX;
+                uint32_t src[kMaxKParts];
+#pragma unroll
+                for (int p = 0; p < kMaxKParts; ++p)
+                    src[p] = cluster_map_shared(red, static_cast<uint32_t>(p < parts ? p : 0));
+                for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += C::kDecThreads) {
+                    float v[kMaxKParts];
+#pragma unroll
+                    for (int p = 0; p < kMaxKParts; ++p)
+                        v[p] = p < parts ? ld_shared_cluster_f32(src[p] + 4u * e) : 0.f;
+                    float sum = v[0];
+#pragma unroll
+                    for (int p = 1; p < kMaxKParts; ++p)
+                        if (p < parts) sum += v[p];
+                    const int nn = n0 + (e & (C::kRows - 1));
+                    const int mm = m0 + e / C::kRows;
+                    if (nn < N && mm < M) y[static_cast<size_t>(mm) * N + nn] = sum;
+                }
+            }
+            __syncwarp();
+            cluster_sync_all();
+        }
     }
 
     tc_fence_before();
@@ -1226,9 +1383,9 @@ bool make_weight_map(CUtensorMap* map, const uint8_t* w, int N, int K, int rows)
 }
 
 template <int kXRows, bool kTmaW>
-cudaError_t launch_wt_kernel(const uint8_t* xa, const uint8_t* w, float* y, float* partial,
-                             unsigned int* tile_count, int splits, int M, int N, int K, int device,
-                             const CUtensorMap& map, cudaStream_t stream) {
+cudaError_t launch_wt_kernel(const uint8_t* xa, const float* xf, const uint8_t* w, float* y,
+                             float* partial, unsigned int* tile_count, int splits, int M, int N,
+                             int K, int device, const CUtensorMap& map, cudaStream_t stream) {
     using C = WtCfg<kXRows, kTmaW>;
     static bool attr_done[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
@@ -1244,26 +1401,34 @@ cudaError_t launch_wt_kernel(const uint8_t* xa, const uint8_t* w, float* y, floa
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_wt_kernel<kXRows, kTmaW>, xa, w, y, partial, tile_count, M,
-                              N, K, map);
+    if (C::kSmall && splits > 1) {
+        // the K parts of a tile: one cluster along z
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 1;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = static_cast<unsigned>(splits);
+        cfg.numAttrs = 2;
+    }
+    return cudaLaunchKernelEx(&cfg, gemm_wt_kernel<kXRows, kTmaW>, xa, xf, w, y, partial,
+                              tile_count, M, N, K, map);
 }
 
 template <int kXRows>
-cudaError_t launch_wt(const uint8_t* xa, const uint8_t* w, float* y, float* partial,
-                      unsigned int* tile_count, int splits, int M, int N, int K, int device,
-                      cudaStream_t stream) {
+cudaError_t launch_wt(const uint8_t* xa, const float* xf, const uint8_t* w, float* y,
+                      float* partial, unsigned int* tile_count, int splits, int M, int N, int K,
+                      int device, cudaStream_t stream) {
     alignas(64) CUtensorMap map;
     if (make_weight_map(&map, w, N, K, 128))
-        return launch_wt_kernel<kXRows, true>(xa, w, y, partial, tile_count, splits, M, N, K,
+        return launch_wt_kernel<kXRows, true>(xa, xf, w, y, partial, tile_count, splits, M, N, K,
                                               device, map, stream);
     memset(&map, 0, sizeof(map));
-    return launch_wt_kernel<kXRows, false>(xa, w, y, partial, tile_count, splits, M, N, K, device,
-                                           map, stream);
+    return launch_wt_kernel<kXRows, false>(xa, xf, w, y, partial, tile_count, splits, M, N, K,
+                                           device, map, stream);
 }
 
 // K parts of the weights-as-A kernel: with fewer than 64 weight tiles (small m
@@ -1290,6 +1455,23 @@ int choose_wt_xrows(int M, int N, int sm_count) {
 
 // Tile width: the smallest estimated time with tiles spread over the SMs; a
 // tile's time grows with BN (decode) plus a fixed share (x conversion, fill).
+// Small m: x tile rows (16, 32 or 64; 0 = not small) and K parts.  All of a
+// part's x stages (4 per block) must fit the kSmallXBytes region, so the parts
+// may have to be more than wt_splits asks for; at most twice as many (and
+// at most kMaxKParts), else the x-image path is used.  Geometry only.
+int small_xrows(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 0; }
+
+int small_splits(int M, int N, int K) {
+    const int xr = small_xrows(M);
+    if (xr == 0) return 0;
+    const int bpr = K / kQK;
+    const int max_blocks = kSmallXBytes / (xr * kKS * 2) / 4;
+    const int base = wt_splits(M, N, K);
+    for (int s = base; s <= kMaxKParts && s <= 2 * base && s <= bpr; ++s)
+        if ((bpr + s - 1) / s <= max_blocks) return s;
+    return 0;
+}
+
 int choose_bn(int M, int N, int sm_count) {
     const int cands[4] = {256, 192, 128, 64};
     int best = 128;
@@ -1322,6 +1504,7 @@ static size_t parts_bytes(int M, int N, int splits) {
 }
 
 size_t gemm_tc_workspace_bytes(int M, int N, int K) {
+    if (small_splits(M, N, K) > 0) return 0;  // x converted in the GEMM, parts summed on chip
     const int splits = wt_splits(M, N, K);
     if (splits == 1) return image_bytes(M, K);
     const size_t img = (image_bytes(M, K) + 255) & ~size_t(255);
@@ -1331,6 +1514,13 @@ size_t gemm_tc_workspace_bytes(int M, int N, int K) {
 
 cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, int N, int K,
                            int device, int sm_count, void* workspace, cudaStream_t stream) {
+    if (const int parts = small_splits(M, N, K)) {
+        switch (small_xrows(M)) {
+            case 16: return launch_wt<16>(nullptr, x, w, y, nullptr, nullptr, parts, M, N, K, device, stream);
+            case 32: return launch_wt<32>(nullptr, x, w, y, nullptr, nullptr, parts, M, N, K, device, stream);
+            default: return launch_wt<64>(nullptr, x, w, y, nullptr, nullptr, parts, M, N, K, device, stream);
+        }
+    }
     const int bn = choose_bn(M, N, sm_count);
     if (workspace == nullptr)
         return launch_width<false>(bn, x, nullptr, w, y, M, N, K, device, stream);
@@ -1355,8 +1545,9 @@ cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, in
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (choose_wt_xrows(M, N, sm_count) == 256)
-        return launch_wt<256>(xa, w, y, partial, tile_count, splits, M, N, K, device, stream);
-    return launch_wt<128>(xa, w, y, partial, tile_count, splits, M, N, K, device, stream);
+        return launch_wt<256>(xa, nullptr, w, y, partial, tile_count, splits, M, N, K, device,
+                              stream);
+    return launch_wt<128>(xa, nullptr, w, y, partial, tile_count, splits, M, N, K, device, stream);
 }
 
 cudaError_t launch_gemm_tc_static(const float* x, const uint8_t* w, float* y, int M, int N, int K,

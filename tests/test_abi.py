@@ -127,17 +127,23 @@ def test_matmul_ex_rejects_unknown_flags(lib):
 def test_workspace_bytes(lib):
     P = q2k.MatmulParams
     assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(1, 8, 256, 10)), 0) == 0      # GEMV
-    assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(9, 8, 256, 10)), 0) == 256 * 256 * 2
-    assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(1, 8, 256, 10)), 2) == 256 * 256 * 2
+    # m <= 64 whose K stages fit on chip: x converted in the GEMM, no workspace
+    assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(9, 8, 256, 10)), 0) == 0
+    assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(1, 8, 256, 10)), 2) == 0
+    assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(16, 4096, 4096, 10)), 0) == 0
+    assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(64, 4000, 8192, 10)), 0) == 0
+    # m = 64 with 16 blocks a row and one K part: its x does not fit, x image
+    assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(64, 14336, 4096, 10)), 0) == 256 * 4096 * 2
     assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(512, 7168, 7168, 10)), 0) == 512 * 7168 * 2
     assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(129, 8, 512, 10)), 0) == 256 * 512 * 2
     assert lib.q2k_matmul_workspace_bytes(ctypes.byref(P(9, 8, 255, 10)), 0) == 0      # invalid
 
 
 def test_workspace_rejected_when_small_or_aliasing(lib):
-    p = q2k.MatmulParams(9, 8, 256, 10)
+    # m = 129 takes the x-image path, so it has a workspace to check
+    p = q2k.MatmulParams(129, 8, 256, 10)
     need = 256 * 256 * 2
-    args = (0x10000, 9 * 256, 0x100000, 8 * 84, 0x1000000, 9 * 8, ctypes.byref(p))
+    args = (0x10000, 129 * 256, 0x100000, 8 * 84, 0x1000000, 129 * 8, ctypes.byref(p))
     assert lib.q2k_matmul_ex(2, 0, *args, 0x2000000, need - 1, None) == INVALID
     assert "workspace" in lib.q2k_last_error().decode()
     assert lib.q2k_matmul_ex(2, 0, *args, 0x2000008, need, None) == INVALID

@@ -213,6 +213,33 @@ def test_tensor_parity(m, n, k):
     check_matmul(2000 + m + n + k, m, n, k, "tensor", TOL_TC)
 
 
+@pytest.mark.parametrize("m,n,k", [
+    (1, 4096, 4096),    # 16-row x tile, 4 K parts (cluster of 4)
+    (8, 8, 256),        # one part, no cluster
+    (17, 333, 2560),    # 32-row x tile, 8 uneven parts of 1 or 2 blocks, ragged N
+    (48, 129, 768),     # 64-row x tile (48 used), 3 parts
+    (64, 4096, 4096),   # full 64-row x tile, 4 parts
+    (16, 14336, 4096),  # one part, 112 CTAs, all 64 K stages of x resident
+])
+def test_tensor_small_m_parity(m, n, k):
+    """m <= 64: x converted to bf16 in the GEMM, K parts summed in the cluster."""
+    check_matmul(2500 + m + n + k, m, n, k, "tensor", TOL_TC)
+
+
+@pytest.mark.parametrize("m,n,k", [
+    (64, 4000, 8192),   # x capacity forces 7 parts (a cluster of 7) where 4 were asked
+    (32, 14336, 4096),  # 2 parts where 1 was asked: 224 CTAs, more than one wave
+    (33, 300, 14336),   # x does not fit even in 8 parts: the x-image path
+])
+def test_tensor_small_m_sampled_rows(m, n, k):
+    x, w = wl.make_matmul_inputs(2600 + m, m, n, k)
+    y = run_matmul(x, w, n, "tensor")
+    rng = np.random.default_rng(m)
+    rows = np.unique(np.concatenate([rng.choice(n, 48, replace=False), [0, 127, 128, n - 1]]))
+    yref, s = oracle.matmul_rows(x, w, n, rows, threads=ORACLE_THREADS)
+    assert_close(y[:, rows], yref, s, TOL_TC, f"m={m} n={n} k={k} sampled")
+
+
 def test_tensor_page_run_dense_rows9():
     """Page fn run_dense(9) and the forced-mm variants (rows > 8).
 
