@@ -14,6 +14,13 @@ What each call follows (mlx-native test page "tests/deepseek_q2_k.rs"):
                         rejects_bad_ids`` (rows by id; id >= vocab is an error).
 * ``matmul``          - fn ``run_dense``'s expected value, ``y[m,n] = sum_k
                         x[m,k] w[n,k]``, summed in f64 instead of f32.
+* ``matmul_batched_mv`` - test ``q2_k_batched_mv_is_byte_identical_to_
+                        independent_dispatches``: batch b's matrix (at b n K/256
+                        84 bytes) times batch b's input row, one ``matmul`` each.
+* ``matmul_id``       - fn ``run_expert``'s expected value: route r = t top_k +
+                        slot (token-major ids) takes token t's input and the
+                        weights of expert ids[r] (at ids[r] expert_stride bytes);
+                        an id >= n_experts is an error.
 """
 
 from __future__ import annotations
@@ -147,6 +154,64 @@ class Oracle:
         return y, s_abs
 
 
+    # ---- batched and routed products: compositions of ``matmul`` ----------
+
+    def matmul_batched_mv(self, x: np.ndarray, w: np.ndarray, n: int, threads: int = 1):
+        """Return ``(y, s_abs)``, float64 ``[batches, n]``: row b is batch b's
+        matrix (the b-th run of ``n * K/256`` blocks of ``w``) times ``x[b]``."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        if x.ndim != 2:
+            raise OracleError("x must be [batches, K]")
+        batches, K = x.shape
+        wb = np.ascontiguousarray(w, dtype=np.uint8).reshape(-1)
+        per = n * (K // QK_K) * BLOCK_BYTES
+        if K % QK_K != 0 or wb.size != batches * per:
+            raise OracleError("w must hold one n x K matrix per batch")
+        y = np.empty((batches, n), dtype=np.float64)
+        s_abs = np.empty((batches, n), dtype=np.float64)
+        for b in range(batches):
+            yb, sb = self.matmul(x[b:b + 1], wb[b * per:(b + 1) * per], n, threads)
+            y[b], s_abs[b] = yb[0], sb[0]
+        return y, s_abs
+
+    def route_token(self, route: int, top_k: int) -> int:
+        """Token of route ``route``: the ids are token-major (t top_k + slot)."""
+        return route // top_k
+
+    def expert_bytes(self, w: np.ndarray, expert: int, n: int, K: int,
+                     expert_stride: int) -> np.ndarray:
+        """Expert ``expert``'s n x K matrix: ``n K/256`` blocks from byte
+        ``expert * expert_stride``."""
+        size = n * (K // QK_K) * BLOCK_BYTES
+        start = expert * expert_stride
+        if start + size > w.size:
+            raise OracleError("expert matrix runs past the end of w")
+        return w[start:start + size]
+
+    def matmul_id(self, x: np.ndarray, w: np.ndarray, ids, n: int, n_experts: int,
+                  expert_stride: int, top_k: int, threads: int = 1):
+        """Return ``(y, s_abs)``, float64 ``[n_tokens * top_k, n]``: row r is
+        expert ``ids[r]``'s matrix times the input of token ``r // top_k``."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        if x.ndim != 2:
+            raise OracleError("x must be [n_tokens, K]")
+        n_tokens, K = x.shape
+        ids = np.ascontiguousarray(ids, dtype=np.uint32).reshape(-1)
+        if top_k < 1 or ids.size != n_tokens * top_k or K % QK_K != 0:
+            raise OracleError("ids must hold top_k experts per token and K a multiple of 256")
+        wb = np.ascontiguousarray(w, dtype=np.uint8).reshape(-1)
+        y = np.empty((ids.size, n), dtype=np.float64)
+        s_abs = np.empty((ids.size, n), dtype=np.float64)
+        for r, e in enumerate(ids.tolist()):
+            if e >= n_experts:
+                raise OracleError(f"expert id {e} out of range (n_experts = {n_experts})")
+            t = self.route_token(r, top_k)
+            yr, sr = self.matmul(x[t:t + 1], self.expert_bytes(wb, e, n, K, expert_stride), n,
+                                 threads)
+            y[r], s_abs[r] = yr[0], sr[0]
+        return y, s_abs
+
+
 def default() -> Oracle:
     global _lib
     with _lock:
@@ -182,3 +247,12 @@ def matmul_rows(x: np.ndarray, w: np.ndarray, n: int, rows, threads: int = 1):
     row_bytes = (K // QK_K) * BLOCK_BYTES
     w2 = np.ascontiguousarray(w, dtype=np.uint8).reshape(n, row_bytes)[rows]
     return default().matmul(x, w2, rows.size, threads=threads)
+
+
+def matmul_batched_mv(x: np.ndarray, w: np.ndarray, n: int, threads: int = 1):
+    return default().matmul_batched_mv(x, w, n, threads)
+
+
+def matmul_id(x: np.ndarray, w: np.ndarray, ids, n: int, n_experts: int, expert_stride: int,
+              top_k: int, threads: int = 1):
+    return default().matmul_id(x, w, ids, n, n_experts, expert_stride, top_k, threads)

@@ -279,6 +279,76 @@ def pin_run_dense_page(o):
         assert abs(y[0, r] - float(acc)) <= 2e-4, f"row {r}"
 
 
+def _fsum_dot(x_row, w_row):
+    terms = x_row.astype(np.float64) * w_row.astype(np.float64)
+    return math.fsum(terms), math.fsum(np.abs(terms))
+
+
+def pin_batched_mv_page(o):
+    """Page test q2_k_batched_mv_is_byte_identical_to_independent_dispatches:
+    3 batches of 8 rows block(8 b + r + 1), inputs input(3); batch b is its own
+    matrix times its own input row (math.fsum of the decoded products)."""
+    batches, n = 3, 8
+    w = np.concatenate([wl.page_block(b * n + r + 1) for b in range(batches) for r in range(n)])
+    x = wl.page_input(batches)
+    y, s = o.matmul_batched_mv(x, w, n)
+    assert y.shape == (batches, n)
+    for b in range(batches):
+        for r in range(n):
+            ref, ref_abs = _fsum_dot(x[b], o.dequant_block(wl.page_block(b * n + r + 1)))
+            assert abs(y[b, r] - ref) <= 1e-12 * ref_abs, f"batch {b} row {r}"
+            assert abs(s[b, r] - ref_abs) <= 1e-12 * ref_abs
+
+
+def _expert_fixture(tokens, top_k, experts, n=8, gap=0):
+    """Page fn run_expert: expert e's row r is block(e n + r + 1), x = input(tokens),
+    ids[t top_k + slot] = (3 t + slot) mod experts.  ``gap`` bytes of 0xFF between
+    experts make expert_stride larger than one expert's matrix."""
+    parts = []
+    for e in range(experts):
+        parts.extend(wl.page_block(e * n + r + 1) for r in range(n))
+        parts.append(np.full(gap, 0xFF, dtype=np.uint8))
+    w = np.concatenate(parts)
+    ids = np.array([(3 * t + slot) % experts for t in range(tokens) for slot in range(top_k)],
+                   dtype=np.uint32)
+    return w, wl.page_input(tokens), ids, n * BLOCK_BYTES + gap
+
+
+def pin_matmul_id_page(o):
+    """Page fn run_expert(2, 2, 3) and run_expert(33, 6, 8): route r (token-major)
+    is expert ids[r]'s rows times token r // top_k's input."""
+    for tokens, top_k, experts in ((2, 2, 3), (33, 6, 8)):
+        n = 8
+        w, x, ids, stride = _expert_fixture(tokens, top_k, experts, n)
+        y, _ = o.matmul_id(x, w, ids, n, experts, stride, top_k)
+        assert y.shape == (tokens * top_k, n)
+        for r in range(tokens * top_k):
+            t, e = r // top_k, int(ids[r])
+            for row in range(n):
+                ref, ref_abs = _fsum_dot(x[t], o.dequant_block(wl.page_block(e * n + row + 1)))
+                assert abs(y[r, row] - ref) <= 1e-12 * ref_abs, f"route {r} row {row}"
+
+
+def pin_matmul_id_stride_and_bad_id(o):
+    """Experts are expert_stride bytes apart (not packed), and an id >= n_experts
+    is an error (the pages reject bad ids)."""
+    tokens, top_k, experts, n = 3, 2, 4, 8
+    w, x, ids, stride = _expert_fixture(tokens, top_k, experts, n, gap=52)
+    y, _ = o.matmul_id(x, w, ids, n, experts, stride, top_k)
+    for r in range(tokens * top_k):
+        t, e = r // top_k, int(ids[r])
+        ref, ref_abs = _fsum_dot(x[t], o.dequant_block(wl.page_block(e * n + n)))
+        assert abs(y[r, n - 1] - ref) <= 1e-12 * ref_abs, f"route {r}"
+    bad = ids.copy()
+    bad[3] = experts
+    try:
+        o.matmul_id(x, w, bad, n, experts, stride, top_k)
+    except OracleError:
+        pass
+    else:
+        raise AssertionError("an expert id >= n_experts was accepted")
+
+
 ALL_PINS = [
     pin_f16_all_patterns,
     pin_block5_hand_values,
@@ -296,4 +366,7 @@ ALL_PINS = [
     pin_matmul_linearity,
     pin_matmul_fsum,
     pin_run_dense_page,
+    pin_batched_mv_page,
+    pin_matmul_id_page,
+    pin_matmul_id_stride_and_bad_id,
 ]

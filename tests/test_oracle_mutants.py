@@ -63,3 +63,33 @@ def test_mutant_is_caught(tmp_path, src_text, name, old, new):
         except (AssertionError, oracle.OracleError):
             caught.append(pin.__name__)
     assert caught, f"no pin caught mutant {name}"
+
+
+# Mistakes in the Python compositions (batched and routed products), planted by
+# overriding one helper of a copy of the oracle object.
+class _SlotAsToken(oracle.Oracle):
+    def route_token(self, route, top_k):
+        return route % top_k
+
+
+class _PackedExperts(oracle.Oracle):
+    def expert_bytes(self, w, expert, n, K, expert_stride):
+        return super().expert_bytes(w, expert, n, K, n * (K // 256) * 84)
+
+
+class _BatchesSwapped(oracle.Oracle):
+    def matmul_batched_mv(self, x, w, n, threads=1):
+        return super().matmul_batched_mv(x[::-1].copy(), w, n, threads)
+
+
+@pytest.mark.parametrize("cls", [_SlotAsToken, _PackedExperts, _BatchesSwapped],
+                         ids=lambda c: c.__name__)
+def test_composition_mutant_is_caught(cls):
+    o = cls(oracle.default().path)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(o)
+        except (AssertionError, oracle.OracleError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught {cls.__name__}"
