@@ -57,6 +57,12 @@ class MatmulParams(ctypes.Structure):
                 ("ggml_type", ctypes.c_uint32)]
 
 
+class MatmulIdParams(ctypes.Structure):
+    _fields_ = [("n_tokens", ctypes.c_uint32), ("top_k", ctypes.c_uint32), ("n", ctypes.c_uint32),
+                ("k", ctypes.c_uint32), ("n_experts", ctypes.c_uint32),
+                ("ggml_type", ctypes.c_uint32), ("expert_stride", ctypes.c_uint64)]
+
+
 class EmbeddingParams(ctypes.Structure):
     _fields_ = [("vocab_size", ctypes.c_uint32), ("embed_dim", ctypes.c_uint32),
                 ("n_tokens", ctypes.c_uint32), ("ggml_type", ctypes.c_uint32)]
@@ -97,10 +103,15 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                       ctypes.POINTER(MatmulParams), vp, sz, vp]
         lib.q2k_matmul_workspace_bytes.argtypes = [ctypes.POINTER(MatmulParams), ctypes.c_int]
         lib.q2k_matmul_workspace_bytes.restype = ctypes.c_size_t
+        lib.q2k_matmul_batched_mv.argtypes = [vp, sz, vp, sz, vp, sz, ctypes.c_uint32,
+                                              ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, vp]
+        lib.q2k_matmul_id.argtypes = [vp, sz, vp, sz, vp, vp, sz, ctypes.POINTER(MatmulIdParams),
+                                      vp, vp]
         lib.q2k_device_error.argtypes = [u32p, vp]
         lib.q2k_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         for fn in ("q2k_dequantize", "q2k_embedding_gather", "q2k_matmul", "q2k_matmul_path",
-                   "q2k_matmul_ex", "q2k_device_error", "q2k_selftest_wait_timeout"):
+                   "q2k_matmul_ex", "q2k_matmul_batched_mv", "q2k_matmul_id", "q2k_device_error",
+                   "q2k_selftest_wait_timeout"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.q2k_last_error.restype = ctypes.c_char_p
         lib.q2k_last_error.argtypes = []
@@ -271,6 +282,63 @@ def matmul(x, w, n: int, out=None, path="auto", const_weights: bool = False,
         _check(lib, lib.q2k_matmul_ex(pcode, flags, x.data_ptr(), x.numel(), w.data_ptr(),
                                       w.numel(), out.data_ptr(), out.numel(), ctypes.byref(p),
                                       ws_ptr, ws_bytes, _stream_handle(x)))
+    return out
+
+
+def matmul_batched_mv(x, w, n: int, out=None):
+    """``batches`` matrix-vector products in one launch: ``x`` f32 ``[batches, k]``
+    (or ``[batches, 1, k]``), ``w`` uint8 holding the batches' ``[n, k]`` Q2_K
+    matrices back to back; returns ``[batches, n]`` (the shape of ``x`` with k
+    replaced by n).  Each batch is bit-identical to ``matmul`` of it alone."""
+    torch = _torch()
+    _require_cuda(x, "x", torch.float32)
+    _require_cuda(w, "w", torch.uint8)
+    k = x.shape[-1]
+    batches = x.shape[0]
+    if out is None:
+        out = torch.empty(tuple(x.shape[:-1]) + (n,), dtype=torch.float32, device=x.device)
+    _require_cuda(out, "out", torch.float32)
+    lib = load()
+    with _on_device(x):
+        _check(lib, lib.q2k_matmul_batched_mv(x.data_ptr(), x.numel(), w.data_ptr(), w.numel(),
+                                              out.data_ptr(), out.numel(), batches, 1, n, k,
+                                              _stream_handle(x)))
+    return out
+
+
+def matmul_id(x, w, ids, n: int, n_experts: int, top_k: int, expert_stride: int | None = None,
+              out=None, check: bool = True):
+    """Expert-routed product: ``x`` f32 ``[n_tokens, k]``, ``ids`` 32-bit ints
+    ``[n_tokens * top_k]`` (token-major), expert e's ``[n, k]`` Q2_K matrix at
+    byte ``e * expert_stride`` of ``w`` (default: packed, ``n * k/256 * 84``).
+    Returns ``[n_tokens * top_k, n]`` with row r = expert ``ids[r]`` times token
+    ``r // top_k``.  With ``check`` the call waits and raises ``InvalidArgument``
+    if an id was >= n_experts; with ``check=False`` it returns ``(out,
+    bad_id_count)`` without waiting."""
+    torch = _torch()
+    _require_cuda(x, "x", torch.float32)
+    _require_cuda(w, "w", torch.uint8)
+    _require_cuda(ids, "ids", ids.dtype)
+    if ids.element_size() != 4 or ids.is_floating_point():
+        raise TypeError("ids must be a 32-bit integer tensor (read as uint32)")
+    n_tokens, k = x.shape
+    if expert_stride is None:
+        expert_stride = n * (k // QK_K) * BLOCK_BYTES
+    if out is None:
+        out = torch.empty((ids.numel(), n), dtype=torch.float32, device=x.device)
+    _require_cuda(out, "out", torch.float32)
+    bad = torch.zeros(1, dtype=torch.int32, device=x.device)
+    p = MatmulIdParams(n_tokens, top_k, n, k, n_experts, GGML_TYPE_Q2_K, expert_stride)
+    lib = load()
+    with _on_device(x):
+        _check(lib, lib.q2k_matmul_id(x.data_ptr(), x.numel(), w.data_ptr(), w.numel(),
+                                      ids.data_ptr(), out.data_ptr(), out.numel(),
+                                      ctypes.byref(p), bad.data_ptr(), _stream_handle(x)))
+    if not check:
+        return out, bad
+    n_bad = int(bad.item())
+    if n_bad:
+        raise InvalidArgument(1, f"{n_bad} expert id(s) >= n_experts {n_experts}")
     return out
 
 

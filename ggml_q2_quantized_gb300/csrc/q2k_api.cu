@@ -18,6 +18,7 @@
 
 static_assert(Q2K_STATIC_WORKSPACE_BYTES == q2k::kStaticWorkspaceBytes,
               "header and library disagree on the fixed scratch size");
+static_assert(sizeof(q2k_matmul_id_params) == 32, "q2k_matmul_id_params layout");
 
 namespace {
 
@@ -271,6 +272,109 @@ q2k_status q2k_matmul_static_workspace(const float* x, size_t x_elems, const voi
                                                int(p->n), int(p->k), dev.device, dev.sm_count,
                                                reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul_static_workspace launch");
+}
+
+q2k_status q2k_matmul_batched_mv(const float* x, size_t x_elems, const void* w, size_t w_bytes,
+                                 float* y, size_t y_elems, uint32_t batches, uint32_t m,
+                                 uint32_t n, uint32_t k, q2k_stream_t stream) {
+    g_last_error[0] = '\0';
+    if (m != 1) return fail(Q2K_ERR_INVALID_ARGUMENT, "batched matrix-vector takes m = 1, got %u", m);
+    if (batches == 0 || batches > 65535)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "batches must be in 1..65535, got %u", batches);
+    // one batch's geometry, checked as a single call would be
+    const q2k_matmul_params one = {1u, n, k, Q2K_GGML_TYPE_Q2_K};
+    size_t per_w = 0, want_x, want_w, want_y;
+    if (k % Q2K_QK_K == 0 && !mul_ok(size_t(n), size_t(k / Q2K_QK_K) * Q2K_BLOCK_BYTES, &per_w))
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "matmul shape overflows size_t");
+    if (!mul_ok(batches, k, &want_x) || !mul_ok(batches, per_w, &want_w) ||
+        !mul_ok(batches, n, &want_y))
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "batched shape overflows size_t");
+    if (x_elems != want_x || w_bytes != want_w || y_elems != want_y)
+        return fail(Q2K_ERR_INVALID_ARGUMENT,
+                    "batched sizes: x %zu (want batches*k = %zu), w %zu (want batches*n*k/256*84 = %zu), "
+                    "y %zu (want batches*n = %zu)", x_elems, want_x, w_bytes, want_w, y_elems, want_y);
+    q2k_status st = check_matmul(x, k, w, per_w, y, n, &one);  // shape, type, nulls, alignment
+    if (st != Q2K_OK) return st;
+    if (overlaps(y, want_y * 4, x, want_x * 4) || overlaps(y, want_y * 4, w, want_w))
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "y must not alias x or w");
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != Q2K_OK) return st;
+    q2k::GemvProblems pr;
+    pr.x_stride = static_cast<long long>(k);
+    pr.w_stride = static_cast<long long>(per_w);
+    pr.y_stride = static_cast<long long>(n);
+    cudaError_t e = q2k::launch_gemv_problems(x, static_cast<const uint8_t*>(w), y, 1, int(n), int(k),
+                                              dev.device, dev.sm_count, 0u, pr, int(batches),
+                                              reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul_batched_mv launch");
+}
+
+q2k_status q2k_matmul_id(const float* x, size_t x_elems, const void* w, size_t w_bytes,
+                         const uint32_t* ids, float* y, size_t y_elems,
+                         const q2k_matmul_id_params* p, uint32_t* bad_id_count,
+                         q2k_stream_t stream) {
+    g_last_error[0] = '\0';
+    if (p == nullptr) return fail(Q2K_ERR_INVALID_ARGUMENT, "params is NULL");
+    if (p->ggml_type != Q2K_GGML_TYPE_Q2_K)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "ggml_type %u is not Q2_K (10)", p->ggml_type);
+    if (p->n_tokens == 0 || p->top_k == 0 || p->n == 0 || p->k == 0 || p->n_experts == 0)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "n_tokens, top_k, n, k and n_experts must be >= 1");
+    if (p->k % Q2K_QK_K != 0)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "k = %u is not a multiple of 256", p->k);
+    if (p->n > INT_MAX || p->k > INT_MAX)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "n and k must fit in a signed 32-bit int");
+    size_t routes, expert_bytes, want_x, want_y, last;
+    if (!mul_ok(p->n_tokens, p->top_k, &routes) ||
+        !mul_ok(p->n, size_t(p->k / Q2K_QK_K) * Q2K_BLOCK_BYTES, &expert_bytes) ||
+        !mul_ok(p->n_tokens, p->k, &want_x) || !mul_ok(routes, p->n, &want_y) ||
+        !mul_ok(p->n_experts - 1u, p->expert_stride, &last) || last > SIZE_MAX - expert_bytes ||
+        want_x > SIZE_MAX / 4 || want_y > SIZE_MAX / 4)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "routed shape overflows size_t");
+    if (routes > 65535)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "n_tokens * top_k must be <= 65535, got %zu", routes);
+    if (p->expert_stride % 4 != 0 || p->expert_stride < expert_bytes)
+        return fail(Q2K_ERR_INVALID_ARGUMENT,
+                    "expert_stride %llu must be a multiple of 4 and >= n*k/256*84 = %zu",
+                    static_cast<unsigned long long>(p->expert_stride), expert_bytes);
+    if (x == nullptr || w == nullptr || ids == nullptr || y == nullptr)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "x, w, ids and y must be non-NULL");
+    if (x_elems != want_x)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "x has %zu elements, expected n_tokens*k = %zu", x_elems, want_x);
+    if (w_bytes < last + expert_bytes)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "w has %zu bytes, expected >= (n_experts-1)*expert_stride + "
+                    "n*k/256*84 = %zu", w_bytes, last + expert_bytes);
+    if (y_elems != want_y)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "y has %zu elements, expected n_tokens*top_k*n = %zu",
+                    y_elems, want_y);
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(w, 4) || !aligned(ids, 4) ||
+        (bad_id_count != nullptr && !aligned(bad_id_count, 4)))
+        return fail(Q2K_ERR_INVALID_ARGUMENT,
+                    "x and y must be 16-byte aligned, w, ids and bad_id_count 4-byte aligned");
+    const size_t y_bytes = want_y * 4;
+    if (overlaps(y, y_bytes, x, want_x * 4) || overlaps(y, y_bytes, w, w_bytes) ||
+        overlaps(y, y_bytes, ids, routes * 4) ||
+        (bad_id_count != nullptr &&
+         (overlaps(bad_id_count, 4, y, y_bytes) || overlaps(bad_id_count, 4, x, want_x * 4) ||
+          overlaps(bad_id_count, 4, w, w_bytes) || overlaps(bad_id_count, 4, ids, routes * 4))))
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "writable buffers must not alias inputs or each other");
+    DeviceInfo dev;
+    q2k_status st = current_device(&dev);
+    if (st != Q2K_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (bad_id_count != nullptr) e = cudaMemsetAsync(bad_id_count, 0, 4, s);
+    if (e != cudaSuccess) return cuda_fail(e, "q2k_matmul_id: clearing bad_id_count");
+    q2k::GemvProblems pr;
+    pr.w_stride = static_cast<long long>(p->expert_stride);
+    pr.y_stride = static_cast<long long>(p->n);
+    pr.ids = ids;
+    pr.n_experts = p->n_experts;
+    pr.top_k = p->top_k;
+    pr.bad_ids = bad_id_count;
+    e = q2k::launch_gemv_problems(x, static_cast<const uint8_t*>(w), y, 1, int(p->n), int(p->k),
+                                  dev.device, dev.sm_count, 0u, pr, int(routes), s);
+    return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul_id launch");
 }
 
 q2k_status q2k_selftest_wait_timeout(uint32_t limit_us, q2k_stream_t stream) {

@@ -231,33 +231,41 @@ __device__ __forceinline__ float transpose_reduce4(float (&v)[kRowBatch], int la
 }
 
 // Bulk copies of the CTA's weight rows into shared memory, kPieceRows rows per
-// mbarrier (each completes when its bytes have landed).  Piece starts are
-// 16-byte aligned (the host plan keeps chunk starts aligned); the ragged end of
-// the last piece (a multiple of 4 bytes below 16) is copied with plain loads
-// before the barrier's arrival.  Lane 0 of warp w issues pieces w, w + nwarps,
-// ...: one thread's bulk copies complete one after another, so spreading them
-// over the warps multiplies the rate at which the chunk lands.
-__device__ __forceinline__ void issue_weight_copies(uint8_t* smem, const uint8_t* gsrc,
+// mbarrier (each completes when its bytes have landed).  W needs only 4-byte
+// alignment: the host plan keeps every piece start at the same offset delta
+// (0, 4, 8 or 12) from a 16-byte boundary, and the chunk sits at smem_w =
+// 16-byte boundary + delta, so the 16-byte-aligned middle of each piece goes by
+// bulk copy and its head and ragged tail (multiples of 4 bytes below 16) by
+// plain loads before the barrier's arrival.  Lane 0 of warp w issues pieces w,
+// w + nwarps, ...: one thread's bulk copies complete one after another, so
+// spreading them over the warps multiplies the rate at which the chunk lands.
+__device__ __forceinline__ void issue_weight_copies(uint8_t* smem_w, const uint8_t* gsrc,
                                                     uint32_t bars, int rows, size_t row_bytes,
-                                                    int first, int step) {
+                                                    uint32_t delta, int first, int step) {
     const int n_pieces = (rows + kPieceRows - 1) / kPieceRows;
+    const size_t head = (16u - delta) & 15u;
     for (int p = first; p < n_pieces; p += step) {
         const int ra = p * kPieceRows;
         const int rb = min(rows, ra + kPieceRows);
         const size_t off = static_cast<size_t>(ra) * row_bytes;
         const size_t bytes = static_cast<size_t>(rb - ra) * row_bytes;
-        const size_t bulk = bytes & ~size_t(15);
-        for (size_t t = bulk; t < bytes; t += 4)
-            *reinterpret_cast<uint32_t*>(smem + off + t) =
+        const size_t bulk = (bytes - head) & ~size_t(15);  // bytes >= 84 > head
+        for (size_t t = 0; t < head; t += 4)
+            *reinterpret_cast<uint32_t*>(smem_w + off + t) =
+                *reinterpret_cast<const uint32_t*>(gsrc + off + t);
+        for (size_t t = head + bulk; t < bytes; t += 4)
+            *reinterpret_cast<uint32_t*>(smem_w + off + t) =
                 *reinterpret_cast<const uint32_t*>(gsrc + off + t);
         mbar_arrive_expect_tx(bars + 8 * p, static_cast<uint32_t>(bulk));
-        bulk_copy_g2s(smem_u32(smem + off), gsrc + off, static_cast<uint32_t>(bulk), bars + 8 * p);
+        bulk_copy_g2s(smem_u32(smem_w + off + head), gsrc + off + head, static_cast<uint32_t>(bulk),
+                      bars + 8 * p);
     }
 }
 
 __global__ void __launch_bounds__(256, 1)
 gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
-               int N, int K, int rows_per_cta, int slices_pad, int groups, uint32_t flags) {
+               int N, int K, int rows_per_cta, int slices_pad, int groups, uint32_t flags,
+               GemvProblems pr) {
     const bool independent = (flags & kGemvIndependent) != 0;
     const bool const_weights = independent || (flags & kGemvConstWeights) != 0;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -269,11 +277,34 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     const size_t row_bytes = static_cast<size_t>(B) * kBlockBytes;
     const int r0 = blockIdx.x * rows_per_cta;
     const int rows = min(rows_per_cta, N - r0);
+    // Problem blockIdx.y of a batch (strided x, W, y) or of a routed product
+    // (x row p / top_k, the W of expert ids[p]); one problem: all strides 0.
+    const int prob = blockIdx.y;
+    if (pr.ids != nullptr) {
+        pdl_wait_prerequisites();  // the ids (and x) may come from the grid before this one
+        const uint32_t e = pr.ids[prob];
+        if (e >= pr.n_experts) {
+            // no such expert: this route's outputs are zeros and the bad id is counted
+            for (int lr = tid; lr < rows; lr += nthreads)
+                y[static_cast<size_t>(prob) * pr.y_stride + r0 + lr] = 0.f;
+            if (blockIdx.x == 0 && tid == 0 && pr.bad_ids != nullptr) atomicAdd(pr.bad_ids, 1u);
+            return;
+        }
+        x += static_cast<size_t>(prob / pr.top_k) * K;
+        w += static_cast<size_t>(e) * pr.w_stride;
+    } else {
+        x += static_cast<size_t>(prob) * pr.x_stride;
+        w += static_cast<size_t>(prob) * pr.w_stride;
+    }
+    y += static_cast<size_t>(prob) * pr.y_stride;
+    const uint32_t delta = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(w) & 15u);
     const int n_pieces = (rows + kPieceRows - 1) / kPieceRows;
     const int max_pieces = (rows_per_cta + kPieceRows - 1) / kPieceRows;
     const int warps_per_group = slices_pad >> 5;
-    // shared layout: W chunk | run planes | run sums | run scales | red | bars | flag
-    const size_t w_smem = (static_cast<size_t>(rows_per_cta) * row_bytes + 15) & ~size_t(15);
+    // shared layout: W chunk (at offset delta) | run planes | run sums | run
+    // scales | red | bars | flag
+    const size_t w_smem = (static_cast<size_t>(rows_per_cta) * row_bytes + 31) & ~size_t(15);
+    uint8_t* smem_w = smem + delta;
     uint32_t* planes = reinterpret_cast<uint32_t*>(smem + w_smem);
     float* run_sum = reinterpret_cast<float*>(planes + (n_runs >> 2) * kSlicePitch);
     float* run_inv = run_sum + n_runs;
@@ -302,19 +333,22 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     if (const_weights) {
         // The caller guarantees the grids that may still run do not write W,
         // so the weight copies may start before the dependency wait.
-        if (issuer) issue_weight_copies(smem, gsrc, bars, rows, row_bytes, tid >> 5, nwarps);
+        if (issuer) issue_weight_copies(smem_w, gsrc, bars, rows, row_bytes, delta, tid >> 5, nwarps);
     } else if (tid == 0) {
-        // An L2 prefetch is coherent with the previous grid's writes.
-        const size_t pre = chunk & ~size_t(15);
+        // An L2 prefetch is coherent with the previous grid's writes (its
+        // 16-byte-aligned part; the few bytes around it come with the copies).
+        const size_t head = (16u - delta) & 15u;
+        const size_t pre = (chunk - head) & ~size_t(15);
         for (size_t off = 0; off < pre; off += (size_t(1) << 20)) {
             const size_t left = pre - off;
-            bulk_prefetch_l2(gsrc + off, static_cast<uint32_t>(left < (size_t(1) << 20) ? left : (size_t(1) << 20)));
+            bulk_prefetch_l2(gsrc + head + off,
+                             static_cast<uint32_t>(left < (size_t(1) << 20) ? left : (size_t(1) << 20)));
         }
     }
     if (!independent) pdl_wait_prerequisites();
     __syncthreads();
     if (issuer && !const_weights)
-        issue_weight_copies(smem, gsrc, bars, rows, row_bytes, tid >> 5, nwarps);
+        issue_weight_copies(smem_w, gsrc, bars, rows, row_bytes, delta, tid >> 5, nwarps);
     // x -> integer planes, once per CTA, while the weights stream in
     for (int r = tid; r < n_runs; r += nthreads) {
         // run r = (block, half, shift j, segment): slice 4 block + 2 half + segment
@@ -360,7 +394,7 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
 
     const int lane = tid & 31;
     const int wig = sl >> 5;  // warp index within the group
-    const uint8_t* my_col = smem + b * kBlockBytes;
+    const uint8_t* my_col = smem_w + b * kBlockBytes;
     int waited = const_weights ? n_pieces - 1 : -1;
     bool ok = !(const_weights && *abort_flag);
     constexpr int kLoad = 2 * kRowBatch;  // rows loaded and decoded together
@@ -422,7 +456,7 @@ size_t m1_smem(int rows, int K, int slices_pad) {
     const size_t row_bytes = static_cast<size_t>(K / 256) * kBlockBytes;
     const int n_runs = K / 16;
     const int pieces = (rows + kPieceRows - 1) / kPieceRows;
-    const size_t w_smem = (static_cast<size_t>(rows) * row_bytes + 15) & ~size_t(15);
+    const size_t w_smem = (static_cast<size_t>(rows) * row_bytes + 31) & ~size_t(15);
     const size_t red_end = w_smem + static_cast<size_t>(n_runs / 4) * kSlicePitch * 4 +
                            static_cast<size_t>(n_runs) * 8 + static_cast<size_t>(rows) * (slices_pad / 32) * 4;
     return ((red_end + 7) & ~size_t(7)) + 8 * pieces + 16;
@@ -455,7 +489,8 @@ bool plan_m1(int N, int K, int sm_count, int threads, bool whole_batches, M1Plan
 }
 
 cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, const M1Plan& p,
-                      int device, uint32_t flags, cudaStream_t stream) {
+                      int device, uint32_t flags, const GemvProblems& pr, int n_problems,
+                      cudaStream_t stream) {
     static bool smem_set[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!smem_set[device]) {
@@ -466,7 +501,7 @@ cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, 
         smem_set[device] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.ctas);
+    cfg.gridDim = dim3(p.ctas, n_problems);
     cfg.blockDim = dim3(p.threads);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
@@ -476,7 +511,7 @@ cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, gemv_m1_kernel, x, w, y, N, K, p.rows_per_cta, p.slices_pad,
-                              p.groups, flags);
+                              p.groups, flags, pr);
 }
 
 // ------------------------------------------------------------------ general m
@@ -484,10 +519,26 @@ cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, 
 template <int MT>
 __global__ void __launch_bounds__(kGemvWarps * 32)
 gemv_rows_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
-                 int M, int N, int K) {
+                 int M, int N, int K, GemvProblems pr) {
     const int lane = threadIdx.x & 31;
     const int n = blockIdx.x * kGemvWarps + (threadIdx.x >> 5);
     if (n >= N) return;  // whole warp leaves together
+    // problem blockIdx.z, as in gemv_m1_kernel (one x row per problem there)
+    const int prob = blockIdx.z;
+    if (pr.ids != nullptr) {
+        const uint32_t e = pr.ids[prob];
+        if (e >= pr.n_experts) {
+            if (lane == 0) y[static_cast<size_t>(prob) * pr.y_stride + n] = 0.f;
+            if (n == 0 && lane == 0 && pr.bad_ids != nullptr) atomicAdd(pr.bad_ids, 1u);
+            return;
+        }
+        x += static_cast<size_t>(prob / pr.top_k) * K;
+        w += static_cast<size_t>(e) * pr.w_stride;
+    } else {
+        x += static_cast<size_t>(prob) * pr.x_stride;
+        w += static_cast<size_t>(prob) * pr.w_stride;
+    }
+    y += static_cast<size_t>(prob) * pr.y_stride;
     const int m0 = blockIdx.y * MT;
     const int mcount = min(MT, M - m0);
     const int B = K >> 8;
@@ -563,31 +614,36 @@ gemv_rows_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, flo
 
 template <int MT>
 cudaError_t launch_rows(const float* x, const uint8_t* w, float* y, int M, int N, int K,
-                        cudaStream_t stream) {
-    dim3 grid((N + kGemvWarps - 1) / kGemvWarps, (M + MT - 1) / MT);
-    gemv_rows_kernel<MT><<<grid, kGemvWarps * 32, 0, stream>>>(x, w, y, M, N, K);
+                        const GemvProblems& pr, int n_problems, cudaStream_t stream) {
+    dim3 grid((N + kGemvWarps - 1) / kGemvWarps, (M + MT - 1) / MT, n_problems);
+    gemv_rows_kernel<MT><<<grid, kGemvWarps * 32, 0, stream>>>(x, w, y, M, N, K, pr);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N, int K,
-                        int device, int sm_count, uint32_t flags, cudaStream_t stream) {
+cudaError_t launch_gemv_problems(const float* x, const uint8_t* w, float* y, int M, int N, int K,
+                                 int device, int sm_count, uint32_t flags,
+                                 const GemvProblems& pr, int n_problems, cudaStream_t stream) {
     M1Plan plan;
     const int threads = (flags & kGemvIndependent) ? kM1ThreadsIndependent : kM1ThreadsDependent;
-    if (M == 1 && (reinterpret_cast<uintptr_t>(w) & 15u) == 0 &&
-        plan_m1(N, K, sm_count, threads, (flags & kGemvIndependent) != 0, &plan))
-        return launch_m1(x, w, y, N, K, plan, device, flags, stream);
+    if (M == 1 && plan_m1(N, K, sm_count, threads, (flags & kGemvIndependent) != 0, &plan))
+        return launch_m1(x, w, y, N, K, plan, device, flags, pr, n_problems, stream);
     switch (M < 8 ? M : 8) {
-        case 1: return launch_rows<1>(x, w, y, M, N, K, stream);
-        case 2: return launch_rows<2>(x, w, y, M, N, K, stream);
-        case 3: return launch_rows<3>(x, w, y, M, N, K, stream);
-        case 4: return launch_rows<4>(x, w, y, M, N, K, stream);
-        case 5: return launch_rows<5>(x, w, y, M, N, K, stream);
-        case 6: return launch_rows<6>(x, w, y, M, N, K, stream);
-        case 7: return launch_rows<7>(x, w, y, M, N, K, stream);
-        default: return launch_rows<8>(x, w, y, M, N, K, stream);
+        case 1: return launch_rows<1>(x, w, y, M, N, K, pr, n_problems, stream);
+        case 2: return launch_rows<2>(x, w, y, M, N, K, pr, n_problems, stream);
+        case 3: return launch_rows<3>(x, w, y, M, N, K, pr, n_problems, stream);
+        case 4: return launch_rows<4>(x, w, y, M, N, K, pr, n_problems, stream);
+        case 5: return launch_rows<5>(x, w, y, M, N, K, pr, n_problems, stream);
+        case 6: return launch_rows<6>(x, w, y, M, N, K, pr, n_problems, stream);
+        case 7: return launch_rows<7>(x, w, y, M, N, K, pr, n_problems, stream);
+        default: return launch_rows<8>(x, w, y, M, N, K, pr, n_problems, stream);
     }
+}
+
+cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N, int K,
+                        int device, int sm_count, uint32_t flags, cudaStream_t stream) {
+    return launch_gemv_problems(x, w, y, M, N, K, device, sm_count, flags, GemvProblems{}, 1, stream);
 }
 
 namespace {

@@ -15,7 +15,7 @@ cudaError_t launch_gather(const uint8_t* table, const uint32_t* ids, float* out,
                           int sm_count, cudaStream_t stream);
 
 // fp32 GEMV path: m = 1 uses the shared-memory streaming kernel when K <= 16384
-// and w is 16-byte aligned; otherwise x rows are handled 8 at a time.
+// (any 4-byte-aligned w); otherwise x rows are handled 8 at a time.
 // flags (m = 1 kernel only):
 //   kGemvConstWeights  the kernels that may still run do not write w: weight
 //                      loads may start before the programmatic-launch wait;
@@ -25,6 +25,27 @@ constexpr uint32_t kGemvConstWeights = 1u;
 constexpr uint32_t kGemvIndependent = 2u;
 cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N, int K,
                         int device, int sm_count, uint32_t flags, cudaStream_t stream);
+
+// Several independent products in one launch of the GEMV kernels, each computed
+// exactly as its own launch_gemv call (same kernel, same arithmetic), problem p
+// being either
+//   batched (ids == nullptr): x + p x_stride, w + p w_stride -> y + p y_stride;
+//   routed: x row p / top_k and the weights of expert ids[p] at w + ids[p]
+//           w_stride -> y + p y_stride.  An id >= n_experts gives zeros and
+//           adds 1 to *bad_ids (when not null).
+// Strides in elements (x, y) and bytes (w).  All zero: one problem.
+struct GemvProblems {
+    long long x_stride = 0;
+    long long w_stride = 0;
+    long long y_stride = 0;
+    const uint32_t* ids = nullptr;
+    uint32_t n_experts = 0;
+    uint32_t top_k = 1;
+    unsigned int* bad_ids = nullptr;
+};
+cudaError_t launch_gemv_problems(const float* x, const uint8_t* w, float* y, int M, int N, int K,
+                                 int device, int sm_count, uint32_t flags,
+                                 const GemvProblems& pr, int n_problems, cudaStream_t stream);
 
 // Self-test of the bounded wait: one CTA waits for about limit_ns on a barrier
 // nothing completes, then sets the GEMV error word's time-out bit.

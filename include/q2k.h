@@ -77,6 +77,20 @@ typedef struct q2k_embedding_params {
     uint32_t ggml_type;  /* must be Q2K_GGML_TYPE_Q2_K */
 } q2k_embedding_params;
 
+/* The pages' GgmlQuantizedMatmulIdParams {n_tokens, top_k, n, k, n_experts,
+ * expert_stride, ggml_type} (page "tests/deepseek_q2_k.rs", fn run_expert),
+ * the 32-bit fields first so the struct has no padding: 32 bytes. */
+typedef struct q2k_matmul_id_params {
+    uint32_t n_tokens;      /* tokens (rows of x), >= 1 */
+    uint32_t top_k;         /* experts per token, >= 1 */
+    uint32_t n;             /* weight rows of each expert = output columns, >= 1 */
+    uint32_t k;             /* reduction length, a positive multiple of 256 */
+    uint32_t n_experts;     /* experts in w, >= 1 */
+    uint32_t ggml_type;     /* must be Q2K_GGML_TYPE_Q2_K */
+    uint64_t expert_stride; /* bytes from one expert's matrix to the next, a multiple
+                               of 4 and >= n * k/256 * 84 */
+} q2k_matmul_id_params;
+
 /* Which kernel q2k_matmul_path runs (the pages' forced-path test hooks
  * dispatch_mm_for_test / dispatch_mm_simd_for_test). */
 typedef enum q2k_path {
@@ -155,6 +169,48 @@ enum {
      * stream order.  Implies Q2K_FLAG_CONST_WEIGHTS.  Other paths ignore it. */
     Q2K_FLAG_INDEPENDENT = 2
 };
+
+/* q2k_matmul_batched_mv - `batches` independent matrix-vector products in one
+ * launch: y[b, 0, :] = W_b x[b, 0, :].
+ * Page "tests/deepseek_q2_k.rs": fn quantized_matmul_q2_k_batched_mv and test
+ * q2_k_batched_mv_is_byte_identical_to_independent_dispatches.
+ *   x   device f32 [batches, m, k], x_elems = batches*m*k, 16-byte aligned
+ *   w   device, w_bytes = batches * n*k/256*84, 4-byte aligned; batch b's
+ *       [n, k] matrix starts at byte b * n*k/256*84
+ *   y   device f32 [batches, m, n], y_elems = batches*m*n, 16-byte aligned;
+ *       fully overwritten, must not alias x or w
+ *   m   must be 1 (the pages' call passes 1: matrix-vector)
+ * Each batch's y is bit-identical to q2k_matmul(m = 1) of that batch's x and W
+ * alone (the same kernel and arithmetic run per batch): fp32, error within
+ * 1e-5 * sum_k |x w|.  batches <= 65535. */
+q2k_status q2k_matmul_batched_mv(const float *x, size_t x_elems, const void *w, size_t w_bytes,
+                                 float *y, size_t y_elems, uint32_t batches, uint32_t m,
+                                 uint32_t n, uint32_t k, q2k_stream_t stream);
+
+/* q2k_matmul_id - the expert-routed product of a mixture-of-experts layer:
+ * y[r, :] = W_{ids[r]} x[r / top_k, :] for every route r = t*top_k + slot.
+ * Page "tests/deepseek_q2_k.rs": fn quantized_matmul_id_ggml, fn run_expert and
+ * tests q2_k_expert_routed_metal_matches_reference / ..._top_k_6_...
+ *   x       device f32 [n_tokens, k], x_elems = n_tokens*k, 16-byte aligned
+ *   w       device, the n_experts matrices [n, k], expert e at byte
+ *           e * expert_stride; w_bytes >= (n_experts - 1) * expert_stride +
+ *           n*k/256*84; 4-byte aligned
+ *   ids     device u32 [n_tokens * top_k], token-major (route t*top_k + slot)
+ *   y       device f32 [n_tokens * top_k, n], y_elems = n_tokens*top_k*n,
+ *           16-byte aligned; fully overwritten, must not alias x, w or ids
+ *   bad_id_count  device u32 or NULL.  Ids live on the device, so they are
+ *           checked in the kernel: a route whose id is >= n_experts gets a
+ *           zero row and, when bad_id_count is not NULL, is counted there
+ *           (the call zeroes it first, stream-ordered).  Read it after the
+ *           stream completes; nonzero means the pages' error.
+ * Every route runs the fp32 GEMV (error within 1e-5 * sum_k |x w|; the pages
+ * allow 2e-4 absolute, 1e-2 for their reduced-precision path); each route's
+ * row is bit-identical to q2k_matmul(m = 1) of its token and expert.
+ * n_tokens * top_k <= 65535. */
+q2k_status q2k_matmul_id(const float *x, size_t x_elems, const void *w, size_t w_bytes,
+                         const uint32_t *ids, float *y, size_t y_elems,
+                         const q2k_matmul_id_params *params, uint32_t *bad_id_count,
+                         q2k_stream_t stream);
 
 /* q2k_matmul_workspace_bytes - device bytes of workspace q2k_matmul_ex can use
  * for this geometry and path (0: the path takes none).  The tensor-core path

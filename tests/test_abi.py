@@ -24,7 +24,8 @@ def lib():
 def test_header_declares_the_calls():
     names = q2k.header_functions()
     for want in ("q2k_dequantize", "q2k_embedding_gather", "q2k_matmul", "q2k_matmul_path",
-                 "q2k_matmul_ex", "q2k_device_error", "q2k_last_error", "q2k_abi_version"):
+                 "q2k_matmul_ex", "q2k_matmul_batched_mv", "q2k_matmul_id", "q2k_device_error",
+                 "q2k_last_error", "q2k_abi_version"):
         assert want in names
 
 
@@ -41,14 +42,19 @@ def test_struct_layout_matches_c(tmp_path):
     src = tmp_path / "layout.c"
     src.write_text(
         '#include <stddef.h>\n#include <stdio.h>\n#include "q2k.h"\n'
-        "int main(void){printf(\"%zu %zu %zu %zu %zu\\n\", sizeof(q2k_matmul_params),"
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(q2k_matmul_params),"
         " offsetof(q2k_matmul_params, ggml_type), sizeof(q2k_embedding_params),"
-        " offsetof(q2k_embedding_params, n_tokens), sizeof(q2k_status));return 0;}\n")
+        " offsetof(q2k_embedding_params, n_tokens), sizeof(q2k_status),"
+        " sizeof(q2k_matmul_id_params), offsetof(q2k_matmul_id_params, ggml_type),"
+        " offsetof(q2k_matmul_id_params, expert_stride));return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", q2k_build.INCLUDE, str(src),
                     "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
-    assert [int(v) for v in out] == [16, 12, 16, 8, 4]
+    assert [int(v) for v in out] == [16, 12, 16, 8, 4, 32, 20, 24]
+    assert ctypes.sizeof(q2k.MatmulIdParams) == 32
+    assert q2k.MatmulIdParams.ggml_type.offset == 20
+    assert q2k.MatmulIdParams.expert_stride.offset == 24
     assert ctypes.sizeof(q2k.MatmulParams) == 16
     assert ctypes.sizeof(q2k.EmbeddingParams) == 16
     assert q2k.MatmulParams.ggml_type.offset == 12
@@ -155,3 +161,58 @@ def test_selftest_wait_timeout_rejects_out_of_range_limits(lib):
     for bad in (0, 100001):
         assert lib.q2k_selftest_wait_timeout(bad, None) == INVALID
         assert "limit_us" in lib.q2k_last_error().decode()
+
+
+def _bmv(lib, batches=3, m=1, n=8, k=256, xe=None, wb=None, ye=None, x=0x10000, w=0x100000,
+         y=0x1000000):
+    xe = batches * k if xe is None else xe
+    wb = batches * n * (k // 256) * 84 if wb is None else wb
+    ye = batches * n if ye is None else ye
+    return lib.q2k_matmul_batched_mv(x, xe, w, wb, y, ye, batches, m, n, k, None)
+
+
+@pytest.mark.parametrize("kw,fragment", [
+    (dict(m=2), "m = 1"),
+    (dict(batches=0), "batches"),
+    (dict(batches=65536), "batches"),
+    (dict(k=255), "multiple of 256"),
+    (dict(xe=3 * 256 - 1), "batched sizes"),
+    (dict(wb=3 * 8 * 84 + 84), "batched sizes"),
+    (dict(ye=3 * 8 + 1), "batched sizes"),
+    (dict(x=0x10004), "aligned"),
+    (dict(y=0x100000 + 112), "alias"),
+])
+def test_batched_mv_rejects(lib, kw, fragment):
+    """Checked before any device work (the fake addresses are never touched)."""
+    assert _bmv(lib, **kw) == INVALID
+    assert fragment in lib.q2k_last_error().decode()
+
+
+def _mid(lib, n_tokens=2, top_k=2, n=8, k=256, n_experts=3, stride=None, xe=None, wb=None,
+         ye=None, ids=0x3000000, x=0x10000, w=0x100000, y=0x1000000, ggml_type=10):
+    stride = n * (k // 256) * 84 if stride is None else stride
+    p = q2k.MatmulIdParams(n_tokens, top_k, n, k, n_experts, ggml_type, stride)
+    xe = n_tokens * k if xe is None else xe
+    wb = (n_experts - 1) * stride + n * (k // 256) * 84 if wb is None else wb
+    ye = n_tokens * top_k * n if ye is None else ye
+    return lib.q2k_matmul_id(x, xe, w, wb, ids, y, ye, ctypes.byref(p), None, None)
+
+
+@pytest.mark.parametrize("kw,fragment", [
+    (dict(ggml_type=12), "Q2_K"),
+    (dict(top_k=0), ">= 1"),
+    (dict(n_experts=0), ">= 1"),
+    (dict(k=300), "multiple of 256"),
+    (dict(stride=8 * 84 - 4), "expert_stride"),
+    (dict(stride=8 * 84 + 2), "expert_stride"),
+    (dict(wb=2 * 8 * 84 + 8 * 84 - 1), "w has"),
+    (dict(xe=511), "x has"),
+    (dict(ye=31), "y has"),
+    (dict(ids=0), "non-NULL"),
+    (dict(n_tokens=40000, top_k=2, xe=40000 * 256, ye=80000 * 8), "65535"),
+    (dict(ids=0x1000000 + 8), "alias"),
+    (dict(w=0x100002), "aligned"),
+])
+def test_matmul_id_rejects(lib, kw, fragment):
+    assert _mid(lib, **kw) == INVALID
+    assert fragment in lib.q2k_last_error().decode()

@@ -1,0 +1,177 @@
+"""GPU parity of the batched matrix-vector and expert-routed (mm_id) products.
+
+Each is checked two ways: against the CPU oracle's definition (fp32 path
+bound, |y - y_ref| <= 1e-5 * S) and bit for bit against the single m = 1
+matmul of the same batch / route, which the pages require of the batched call
+(test q2_k_batched_mv_is_byte_identical_to_independent_dispatches) and which
+holds here for the routed call too (the same kernel runs per route).
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import q2k_workloads as wl
+
+torch = pytest.importorskip("torch")
+import ggml_q2_quantized_gb300 as q2k  # noqa: E402
+from ggml_q2_quantized_gb300 import build as q2k_build  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+TOL_GEMV = 1e-5
+ORACLE_THREADS = 16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    q2k_build.build()
+    q2k.load()
+    yield
+    assert q2k.device_error() == 0, "a kernel gave up waiting on a barrier"
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def assert_close(y, yref, s, tol, what):
+    err = np.abs(y - yref)
+    assert not np.isnan(y).any(), f"{what}: NaN"
+    bad = err > tol * s
+    assert not bad.any(), f"{what}: {int(bad.sum())} outputs out of tolerance"
+
+
+def bits_equal(a, b):
+    return torch.equal(a.contiguous().view(torch.int32), b.contiguous().view(torch.int32))
+
+
+# ------------------------------------------------------------------ batched mv
+
+def test_batched_mv_page_case_byte_identical():
+    """The page's case: 3 batches of 8 rows block(8 b + r + 1), inputs input(3)."""
+    batches, n = 3, 8
+    w = np.concatenate([wl.page_block(b * n + r + 1) for b in range(batches) for r in range(n)])
+    x = wl.page_input(batches)
+    wd, xd = dev(w), dev(x)
+    y = q2k.matmul_batched_mv(xd, wd, n)
+    per = n * 84
+    serial = torch.stack([q2k.matmul(xd[b:b + 1], wd[b * per:(b + 1) * per], n)[0]
+                          for b in range(batches)])
+    torch.cuda.synchronize()
+    assert bits_equal(y, serial)
+    yref, s = oracle.matmul_batched_mv(x, w, n)
+    assert_close(y.cpu().numpy().astype(np.float64), yref, s, TOL_GEMV, "page batched")
+    assert np.abs(y.cpu().numpy() - yref).max() <= 2e-4   # the page's dense tolerance
+
+
+@pytest.mark.parametrize("batches,n,k", [
+    (5, 333, 512),     # batch strides 55944 B: every other batch's W is 8 bytes off 16
+    (4, 1000, 4096),   # aligned strides, several CTAs per batch
+    (2, 40, 16640),    # k > 16384: the row-per-warp kernel for every batch
+])
+def test_batched_mv_random_byte_identical(batches, n, k):
+    rng = np.random.default_rng(batches * n + k)
+    w = wl.random_blocks(rng, batches * n * (k // 256)).reshape(-1)
+    x = wl.random_activations(rng, batches, k)
+    wd, xd = dev(w), dev(x)
+    y = q2k.matmul_batched_mv(xd, wd, n)
+    per = n * (k // 256) * 84
+    serial = torch.stack([q2k.matmul(xd[b:b + 1], wd[b * per:(b + 1) * per], n)[0]
+                          for b in range(batches)])
+    torch.cuda.synchronize()
+    assert bits_equal(y, serial)
+    yref, s = oracle.matmul_batched_mv(x, w, n, threads=ORACLE_THREADS)
+    assert_close(y.cpu().numpy().astype(np.float64), yref, s, TOL_GEMV, f"batched {batches}x{n}x{k}")
+
+
+@pytest.mark.parametrize("offset", [4, 8, 12])
+def test_single_matmul_with_w_off_16_byte_boundary(offset):
+    """The m = 1 kernel takes any 4-byte-aligned W (head bytes by plain loads)."""
+    n, k = 77, 1024
+    x, w = wl.make_matmul_inputs(31 + offset, 1, n, k)
+    buf = torch.zeros(w.size + 16, dtype=torch.uint8, device="cuda")
+    buf[offset:offset + w.size].copy_(dev(w))
+    y = q2k.matmul(dev(x), buf[offset:offset + w.size], n)
+    torch.cuda.synchronize()
+    yref, s = oracle.matmul(x, w, n)
+    assert_close(y.cpu().numpy().astype(np.float64), yref, s, TOL_GEMV, f"offset {offset}")
+
+
+# ------------------------------------------------------------------ mm_id
+
+def _expert_case(tokens, top_k, experts, n=8, gap=0):
+    parts = []
+    for e in range(experts):
+        parts.extend(wl.page_block(e * n + r + 1) for r in range(n))
+        parts.append(np.full(gap, 0xFF, dtype=np.uint8))
+    w = np.concatenate(parts)
+    ids = np.array([(3 * t + slot) % experts for t in range(tokens) for slot in range(top_k)],
+                   dtype=np.uint32)
+    return w, wl.page_input(tokens), ids, n * 84 + gap
+
+
+def _route_serial(xd, wd, ids, n, k, top_k, stride):
+    rows = []
+    size = n * (k // 256) * 84
+    for r, e in enumerate(ids.tolist()):
+        t = r // top_k
+        rows.append(q2k.matmul(xd[t:t + 1], wd[e * stride:e * stride + size], n)[0])
+    return torch.stack(rows)
+
+
+@pytest.mark.parametrize("tokens,top_k,experts", [(2, 2, 3), (33, 6, 8)])
+def test_matmul_id_page_cases(tokens, top_k, experts):
+    """Page fn run_expert (2, 2, 3) and (33, 6, 8)."""
+    n = 8
+    w, x, ids, stride = _expert_case(tokens, top_k, experts, n)
+    wd, xd, idd = dev(w), dev(x), dev(ids.view(np.int32))
+    y = q2k.matmul_id(xd, wd, idd, n, experts, top_k)
+    serial = _route_serial(xd, wd, ids, n, 256, top_k, stride)
+    torch.cuda.synchronize()
+    assert bits_equal(y, serial)
+    yref, s = oracle.matmul_id(x, w, ids, n, experts, stride, top_k)
+    got = y.cpu().numpy().astype(np.float64)
+    assert_close(got, yref, s, TOL_GEMV, f"run_expert({tokens}, {top_k}, {experts})")
+    assert np.abs(got - yref).max() <= 2e-4   # the page's tolerance for this case
+
+
+def test_matmul_id_random_strided_experts():
+    """Larger experts, an expert stride 20 bytes past the matrix (so experts sit
+    at different offsets from a 16-byte boundary), random ids."""
+    tokens, top_k, experts, n, k = 16, 4, 8, 512, 2048
+    rng = np.random.default_rng(5)
+    size = n * (k // 256) * 84
+    stride = size + 20
+    w = np.zeros((experts - 1) * stride + size, dtype=np.uint8)
+    for e in range(experts):
+        w[e * stride:e * stride + size] = wl.random_blocks(rng, n * (k // 256)).reshape(-1)
+    x = wl.random_activations(rng, tokens, k)
+    ids = rng.integers(0, experts, tokens * top_k).astype(np.uint32)
+    wd, xd, idd = dev(w), dev(x), dev(ids.view(np.int32))
+    y = q2k.matmul_id(xd, wd, idd, n, experts, top_k, expert_stride=stride)
+    serial = _route_serial(xd, wd, ids, n, k, top_k, stride)
+    torch.cuda.synchronize()
+    assert bits_equal(y, serial)
+    yref, s = oracle.matmul_id(x, w, ids, n, experts, stride, top_k, threads=ORACLE_THREADS)
+    assert_close(y.cpu().numpy().astype(np.float64), yref, s, TOL_GEMV, "random mm_id")
+
+
+def test_matmul_id_bad_id_gives_zero_row_and_count():
+    tokens, top_k, experts, n = 4, 2, 3, 8
+    w, x, ids, stride = _expert_case(tokens, top_k, experts, n)
+    bad = ids.copy()
+    bad[5] = experts          # out of range
+    bad[6] = 0xFFFFFFFF       # far out of range
+    wd, xd, idd = dev(w), dev(x), dev(bad.view(np.int32))
+    with pytest.raises(q2k.InvalidArgument):
+        q2k.matmul_id(xd, wd, idd, n, experts, top_k)
+    y, count = q2k.matmul_id(xd, wd, idd, n, experts, top_k, check=False)
+    torch.cuda.synchronize()
+    assert int(count.item()) == 2
+    got = y.cpu().numpy()
+    assert (got[5] == 0).all() and (got[6] == 0).all()
+    good = [r for r in range(tokens * top_k) if r not in (5, 6)]
+    yref, s = oracle.matmul_id(x, w, ids, n, experts, stride, top_k)
+    assert_close(got[good].astype(np.float64), yref[good], s[good], TOL_GEMV, "good routes")
