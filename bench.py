@@ -280,6 +280,67 @@ def bench_chain(torch, q2k, w: wl.Workload, steps, warmup, l2_bytes, device):
             "calls": "each call's x is the previous call's y (Q2K_FLAG_CONST_WEIGHTS)"}
 
 
+def bench_batched(torch, q2k, w: wl.Workload, batches, steps, warmup, l2_bytes, device):
+    """``batches`` GEMVs of workload ``w`` per batched launch, a stack of distinct
+    batched weight buffers (larger than L2 together), one launch each."""
+    assert w.m == 1
+    per = w.weight_bytes
+    layers = layers_for(per * batches, l2_bytes)
+    inp = wl.make_inputs(w, with_gather=False)
+    mats = stack_of_weights(w, batches, inp.w)  # `batches` distinct matrices
+    bufs = []
+    for l in range(layers):
+        # rotate the matrices so every buffer differs in order (distinct addresses anyway)
+        bufs.append(torch.from_numpy(np.concatenate(mats[l % batches:] + mats[:l % batches]))
+                    .to(device))
+    x = torch.from_numpy(wl.random_activations(np.random.default_rng([w.seed, 99]), batches,
+                                               w.k)).to(device)
+    ys = torch.empty((layers, batches, w.n), dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def step():
+        for l in range(layers):
+            q2k.matmul_batched_mv(x, bufs[l], w.n, out=ys[l])
+
+    g = capture(torch, stream, step)
+    ms = time_graph(torch, g, stream, steps, warmup)
+    us = ms * 1e3 / layers
+    return {"us_per_launch": us, "weight_GBps": batches * per / (us * 1e-6) / 1e9,
+            "batches": batches, "n": w.n, "k": w.k, "launches_per_step": layers,
+            "path": "gemv (batched, one launch)"}
+
+
+def bench_routed(torch, q2k, rw, steps, warmup, device):
+    """mm_id over a pool of ``rw.n_experts`` experts; each launch of a step uses
+    its own ids (fresh experts), so weights come from HBM, not L2."""
+    rng = np.random.default_rng(rw.seed)
+    distinct = 4  # distinct expert matrices, tiled over the pool (timing only)
+    base = [wl.random_blocks(rng, rw.n * (rw.k // wl.QK_K)) for _ in range(distinct)]
+    pool = torch.from_numpy(np.concatenate([base[e % distinct] for e in range(rw.n_experts)])
+                            ).to(device)
+    x = torch.from_numpy(wl.random_activations(rng, rw.n_tokens, rw.k)).to(device)
+    launches = 16
+    ids = [torch.from_numpy(wl.make_routed_ids(rw, i).view(np.int32)).to(device)
+           for i in range(launches)]
+    routes = rw.n_tokens * rw.top_k
+    ys = torch.empty((launches, routes, rw.n), dtype=torch.float32, device=device)
+    bad = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def step():
+        for i in range(launches):
+            q2k.matmul_id(x, pool, ids[i], rw.n, rw.n_experts, rw.top_k, out=ys[i], check=False)
+
+    g = capture(torch, stream, step)
+    ms = time_graph(torch, g, stream, steps, warmup)
+    us = ms * 1e3 / launches
+    uniq = np.mean([len(set(wl.make_routed_ids(rw, i).tolist())) for i in range(launches)])
+    return {"us_per_launch": us, "weight_GBps": uniq * rw.expert_bytes / (us * 1e-6) / 1e9,
+            "n_tokens": rw.n_tokens, "top_k": rw.top_k, "n": rw.n, "k": rw.k,
+            "n_experts": rw.n_experts, "expert_bytes": rw.expert_bytes,
+            "unique_experts_per_launch": float(uniq), "path": "gemv per route (one launch)"}
+
+
 def bench_gather(torch, q2k, w: wl.Workload, steps, warmup, device):
     inp = wl.make_inputs(w)
     table = torch.from_numpy(inp.table).to(device)
@@ -493,6 +554,14 @@ def run_ours(args):
                                                            l2_bytes, device)
         sec["spec_verify_gather"] = bench_gather(torch, q2k, wl.by_name("spec_verify_m16"),
                                                  max(3, steps // 4), 3, device)
+        bb = wl.BATCHED_DECODE_BATCHES
+        r = bench_batched(torch, q2k, wl.by_name("decode_gemv_4096"), bb, max(3, steps // 4), 3,
+                          l2_bytes, device)
+        r["frac_hbm_measured"] = r["weight_GBps"] / peaks["hbm_gbs"]
+        sec[f"batched_mv_{bb}x4096"] = r
+        r = bench_routed(torch, q2k, wl.MOE_DECODE, max(3, steps // 4), 3, device)
+        r["frac_hbm_measured"] = r["weight_GBps"] / peaks["hbm_gbs"]
+        sec[wl.MOE_DECODE.name] = r
         line["secondary"] = sec
         assert q2k.device_error() == 0
 

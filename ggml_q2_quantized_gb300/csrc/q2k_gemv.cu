@@ -472,12 +472,18 @@ bool plan_m1(int N, int K, int sm_count, int threads, bool whole_batches, M1Plan
     // 8 rows) when asked: the loop then never decodes a row twice at the end.
     // Independent calls share the SMs, so fewer CTAs than SMs costs nothing there.
     const int quantum = whole_batches ? groups * 2 * kRowBatch : 1;
+    // Independent calls overlap on the SMs: their CTAs are kept to 72 KB of
+    // shared memory (three share an SM) when 32 rows still fit there, so that
+    // the x conversion every CTA repeats stays a small share of its work;
+    // otherwise, and for dependent calls, the largest chunk that fits is taken.
+    size_t cap = size_t(200) * 1024;
+    if (whole_batches && m1_smem(32, K, slices_pad) <= size_t(72) * 1024) cap = size_t(72) * 1024;
     int rows = 0;
     for (int waves = 1;; ++waves) {
         rows = (N + sm_count * waves - 1) / (sm_count * waves);
         rows = (rows + quantum - 1) / quantum * quantum;
         if (B % 4) rows = (rows + 3) / 4 * 4;  // chunk starts stay 16-byte aligned
-        if (m1_smem(rows, K, slices_pad) <= 200 * 1024 || rows <= kPieceRows) break;
+        if (m1_smem(rows, K, slices_pad) <= cap || rows <= kPieceRows || rows <= quantum) break;
     }
     p->rows_per_cta = rows;
     p->ctas = (N + rows - 1) / rows;
@@ -626,8 +632,13 @@ cudaError_t launch_gemv_problems(const float* x, const uint8_t* w, float* y, int
                                  int device, int sm_count, uint32_t flags,
                                  const GemvProblems& pr, int n_problems, cudaStream_t stream) {
     M1Plan plan;
-    const int threads = (flags & kGemvIndependent) ? kM1ThreadsIndependent : kM1ThreadsDependent;
-    if (M == 1 && plan_m1(N, K, sm_count, threads, (flags & kGemvIndependent) != 0, &plan))
+    // Several problems in one grid overlap on the SMs like independent calls
+    // do, so they take the same small CTAs of whole row batches, planned per
+    // problem.  (Only the K slicing decides the arithmetic of a row, so the
+    // plan never changes a result bit.)
+    const bool small_ctas = (flags & kGemvIndependent) != 0 || n_problems > 1;
+    const int threads = small_ctas ? kM1ThreadsIndependent : kM1ThreadsDependent;
+    if (M == 1 && plan_m1(N, K, sm_count, threads, small_ctas, &plan))
         return launch_m1(x, w, y, N, K, plan, device, flags, pr, n_problems, stream);
     switch (M < 8 ? M : 8) {
         case 1: return launch_rows<1>(x, w, y, M, N, K, pr, n_problems, stream);

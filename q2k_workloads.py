@@ -121,6 +121,38 @@ WORKLOADS = (
 FFN_DOWN = Workload("ffn_pair_down", 2, 1, 4096, 14336)
 
 
+@dataclasses.dataclass(frozen=True)
+class RoutedWorkload:
+    """An expert-routed (mm_id) product: n_tokens tokens, top_k experts each, from
+    a pool of n_experts [n, k] matrices packed back to back."""
+    name: str
+    seed: int
+    n_tokens: int
+    top_k: int
+    n: int
+    k: int
+    n_experts: int
+
+    @property
+    def expert_bytes(self) -> int:
+        return self.n * (self.k // QK_K) * BLOCK_BYTES
+
+
+# Decode step of a DeepSeek-style MoE layer: one token, 8 of 64 experts of hidden
+# size 7168 and expert width 2048 (a 308 MB pool, larger than L2).
+MOE_DECODE = RoutedWorkload("moe_decode_top8", 5, 1, 8, 2048, 7168, 64)
+# Eight decode GEMVs of the 4096 x 4096 workload in one batched launch.
+BATCHED_DECODE_BATCHES = 8
+
+
+def make_routed_ids(wl: RoutedWorkload, draw: int) -> np.ndarray:
+    """Token-major expert ids: each token's top_k distinct experts, drawn from
+    seed (wl.seed, draw)."""
+    rng = np.random.default_rng([wl.seed, draw])
+    return np.concatenate([rng.choice(wl.n_experts, wl.top_k, replace=False)
+                           for _ in range(wl.n_tokens)]).astype(np.uint32)
+
+
 def by_name(name: str) -> Workload:
     for w in WORKLOADS + (FFN_DOWN,):
         if w.name == name:
