@@ -33,7 +33,7 @@ _PATHS = {"auto": PATH_AUTO, "gemv": PATH_GEMV, "tensor": PATH_TENSOR,
           PATH_AUTO: PATH_AUTO, PATH_GEMV: PATH_GEMV, PATH_TENSOR: PATH_TENSOR}
 
 STATUS = {0: "Q2K_OK", 1: "Q2K_ERR_INVALID_ARGUMENT", 2: "Q2K_ERR_BAD_ID",
-          3: "Q2K_ERR_CUDA", 4: "Q2K_ERR_TIMEOUT", 5: "Q2K_ERR_NO_DEVICE"}
+          3: "Q2K_ERR_CUDA", 4: "Q2K_ERR_TIMEOUT", 5: "Q2K_ERR_NO_DEVICE", 6: "Q2K_ERR_IO"}
 
 HEADER = os.path.join(_build.INCLUDE, "q2k.h")
 LIB_PATH = _build.LIB_PATH
@@ -61,6 +61,12 @@ class MatmulIdParams(ctypes.Structure):
     _fields_ = [("n_tokens", ctypes.c_uint32), ("top_k", ctypes.c_uint32), ("n", ctypes.c_uint32),
                 ("k", ctypes.c_uint32), ("n_experts", ctypes.c_uint32),
                 ("ggml_type", ctypes.c_uint32), ("expert_stride", ctypes.c_uint64)]
+
+
+class GgufTensor(ctypes.Structure):
+    _fields_ = [("ggml_type", ctypes.c_uint32), ("n_dims", ctypes.c_uint32),
+                ("dims", ctypes.c_uint64 * 4), ("n_elements", ctypes.c_uint64),
+                ("offset", ctypes.c_uint64), ("byte_len", ctypes.c_uint64)]
 
 
 class EmbeddingParams(ctypes.Structure):
@@ -107,11 +113,21 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                               ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, vp]
         lib.q2k_matmul_id.argtypes = [vp, sz, vp, sz, vp, vp, sz, ctypes.POINTER(MatmulIdParams),
                                       vp, vp]
+        lib.q2k_gguf_open.argtypes = [ctypes.c_char_p, ctypes.POINTER(vp)]
+        lib.q2k_gguf_close.argtypes = [vp]
+        lib.q2k_gguf_close.restype = None
+        lib.q2k_gguf_tensor_count.argtypes = [vp]
+        lib.q2k_gguf_tensor_count.restype = ctypes.c_uint64
+        lib.q2k_gguf_tensor_name.argtypes = [vp, ctypes.c_uint64]
+        lib.q2k_gguf_tensor_name.restype = ctypes.c_char_p
+        lib.q2k_gguf_tensor_info.argtypes = [vp, ctypes.c_char_p, ctypes.POINTER(GgufTensor)]
+        lib.q2k_gguf_read_tensor.argtypes = [vp, ctypes.c_char_p, vp, sz]
         lib.q2k_device_error.argtypes = [u32p, vp]
         lib.q2k_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         for fn in ("q2k_dequantize", "q2k_embedding_gather", "q2k_matmul", "q2k_matmul_path",
                    "q2k_matmul_ex", "q2k_matmul_batched_mv", "q2k_matmul_id", "q2k_device_error",
-                   "q2k_selftest_wait_timeout"):
+                   "q2k_selftest_wait_timeout", "q2k_gguf_open", "q2k_gguf_tensor_info",
+                   "q2k_gguf_read_tensor"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.q2k_last_error.restype = ctypes.c_char_p
         lib.q2k_last_error.argtypes = []
@@ -340,6 +356,59 @@ def matmul_id(x, w, ids, n: int, n_experts: int, top_k: int, expert_stride: int 
     if n_bad:
         raise InvalidArgument(1, f"{n_bad} expert id(s) >= n_experts {n_experts}")
     return out
+
+
+class GgufFile:
+    """An open GGUF file (host only): ``names``, ``info(name)`` (a ``GgufTensor``:
+    ggml_type, n_dims, dims innermost first, n_elements, offset, byte_len),
+    ``read(name)`` (the bytes as a numpy uint8 array) and ``to_device(name)``
+    (those bytes in a CUDA uint8 tensor, ready for ``matmul`` when the type is
+    Q2_K).  Use as a context manager or call ``close``."""
+
+    def __init__(self, path):
+        self._lib = load()
+        h = ctypes.c_void_p()
+        _check(self._lib, self._lib.q2k_gguf_open(os.fsencode(path), ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            self._lib.q2k_gguf_close(self._h)
+        self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def names(self) -> list[str]:
+        n = self._lib.q2k_gguf_tensor_count(self._h)
+        return [self._lib.q2k_gguf_tensor_name(self._h, i).decode() for i in range(n)]
+
+    def info(self, name: str) -> GgufTensor:
+        out = GgufTensor()
+        _check(self._lib, self._lib.q2k_gguf_tensor_info(self._h, name.encode(), ctypes.byref(out)))
+        return out
+
+    def read(self, name: str):
+        import numpy as np
+        n = self.info(name).byte_len
+        buf = np.empty(n, dtype=np.uint8)
+        _check(self._lib, self._lib.q2k_gguf_read_tensor(self._h, name.encode(),
+                                                         buf.ctypes.data, n))
+        return buf
+
+    def to_device(self, name: str, device="cuda"):
+        torch = _torch()
+        return torch.from_numpy(self.read(name)).to(device)
 
 
 def selftest_wait_timeout(limit_us: int = 2000, device=None) -> None:

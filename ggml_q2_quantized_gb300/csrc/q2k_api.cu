@@ -113,6 +113,10 @@ q2k_status check_matmul(const float* x, size_t x_elems, const void* w, size_t w_
 
 }  // namespace
 
+void q2k::set_last_error(const char* msg) {
+    snprintf(g_last_error, sizeof g_last_error, "%s", msg);
+}
+
 extern "C" {
 
 const char* q2k_last_error(void) { return g_last_error; }

@@ -7,6 +7,10 @@
 
 namespace q2k {
 
+// Set the calling thread's message for q2k_last_error (the GGUF reader's
+// translation unit reports through the same one).
+void set_last_error(const char* msg);
+
 cudaError_t launch_dequant(const uint8_t* blocks, float* out, size_t n_blocks, int sm_count,
                            cudaStream_t stream);
 

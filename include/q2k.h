@@ -49,7 +49,8 @@ typedef enum q2k_status {
     Q2K_ERR_BAD_ID = 2,           /* reserved: gather reports bad ids through bad_id_count */
     Q2K_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed */
     Q2K_ERR_TIMEOUT = 4,          /* a kernel gave up waiting (see q2k_device_error) */
-    Q2K_ERR_NO_DEVICE = 5         /* no sm_103 device is current */
+    Q2K_ERR_NO_DEVICE = 5,        /* no sm_103 device is current */
+    Q2K_ERR_IO = 6                /* a file could not be opened or read (GGUF reader) */
 } q2k_status;
 
 enum {
@@ -211,6 +212,48 @@ q2k_status q2k_matmul_id(const float *x, size_t x_elems, const void *w, size_t w
                          const uint32_t *ids, float *y, size_t y_elems,
                          const q2k_matmul_id_params *params, uint32_t *bad_id_count,
                          q2k_stream_t stream);
+
+/* ---- GGUF reader (host only: no device is needed or touched) -------------
+ * The tensor directory of a GGUF file (versions 2 and 3) and its tensors'
+ * bytes, to load Q2_K (type 10) weights into the calls above.
+ * Page "tests/deepseek_q2_k.rs": test q2_k_gguf_type_10_parses_with_exact_block_size
+ * (GgufFile::open, tensor_info: ggml_type Q2_K and byte_len 84 for a 256-element
+ * tensor).  A malformed file (bad magic or version, truncated entries, more than
+ * 4 dimensions, an innermost extent that is not a whole number of blocks, a
+ * duplicate name, data past the end of the file, an offset off the alignment)
+ * is Q2K_ERR_INVALID_ARGUMENT with the reason in q2k_last_error; a file that
+ * cannot be opened or read is Q2K_ERR_IO.  Calls on one open file must not run
+ * concurrently (they share its read position). */
+typedef struct q2k_gguf q2k_gguf;  /* an open file; opaque */
+
+typedef struct q2k_gguf_tensor {
+    uint32_t ggml_type;   /* GGML type number: 10 = Q2_K (0 = F32, 1 = F16, ...) */
+    uint32_t n_dims;      /* 1 to 4 */
+    uint64_t dims[4];     /* extents, innermost first (a weight matrix: dims[0] = k,
+                             dims[1] = n); unused ones are 1 */
+    uint64_t n_elements;  /* product of the extents */
+    uint64_t offset;      /* absolute byte offset of the data in the file */
+    uint64_t byte_len;    /* bytes of the data (Q2_K: n_elements / 256 * 84); 0 when
+                             the reader does not know the type's block size */
+} q2k_gguf_tensor;   /* 64 bytes */
+
+/* Parse the header and tensor directory of `path`; *out is the open file
+ * (close it with q2k_gguf_close), NULL on error.  Tensor data is not read. */
+q2k_status q2k_gguf_open(const char *path, q2k_gguf **out);
+/* Close a file q2k_gguf_open returned (NULL is ignored). */
+void q2k_gguf_close(q2k_gguf *file);
+/* Number of tensors in the directory (0 for NULL). */
+uint64_t q2k_gguf_tensor_count(const q2k_gguf *file);
+/* Name of tensor `index` in directory order, valid until the file is closed;
+ * NULL when index is out of range. */
+const char *q2k_gguf_tensor_name(const q2k_gguf *file, uint64_t index);
+/* The directory entry of tensor `name`. */
+q2k_status q2k_gguf_tensor_info(const q2k_gguf *file, const char *name,
+                                q2k_gguf_tensor *out);
+/* Copy tensor `name`'s bytes into host memory `dst`; dst_bytes must equal its
+ * byte_len (nonzero). */
+q2k_status q2k_gguf_read_tensor(const q2k_gguf *file, const char *name, void *dst,
+                                size_t dst_bytes);
 
 /* q2k_matmul_workspace_bytes - device bytes of workspace q2k_matmul_ex can use
  * for this geometry and path (0: the path takes none).  The tensor-core path

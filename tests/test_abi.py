@@ -46,12 +46,14 @@ def test_struct_layout_matches_c(tmp_path):
         " offsetof(q2k_matmul_params, ggml_type), sizeof(q2k_embedding_params),"
         " offsetof(q2k_embedding_params, n_tokens), sizeof(q2k_status),"
         " sizeof(q2k_matmul_id_params), offsetof(q2k_matmul_id_params, ggml_type),"
-        " offsetof(q2k_matmul_id_params, expert_stride));return 0;}\n")
+        " offsetof(q2k_matmul_id_params, expert_stride));"
+        "printf(\"%zu %zu\\n\", sizeof(q2k_gguf_tensor), offsetof(q2k_gguf_tensor, byte_len));return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", q2k_build.INCLUDE, str(src),
                     "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
-    assert [int(v) for v in out] == [16, 12, 16, 8, 4, 32, 20, 24]
+    assert [int(v) for v in out] == [16, 12, 16, 8, 4, 32, 20, 24, 64, 56]
+    assert ctypes.sizeof(q2k.GgufTensor) == 64 and q2k.GgufTensor.byte_len.offset == 56
     assert ctypes.sizeof(q2k.MatmulIdParams) == 32
     assert q2k.MatmulIdParams.ggml_type.offset == 20
     assert q2k.MatmulIdParams.expert_stride.offset == 24
