@@ -20,7 +20,10 @@ What each call follows (mlx-native test page "tests/deepseek_q2_k.rs"):
 * ``matmul_id``       - fn ``run_expert``'s expected value: route r = t top_k +
                         slot (token-major ids) takes token t's input and the
                         weights of expert ids[r] (at ids[r] expert_stride bytes);
-                        an id >= n_experts is an error.
+                        an id >= n_experts is an error.  ``slotted``: route r
+                        takes input row r instead (test ``q2_k_slotted_down_mm_
+                        is_byte_identical_to_flattened_rows``: x [tokens, top_k,
+                        k], the same values as the flattened call with top_k 1).
 """
 
 from __future__ import annotations
@@ -189,15 +192,18 @@ class Oracle:
         return w[start:start + size]
 
     def matmul_id(self, x: np.ndarray, w: np.ndarray, ids, n: int, n_experts: int,
-                  expert_stride: int, top_k: int, threads: int = 1):
+                  expert_stride: int, top_k: int, threads: int = 1, slotted: bool = False):
         """Return ``(y, s_abs)``, float64 ``[n_tokens * top_k, n]``: row r is
-        expert ``ids[r]``'s matrix times the input of token ``r // top_k``."""
+        expert ``ids[r]``'s matrix times the input of token ``r // top_k`` (of
+        route r itself when ``slotted``: x is then ``[n_tokens * top_k, K]``)."""
         x = np.ascontiguousarray(x, dtype=np.float32)
         if x.ndim != 2:
-            raise OracleError("x must be [n_tokens, K]")
-        n_tokens, K = x.shape
+            raise OracleError("x must be [rows, K]")
+        rows, K = x.shape
         ids = np.ascontiguousarray(ids, dtype=np.uint32).reshape(-1)
-        if top_k < 1 or ids.size != n_tokens * top_k or K % QK_K != 0:
+        n_tokens = rows // top_k if slotted and top_k >= 1 else rows
+        if top_k < 1 or ids.size != n_tokens * top_k or K % QK_K != 0 or \
+                (slotted and rows != ids.size):
             raise OracleError("ids must hold top_k experts per token and K a multiple of 256")
         wb = np.ascontiguousarray(w, dtype=np.uint8).reshape(-1)
         y = np.empty((ids.size, n), dtype=np.float64)
@@ -205,7 +211,7 @@ class Oracle:
         for r, e in enumerate(ids.tolist()):
             if e >= n_experts:
                 raise OracleError(f"expert id {e} out of range (n_experts = {n_experts})")
-            t = self.route_token(r, top_k)
+            t = r if slotted else self.route_token(r, top_k)
             yr, sr = self.matmul(x[t:t + 1], self.expert_bytes(wb, e, n, K, expert_stride), n,
                                  threads)
             y[r], s_abs[r] = yr[0], sr[0]
@@ -254,5 +260,5 @@ def matmul_batched_mv(x: np.ndarray, w: np.ndarray, n: int, threads: int = 1):
 
 
 def matmul_id(x: np.ndarray, w: np.ndarray, ids, n: int, n_experts: int, expert_stride: int,
-              top_k: int, threads: int = 1):
-    return default().matmul_id(x, w, ids, n, n_experts, expert_stride, top_k, threads)
+              top_k: int, threads: int = 1, slotted: bool = False):
+    return default().matmul_id(x, w, ids, n, n_experts, expert_stride, top_k, threads, slotted)

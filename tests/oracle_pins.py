@@ -349,6 +349,24 @@ def pin_matmul_id_stride_and_bad_id(o):
         raise AssertionError("an expert id >= n_experts was accepted")
 
 
+def pin_matmul_id_slotted_page(o):
+    """Page test q2_k_slotted_down_mm_is_byte_identical_to_flattened_rows: 33 tokens,
+    top_k 6, 8 experts, one input row per route (input(198)); the slotted product
+    equals the flattened one (n_tokens 198, top_k 1), and route r is expert ids[r]
+    times input row r."""
+    tokens, top_k, experts, n = 33, 6, 8, 8
+    w, _, ids, stride = _expert_fixture(tokens, top_k, experts, n)
+    x = wl.page_input(tokens * top_k)
+    ys, _ = o.matmul_id(x, w, ids, n, experts, stride, top_k, slotted=True)
+    yf, _ = o.matmul_id(x, w, ids, n, experts, stride, 1)
+    assert np.array_equal(ys, yf)
+    for r in (0, 5, 6, 100, 197):
+        e = int(ids[r])
+        for row in (0, n - 1):
+            ref, ref_abs = _fsum_dot(x[r], o.dequant_block(wl.page_block(e * n + row + 1)))
+            assert abs(ys[r, row] - ref) <= 1e-12 * ref_abs, f"route {r} row {row}"
+
+
 ALL_PINS = [
     pin_f16_all_patterns,
     pin_block5_hand_values,
@@ -369,4 +387,5 @@ ALL_PINS = [
     pin_batched_mv_page,
     pin_matmul_id_page,
     pin_matmul_id_stride_and_bad_id,
+    pin_matmul_id_slotted_page,
 ]

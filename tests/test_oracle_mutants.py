@@ -77,12 +77,20 @@ class _PackedExperts(oracle.Oracle):
         return super().expert_bytes(w, expert, n, K, n * (K // 256) * 84)
 
 
+class _SlottedUsesToken(oracle.Oracle):
+    def matmul_id(self, x, w, ids, n, n_experts, expert_stride, top_k, threads=1, slotted=False):
+        if slotted:  # the mistake: read the token's row as the unslotted product does
+            x = x[::top_k].copy()
+            slotted = False
+        return super().matmul_id(x, w, ids, n, n_experts, expert_stride, top_k, threads, slotted)
+
+
 class _BatchesSwapped(oracle.Oracle):
     def matmul_batched_mv(self, x, w, n, threads=1):
         return super().matmul_batched_mv(x[::-1].copy(), w, n, threads)
 
 
-@pytest.mark.parametrize("cls", [_SlotAsToken, _PackedExperts, _BatchesSwapped],
+@pytest.mark.parametrize("cls", [_SlotAsToken, _PackedExperts, _BatchesSwapped, _SlottedUsesToken],
                          ids=lambda c: c.__name__)
 def test_composition_mutant_is_caught(cls):
     o = cls(oracle.default().path)
