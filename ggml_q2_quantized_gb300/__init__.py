@@ -113,6 +113,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                               ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, vp]
         lib.q2k_matmul_id.argtypes = [vp, sz, vp, sz, vp, vp, sz, ctypes.POINTER(MatmulIdParams),
                                       vp, vp]
+        lib.q2k_matmul_id_slotted.argtypes = lib.q2k_matmul_id.argtypes
+        lib.q2k_matmul_id_pair.argtypes = [vp, sz, vp, sz, vp, sz, vp, vp, vp, sz,
+                                           ctypes.POINTER(MatmulIdParams), vp, vp]
         lib.q2k_gguf_open.argtypes = [ctypes.c_char_p, ctypes.POINTER(vp)]
         lib.q2k_gguf_close.argtypes = [vp]
         lib.q2k_gguf_close.restype = None
@@ -125,7 +128,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q2k_device_error.argtypes = [u32p, vp]
         lib.q2k_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         for fn in ("q2k_dequantize", "q2k_embedding_gather", "q2k_matmul", "q2k_matmul_path",
-                   "q2k_matmul_ex", "q2k_matmul_batched_mv", "q2k_matmul_id", "q2k_device_error",
+                   "q2k_matmul_ex", "q2k_matmul_batched_mv", "q2k_matmul_id",
+                   "q2k_matmul_id_slotted", "q2k_matmul_id_pair", "q2k_device_error",
                    "q2k_selftest_wait_timeout", "q2k_gguf_open", "q2k_gguf_tensor_info",
                    "q2k_gguf_read_tensor"):
             getattr(lib, fn).restype = ctypes.c_int
@@ -320,6 +324,69 @@ def matmul_batched_mv(x, w, n: int, out=None):
                                               out.data_ptr(), out.numel(), batches, 1, n, k,
                                               _stream_handle(x)))
     return out
+
+
+def _routed_finish(bad, check, outs, n_experts):
+    if not check:
+        return (*outs, bad) if len(outs) > 1 else (outs[0], bad)
+    n_bad = int(bad.item())
+    if n_bad:
+        raise InvalidArgument(1, f"{n_bad} expert id(s) >= n_experts {n_experts}")
+    return outs if len(outs) > 1 else outs[0]
+
+
+def matmul_id_slotted(x, w, ids, n: int, n_experts: int, expert_stride: int | None = None,
+                      out=None, check: bool = True):
+    """Routed product with one input row per route: ``x`` f32 ``[n_tokens, top_k,
+    k]``, ``ids`` ``[n_tokens, top_k]``; returns ``[n_tokens, top_k, n]``, route
+    (t, s) = expert ``ids[t, s]`` times ``x[t, s]``.  ``check`` as ``matmul_id``."""
+    torch = _torch()
+    _require_cuda(x, "x", torch.float32)
+    _require_cuda(w, "w", torch.uint8)
+    _require_cuda(ids, "ids", ids.dtype)
+    if ids.element_size() != 4 or ids.is_floating_point():
+        raise TypeError("ids must be a 32-bit integer tensor (read as uint32)")
+    n_tokens, top_k, k = x.shape
+    if expert_stride is None:
+        expert_stride = n * (k // QK_K) * BLOCK_BYTES
+    if out is None:
+        out = torch.empty((n_tokens, top_k, n), dtype=torch.float32, device=x.device)
+    _require_cuda(out, "out", torch.float32)
+    bad = torch.zeros(1, dtype=torch.int32, device=x.device)
+    p = MatmulIdParams(n_tokens, top_k, n, k, n_experts, GGML_TYPE_Q2_K, expert_stride)
+    lib = load()
+    with _on_device(x):
+        _check(lib, lib.q2k_matmul_id_slotted(x.data_ptr(), x.numel(), w.data_ptr(), w.numel(),
+                                              ids.data_ptr(), out.data_ptr(), out.numel(),
+                                              ctypes.byref(p), bad.data_ptr(), _stream_handle(x)))
+    return _routed_finish(bad, check, (out,), n_experts)
+
+
+def matmul_id_pair(x, w_a, w_b, ids, n: int, n_experts: int, top_k: int,
+                   expert_stride: int | None = None, check: bool = True):
+    """Two routed products sharing ``x`` and ``ids`` (e.g. the gate and up
+    projections) in one launch; returns ``(y_a, y_b)`` as ``matmul_id`` would."""
+    torch = _torch()
+    _require_cuda(x, "x", torch.float32)
+    _require_cuda(w_a, "w_a", torch.uint8)
+    _require_cuda(w_b, "w_b", torch.uint8)
+    _require_cuda(ids, "ids", ids.dtype)
+    if ids.element_size() != 4 or ids.is_floating_point():
+        raise TypeError("ids must be a 32-bit integer tensor (read as uint32)")
+    n_tokens, k = x.shape
+    if expert_stride is None:
+        expert_stride = n * (k // QK_K) * BLOCK_BYTES
+    y_a = torch.empty((ids.numel(), n), dtype=torch.float32, device=x.device)
+    y_b = torch.empty((ids.numel(), n), dtype=torch.float32, device=x.device)
+    bad = torch.zeros(1, dtype=torch.int32, device=x.device)
+    p = MatmulIdParams(n_tokens, top_k, n, k, n_experts, GGML_TYPE_Q2_K, expert_stride)
+    lib = load()
+    with _on_device(x):
+        _check(lib, lib.q2k_matmul_id_pair(x.data_ptr(), x.numel(), w_a.data_ptr(), w_a.numel(),
+                                           w_b.data_ptr(), w_b.numel(), ids.data_ptr(),
+                                           y_a.data_ptr(), y_b.data_ptr(), y_a.numel(),
+                                           ctypes.byref(p), bad.data_ptr(), _stream_handle(x)))
+    return _routed_finish(bad, check, (y_a, y_b), n_experts)
 
 
 def matmul_id(x, w, ids, n: int, n_experts: int, top_k: int, expert_stride: int | None = None,

@@ -314,11 +314,20 @@ q2k_status q2k_matmul_batched_mv(const float* x, size_t x_elems, const void* w, 
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul_batched_mv launch");
 }
 
-q2k_status q2k_matmul_id(const float* x, size_t x_elems, const void* w, size_t w_bytes,
-                         const uint32_t* ids, float* y, size_t y_elems,
-                         const q2k_matmul_id_params* p, uint32_t* bad_id_count,
-                         q2k_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks and launch shared by the routed products: x has one row per token
+// (or per route when `slotted`); wb / yb are the second weight set and output
+// of a pair (NULL otherwise).  Every malformed argument is rejected before any
+// device work.
+q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void* wa, size_t wa_bytes,
+                       const void* wb, size_t wb_bytes, const uint32_t* ids, float* ya, float* yb,
+                       size_t y_elems, const q2k_matmul_id_params* p, uint32_t* bad_id_count,
+                       q2k_stream_t stream, const char* what) {
     g_last_error[0] = '\0';
+    const bool pair = yb != nullptr || wb != nullptr;
     if (p == nullptr) return fail(Q2K_ERR_INVALID_ARGUMENT, "params is NULL");
     if (p->ggml_type != Q2K_GGML_TYPE_Q2_K)
         return fail(Q2K_ERR_INVALID_ARGUMENT, "ggml_type %u is not Q2_K (10)", p->ggml_type);
@@ -331,54 +340,102 @@ q2k_status q2k_matmul_id(const float* x, size_t x_elems, const void* w, size_t w
     size_t routes, expert_bytes, want_x, want_y, last;
     if (!mul_ok(p->n_tokens, p->top_k, &routes) ||
         !mul_ok(p->n, size_t(p->k / Q2K_QK_K) * Q2K_BLOCK_BYTES, &expert_bytes) ||
-        !mul_ok(p->n_tokens, p->k, &want_x) || !mul_ok(routes, p->n, &want_y) ||
+        !mul_ok(slotted ? routes : size_t(p->n_tokens), p->k, &want_x) ||
+        !mul_ok(routes, p->n, &want_y) ||
         !mul_ok(p->n_experts - 1u, p->expert_stride, &last) || last > SIZE_MAX - expert_bytes ||
         want_x > SIZE_MAX / 4 || want_y > SIZE_MAX / 4)
         return fail(Q2K_ERR_INVALID_ARGUMENT, "routed shape overflows size_t");
-    if (routes > 65535)
-        return fail(Q2K_ERR_INVALID_ARGUMENT, "n_tokens * top_k must be <= 65535, got %zu", routes);
+    if (routes > (pair ? 32767u : 65535u))
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "n_tokens * top_k must be <= %u, got %zu",
+                    pair ? 32767u : 65535u, routes);
     if (p->expert_stride % 4 != 0 || p->expert_stride < expert_bytes)
         return fail(Q2K_ERR_INVALID_ARGUMENT,
                     "expert_stride %llu must be a multiple of 4 and >= n*k/256*84 = %zu",
                     static_cast<unsigned long long>(p->expert_stride), expert_bytes);
-    if (x == nullptr || w == nullptr || ids == nullptr || y == nullptr)
+    if (x == nullptr || wa == nullptr || ids == nullptr || ya == nullptr ||
+        (pair && (wb == nullptr || yb == nullptr)))
         return fail(Q2K_ERR_INVALID_ARGUMENT, "x, w, ids and y must be non-NULL");
     if (x_elems != want_x)
-        return fail(Q2K_ERR_INVALID_ARGUMENT, "x has %zu elements, expected n_tokens*k = %zu", x_elems, want_x);
-    if (w_bytes < last + expert_bytes)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "x has %zu elements, expected %s*k = %zu", x_elems,
+                    slotted ? "n_tokens*top_k" : "n_tokens", want_x);
+    if (wa_bytes < last + expert_bytes || (pair && wb_bytes < last + expert_bytes))
         return fail(Q2K_ERR_INVALID_ARGUMENT, "w has %zu bytes, expected >= (n_experts-1)*expert_stride + "
-                    "n*k/256*84 = %zu", w_bytes, last + expert_bytes);
+                    "n*k/256*84 = %zu", pair && wb_bytes < wa_bytes ? wb_bytes : wa_bytes, last + expert_bytes);
     if (y_elems != want_y)
         return fail(Q2K_ERR_INVALID_ARGUMENT, "y has %zu elements, expected n_tokens*top_k*n = %zu",
                     y_elems, want_y);
-    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(w, 4) || !aligned(ids, 4) ||
+    if (!aligned(x, 16) || !aligned(ya, 16) || !aligned(wa, 4) || !aligned(ids, 4) ||
+        (pair && (!aligned(yb, 16) || !aligned(wb, 4))) ||
         (bad_id_count != nullptr && !aligned(bad_id_count, 4)))
         return fail(Q2K_ERR_INVALID_ARGUMENT,
                     "x and y must be 16-byte aligned, w, ids and bad_id_count 4-byte aligned");
-    const size_t y_bytes = want_y * 4;
-    if (overlaps(y, y_bytes, x, want_x * 4) || overlaps(y, y_bytes, w, w_bytes) ||
-        overlaps(y, y_bytes, ids, routes * 4) ||
-        (bad_id_count != nullptr &&
-         (overlaps(bad_id_count, 4, y, y_bytes) || overlaps(bad_id_count, 4, x, want_x * 4) ||
-          overlaps(bad_id_count, 4, w, w_bytes) || overlaps(bad_id_count, 4, ids, routes * 4))))
-        return fail(Q2K_ERR_INVALID_ARGUMENT, "writable buffers must not alias inputs or each other");
+    const size_t y_bytes = want_y * 4, x_bytes = want_x * 4, id_bytes = routes * 4;
+    const void* in[4] = {x, wa, ids, wb};
+    const size_t in_bytes[4] = {x_bytes, wa_bytes, id_bytes, pair ? wb_bytes : 0};
+    const void* outs[3] = {ya, yb, bad_id_count};
+    const size_t out_bytes[3] = {y_bytes, pair ? y_bytes : 0, bad_id_count ? 4u : 0u};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 4; ++i)
+            if (overlaps(outs[o], out_bytes[o], in[i], in_bytes[i]))
+                return fail(Q2K_ERR_INVALID_ARGUMENT, "writable buffers must not alias inputs or each other");
+        for (int o2 = o + 1; o2 < 3; ++o2)
+            if (overlaps(outs[o], out_bytes[o], outs[o2], out_bytes[o2]))
+                return fail(Q2K_ERR_INVALID_ARGUMENT, "writable buffers must not alias inputs or each other");
+    }
     DeviceInfo dev;
     q2k_status st = current_device(&dev);
     if (st != Q2K_OK) return st;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     if (bad_id_count != nullptr) e = cudaMemsetAsync(bad_id_count, 0, 4, s);
-    if (e != cudaSuccess) return cuda_fail(e, "q2k_matmul_id: clearing bad_id_count");
+    if (e != cudaSuccess) return cuda_fail(e, "clearing bad_id_count");
     q2k::GemvProblems pr;
     pr.w_stride = static_cast<long long>(p->expert_stride);
     pr.y_stride = static_cast<long long>(p->n);
     pr.ids = ids;
     pr.n_experts = p->n_experts;
-    pr.top_k = p->top_k;
+    pr.top_k = slotted ? 1u : p->top_k;  // x row of route r: r / top_k, or r itself
     pr.bad_ids = bad_id_count;
-    e = q2k::launch_gemv_problems(x, static_cast<const uint8_t*>(w), y, 1, int(p->n), int(p->k),
-                                  dev.device, dev.sm_count, 0u, pr, int(routes), s);
-    return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul_id launch");
+    if (pair) {
+        pr.second_from = static_cast<int>(routes);
+        pr.w2 = static_cast<const uint8_t*>(wb);
+        pr.y2 = yb;
+    }
+    e = q2k::launch_gemv_problems(x, static_cast<const uint8_t*>(wa), ya, 1, int(p->n), int(p->k),
+                                  dev.device, dev.sm_count, 0u, pr, int(pair ? 2 * routes : routes), s);
+    return e == cudaSuccess ? Q2K_OK : cuda_fail(e, what);
+}
+
+}  // namespace
+
+extern "C" {
+
+q2k_status q2k_matmul_id(const float* x, size_t x_elems, const void* w, size_t w_bytes,
+                         const uint32_t* ids, float* y, size_t y_elems,
+                         const q2k_matmul_id_params* p, uint32_t* bad_id_count,
+                         q2k_stream_t stream) {
+    return routed_call(x, x_elems, false, w, w_bytes, nullptr, 0, ids, y, nullptr, y_elems, p,
+                       bad_id_count, stream, "q2k_matmul_id launch");
+}
+
+q2k_status q2k_matmul_id_slotted(const float* x, size_t x_elems, const void* w, size_t w_bytes,
+                                 const uint32_t* ids, float* y, size_t y_elems,
+                                 const q2k_matmul_id_params* p, uint32_t* bad_id_count,
+                                 q2k_stream_t stream) {
+    return routed_call(x, x_elems, true, w, w_bytes, nullptr, 0, ids, y, nullptr, y_elems, p,
+                       bad_id_count, stream, "q2k_matmul_id_slotted launch");
+}
+
+q2k_status q2k_matmul_id_pair(const float* x, size_t x_elems, const void* w_a, size_t w_a_bytes,
+                              const void* w_b, size_t w_b_bytes, const uint32_t* ids, float* y_a,
+                              float* y_b, size_t y_elems, const q2k_matmul_id_params* p,
+                              uint32_t* bad_id_count, q2k_stream_t stream) {
+    if (y_b == nullptr || w_b == nullptr) {
+        g_last_error[0] = '\0';
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "x, w, ids and y must be non-NULL");
+    }
+    return routed_call(x, x_elems, false, w_a, w_a_bytes, w_b, w_b_bytes, ids, y_a, y_b, y_elems, p,
+                       bad_id_count, stream, "q2k_matmul_id_pair launch");
 }
 
 q2k_status q2k_selftest_wait_timeout(uint32_t limit_us, q2k_stream_t stream) {

@@ -278,25 +278,32 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     const int r0 = blockIdx.x * rows_per_cta;
     const int rows = min(rows_per_cta, N - r0);
     // Problem blockIdx.y of a batch (strided x, W, y) or of a routed product
-    // (x row p / top_k, the W of expert ids[p]); one problem: all strides 0.
+    // (x row route / top_k, the W of expert ids[route]; a pair's second set of
+    // routes uses w2 and y2); one problem: all strides 0.
     const int prob = blockIdx.y;
     if (pr.ids != nullptr) {
         pdl_wait_prerequisites();  // the ids (and x) may come from the grid before this one
-        const uint32_t e = pr.ids[prob];
+        const bool second = pr.second_from > 0 && prob >= pr.second_from;
+        const int route = second ? prob - pr.second_from : prob;
+        if (second) {
+            w = pr.w2;
+            y = pr.y2;
+        }
+        y += static_cast<size_t>(route) * pr.y_stride;
+        const uint32_t e = pr.ids[route];
         if (e >= pr.n_experts) {
             // no such expert: this route's outputs are zeros and the bad id is counted
-            for (int lr = tid; lr < rows; lr += nthreads)
-                y[static_cast<size_t>(prob) * pr.y_stride + r0 + lr] = 0.f;
+            for (int lr = tid; lr < rows; lr += nthreads) y[r0 + lr] = 0.f;
             if (blockIdx.x == 0 && tid == 0 && pr.bad_ids != nullptr) atomicAdd(pr.bad_ids, 1u);
             return;
         }
-        x += static_cast<size_t>(prob / pr.top_k) * K;
+        x += static_cast<size_t>(route / pr.top_k) * K;
         w += static_cast<size_t>(e) * pr.w_stride;
     } else {
         x += static_cast<size_t>(prob) * pr.x_stride;
         w += static_cast<size_t>(prob) * pr.w_stride;
+        y += static_cast<size_t>(prob) * pr.y_stride;
     }
-    y += static_cast<size_t>(prob) * pr.y_stride;
     const uint32_t delta = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(w) & 15u);
     const int n_pieces = (rows + kPieceRows - 1) / kPieceRows;
     const int max_pieces = (rows_per_cta + kPieceRows - 1) / kPieceRows;
@@ -532,19 +539,26 @@ gemv_rows_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, flo
     // problem blockIdx.z, as in gemv_m1_kernel (one x row per problem there)
     const int prob = blockIdx.z;
     if (pr.ids != nullptr) {
-        const uint32_t e = pr.ids[prob];
+        const bool second = pr.second_from > 0 && prob >= pr.second_from;
+        const int route = second ? prob - pr.second_from : prob;
+        if (second) {
+            w = pr.w2;
+            y = pr.y2;
+        }
+        y += static_cast<size_t>(route) * pr.y_stride;
+        const uint32_t e = pr.ids[route];
         if (e >= pr.n_experts) {
-            if (lane == 0) y[static_cast<size_t>(prob) * pr.y_stride + n] = 0.f;
+            if (lane == 0) y[n] = 0.f;
             if (n == 0 && lane == 0 && pr.bad_ids != nullptr) atomicAdd(pr.bad_ids, 1u);
             return;
         }
-        x += static_cast<size_t>(prob / pr.top_k) * K;
+        x += static_cast<size_t>(route / pr.top_k) * K;
         w += static_cast<size_t>(e) * pr.w_stride;
     } else {
         x += static_cast<size_t>(prob) * pr.x_stride;
         w += static_cast<size_t>(prob) * pr.w_stride;
+        y += static_cast<size_t>(prob) * pr.y_stride;
     }
-    y += static_cast<size_t>(prob) * pr.y_stride;
     const int m0 = blockIdx.y * MT;
     const int mcount = min(MT, M - m0);
     const int B = K >> 8;

@@ -36,7 +36,9 @@ cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N
 //   batched (ids == nullptr): x + p x_stride, w + p w_stride -> y + p y_stride;
 //   routed: x row p / top_k and the weights of expert ids[p] at w + ids[p]
 //           w_stride -> y + p y_stride.  An id >= n_experts gives zeros and
-//           adds 1 to *bad_ids (when not null).
+//           adds 1 to *bad_ids (when not null).  With second_from > 0, problems
+//           p >= second_from are route p - second_from again with w2 and y2 in
+//           place of w and y (two weight sets sharing the routing).
 // Strides in elements (x, y) and bytes (w).  All zero: one problem.
 struct GemvProblems {
     long long x_stride = 0;
@@ -46,6 +48,9 @@ struct GemvProblems {
     uint32_t n_experts = 0;
     uint32_t top_k = 1;
     unsigned int* bad_ids = nullptr;
+    int second_from = 0;
+    const uint8_t* w2 = nullptr;
+    float* y2 = nullptr;
 };
 cudaError_t launch_gemv_problems(const float* x, const uint8_t* w, float* y, int M, int N, int K,
                                  int device, int sm_count, uint32_t flags,

@@ -255,6 +255,33 @@ q2k_status q2k_gguf_tensor_info(const q2k_gguf *file, const char *name,
 q2k_status q2k_gguf_read_tensor(const q2k_gguf *file, const char *name, void *dst,
                                 size_t dst_bytes);
 
+/* q2k_matmul_id_slotted - q2k_matmul_id with one input row per route (the
+ * down projection of a MoE layer, whose input is each route's own activation):
+ * y[r, :] = W_{ids[r]} x[r, :], x f32 [n_tokens, top_k, k] (x_elems =
+ * n_tokens*top_k*k).  Page "tests/deepseek_q2_k.rs":
+ * quantized_matmul_id_ggml_pooled_slotted and test
+ * q2_k_slotted_down_mm_is_byte_identical_to_flattened_rows: the result is
+ * bit-identical to q2k_matmul_id with n_tokens*top_k tokens and top_k = 1.
+ * Other arguments, checks and bad-id handling as q2k_matmul_id. */
+q2k_status q2k_matmul_id_slotted(const float *x, size_t x_elems, const void *w, size_t w_bytes,
+                                 const uint32_t *ids, float *y, size_t y_elems,
+                                 const q2k_matmul_id_params *params, uint32_t *bad_id_count,
+                                 q2k_stream_t stream);
+
+/* q2k_matmul_id_pair - two routed products sharing x and the routing (the gate
+ * and up projections of a MoE layer) in one launch: y_a = routed(W_a), y_b =
+ * routed(W_b), each bit-identical to its own q2k_matmul_id.  Page
+ * "tests/deepseek_q2_k.rs": quantized_matmul_id_ggml_pooled_pair (fn run_expert
+ * with force_mm, whose two outputs must agree bit for bit when both weight sets
+ * are the same).  w_a and w_b follow q2k_matmul_id's layout with the same
+ * expert_stride (w_a_bytes and w_b_bytes checked each); y_a and y_b are
+ * [n_tokens*top_k, n] with y_elems each.  A bad id is counted once per product.
+ * n_tokens * top_k <= 32767. */
+q2k_status q2k_matmul_id_pair(const float *x, size_t x_elems, const void *w_a, size_t w_a_bytes,
+                              const void *w_b, size_t w_b_bytes, const uint32_t *ids, float *y_a,
+                              float *y_b, size_t y_elems, const q2k_matmul_id_params *params,
+                              uint32_t *bad_id_count, q2k_stream_t stream);
+
 /* q2k_matmul_workspace_bytes - device bytes of workspace q2k_matmul_ex can use
  * for this geometry and path (0: the path takes none).  The tensor-core path
  * stores x there as bf16 in the tile layout its shared memory uses,

@@ -218,3 +218,28 @@ def _mid(lib, n_tokens=2, top_k=2, n=8, k=256, n_experts=3, stride=None, xe=None
 def test_matmul_id_rejects(lib, kw, fragment):
     assert _mid(lib, **kw) == INVALID
     assert fragment in lib.q2k_last_error().decode()
+
+
+def test_matmul_id_slotted_and_pair_reject(lib):
+    n_tokens, top_k, n, k, experts = 2, 2, 8, 256, 3
+    p = q2k.MatmulIdParams(n_tokens, top_k, n, k, experts, 10, n * 84)
+    wb = experts * n * 84
+    # slotted: x holds one row per route (n_tokens*top_k*k), not per token
+    assert lib.q2k_matmul_id_slotted(0x10000, n_tokens * k, 0x100000, wb, 0x3000000, 0x1000000,
+                                     n_tokens * top_k * n, ctypes.byref(p), None, None) == INVALID
+    assert "n_tokens*top_k*k" in lib.q2k_last_error().decode()
+    args = (0x10000, n_tokens * k, 0x100000, wb)
+    # pair: missing second weight set, short second weight set, aliasing outputs
+    assert lib.q2k_matmul_id_pair(*args, None, wb, 0x3000000, 0x1000000, 0x2000000,
+                                  n_tokens * top_k * n, ctypes.byref(p), None, None) == INVALID
+    assert lib.q2k_matmul_id_pair(*args, 0x200000, wb - 4, 0x3000000, 0x1000000, 0x2000000,
+                                  n_tokens * top_k * n, ctypes.byref(p), None, None) == INVALID
+    assert "w has" in lib.q2k_last_error().decode()
+    assert lib.q2k_matmul_id_pair(*args, 0x200000, wb, 0x3000000, 0x1000000, 0x1000000 + 32,
+                                  n_tokens * top_k * n, ctypes.byref(p), None, None) == INVALID
+    assert "alias" in lib.q2k_last_error().decode()
+    big = q2k.MatmulIdParams(16384, 2, n, k, experts, 10, n * 84)
+    assert lib.q2k_matmul_id_pair(0x10000, 16384 * k, 0x100000, wb, 0x200000, wb, 0x3000000,
+                                  0x1000000, 0x8000000, 32768 * n, ctypes.byref(big), None,
+                                  None) == INVALID
+    assert "32767" in lib.q2k_last_error().decode()

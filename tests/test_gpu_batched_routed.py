@@ -175,3 +175,58 @@ def test_matmul_id_bad_id_gives_zero_row_and_count():
     good = [r for r in range(tokens * top_k) if r not in (5, 6)]
     yref, s = oracle.matmul_id(x, w, ids, n, experts, stride, top_k)
     assert_close(got[good].astype(np.float64), yref[good], s[good], TOL_GEMV, "good routes")
+
+
+def test_matmul_id_slotted_equals_flattened_page_case():
+    """Page test q2_k_slotted_down_mm_is_byte_identical_to_flattened_rows:
+    33 tokens x top_k 6 routes, 8 experts, input(198) as [33, 6, 256]."""
+    tokens, top_k, experts, n = 33, 6, 8, 8
+    w, _, ids, stride = _expert_case(tokens, top_k, experts, n)
+    x = wl.page_input(tokens * top_k)
+    wd, idd = dev(w), dev(ids.view(np.int32))
+    xd = dev(x)
+    slotted = q2k.matmul_id_slotted(xd.view(tokens, top_k, 256), wd, idd.view(tokens, top_k), n,
+                                    experts)
+    flat = q2k.matmul_id(xd, wd, idd, n, experts, 1)
+    torch.cuda.synchronize()
+    assert bits_equal(slotted.view(-1, n), flat)
+    yref, s = oracle.matmul_id(x, w, ids, n, experts, stride, top_k, slotted=True)
+    got = slotted.view(-1, n).cpu().numpy().astype(np.float64)
+    assert_close(got, yref, s, TOL_GEMV, "slotted")
+    assert np.abs(got - yref).max() <= 2e-4
+
+
+def test_matmul_id_pair_page_case_and_distinct_weights():
+    """Page fn run_expert(33, 6, 8, force_mm): both weight sets the same, both
+    outputs agree bit for bit; then distinct sets, each equal to its own call."""
+    tokens, top_k, experts, n = 33, 6, 8, 8
+    w, x, ids, stride = _expert_case(tokens, top_k, experts, n)
+    wd, xd, idd = dev(w), dev(x), dev(ids.view(np.int32))
+    ya, yb = q2k.matmul_id_pair(xd, wd, wd, idd, n, experts, top_k)
+    single = q2k.matmul_id(xd, wd, idd, n, experts, top_k)
+    torch.cuda.synchronize()
+    assert bits_equal(ya, yb) and bits_equal(ya, single)
+    yref, s = oracle.matmul_id(x, w, ids, n, experts, stride, top_k)
+    assert np.abs(ya.cpu().numpy().astype(np.float64) - yref).max() <= 1e-2  # the page's mm bound
+    assert_close(ya.cpu().numpy().astype(np.float64), yref, s, TOL_GEMV, "pair a")
+    # distinct second set: experts drawn at random, stride with a gap
+    rng = np.random.default_rng(77)
+    w2 = np.concatenate([wl.random_blocks(rng, n) for _ in range(experts)])
+    ya, yb = q2k.matmul_id_pair(xd, wd, dev(w2), idd, n, experts, top_k)
+    sb = q2k.matmul_id(xd, dev(w2), idd, n, experts, top_k)
+    torch.cuda.synchronize()
+    assert bits_equal(ya, single) and bits_equal(yb, sb)
+    yref2, s2 = oracle.matmul_id(x, w2, ids, n, experts, n * 84, top_k)
+    assert_close(yb.cpu().numpy().astype(np.float64), yref2, s2, TOL_GEMV, "pair b")
+
+
+def test_matmul_id_pair_counts_bad_ids_per_product():
+    tokens, top_k, experts, n = 3, 2, 3, 8
+    w, x, ids, _ = _expert_case(tokens, top_k, experts, n)
+    bad = ids.copy()
+    bad[1] = 7
+    ya, yb, count = q2k.matmul_id_pair(dev(x), dev(w), dev(w), dev(bad.view(np.int32)), n, experts,
+                                       top_k, check=False)
+    torch.cuda.synchronize()
+    assert int(count.item()) == 2
+    assert (ya[1] == 0).all() and (yb[1] == 0).all()
