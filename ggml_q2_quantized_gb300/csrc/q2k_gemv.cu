@@ -262,6 +262,90 @@ __device__ __forceinline__ void issue_weight_copies(uint8_t* smem_w, const uint8
     }
 }
 
+// x (K floats) -> the run planes, run sums and run scales in shared memory,
+// spread over the CTA's threads.
+__device__ __forceinline__ void convert_x(const float* __restrict__ x, uint32_t* planes,
+                                          float* run_sum, float* run_inv, int n_runs, int tid,
+                                          int nthreads) {
+    for (int r = tid; r < n_runs; r += nthreads) {
+        // run r = (block, half, shift j, segment): slice 4 block + 2 half + segment
+        const int slr = ((r >> 4) << 2) | (((r >> 3) & 1) << 1) | (r & 1);
+        convert_run(x + 16 * r, planes + slr * kSlicePitch + 12 * ((r >> 1) & 3), &run_sum[r],
+                    &run_inv[r]);
+    }
+}
+
+// This thread's slice (block b, half h, segment seg) of the converted x, into
+// registers: the planes of its four runs, their scales and quantized sums.
+__device__ __forceinline__ void load_slice_planes(const uint32_t* planes, const float* run_sum,
+                                                  const float* run_inv, int sl, bool active, int b,
+                                                  int h, int seg, SlicePlanes& s) {
+    float X[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        // run of (block b, half h, shift j, segment seg)
+        const int run = active ? 16 * b + 8 * h + 2 * j + seg : 0;
+        const uint32_t* pj = planes + (active ? sl : 0) * kSlicePitch + 12 * j;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            s.r[j].p0[q] = pj[q];
+            s.r[j].p1[q] = pj[4 + q];
+            s.r[j].p2[q] = pj[8 + q];
+        }
+        X[j] = active ? run_sum[run] : 0.f;
+        s.inv[j] = active ? run_inv[run] * ((j & 1) ? 0.25f : 1.f) : 0.f;
+    }
+    quantize_run_sums(X, s);
+}
+
+// Rows [0, rows) of a weight chunk in shared memory (this thread's slice of
+// row r at my_col + r row_bytes) against the slice planes s: group g takes rows
+// g, g + groups, ... eight at a time, and each row's total over the group's
+// warps goes to red[row * warps_per_group + warp in group].  Piece p (rows
+// 4p .. 4p + 3) is waited for, once, before its rows are read: from piece
+// waited + 1 on, with the parity of bit p of `parity`.  Returns false once a
+// wait gave up (the rows after it count as zero).
+__device__ __forceinline__ bool dot_rows(const uint8_t* my_col, size_t row_bytes, int rows, int g,
+                                         int groups, int lane, int wig, int warps_per_group,
+                                         bool active, int h, int seg, uint32_t ssel,
+                                         const SlicePlanes& s, float* red, uint32_t bars,
+                                         uint32_t parity, int waited, volatile int* abort_flag,
+                                         bool ok) {
+    constexpr int kLoad = 2 * kRowBatch;  // rows loaded and decoded together
+    for (int base = g; base < rows; base += groups * kLoad) {
+        // Make sure every piece this batch touches has landed, then issue all
+        // shared-memory loads of the batch before any arithmetic.
+        const int last = min(rows - 1, base + (kLoad - 1) * groups);
+        for (int pw = waited + 1; pw <= last / kPieceRows; ++pw)
+            ok = ok && mbar_wait_backoff(bars + 8 * pw, (parity >> pw) & 1u, abort_flag,
+                                         &g_gemv_error, kErrTimeoutGemv, 64);
+        waited = max(waited, last / kPieceRows);
+        RowWords rw[kLoad];
+#pragma unroll
+        for (int u = 0; u < kLoad; ++u) {
+            const int lr = min(base + u * groups, last);
+            rw[u] = load_row_words(my_col + static_cast<size_t>(lr) * row_bytes, h, seg, ssel);
+        }
+        float part[kLoad];
+#pragma unroll
+        for (int u = 0; u < kLoad; ++u) {
+            const float v = slice_dot(rw[u], s);
+            part[u] = (active && ok && base + u * groups < rows) ? v : 0.f;
+        }
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            float p4[kRowBatch];
+#pragma unroll
+            for (int u = 0; u < kRowBatch; ++u) p4[u] = part[hb * kRowBatch + u];
+            int which;
+            const float tot = transpose_reduce4(p4, lane, &which);
+            const int lr = base + (hb * kRowBatch + which) * groups;
+            if ((lane & 7) == 0 && lr < rows) red[lr * warps_per_group + wig] = tot;
+        }
+    }
+    return ok;
+}
+
 __global__ void __launch_bounds__(256, 1)
 gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
                int N, int K, int rows_per_cta, int slices_pad, int groups, uint32_t flags,
@@ -357,12 +441,7 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     if (issuer && !const_weights)
         issue_weight_copies(smem_w, gsrc, bars, rows, row_bytes, delta, tid >> 5, nwarps);
     // x -> integer planes, once per CTA, while the weights stream in
-    for (int r = tid; r < n_runs; r += nthreads) {
-        // run r = (block, half, shift j, segment): slice 4 block + 2 half + segment
-        const int slr = ((r >> 4) << 2) | (((r >> 3) & 1) << 1) | (r & 1);
-        convert_run(x + 16 * r, planes + slr * kSlicePitch + 12 * ((r >> 1) & 3), &run_sum[r],
-                    &run_inv[r]);
-    }
+    convert_x(x, planes, run_sum, run_inv, n_runs, tid, nthreads);
     // With the copies issued before the dependency wait they have (nearly)
     // landed by now: one thread waits for all of them, and the barrier below
     // publishes that, so the row loop needs no barrier polls of its own.
@@ -380,61 +459,15 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     const int b = sl >> 2, h = (sl >> 1) & 1, seg = sl & 1;
     const uint32_t ssel = seg | ((seg + 2) << 4) | ((seg + 4) << 8) | ((seg + 6) << 12);
     SlicePlanes s;
-    {
-        float X[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            // run of (block b, half h, shift j, segment seg)
-            const int run = active ? 16 * b + 8 * h + 2 * j + seg : 0;
-            const uint32_t* pj = planes + (active ? sl : 0) * kSlicePitch + 12 * j;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                s.r[j].p0[q] = pj[q];
-                s.r[j].p1[q] = pj[4 + q];
-                s.r[j].p2[q] = pj[8 + q];
-            }
-            X[j] = active ? run_sum[run] : 0.f;
-            s.inv[j] = active ? run_inv[run] * ((j & 1) ? 0.25f : 1.f) : 0.f;
-        }
-        quantize_run_sums(X, s);
-    }
+    load_slice_planes(planes, run_sum, run_inv, sl, active, b, h, seg, s);
 
     const int lane = tid & 31;
     const int wig = sl >> 5;  // warp index within the group
     const uint8_t* my_col = smem_w + b * kBlockBytes;
-    int waited = const_weights ? n_pieces - 1 : -1;
-    bool ok = !(const_weights && *abort_flag);
-    constexpr int kLoad = 2 * kRowBatch;  // rows loaded and decoded together
-    for (int base = g; base < rows; base += groups * kLoad) {
-        // Make sure every piece this batch touches has landed, then issue all
-        // shared-memory loads of the batch before any arithmetic.
-        const int last = min(rows - 1, base + (kLoad - 1) * groups);
-        for (int pw = waited + 1; pw <= last / kPieceRows; ++pw)
-            ok = ok && mbar_wait_backoff(bars + 8 * pw, 0, abort_flag, &g_gemv_error, kErrTimeoutGemv, 64);
-        waited = max(waited, last / kPieceRows);
-        RowWords rw[kLoad];
-#pragma unroll
-        for (int u = 0; u < kLoad; ++u) {
-            const int lr = min(base + u * groups, last);
-            rw[u] = load_row_words(my_col + static_cast<size_t>(lr) * row_bytes, h, seg, ssel);
-        }
-        float part[kLoad];
-#pragma unroll
-        for (int u = 0; u < kLoad; ++u) {
-            const float v = slice_dot(rw[u], s);
-            part[u] = (active && ok && base + u * groups < rows) ? v : 0.f;
-        }
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-            float p4[kRowBatch];
-#pragma unroll
-            for (int u = 0; u < kRowBatch; ++u) p4[u] = part[hb * kRowBatch + u];
-            int which;
-            const float tot = transpose_reduce4(p4, lane, &which);
-            const int lr = base + (hb * kRowBatch + which) * groups;
-            if ((lane & 7) == 0 && lr < rows) red[lr * warps_per_group + wig] = tot;
-        }
-    }
+    const int waited = const_weights ? n_pieces - 1 : -1;
+    const bool ok = !(const_weights && *abort_flag);
+    dot_rows(my_col, row_bytes, rows, g, groups, lane, wig, warps_per_group, active, h, seg, ssel, s,
+             red, bars, 0u, waited, abort_flag, ok);
     __syncthreads();
     for (int lr = tid; lr < rows; lr += nthreads) {
         float v = 0.f;
