@@ -69,6 +69,14 @@ class GgufTensor(ctypes.Structure):
                 ("offset", ctypes.c_uint64), ("byte_len", ctypes.c_uint64)]
 
 
+class MatmulCall(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("x_elems", ctypes.c_size_t), ("w", ctypes.c_void_p),
+                ("w_bytes", ctypes.c_size_t), ("y", ctypes.c_void_p), ("y_elems", ctypes.c_size_t),
+                ("params", MatmulParams), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("path", ctypes.c_uint32),
+                ("flags", ctypes.c_uint32)]
+
+
 class EmbeddingParams(ctypes.Structure):
     _fields_ = [("vocab_size", ctypes.c_uint32), ("embed_dim", ctypes.c_uint32),
                 ("n_tokens", ctypes.c_uint32), ("ggml_type", ctypes.c_uint32)]
@@ -125,10 +133,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q2k_gguf_tensor_name.restype = ctypes.c_char_p
         lib.q2k_gguf_tensor_info.argtypes = [vp, ctypes.c_char_p, ctypes.POINTER(GgufTensor)]
         lib.q2k_gguf_read_tensor.argtypes = [vp, ctypes.c_char_p, vp, sz]
+        lib.q2k_matmul_ex_batch.argtypes = [ctypes.POINTER(MatmulCall), sz, vp]
         lib.q2k_device_error.argtypes = [u32p, vp]
         lib.q2k_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         for fn in ("q2k_dequantize", "q2k_embedding_gather", "q2k_matmul", "q2k_matmul_path",
-                   "q2k_matmul_ex", "q2k_matmul_batched_mv", "q2k_matmul_id",
+                   "q2k_matmul_ex", "q2k_matmul_ex_batch", "q2k_matmul_batched_mv", "q2k_matmul_id",
                    "q2k_matmul_id_slotted", "q2k_matmul_id_pair", "q2k_device_error",
                    "q2k_selftest_wait_timeout", "q2k_gguf_open", "q2k_gguf_tensor_info",
                    "q2k_gguf_read_tensor"):
@@ -303,6 +312,75 @@ def matmul(x, w, n: int, out=None, path="auto", const_weights: bool = False,
                                       w.numel(), out.data_ptr(), out.numel(), ctypes.byref(p),
                                       ws_ptr, ws_bytes, _stream_handle(x)))
     return out
+
+
+class MatmulBatch:
+    """A fixed list of matmuls enqueued by one library call per ``run()``.
+
+    ``calls`` holds dicts with the arguments of ``matmul``: ``x``, ``w``, ``n``
+    and optionally ``out``, ``path``, ``const_weights``, ``independent``,
+    ``workspace`` (a uint8 CUDA tensor; "auto" allocates one per distinct
+    geometry, shared by its calls).  Everything is checked and packed once;
+    ``run()`` enqueues all calls in order on the current stream of the first
+    call's device with ``q2k_matmul_ex_batch`` (results bit-identical to
+    separate ``matmul`` calls).  The tensors stay bound: update their contents
+    in place between runs.  ``outs`` lists the output tensors in call order.
+    """
+
+    def __init__(self, calls):
+        torch = _torch()
+        calls = list(calls)
+        self._lib = load()
+        self._arr = (MatmulCall * max(1, len(calls)))()
+        self._keep = []
+        self.outs = []
+        shared_ws = {}
+        for i, c in enumerate(calls):
+            x, w, n = c["x"], c["w"], int(c["n"])
+            _require_cuda(x, "x", torch.float32)
+            _require_cuda(w, "w", torch.uint8)
+            if x.dim() != 2:
+                raise ValueError("x must be [m, k]")
+            m, k = x.shape
+            out = c.get("out")
+            if out is None:
+                out = torch.empty((m, n), dtype=torch.float32, device=x.device)
+            _require_cuda(out, "out", torch.float32)
+            pcode = _PATHS[c.get("path", "auto")]
+            ws = c.get("workspace", "auto")
+            p = MatmulParams(m, n, k, GGML_TYPE_Q2_K)
+            if isinstance(ws, str):
+                tensor_path = pcode == PATH_TENSOR or (pcode == PATH_AUTO and m > 8)
+                ws = None
+                if tensor_path:
+                    need = self._lib.q2k_matmul_workspace_bytes(ctypes.byref(p), pcode)
+                    if need:
+                        key = (x.device.index, need)
+                        if key not in shared_ws:
+                            shared_ws[key] = torch.empty(need, dtype=torch.uint8, device=x.device)
+                        ws = shared_ws[key]
+            if ws is not None:
+                _require_cuda(ws, "workspace", torch.uint8)
+            flags = (FLAG_CONST_WEIGHTS if c.get("const_weights") else 0) | \
+                    (FLAG_INDEPENDENT if c.get("independent") else 0)
+            a = self._arr[i]
+            a.x, a.x_elems, a.w, a.w_bytes = x.data_ptr(), x.numel(), w.data_ptr(), w.numel()
+            a.y, a.y_elems, a.params = out.data_ptr(), out.numel(), p
+            a.workspace = ws.data_ptr() if ws is not None else None
+            a.workspace_bytes = ws.numel() if ws is not None else 0
+            a.path, a.flags = pcode, flags
+            self._keep.append((x, w, out, ws))
+            self.outs.append(out)
+        self._count = len(calls)
+        self._device = calls[0]["x"].device if calls else None
+
+    def run(self):
+        if self._count == 0:
+            return self.outs
+        with _on_device(self._keep[0][0]):
+            _check(self._lib, self._lib.q2k_matmul_ex_batch(self._arr, self._count,
+                                                            _stream_handle(self._keep[0][0])))
+        return self.outs
 
 
 def matmul_batched_mv(x, w, n: int, out=None):

@@ -19,6 +19,7 @@
 static_assert(Q2K_STATIC_WORKSPACE_BYTES == q2k::kStaticWorkspaceBytes,
               "header and library disagree on the fixed scratch size");
 static_assert(sizeof(q2k_matmul_id_params) == 32, "q2k_matmul_id_params layout");
+static_assert(sizeof(q2k_matmul_call) == 88, "q2k_matmul_call layout");
 
 namespace {
 
@@ -202,11 +203,16 @@ size_t q2k_matmul_workspace_bytes(const q2k_matmul_params* p, q2k_path path) {
     return q2k::gemm_tc_workspace_bytes(int(p->m), int(p->n), int(p->k));
 }
 
-q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float* x, size_t x_elems,
-                         const void* w, size_t w_bytes, float* y, size_t y_elems,
-                         const q2k_matmul_params* p, void* workspace, size_t workspace_bytes,
-                         q2k_stream_t stream) {
-    g_last_error[0] = '\0';
+}  // extern "C"
+
+namespace {
+
+// q2k_matmul_ex's checks: on success *path_out is the resolved path and
+// *ws_out the workspace to use (NULL when none).  Nothing is launched.
+q2k_status check_matmul_ex(q2k_path path, uint32_t flags, const float* x, size_t x_elems,
+                           const void* w, size_t w_bytes, const float* y, size_t y_elems,
+                           const q2k_matmul_params* p, void* workspace, size_t workspace_bytes,
+                           q2k_path* path_out, void** ws_out) {
     q2k_status st = check_matmul(x, x_elems, w, w_bytes, y, y_elems, p);
     if (st != Q2K_OK) return st;
     if ((flags & ~static_cast<uint32_t>(Q2K_FLAG_CONST_WEIGHTS | Q2K_FLAG_INDEPENDENT)) != 0)
@@ -230,20 +236,81 @@ q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float* x, size_t x
         return fail(Q2K_ERR_INVALID_ARGUMENT, "GEMV path supports m <= 524280");
     if (path == Q2K_PATH_TENSOR && (p->m + 127u) / 128u > 65535u)
         return fail(Q2K_ERR_INVALID_ARGUMENT, "tensor-core path supports m <= 8388480");
+    *path_out = path;
+    *ws_out = ws;
+    return Q2K_OK;
+}
+
+// Enqueue one checked call.
+cudaError_t launch_matmul_ex(q2k_path path, uint32_t flags, const float* x, const void* w, float* y,
+                             const q2k_matmul_params* p, void* ws, const DeviceInfo& dev,
+                             cudaStream_t s) {
+    const uint8_t* wb = static_cast<const uint8_t*>(w);
+    if (path == Q2K_PATH_GEMV)
+        return q2k::launch_gemv(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count,
+                                ((flags & Q2K_FLAG_CONST_WEIGHTS) ? q2k::kGemvConstWeights : 0u) |
+                                    ((flags & Q2K_FLAG_INDEPENDENT) ? q2k::kGemvIndependent : 0u),
+                                s);
+    return q2k::launch_gemm_tc(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count, ws, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float* x, size_t x_elems,
+                         const void* w, size_t w_bytes, float* y, size_t y_elems,
+                         const q2k_matmul_params* p, void* workspace, size_t workspace_bytes,
+                         q2k_stream_t stream) {
+    g_last_error[0] = '\0';
+    q2k_path rpath;
+    void* ws;
+    q2k_status st = check_matmul_ex(path, flags, x, x_elems, w, w_bytes, y, y_elems, p, workspace,
+                                    workspace_bytes, &rpath, &ws);
+    if (st != Q2K_OK) return st;
     DeviceInfo dev;
     st = current_device(&dev);
     if (st != Q2K_OK) return st;
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const uint8_t* wb = static_cast<const uint8_t*>(w);
-    cudaError_t e;
-    if (path == Q2K_PATH_GEMV)
-        e = q2k::launch_gemv(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count,
-                             ((flags & Q2K_FLAG_CONST_WEIGHTS) ? q2k::kGemvConstWeights : 0u) |
-                                 ((flags & Q2K_FLAG_INDEPENDENT) ? q2k::kGemvIndependent : 0u),
-                             s);
-    else
-        e = q2k::launch_gemm_tc(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count, ws, s);
+    cudaError_t e = launch_matmul_ex(rpath, flags, x, w, y, p, ws, dev, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul launch");
+}
+
+q2k_status q2k_matmul_ex_batch(const q2k_matmul_call* calls, size_t count, q2k_stream_t stream) {
+    g_last_error[0] = '\0';
+    if (count == 0) return Q2K_OK;
+    if (calls == nullptr) return fail(Q2K_ERR_INVALID_ARGUMENT, "calls is NULL");
+    for (size_t i = 0; i < count; ++i) {
+        const q2k_matmul_call& c = calls[i];
+        q2k_path rpath;
+        void* ws;
+        q2k_status st = check_matmul_ex(static_cast<q2k_path>(c.path), c.flags, c.x, c.x_elems, c.w,
+                                        c.w_bytes, c.y, c.y_elems, &c.params, c.workspace,
+                                        c.workspace_bytes, &rpath, &ws);
+        if (st != Q2K_OK) {
+            char msg[512];
+            snprintf(msg, sizeof msg, "call %zu: %s", i, g_last_error);
+            snprintf(g_last_error, sizeof g_last_error, "%s", msg);
+            return st;
+        }
+    }
+    DeviceInfo dev;
+    q2k_status st = current_device(&dev);
+    if (st != Q2K_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (size_t i = 0; i < count; ++i) {
+        const q2k_matmul_call& c = calls[i];
+        q2k_path rpath;
+        void* ws;
+        check_matmul_ex(static_cast<q2k_path>(c.path), c.flags, c.x, c.x_elems, c.w, c.w_bytes, c.y,
+                        c.y_elems, &c.params, c.workspace, c.workspace_bytes, &rpath, &ws);
+        cudaError_t e = launch_matmul_ex(rpath, c.flags, c.x, c.w, c.y, &c.params, ws, dev, s);
+        if (e != cudaSuccess) {
+            char what[64];
+            snprintf(what, sizeof what, "q2k_matmul_ex_batch launch of call %zu", i);
+            return cuda_fail(e, what);
+        }
+    }
+    return Q2K_OK;
 }
 
 q2k_status q2k_matmul_path(q2k_path path, const float* x, size_t x_elems, const void* w,

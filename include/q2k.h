@@ -309,6 +309,31 @@ q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float *x, size_t x
                          const q2k_matmul_params *params, void *workspace,
                          size_t workspace_bytes, q2k_stream_t stream);
 
+/* One call of q2k_matmul_ex, for q2k_matmul_ex_batch (88 bytes). */
+typedef struct q2k_matmul_call {
+    const float *x;               /* as q2k_matmul_ex */
+    size_t x_elems;
+    const void *w;
+    size_t w_bytes;
+    float *y;
+    size_t y_elems;
+    q2k_matmul_params params;
+    void *workspace;              /* NULL or as q2k_matmul_ex */
+    size_t workspace_bytes;
+    uint32_t path;                /* a q2k_path */
+    uint32_t flags;               /* a mask of Q2K_FLAG_* */
+} q2k_matmul_call;
+
+/* q2k_matmul_ex_batch - `count` q2k_matmul_ex calls enqueued in order on one
+ * stream with one crossing of the boundary (for the many projections of a
+ * decode step: the host cost per call falls from a binding's argument handling
+ * to the launch itself).  Every call is checked first; the first malformed
+ * one returns its q2k_matmul_ex error (the message names its index) and
+ * nothing is launched.  Results are those of the separate calls, bit for bit.
+ * Calls may share a workspace (they run in stream order).  `calls` is host
+ * memory, read during the call only. */
+q2k_status q2k_matmul_ex_batch(const q2k_matmul_call *calls, size_t count, q2k_stream_t stream);
+
 /* q2k_matmul_static_workspace - the tensor-core matmul (as q2k_matmul_path
  * with Q2K_PATH_TENSOR and a workspace) for callers that cannot allocate
  * device memory at the point of the call: code being captured into a CUDA

@@ -47,12 +47,14 @@ def test_struct_layout_matches_c(tmp_path):
         " offsetof(q2k_embedding_params, n_tokens), sizeof(q2k_status),"
         " sizeof(q2k_matmul_id_params), offsetof(q2k_matmul_id_params, ggml_type),"
         " offsetof(q2k_matmul_id_params, expert_stride));"
-        "printf(\"%zu %zu\\n\", sizeof(q2k_gguf_tensor), offsetof(q2k_gguf_tensor, byte_len));return 0;}\n")
+        "printf(\"%zu %zu\\n\", sizeof(q2k_gguf_tensor), offsetof(q2k_gguf_tensor, byte_len));"
+        "printf(\"%zu %zu\\n\", sizeof(q2k_matmul_call), offsetof(q2k_matmul_call, flags));return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", q2k_build.INCLUDE, str(src),
                     "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
-    assert [int(v) for v in out] == [16, 12, 16, 8, 4, 32, 20, 24, 64, 56]
+    assert [int(v) for v in out] == [16, 12, 16, 8, 4, 32, 20, 24, 64, 56, 88, 84]
+    assert ctypes.sizeof(q2k.MatmulCall) == 88 and q2k.MatmulCall.flags.offset == 84
     assert ctypes.sizeof(q2k.GgufTensor) == 64 and q2k.GgufTensor.byte_len.offset == 56
     assert ctypes.sizeof(q2k.MatmulIdParams) == 32
     assert q2k.MatmulIdParams.ggml_type.offset == 20
@@ -243,3 +245,21 @@ def test_matmul_id_slotted_and_pair_reject(lib):
                                   0x1000000, 0x8000000, 32768 * n, ctypes.byref(big), None,
                                   None) == INVALID
     assert "32767" in lib.q2k_last_error().decode()
+
+
+def test_matmul_ex_batch_checks_every_call_first(lib):
+    """A malformed call anywhere rejects the batch before any launch; its index is named."""
+    calls = (q2k.MatmulCall * 2)()
+    for i, c in enumerate(calls):
+        c.x, c.x_elems, c.w, c.w_bytes = 0x10000, 256, 0x100000, 8 * 84
+        c.y, c.y_elems = 0x1000000 + 4096 * i, 8
+        c.params = q2k.MatmulParams(1, 8, 256, 10)
+        c.path, c.flags = 0, 0
+    calls[1].params = q2k.MatmulParams(1, 8, 255, 10)
+    assert lib.q2k_matmul_ex_batch(calls, 2, None) == INVALID
+    assert "call 1:" in lib.q2k_last_error().decode()
+    calls[1].params = q2k.MatmulParams(1, 8, 256, 10)
+    calls[0].flags = 8
+    assert lib.q2k_matmul_ex_batch(calls, 2, None) == INVALID
+    assert "call 0:" in lib.q2k_last_error().decode()
+    assert lib.q2k_matmul_ex_batch(None, 0, None) == 0   # nothing to do

@@ -240,6 +240,30 @@ def test_tensor_small_m_sampled_rows(m, n, k):
     assert_close(y[:, rows], yref, s, TOL_TC, f"m={m} n={n} k={k} sampled")
 
 
+def test_matmul_batch_equals_separate_calls():
+    """q2k_matmul_ex_batch (MatmulBatch): GEMV and tensor calls of several
+    geometries, the tensor ones sharing a workspace, bit-identical to separate
+    q2k.matmul calls; a second run gives the same bits again."""
+    specs = [(1, 4096, 4096, dict(independent=True)), (1, 333, 1024, {}), (3, 200, 512, {}),
+             (20, 300, 1024, {}), (300, 1000, 512, {}), (300, 1000, 512, {})]
+    calls, ref = [], []
+    for i, (m, n, k, kw) in enumerate(specs):
+        x, w = wl.make_matmul_inputs(3100 + i, m, n, k)
+        xd, wd = dev(x), dev(w)
+        calls.append(dict(x=xd, w=wd, n=n, **kw))
+        ref.append(q2k.matmul(xd, wd, n, **kw))
+    batch = q2k.MatmulBatch(calls)
+    outs = batch.run()
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(zip(outs, ref)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32)), f"call {i}"
+    first = [o.clone() for o in outs]
+    batch.run()
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(zip(batch.outs, first)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32)), f"rerun call {i}"
+
+
 def test_tensor_page_run_dense_rows9():
     """Page fn run_dense(9) and the forced-mm variants (rows > 8).
 
