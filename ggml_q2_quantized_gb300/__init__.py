@@ -133,7 +133,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q2k_gguf_tensor_name.restype = ctypes.c_char_p
         lib.q2k_gguf_tensor_info.argtypes = [vp, ctypes.c_char_p, ctypes.POINTER(GgufTensor)]
         lib.q2k_gguf_read_tensor.argtypes = [vp, ctypes.c_char_p, vp, sz]
-        lib.q2k_matmul_ex_batch.argtypes = [ctypes.POINTER(MatmulCall), sz, vp]
+        lib.q2k_matmul_ex_batch.argtypes = [ctypes.POINTER(MatmulCall), sz, vp, sz, vp]
+        lib.q2k_matmul_batch_scratch_bytes.argtypes = [ctypes.POINTER(MatmulCall), sz]
+        lib.q2k_matmul_batch_scratch_bytes.restype = sz
         lib.q2k_device_error.argtypes = [u32p, vp]
         lib.q2k_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         for fn in ("q2k_dequantize", "q2k_embedding_gather", "q2k_matmul", "q2k_matmul_path",
@@ -323,8 +325,9 @@ class MatmulBatch:
     geometry, shared by its calls).  Everything is checked and packed once;
     ``run()`` enqueues all calls in order on the current stream of the first
     call's device with ``q2k_matmul_ex_batch`` (results bit-identical to
-    separate ``matmul`` calls).  The tensors stay bound: update their contents
-    in place between runs.  ``outs`` lists the output tensors in call order.
+    separate ``matmul`` calls; m = 1 calls reading one x convert it once).  The
+    tensors stay bound: update their contents in place between runs.  ``outs``
+    lists the output tensors in call order.
     """
 
     def __init__(self, calls):
@@ -372,14 +375,19 @@ class MatmulBatch:
             self._keep.append((x, w, out, ws))
             self.outs.append(out)
         self._count = len(calls)
-        self._device = calls[0]["x"].device if calls else None
+        # scratch for the x rows several m = 1 calls share (converted once)
+        need = self._lib.q2k_matmul_batch_scratch_bytes(self._arr, self._count) if calls else 0
+        self._scratch = (torch.empty(need, dtype=torch.uint8, device=calls[0]["x"].device)
+                         if need else None)
 
     def run(self):
         if self._count == 0:
             return self.outs
         with _on_device(self._keep[0][0]):
-            _check(self._lib, self._lib.q2k_matmul_ex_batch(self._arr, self._count,
-                                                            _stream_handle(self._keep[0][0])))
+            sp = self._scratch
+            _check(self._lib, self._lib.q2k_matmul_ex_batch(
+                self._arr, self._count, sp.data_ptr() if sp is not None else None,
+                sp.numel() if sp is not None else 0, _stream_handle(self._keep[0][0])))
         return self.outs
 
 

@@ -12,6 +12,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <vector>
 
 #include "q2k.h"
 #include "q2k_internal.h"
@@ -275,35 +276,123 @@ q2k_status q2k_matmul_ex(q2k_path path, uint32_t flags, const float* x, size_t x
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul launch");
 }
 
-q2k_status q2k_matmul_ex_batch(const q2k_matmul_call* calls, size_t count, q2k_stream_t stream) {
-    g_last_error[0] = '\0';
-    if (count == 0) return Q2K_OK;
-    if (calls == nullptr) return fail(Q2K_ERR_INVALID_ARGUMENT, "calls is NULL");
+}  // extern "C"
+
+namespace {
+
+// Which calls of a batch convert x once: m = 1 GEMV calls reading the same x
+// row (same pointer and k) form a group until a call of the batch writes that
+// row; groups of two or more calls get a 256-byte-aligned slot of the scratch.
+struct BatchPlan {
+    std::vector<q2k_path> path;
+    std::vector<void*> ws;
+    std::vector<int> group;          // per call: its group or -1
+    std::vector<size_t> slot;        // per group: scratch offset (SIZE_MAX: alone, no slot)
+    size_t scratch = 0;
+};
+
+q2k_status plan_batch(const q2k_matmul_call* calls, size_t count, BatchPlan* bp) {
+    bp->path.resize(count);
+    bp->ws.resize(count);
+    bp->group.assign(count, -1);
+    struct Open { const float* x; uint32_t k; int id; };
+    std::vector<Open> open;
+    std::vector<int> uses;
+    std::vector<uint32_t> ks;
     for (size_t i = 0; i < count; ++i) {
         const q2k_matmul_call& c = calls[i];
-        q2k_path rpath;
-        void* ws;
         q2k_status st = check_matmul_ex(static_cast<q2k_path>(c.path), c.flags, c.x, c.x_elems, c.w,
                                         c.w_bytes, c.y, c.y_elems, &c.params, c.workspace,
-                                        c.workspace_bytes, &rpath, &ws);
+                                        c.workspace_bytes, &bp->path[i], &bp->ws[i]);
         if (st != Q2K_OK) {
             char msg[512];
             snprintf(msg, sizeof msg, "call %zu: %s", i, g_last_error);
             snprintf(g_last_error, sizeof g_last_error, "%s", msg);
             return st;
         }
+        if (bp->path[i] == Q2K_PATH_GEMV && q2k::gemv_shares_planes(int(c.params.m), int(c.params.k))) {
+            int id = -1;
+            for (const Open& o : open)
+                if (o.x == c.x && o.k == c.params.k) id = o.id;
+            if (id < 0) {
+                id = static_cast<int>(uses.size());
+                uses.push_back(0);
+                ks.push_back(c.params.k);
+                open.push_back({c.x, c.params.k, id});
+            }
+            ++uses[id];
+            bp->group[i] = id;
+        }
+        // this call's output ends every group whose x it overlaps
+        const size_t y_bytes = c.y_elems * 4;
+        for (size_t j = 0; j < open.size();)
+            if (overlaps(c.y, y_bytes, open[j].x, size_t(open[j].k) * 4)) open.erase(open.begin() + j);
+            else ++j;
     }
+    bp->slot.assign(uses.size(), SIZE_MAX);
+    for (size_t g = 0; g < uses.size(); ++g)
+        if (uses[g] >= 2) {
+            bp->slot[g] = bp->scratch;
+            bp->scratch += (q2k::gemv_planes_bytes(int(ks[g])) + 255) & ~size_t(255);
+        }
+    return Q2K_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t q2k_matmul_batch_scratch_bytes(const q2k_matmul_call* calls, size_t count) {
+    if (calls == nullptr || count == 0) return 0;
+    BatchPlan bp;
+    return plan_batch(calls, count, &bp) == Q2K_OK ? bp.scratch : 0;
+}
+
+q2k_status q2k_matmul_ex_batch(const q2k_matmul_call* calls, size_t count, void* scratch,
+                               size_t scratch_bytes, q2k_stream_t stream) {
+    g_last_error[0] = '\0';
+    if (count == 0) return Q2K_OK;
+    if (calls == nullptr) return fail(Q2K_ERR_INVALID_ARGUMENT, "calls is NULL");
+    BatchPlan bp;
+    q2k_status st = plan_batch(calls, count, &bp);
+    if (st != Q2K_OK) return st;
+    // without room for every slot, every call converts x itself
+    const bool share = scratch != nullptr && scratch_bytes >= bp.scratch && bp.scratch > 0;
+    if (share && !aligned(scratch, 16))
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "scratch must be 16-byte aligned");
+    if (share)
+        for (size_t i = 0; i < count; ++i) {
+            const q2k_matmul_call& c = calls[i];
+            if (overlaps(scratch, bp.scratch, c.x, c.x_elems * 4) ||
+                overlaps(scratch, bp.scratch, c.w, c.w_bytes) ||
+                overlaps(scratch, bp.scratch, c.y, c.y_elems * 4) ||
+                (bp.ws[i] != nullptr && overlaps(scratch, bp.scratch, bp.ws[i], c.workspace_bytes)))
+                return fail(Q2K_ERR_INVALID_ARGUMENT, "scratch must not alias call %zu's buffers", i);
+        }
     DeviceInfo dev;
-    q2k_status st = current_device(&dev);
+    st = current_device(&dev);
     if (st != Q2K_OK) return st;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    std::vector<char> prepared(bp.slot.size(), 0);
     for (size_t i = 0; i < count; ++i) {
         const q2k_matmul_call& c = calls[i];
-        q2k_path rpath;
-        void* ws;
-        check_matmul_ex(static_cast<q2k_path>(c.path), c.flags, c.x, c.x_elems, c.w, c.w_bytes, c.y,
-                        c.y_elems, &c.params, c.workspace, c.workspace_bytes, &rpath, &ws);
-        cudaError_t e = launch_matmul_ex(rpath, c.flags, c.x, c.w, c.y, &c.params, ws, dev, s);
+        cudaError_t e = cudaSuccess;
+        const int g = bp.group[i];
+        if (share && g >= 0 && bp.slot[g] != SIZE_MAX) {
+            uint8_t* planes = static_cast<uint8_t*>(scratch) + bp.slot[g];
+            if (!prepared[g]) {
+                e = q2k::launch_prep_x_planes(c.x, int(c.params.k), planes, s);
+                prepared[g] = 1;
+            }
+            if (e == cudaSuccess)
+                e = q2k::launch_gemv(c.x, static_cast<const uint8_t*>(c.w), c.y, 1, int(c.params.n),
+                                     int(c.params.k), dev.device, dev.sm_count,
+                                     ((c.flags & Q2K_FLAG_CONST_WEIGHTS) ? q2k::kGemvConstWeights : 0u) |
+                                         ((c.flags & Q2K_FLAG_INDEPENDENT) ? q2k::kGemvIndependent : 0u),
+                                     s, planes);
+        } else {
+            e = launch_matmul_ex(bp.path[i], c.flags, c.x, c.w, c.y, &c.params, bp.ws[i], dev, s);
+        }
         if (e != cudaSuccess) {
             char what[64];
             snprintf(what, sizeof what, "q2k_matmul_ex_batch launch of call %zu", i);

@@ -349,7 +349,7 @@ __device__ __forceinline__ bool dot_rows(const uint8_t* my_col, size_t row_bytes
 __global__ void __launch_bounds__(256, 1)
 gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
                int N, int K, int rows_per_cta, int slices_pad, int groups, uint32_t flags,
-               GemvProblems pr) {
+               GemvProblems pr, const uint8_t* __restrict__ xplanes) {
     const bool independent = (flags & kGemvIndependent) != 0;
     const bool const_weights = independent || (flags & kGemvConstWeights) != 0;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -405,7 +405,8 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
                            static_cast<size_t>(rows_per_cta) * warps_per_group * 4;
     const size_t bar_off = (red_end + 7) & ~size_t(7);
     const uint32_t bars = smem_u32(smem + bar_off);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + bar_off + 8 * max_pieces);
+    const uint32_t planes_bar = bars + 8 * max_pieces;  // x planes copied in (xplanes)
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + bar_off + 8 * (max_pieces + 1));
     const uint8_t* gsrc = w + static_cast<size_t>(r0) * row_bytes;
     const size_t chunk = static_cast<size_t>(rows) * row_bytes;
 
@@ -417,10 +418,20 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     const bool issuer = (tid & 31) == 0;
     if (tid == 0) {
         for (int p = 0; p < n_pieces; ++p) mbar_init(bars + 8 * p, 1);
+        mbar_init(planes_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // x converted once for several calls (prep_x_planes_kernel, a grid that
+    // completed before this one started): one bulk copy of its planes, run
+    // sums and run scales, laid out as convert_x lays them out here
+    const uint32_t planes_bytes = static_cast<uint32_t>(
+        static_cast<size_t>(n_runs >> 2) * kSlicePitch * 4 + static_cast<size_t>(n_runs) * 8);
+    if (xplanes != nullptr && tid == 0) {
+        mbar_arrive_expect_tx(planes_bar, planes_bytes);
+        bulk_copy_g2s(smem_u32(planes), xplanes, planes_bytes, planes_bar);
+    }
     if (const_weights) {
         // The caller guarantees the grids that may still run do not write W,
         // so the weight copies may start before the dependency wait.
@@ -441,11 +452,13 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     if (issuer && !const_weights)
         issue_weight_copies(smem_w, gsrc, bars, rows, row_bytes, delta, tid >> 5, nwarps);
     // x -> integer planes, once per CTA, while the weights stream in
-    convert_x(x, planes, run_sum, run_inv, n_runs, tid, nthreads);
+    if (xplanes == nullptr) convert_x(x, planes, run_sum, run_inv, n_runs, tid, nthreads);
     // With the copies issued before the dependency wait they have (nearly)
     // landed by now: one thread waits for all of them, and the barrier below
     // publishes that, so the row loop needs no barrier polls of its own.
     bool all_ok = true;
+    if (xplanes != nullptr && tid == 0)
+        all_ok = mbar_wait_backoff(planes_bar, 0, abort_flag, &g_gemv_error, kErrTimeoutGemv, 64);
     if (const_weights && tid == 0) {
         for (int p = 0; p < n_pieces; ++p)
             all_ok = all_ok && mbar_wait_backoff(bars + 8 * p, 0, abort_flag, &g_gemv_error,
@@ -479,6 +492,8 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
         volatile int no_abort = 0;
         for (int p = 0; p < n_pieces; ++p)
             mbar_wait_bounded(bars + 8 * p, 0, &no_abort, &g_gemv_error, kErrTimeoutGemv);
+        if (xplanes != nullptr)
+            mbar_wait_bounded(planes_bar, 0, &no_abort, &g_gemv_error, kErrTimeoutGemv);
     }
     // Independent calls finish only after the grid before them, so work
     // enqueued later on the stream sees every earlier call complete.  One CTA
@@ -499,7 +514,7 @@ size_t m1_smem(int rows, int K, int slices_pad) {
     const size_t w_smem = (static_cast<size_t>(rows) * row_bytes + 31) & ~size_t(15);
     const size_t red_end = w_smem + static_cast<size_t>(n_runs / 4) * kSlicePitch * 4 +
                            static_cast<size_t>(n_runs) * 8 + static_cast<size_t>(rows) * (slices_pad / 32) * 4;
-    return ((red_end + 7) & ~size_t(7)) + 8 * pieces + 16;
+    return ((red_end + 7) & ~size_t(7)) + 8 * (pieces + 1) + 16;
 }
 
 bool plan_m1(int N, int K, int sm_count, int threads, bool whole_batches, M1Plan* p) {
@@ -536,7 +551,7 @@ bool plan_m1(int N, int K, int sm_count, int threads, bool whole_batches, M1Plan
 
 cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, const M1Plan& p,
                       int device, uint32_t flags, const GemvProblems& pr, int n_problems,
-                      cudaStream_t stream) {
+                      const uint8_t* xplanes, cudaStream_t stream) {
     static bool smem_set[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!smem_set[device]) {
@@ -557,7 +572,7 @@ cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, gemv_m1_kernel, x, w, y, N, K, p.rows_per_cta, p.slices_pad,
-                              p.groups, flags, pr);
+                              p.groups, flags, pr, xplanes);
 }
 
 // ------------------------------------------------------------------ general m
@@ -677,7 +692,8 @@ cudaError_t launch_rows(const float* x, const uint8_t* w, float* y, int M, int N
 
 cudaError_t launch_gemv_problems(const float* x, const uint8_t* w, float* y, int M, int N, int K,
                                  int device, int sm_count, uint32_t flags,
-                                 const GemvProblems& pr, int n_problems, cudaStream_t stream) {
+                                 const GemvProblems& pr, int n_problems, cudaStream_t stream,
+                                 const uint8_t* xplanes) {
     M1Plan plan;
     // Several problems in one grid overlap on the SMs like independent calls
     // do, so they take the same small CTAs of whole row batches, planned per
@@ -686,7 +702,8 @@ cudaError_t launch_gemv_problems(const float* x, const uint8_t* w, float* y, int
     const bool small_ctas = (flags & kGemvIndependent) != 0 || n_problems > 1;
     const int threads = small_ctas ? kM1ThreadsIndependent : kM1ThreadsDependent;
     if (M == 1 && plan_m1(N, K, sm_count, threads, small_ctas, &plan))
-        return launch_m1(x, w, y, N, K, plan, device, flags, pr, n_problems, stream);
+        return launch_m1(x, w, y, N, K, plan, device, flags, pr, n_problems,
+                         n_problems == 1 ? xplanes : nullptr, stream);
     switch (M < 8 ? M : 8) {
         case 1: return launch_rows<1>(x, w, y, M, N, K, pr, n_problems, stream);
         case 2: return launch_rows<2>(x, w, y, M, N, K, pr, n_problems, stream);
@@ -700,8 +717,35 @@ cudaError_t launch_gemv_problems(const float* x, const uint8_t* w, float* y, int
 }
 
 cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N, int K,
-                        int device, int sm_count, uint32_t flags, cudaStream_t stream) {
-    return launch_gemv_problems(x, w, y, M, N, K, device, sm_count, flags, GemvProblems{}, 1, stream);
+                        int device, int sm_count, uint32_t flags, cudaStream_t stream,
+                        const uint8_t* xplanes) {
+    return launch_gemv_problems(x, w, y, M, N, K, device, sm_count, flags, GemvProblems{}, 1, stream,
+                                xplanes);
+}
+
+bool gemv_shares_planes(int M, int K) { return M == 1 && K / 64 <= kM1MaxSlices; }
+
+size_t gemv_planes_bytes(int K) {
+    return static_cast<size_t>(K / 64) * kSlicePitch * 4 + static_cast<size_t>(K / 16) * 8;
+}
+
+// x (one row) -> the integer planes, run sums and run scales in the layout the
+// m = 1 kernel keeps in shared memory, for several of its calls to copy.  It
+// never lets the next grid start early, so every later grid sees it complete.
+__global__ void __launch_bounds__(128)
+prep_x_planes_kernel(const float* __restrict__ x, int K, uint8_t* __restrict__ dst) {
+    const int n_runs = K >> 4;
+    uint32_t* planes = reinterpret_cast<uint32_t*>(dst);
+    float* run_sum = reinterpret_cast<float*>(planes + (n_runs >> 2) * kSlicePitch);
+    float* run_inv = run_sum + n_runs;
+    convert_x(x, planes, run_sum, run_inv, n_runs, blockIdx.x * blockDim.x + threadIdx.x,
+              gridDim.x * blockDim.x);
+}
+
+cudaError_t launch_prep_x_planes(const float* x, int K, uint8_t* dst, cudaStream_t stream) {
+    const int n_runs = K / 16;
+    prep_x_planes_kernel<<<(n_runs + 127) / 128, 128, 0, stream>>>(x, K, dst);
+    return cudaGetLastError();
 }
 
 namespace {

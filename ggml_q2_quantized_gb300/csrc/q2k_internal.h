@@ -28,7 +28,17 @@ cudaError_t launch_gather(const uint8_t* table, const uint32_t* ids, float* out,
 constexpr uint32_t kGemvConstWeights = 1u;
 constexpr uint32_t kGemvIndependent = 2u;
 cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N, int K,
-                        int device, int sm_count, uint32_t flags, cudaStream_t stream);
+                        int device, int sm_count, uint32_t flags, cudaStream_t stream,
+                        const uint8_t* xplanes = nullptr);
+
+// x converted once for several m = 1 calls: when gemv_shares_planes(M, K),
+// launch_prep_x_planes writes gemv_planes_bytes(K) bytes (16-byte aligned
+// destination) that launch_gemv(..., xplanes) calls then copy instead of
+// converting x themselves (same values, so the same bits).  The prep grid
+// completes before any later grid of the stream starts.
+bool gemv_shares_planes(int M, int K);
+size_t gemv_planes_bytes(int K);
+cudaError_t launch_prep_x_planes(const float* x, int K, uint8_t* dst, cudaStream_t stream);
 
 // Several independent products in one launch of the GEMV kernels, each computed
 // exactly as its own launch_gemv call (same kernel, same arithmetic), problem p
@@ -54,7 +64,8 @@ struct GemvProblems {
 };
 cudaError_t launch_gemv_problems(const float* x, const uint8_t* w, float* y, int M, int N, int K,
                                  int device, int sm_count, uint32_t flags,
-                                 const GemvProblems& pr, int n_problems, cudaStream_t stream);
+                                 const GemvProblems& pr, int n_problems, cudaStream_t stream,
+                                 const uint8_t* xplanes = nullptr);
 
 // Self-test of the bounded wait: one CTA waits for about limit_ns on a barrier
 // nothing completes, then sets the GEMV error word's time-out bit.

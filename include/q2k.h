@@ -331,8 +331,21 @@ typedef struct q2k_matmul_call {
  * one returns its q2k_matmul_ex error (the message names its index) and
  * nothing is launched.  Results are those of the separate calls, bit for bit.
  * Calls may share a workspace (they run in stream order).  `calls` is host
- * memory, read during the call only. */
-q2k_status q2k_matmul_ex_batch(const q2k_matmul_call *calls, size_t count, q2k_stream_t stream);
+ * memory, read during the call only.
+ *   scratch  device, NULL or at least q2k_matmul_batch_scratch_bytes(calls,
+ *            count) bytes, 16-byte aligned, not overlapping any call's
+ *            buffers.  With it, m = 1 calls on the fp32 GEMV path (k <= 16384)
+ *            that read the same x row convert x to their integer form once,
+ *            into the scratch, instead of once per CTA of every call (the
+ *            same values: same bits).  A call of the batch that writes that
+ *            row ends the sharing.  Without it (or smaller) every call
+ *            converts x itself. */
+q2k_status q2k_matmul_ex_batch(const q2k_matmul_call *calls, size_t count, void *scratch,
+                               size_t scratch_bytes, q2k_stream_t stream);
+
+/* q2k_matmul_batch_scratch_bytes - device bytes of scratch q2k_matmul_ex_batch
+ * uses for these calls (0: none, or malformed calls). */
+size_t q2k_matmul_batch_scratch_bytes(const q2k_matmul_call *calls, size_t count);
 
 /* q2k_matmul_static_workspace - the tensor-core matmul (as q2k_matmul_path
  * with Q2K_PATH_TENSOR and a workspace) for callers that cannot allocate

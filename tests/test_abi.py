@@ -256,10 +256,16 @@ def test_matmul_ex_batch_checks_every_call_first(lib):
         c.params = q2k.MatmulParams(1, 8, 256, 10)
         c.path, c.flags = 0, 0
     calls[1].params = q2k.MatmulParams(1, 8, 255, 10)
-    assert lib.q2k_matmul_ex_batch(calls, 2, None) == INVALID
+    assert lib.q2k_matmul_ex_batch(calls, 2, None, 0, None) == INVALID
     assert "call 1:" in lib.q2k_last_error().decode()
+    assert lib.q2k_matmul_batch_scratch_bytes(calls, 2) == 0
     calls[1].params = q2k.MatmulParams(1, 8, 256, 10)
+    # two m = 1 calls on one x: one slot of x planes (K/64 slices x 49 words + K/16 x 8 bytes)
+    assert lib.q2k_matmul_batch_scratch_bytes(calls, 2) == (4 * 49 * 4 + 16 * 8 + 255) // 256 * 256
     calls[0].flags = 8
-    assert lib.q2k_matmul_ex_batch(calls, 2, None) == INVALID
+    assert lib.q2k_matmul_ex_batch(calls, 2, None, 0, None) == INVALID
     assert "call 0:" in lib.q2k_last_error().decode()
-    assert lib.q2k_matmul_ex_batch(None, 0, None) == 0   # nothing to do
+    calls[0].flags = 0
+    assert lib.q2k_matmul_ex_batch(calls, 2, 0x3000008, 1024, None) == INVALID
+    assert "aligned" in lib.q2k_last_error().decode()
+    assert lib.q2k_matmul_ex_batch(None, 0, None, 0, None) == 0   # nothing to do

@@ -252,12 +252,37 @@ def test_matmul_batch_equals_separate_calls():
         xd, wd = dev(x), dev(w)
         calls.append(dict(x=xd, w=wd, n=n, **kw))
         ref.append(q2k.matmul(xd, wd, n, **kw))
+    # m = 1 calls sharing one x (converted once into the batch scratch), one of
+    # them tensor-path, then a call that overwrites that x, then two more on it
+    k = 2048
+    xs = dev(wl.random_activations(np.random.default_rng(31), 1, k))
+    shared = []
+    for i, n in enumerate((500, 4096, 77)):
+        _, w = wl.make_matmul_inputs(3200 + i, 1, n, k)
+        shared.append((n, dev(w)))
+    for n, wd in shared:
+        calls.append(dict(x=xs, w=wd, n=n, independent=True))
+    calls.append(dict(x=xs, w=shared[0][1], n=shared[0][0], path="tensor"))
+    x_src = dev(wl.random_activations(np.random.default_rng(32), 1, 256))
+    _, w_over = wl.make_matmul_inputs(3300, 1, k, 256)   # writes a fresh x of length k over xs
+    calls.append(dict(x=x_src, w=dev(w_over), n=k, out=xs))
+    for n, wd in shared[1:]:
+        calls.append(dict(x=xs, w=wd, n=n))
+    x_keep = xs.clone()
+    ref += [q2k.matmul(xs, wd, n, independent=True) for n, wd in shared]
+    ref.append(q2k.matmul(xs, shared[0][1], shared[0][0], path="tensor"))
+    ref.append(q2k.matmul(x_src, calls[-3]["w"], k))
+    ref += [q2k.matmul(ref[-1], wd, n) for n, wd in shared[1:]]
+    torch.cuda.synchronize()
+    xs.copy_(x_keep)   # the batch starts from the same x
     batch = q2k.MatmulBatch(calls)
+    assert batch._scratch is not None  # two groups on xs: before and after the overwrite
     outs = batch.run()
     torch.cuda.synchronize()
     for i, (a, b) in enumerate(zip(outs, ref)):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32)), f"call {i}"
     first = [o.clone() for o in outs]
+    xs.copy_(x_keep)
     batch.run()
     torch.cuda.synchronize()
     for i, (a, b) in enumerate(zip(batch.outs, first)):
