@@ -118,12 +118,15 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q2k_matmul_workspace_bytes.argtypes = [ctypes.POINTER(MatmulParams), ctypes.c_int]
         lib.q2k_matmul_workspace_bytes.restype = ctypes.c_size_t
         lib.q2k_matmul_batched_mv.argtypes = [vp, sz, vp, sz, vp, sz, ctypes.c_uint32,
-                                              ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, vp]
+                                              ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
+                                              vp, sz, vp]
         lib.q2k_matmul_id.argtypes = [vp, sz, vp, sz, vp, vp, sz, ctypes.POINTER(MatmulIdParams),
-                                      vp, vp]
+                                      vp, vp, sz, vp]
         lib.q2k_matmul_id_slotted.argtypes = lib.q2k_matmul_id.argtypes
         lib.q2k_matmul_id_pair.argtypes = [vp, sz, vp, sz, vp, sz, vp, vp, vp, sz,
-                                           ctypes.POINTER(MatmulIdParams), vp, vp]
+                                           ctypes.POINTER(MatmulIdParams), vp, vp, sz, vp]
+        lib.q2k_x_planes_bytes.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
+        lib.q2k_x_planes_bytes.restype = sz
         lib.q2k_gguf_open.argtypes = [ctypes.c_char_p, ctypes.POINTER(vp)]
         lib.q2k_gguf_close.argtypes = [vp]
         lib.q2k_gguf_close.restype = None
@@ -391,11 +394,26 @@ class MatmulBatch:
         return self.outs
 
 
-def matmul_batched_mv(x, w, n: int, out=None):
+def _planes_scratch(lib, k, rows, device, scratch):
+    """(pointer, bytes) of the x-planes scratch: "auto" allocates one."""
+    if scratch is None:
+        return None, 0, None
+    if isinstance(scratch, str):
+        need = lib.q2k_x_planes_bytes(k, rows)
+        if not need:
+            return None, 0, None
+        scratch = _torch().empty(need, dtype=_torch().uint8, device=device)
+    return scratch.data_ptr(), scratch.numel(), scratch
+
+
+def matmul_batched_mv(x, w, n: int, out=None, scratch=None):
     """``batches`` matrix-vector products in one launch: ``x`` f32 ``[batches, k]``
     (or ``[batches, 1, k]``), ``w`` uint8 holding the batches' ``[n, k]`` Q2_K
     matrices back to back; returns ``[batches, n]`` (the shape of ``x`` with k
-    replaced by n).  Each batch is bit-identical to ``matmul`` of it alone."""
+    replaced by n).  Each batch is bit-identical to ``matmul`` of it alone.
+    ``scratch="auto"`` converts each batch's x once instead of per CTA (an
+    extra launch; it pays for long k), or pass a uint8 tensor of
+    ``q2k_x_planes_bytes(k, batches)`` bytes."""
     torch = _torch()
     _require_cuda(x, "x", torch.float32)
     _require_cuda(w, "w", torch.uint8)
@@ -405,9 +423,10 @@ def matmul_batched_mv(x, w, n: int, out=None):
         out = torch.empty(tuple(x.shape[:-1]) + (n,), dtype=torch.float32, device=x.device)
     _require_cuda(out, "out", torch.float32)
     lib = load()
+    sp, sb, _keep = _planes_scratch(lib, k, batches, x.device, scratch)
     with _on_device(x):
         _check(lib, lib.q2k_matmul_batched_mv(x.data_ptr(), x.numel(), w.data_ptr(), w.numel(),
-                                              out.data_ptr(), out.numel(), batches, 1, n, k,
+                                              out.data_ptr(), out.numel(), batches, 1, n, k, sp, sb,
                                               _stream_handle(x)))
     return out
 
@@ -422,7 +441,7 @@ def _routed_finish(bad, check, outs, n_experts):
 
 
 def matmul_id_slotted(x, w, ids, n: int, n_experts: int, expert_stride: int | None = None,
-                      out=None, check: bool = True):
+                      out=None, check: bool = True, scratch=None):
     """Routed product with one input row per route: ``x`` f32 ``[n_tokens, top_k,
     k]``, ``ids`` ``[n_tokens, top_k]``; returns ``[n_tokens, top_k, n]``, route
     (t, s) = expert ``ids[t, s]`` times ``x[t, s]``.  ``check`` as ``matmul_id``."""
@@ -441,15 +460,17 @@ def matmul_id_slotted(x, w, ids, n: int, n_experts: int, expert_stride: int | No
     bad = torch.zeros(1, dtype=torch.int32, device=x.device)
     p = MatmulIdParams(n_tokens, top_k, n, k, n_experts, GGML_TYPE_Q2_K, expert_stride)
     lib = load()
+    sp, sb, _keep = _planes_scratch(lib, k, n_tokens * top_k, x.device, scratch)
     with _on_device(x):
         _check(lib, lib.q2k_matmul_id_slotted(x.data_ptr(), x.numel(), w.data_ptr(), w.numel(),
                                               ids.data_ptr(), out.data_ptr(), out.numel(),
-                                              ctypes.byref(p), bad.data_ptr(), _stream_handle(x)))
+                                              ctypes.byref(p), bad.data_ptr(), sp, sb,
+                                              _stream_handle(x)))
     return _routed_finish(bad, check, (out,), n_experts)
 
 
 def matmul_id_pair(x, w_a, w_b, ids, n: int, n_experts: int, top_k: int,
-                   expert_stride: int | None = None, check: bool = True):
+                   expert_stride: int | None = None, check: bool = True, scratch="auto"):
     """Two routed products sharing ``x`` and ``ids`` (e.g. the gate and up
     projections) in one launch; returns ``(y_a, y_b)`` as ``matmul_id`` would."""
     torch = _torch()
@@ -467,16 +488,18 @@ def matmul_id_pair(x, w_a, w_b, ids, n: int, n_experts: int, top_k: int,
     bad = torch.zeros(1, dtype=torch.int32, device=x.device)
     p = MatmulIdParams(n_tokens, top_k, n, k, n_experts, GGML_TYPE_Q2_K, expert_stride)
     lib = load()
+    sp, sb, _keep = _planes_scratch(lib, k, n_tokens, x.device, scratch)
     with _on_device(x):
         _check(lib, lib.q2k_matmul_id_pair(x.data_ptr(), x.numel(), w_a.data_ptr(), w_a.numel(),
                                            w_b.data_ptr(), w_b.numel(), ids.data_ptr(),
                                            y_a.data_ptr(), y_b.data_ptr(), y_a.numel(),
-                                           ctypes.byref(p), bad.data_ptr(), _stream_handle(x)))
+                                           ctypes.byref(p), bad.data_ptr(), sp, sb,
+                                           _stream_handle(x)))
     return _routed_finish(bad, check, (y_a, y_b), n_experts)
 
 
 def matmul_id(x, w, ids, n: int, n_experts: int, top_k: int, expert_stride: int | None = None,
-              out=None, check: bool = True):
+              out=None, check: bool = True, scratch="auto"):
     """Expert-routed product: ``x`` f32 ``[n_tokens, k]``, ``ids`` 32-bit ints
     ``[n_tokens * top_k]`` (token-major), expert e's ``[n, k]`` Q2_K matrix at
     byte ``e * expert_stride`` of ``w`` (default: packed, ``n * k/256 * 84``).
@@ -499,10 +522,11 @@ def matmul_id(x, w, ids, n: int, n_experts: int, top_k: int, expert_stride: int 
     bad = torch.zeros(1, dtype=torch.int32, device=x.device)
     p = MatmulIdParams(n_tokens, top_k, n, k, n_experts, GGML_TYPE_Q2_K, expert_stride)
     lib = load()
+    sp, sb, _keep = _planes_scratch(lib, k, n_tokens, x.device, scratch)
     with _on_device(x):
         _check(lib, lib.q2k_matmul_id(x.data_ptr(), x.numel(), w.data_ptr(), w.numel(),
                                       ids.data_ptr(), out.data_ptr(), out.numel(),
-                                      ctypes.byref(p), bad.data_ptr(), _stream_handle(x)))
+                                      ctypes.byref(p), bad.data_ptr(), sp, sb, _stream_handle(x)))
     if not check:
         return out, bad
     n_bad = int(bad.item())

@@ -113,6 +113,26 @@ q2k_status check_matmul(const float* x, size_t x_elems, const void* w, size_t w_
     return Q2K_OK;
 }
 
+// An optional scratch for x converted once per x row (rows rows of k): NULL,
+// or at least q2k_x_planes_bytes(k, rows) bytes, 16-byte aligned, not
+// overlapping the call's buffers.  *planes is the scratch when it will be
+// used (k small enough for the m = 1 kernel), else NULL.
+q2k_status check_planes_scratch(void* scratch, size_t scratch_bytes, uint32_t k, size_t rows,
+                                const void* x, size_t x_bytes, const void* w, size_t w_bytes,
+                                const void* y, size_t y_bytes, uint8_t** planes) {
+    *planes = nullptr;
+    if (scratch == nullptr || !q2k::gemv_shares_planes(1, int(k))) return Q2K_OK;
+    const size_t need = q2k::gemv_planes_stride(int(k)) * rows;
+    if (scratch_bytes < need)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "scratch has %zu bytes, needs %zu", scratch_bytes, need);
+    if (!aligned(scratch, 16)) return fail(Q2K_ERR_INVALID_ARGUMENT, "scratch must be 16-byte aligned");
+    if (overlaps(scratch, need, x, x_bytes) || overlaps(scratch, need, w, w_bytes) ||
+        overlaps(scratch, need, y, y_bytes))
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "scratch must not alias x, w or y");
+    *planes = static_cast<uint8_t*>(scratch);
+    return Q2K_OK;
+}
+
 }  // namespace
 
 void q2k::set_last_error(const char* msg) {
@@ -436,7 +456,8 @@ q2k_status q2k_matmul_static_workspace(const float* x, size_t x_elems, const voi
 
 q2k_status q2k_matmul_batched_mv(const float* x, size_t x_elems, const void* w, size_t w_bytes,
                                  float* y, size_t y_elems, uint32_t batches, uint32_t m,
-                                 uint32_t n, uint32_t k, q2k_stream_t stream) {
+                                 uint32_t n, uint32_t k, void* scratch, size_t scratch_bytes,
+                                 q2k_stream_t stream) {
     g_last_error[0] = '\0';
     if (m != 1) return fail(Q2K_ERR_INVALID_ARGUMENT, "batched matrix-vector takes m = 1, got %u", m);
     if (batches == 0 || batches > 65535)
@@ -457,16 +478,24 @@ q2k_status q2k_matmul_batched_mv(const float* x, size_t x_elems, const void* w, 
     if (st != Q2K_OK) return st;
     if (overlaps(y, want_y * 4, x, want_x * 4) || overlaps(y, want_y * 4, w, want_w))
         return fail(Q2K_ERR_INVALID_ARGUMENT, "y must not alias x or w");
+    uint8_t* planes = nullptr;
+    st = check_planes_scratch(scratch, scratch_bytes, k, batches, x, want_x * 4, w, want_w, y,
+                              want_y * 4, &planes);
+    if (st != Q2K_OK) return st;
     DeviceInfo dev;
     st = current_device(&dev);
     if (st != Q2K_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     q2k::GemvProblems pr;
     pr.x_stride = static_cast<long long>(k);
     pr.w_stride = static_cast<long long>(per_w);
     pr.y_stride = static_cast<long long>(n);
-    cudaError_t e = q2k::launch_gemv_problems(x, static_cast<const uint8_t*>(w), y, 1, int(n), int(k),
-                                              dev.device, dev.sm_count, 0u, pr, int(batches),
-                                              reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = cudaSuccess;
+    if (planes != nullptr) e = q2k::launch_prep_x_planes(x, int(k), planes, s, int(batches));
+    if (e == cudaSuccess)
+        e = q2k::launch_gemv_problems(x, static_cast<const uint8_t*>(w), y, 1, int(n), int(k),
+                                      dev.device, dev.sm_count, 0u, pr, int(batches), s, planes,
+                                      planes ? uint32_t(q2k::gemv_planes_stride(int(k))) : 0u);
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_matmul_batched_mv launch");
 }
 
@@ -481,7 +510,7 @@ namespace {
 q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void* wa, size_t wa_bytes,
                        const void* wb, size_t wb_bytes, const uint32_t* ids, float* ya, float* yb,
                        size_t y_elems, const q2k_matmul_id_params* p, uint32_t* bad_id_count,
-                       q2k_stream_t stream, const char* what) {
+                       void* scratch, size_t scratch_bytes, q2k_stream_t stream, const char* what) {
     g_last_error[0] = '\0';
     const bool pair = yb != nullptr || wb != nullptr;
     if (p == nullptr) return fail(Q2K_ERR_INVALID_ARGUMENT, "params is NULL");
@@ -538,8 +567,20 @@ q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void*
             if (overlaps(outs[o], out_bytes[o], outs[o2], out_bytes[o2]))
                 return fail(Q2K_ERR_INVALID_ARGUMENT, "writable buffers must not alias inputs or each other");
     }
+    // x rows: tokens, or routes when slotted
+    const size_t x_rows = slotted ? routes : size_t(p->n_tokens);
+    uint8_t* planes = nullptr;
+    q2k_status st = check_planes_scratch(scratch, scratch_bytes, p->k, x_rows, x, x_bytes, wa,
+                                         wa_bytes, ya, y_bytes, &planes);
+    if (st == Q2K_OK && planes != nullptr && pair) {
+        const size_t need = q2k::gemv_planes_stride(int(p->k)) * x_rows;
+        if (overlaps(planes, need, wb, wb_bytes) || overlaps(planes, need, yb, y_bytes) ||
+            overlaps(planes, need, ids, id_bytes))
+            st = fail(Q2K_ERR_INVALID_ARGUMENT, "scratch must not alias x, w or y");
+    }
+    if (st != Q2K_OK) return st;
     DeviceInfo dev;
-    q2k_status st = current_device(&dev);
+    st = current_device(&dev);
     if (st != Q2K_OK) return st;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
@@ -557,8 +598,11 @@ q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void*
         pr.w2 = static_cast<const uint8_t*>(wb);
         pr.y2 = yb;
     }
-    e = q2k::launch_gemv_problems(x, static_cast<const uint8_t*>(wa), ya, 1, int(p->n), int(p->k),
-                                  dev.device, dev.sm_count, 0u, pr, int(pair ? 2 * routes : routes), s);
+    if (planes != nullptr) e = q2k::launch_prep_x_planes(x, int(p->k), planes, s, int(x_rows));
+    if (e == cudaSuccess)
+        e = q2k::launch_gemv_problems(x, static_cast<const uint8_t*>(wa), ya, 1, int(p->n), int(p->k),
+                                      dev.device, dev.sm_count, 0u, pr, int(pair ? 2 * routes : routes),
+                                      s, planes, planes ? uint32_t(q2k::gemv_planes_stride(int(p->k))) : 0u);
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, what);
 }
 
@@ -566,32 +610,38 @@ q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void*
 
 extern "C" {
 
+size_t q2k_x_planes_bytes(uint32_t k, uint32_t rows) {
+    if (k == 0 || k % Q2K_QK_K != 0 || k > INT_MAX || !q2k::gemv_shares_planes(1, int(k))) return 0;
+    return q2k::gemv_planes_stride(int(k)) * rows;
+}
+
 q2k_status q2k_matmul_id(const float* x, size_t x_elems, const void* w, size_t w_bytes,
                          const uint32_t* ids, float* y, size_t y_elems,
-                         const q2k_matmul_id_params* p, uint32_t* bad_id_count,
-                         q2k_stream_t stream) {
+                         const q2k_matmul_id_params* p, uint32_t* bad_id_count, void* scratch,
+                         size_t scratch_bytes, q2k_stream_t stream) {
     return routed_call(x, x_elems, false, w, w_bytes, nullptr, 0, ids, y, nullptr, y_elems, p,
-                       bad_id_count, stream, "q2k_matmul_id launch");
+                       bad_id_count, scratch, scratch_bytes, stream, "q2k_matmul_id launch");
 }
 
 q2k_status q2k_matmul_id_slotted(const float* x, size_t x_elems, const void* w, size_t w_bytes,
                                  const uint32_t* ids, float* y, size_t y_elems,
                                  const q2k_matmul_id_params* p, uint32_t* bad_id_count,
-                                 q2k_stream_t stream) {
+                                 void* scratch, size_t scratch_bytes, q2k_stream_t stream) {
     return routed_call(x, x_elems, true, w, w_bytes, nullptr, 0, ids, y, nullptr, y_elems, p,
-                       bad_id_count, stream, "q2k_matmul_id_slotted launch");
+                       bad_id_count, scratch, scratch_bytes, stream, "q2k_matmul_id_slotted launch");
 }
 
 q2k_status q2k_matmul_id_pair(const float* x, size_t x_elems, const void* w_a, size_t w_a_bytes,
                               const void* w_b, size_t w_b_bytes, const uint32_t* ids, float* y_a,
                               float* y_b, size_t y_elems, const q2k_matmul_id_params* p,
-                              uint32_t* bad_id_count, q2k_stream_t stream) {
+                              uint32_t* bad_id_count, void* scratch, size_t scratch_bytes,
+                              q2k_stream_t stream) {
     if (y_b == nullptr || w_b == nullptr) {
         g_last_error[0] = '\0';
         return fail(Q2K_ERR_INVALID_ARGUMENT, "x, w, ids and y must be non-NULL");
     }
     return routed_call(x, x_elems, false, w_a, w_a_bytes, w_b, w_b_bytes, ids, y_a, y_b, y_elems, p,
-                       bad_id_count, stream, "q2k_matmul_id_pair launch");
+                       bad_id_count, scratch, scratch_bytes, stream, "q2k_matmul_id_pair launch");
 }
 
 q2k_status q2k_selftest_wait_timeout(uint32_t limit_us, q2k_stream_t stream) {

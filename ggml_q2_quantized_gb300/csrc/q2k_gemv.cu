@@ -349,7 +349,7 @@ __device__ __forceinline__ bool dot_rows(const uint8_t* my_col, size_t row_bytes
 __global__ void __launch_bounds__(256, 1)
 gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
                int N, int K, int rows_per_cta, int slices_pad, int groups, uint32_t flags,
-               GemvProblems pr, const uint8_t* __restrict__ xplanes) {
+               GemvProblems pr, const uint8_t* __restrict__ xplanes, uint32_t xplanes_stride) {
     const bool independent = (flags & kGemvIndependent) != 0;
     const bool const_weights = independent || (flags & kGemvConstWeights) != 0;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -383,10 +383,12 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
         }
         x += static_cast<size_t>(route / pr.top_k) * K;
         w += static_cast<size_t>(e) * pr.w_stride;
+        if (xplanes != nullptr) xplanes += static_cast<size_t>(route / pr.top_k) * xplanes_stride;
     } else {
         x += static_cast<size_t>(prob) * pr.x_stride;
         w += static_cast<size_t>(prob) * pr.w_stride;
         y += static_cast<size_t>(prob) * pr.y_stride;
+        if (xplanes != nullptr) xplanes += static_cast<size_t>(prob) * xplanes_stride;
     }
     const uint32_t delta = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(w) & 15u);
     const int n_pieces = (rows + kPieceRows - 1) / kPieceRows;
@@ -551,7 +553,7 @@ bool plan_m1(int N, int K, int sm_count, int threads, bool whole_batches, M1Plan
 
 cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, const M1Plan& p,
                       int device, uint32_t flags, const GemvProblems& pr, int n_problems,
-                      const uint8_t* xplanes, cudaStream_t stream) {
+                      const uint8_t* xplanes, uint32_t xplanes_stride, cudaStream_t stream) {
     static bool smem_set[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!smem_set[device]) {
@@ -572,7 +574,7 @@ cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, gemv_m1_kernel, x, w, y, N, K, p.rows_per_cta, p.slices_pad,
-                              p.groups, flags, pr, xplanes);
+                              p.groups, flags, pr, xplanes, xplanes_stride);
 }
 
 // ------------------------------------------------------------------ general m
@@ -693,7 +695,7 @@ cudaError_t launch_rows(const float* x, const uint8_t* w, float* y, int M, int N
 cudaError_t launch_gemv_problems(const float* x, const uint8_t* w, float* y, int M, int N, int K,
                                  int device, int sm_count, uint32_t flags,
                                  const GemvProblems& pr, int n_problems, cudaStream_t stream,
-                                 const uint8_t* xplanes) {
+                                 const uint8_t* xplanes, uint32_t xplanes_stride) {
     M1Plan plan;
     // Several problems in one grid overlap on the SMs like independent calls
     // do, so they take the same small CTAs of whole row batches, planned per
@@ -702,8 +704,8 @@ cudaError_t launch_gemv_problems(const float* x, const uint8_t* w, float* y, int
     const bool small_ctas = (flags & kGemvIndependent) != 0 || n_problems > 1;
     const int threads = small_ctas ? kM1ThreadsIndependent : kM1ThreadsDependent;
     if (M == 1 && plan_m1(N, K, sm_count, threads, small_ctas, &plan))
-        return launch_m1(x, w, y, N, K, plan, device, flags, pr, n_problems,
-                         n_problems == 1 ? xplanes : nullptr, stream);
+        return launch_m1(x, w, y, N, K, plan, device, flags, pr, n_problems, xplanes,
+                         xplanes_stride, stream);
     switch (M < 8 ? M : 8) {
         case 1: return launch_rows<1>(x, w, y, M, N, K, pr, n_problems, stream);
         case 2: return launch_rows<2>(x, w, y, M, N, K, pr, n_problems, stream);
@@ -720,7 +722,7 @@ cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N
                         int device, int sm_count, uint32_t flags, cudaStream_t stream,
                         const uint8_t* xplanes) {
     return launch_gemv_problems(x, w, y, M, N, K, device, sm_count, flags, GemvProblems{}, 1, stream,
-                                xplanes);
+                                xplanes, 0u);
 }
 
 bool gemv_shares_planes(int M, int K) { return M == 1 && K / 64 <= kM1MaxSlices; }
@@ -729,12 +731,18 @@ size_t gemv_planes_bytes(int K) {
     return static_cast<size_t>(K / 64) * kSlicePitch * 4 + static_cast<size_t>(K / 16) * 8;
 }
 
+size_t gemv_planes_stride(int K) { return (gemv_planes_bytes(K) + 255) & ~size_t(255); }
+
 // x (one row) -> the integer planes, run sums and run scales in the layout the
 // m = 1 kernel keeps in shared memory, for several of its calls to copy.  It
 // never lets the next grid start early, so every later grid sees it complete.
 __global__ void __launch_bounds__(128)
-prep_x_planes_kernel(const float* __restrict__ x, int K, uint8_t* __restrict__ dst) {
+prep_x_planes_kernel(const float* __restrict__ x, int K, uint8_t* __restrict__ dst,
+                     size_t stride) {
+    // x row blockIdx.y -> planes at dst + blockIdx.y stride
     const int n_runs = K >> 4;
+    x += static_cast<size_t>(blockIdx.y) * K;
+    dst += static_cast<size_t>(blockIdx.y) * stride;
     uint32_t* planes = reinterpret_cast<uint32_t*>(dst);
     float* run_sum = reinterpret_cast<float*>(planes + (n_runs >> 2) * kSlicePitch);
     float* run_inv = run_sum + n_runs;
@@ -742,9 +750,11 @@ prep_x_planes_kernel(const float* __restrict__ x, int K, uint8_t* __restrict__ d
               gridDim.x * blockDim.x);
 }
 
-cudaError_t launch_prep_x_planes(const float* x, int K, uint8_t* dst, cudaStream_t stream) {
+cudaError_t launch_prep_x_planes(const float* x, int K, uint8_t* dst, cudaStream_t stream,
+                                 int rows) {
     const int n_runs = K / 16;
-    prep_x_planes_kernel<<<(n_runs + 127) / 128, 128, 0, stream>>>(x, K, dst);
+    prep_x_planes_kernel<<<dim3((n_runs + 127) / 128, rows), 128, 0, stream>>>(
+        x, K, dst, gemv_planes_stride(K));
     return cudaGetLastError();
 }
 

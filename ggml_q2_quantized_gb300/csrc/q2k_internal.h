@@ -36,9 +36,14 @@ cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N
 // destination) that launch_gemv(..., xplanes) calls then copy instead of
 // converting x themselves (same values, so the same bits).  The prep grid
 // completes before any later grid of the stream starts.
+// Several x rows (rows of K floats, consecutive): planes of row r at dst + r
+// gemv_planes_stride(K), for launch_gemv_problems(..., xplanes, stride) whose
+// problems then find their x row's planes there.
 bool gemv_shares_planes(int M, int K);
 size_t gemv_planes_bytes(int K);
-cudaError_t launch_prep_x_planes(const float* x, int K, uint8_t* dst, cudaStream_t stream);
+size_t gemv_planes_stride(int K);
+cudaError_t launch_prep_x_planes(const float* x, int K, uint8_t* dst, cudaStream_t stream,
+                                 int rows = 1);
 
 // Several independent products in one launch of the GEMV kernels, each computed
 // exactly as its own launch_gemv call (same kernel, same arithmetic), problem p
@@ -65,7 +70,7 @@ struct GemvProblems {
 cudaError_t launch_gemv_problems(const float* x, const uint8_t* w, float* y, int M, int N, int K,
                                  int device, int sm_count, uint32_t flags,
                                  const GemvProblems& pr, int n_problems, cudaStream_t stream,
-                                 const uint8_t* xplanes = nullptr);
+                                 const uint8_t* xplanes = nullptr, uint32_t xplanes_stride = 0);
 
 // Self-test of the bounded wait: one CTA waits for about limit_ns on a barrier
 // nothing completes, then sets the GEMV error word's time-out bit.

@@ -183,10 +183,22 @@ enum {
  *   m   must be 1 (the pages' call passes 1: matrix-vector)
  * Each batch's y is bit-identical to q2k_matmul(m = 1) of that batch's x and W
  * alone (the same kernel and arithmetic run per batch): fp32, error within
- * 1e-5 * sum_k |x w|.  batches <= 65535. */
+ * 1e-5 * sum_k |x w|.  batches <= 65535.
+ *   scratch  NULL or q2k_x_planes_bytes(k, batches) bytes (see there). */
 q2k_status q2k_matmul_batched_mv(const float *x, size_t x_elems, const void *w, size_t w_bytes,
                                  float *y, size_t y_elems, uint32_t batches, uint32_t m,
-                                 uint32_t n, uint32_t k, q2k_stream_t stream);
+                                 uint32_t n, uint32_t k, void *scratch, size_t scratch_bytes,
+                                 q2k_stream_t stream);
+
+/* q2k_x_planes_bytes - device bytes of scratch the batched and routed calls
+ * use to convert x to its integer form once per x row (rows rows of k)
+ * instead of once per CTA: k/64 * 196 + k/2 bytes per row, rounded up to 256.
+ * 0 when k is not a positive multiple of 256 or above 16384 (no such
+ * sharing).  Those calls take such a scratch as their `scratch` argument:
+ * NULL (or smaller) keeps the conversion per CTA; results are the same bits
+ * either way.  It must be 16-byte aligned and overlap none of the call's
+ * buffers. */
+size_t q2k_x_planes_bytes(uint32_t k, uint32_t rows);
 
 /* q2k_matmul_id - the expert-routed product of a mixture-of-experts layer:
  * y[r, :] = W_{ids[r]} x[r / top_k, :] for every route r = t*top_k + slot.
@@ -207,11 +219,14 @@ q2k_status q2k_matmul_batched_mv(const float *x, size_t x_elems, const void *w, 
  * Every route runs the fp32 GEMV (error within 1e-5 * sum_k |x w|; the pages
  * allow 2e-4 absolute, 1e-2 for their reduced-precision path); each route's
  * row is bit-identical to q2k_matmul(m = 1) of its token and expert.
- * n_tokens * top_k <= 65535. */
+ * n_tokens * top_k <= 65535.
+ *   scratch  NULL or q2k_x_planes_bytes(k, n_tokens) bytes (n_tokens * top_k
+ *            for the slotted call): each x row converted once for all its
+ *            routes (see q2k_x_planes_bytes). */
 q2k_status q2k_matmul_id(const float *x, size_t x_elems, const void *w, size_t w_bytes,
                          const uint32_t *ids, float *y, size_t y_elems,
                          const q2k_matmul_id_params *params, uint32_t *bad_id_count,
-                         q2k_stream_t stream);
+                         void *scratch, size_t scratch_bytes, q2k_stream_t stream);
 
 /* ---- GGUF reader (host only: no device is needed or touched) -------------
  * The tensor directory of a GGUF file (versions 2 and 3) and its tensors'
@@ -266,7 +281,7 @@ q2k_status q2k_gguf_read_tensor(const q2k_gguf *file, const char *name, void *ds
 q2k_status q2k_matmul_id_slotted(const float *x, size_t x_elems, const void *w, size_t w_bytes,
                                  const uint32_t *ids, float *y, size_t y_elems,
                                  const q2k_matmul_id_params *params, uint32_t *bad_id_count,
-                                 q2k_stream_t stream);
+                                 void *scratch, size_t scratch_bytes, q2k_stream_t stream);
 
 /* q2k_matmul_id_pair - two routed products sharing x and the routing (the gate
  * and up projections of a MoE layer) in one launch: y_a = routed(W_a), y_b =
@@ -280,7 +295,8 @@ q2k_status q2k_matmul_id_slotted(const float *x, size_t x_elems, const void *w, 
 q2k_status q2k_matmul_id_pair(const float *x, size_t x_elems, const void *w_a, size_t w_a_bytes,
                               const void *w_b, size_t w_b_bytes, const uint32_t *ids, float *y_a,
                               float *y_b, size_t y_elems, const q2k_matmul_id_params *params,
-                              uint32_t *bad_id_count, q2k_stream_t stream);
+                              uint32_t *bad_id_count, void *scratch, size_t scratch_bytes,
+                              q2k_stream_t stream);
 
 /* q2k_matmul_workspace_bytes - device bytes of workspace q2k_matmul_ex can use
  * for this geometry and path (0: the path takes none).  The tensor-core path

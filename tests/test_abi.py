@@ -172,7 +172,7 @@ def _bmv(lib, batches=3, m=1, n=8, k=256, xe=None, wb=None, ye=None, x=0x10000, 
     xe = batches * k if xe is None else xe
     wb = batches * n * (k // 256) * 84 if wb is None else wb
     ye = batches * n if ye is None else ye
-    return lib.q2k_matmul_batched_mv(x, xe, w, wb, y, ye, batches, m, n, k, None)
+    return lib.q2k_matmul_batched_mv(x, xe, w, wb, y, ye, batches, m, n, k, None, 0, None)
 
 
 @pytest.mark.parametrize("kw,fragment", [
@@ -199,7 +199,7 @@ def _mid(lib, n_tokens=2, top_k=2, n=8, k=256, n_experts=3, stride=None, xe=None
     xe = n_tokens * k if xe is None else xe
     wb = (n_experts - 1) * stride + n * (k // 256) * 84 if wb is None else wb
     ye = n_tokens * top_k * n if ye is None else ye
-    return lib.q2k_matmul_id(x, xe, w, wb, ids, y, ye, ctypes.byref(p), None, None)
+    return lib.q2k_matmul_id(x, xe, w, wb, ids, y, ye, ctypes.byref(p), None, None, 0, None)
 
 
 @pytest.mark.parametrize("kw,fragment", [
@@ -228,22 +228,23 @@ def test_matmul_id_slotted_and_pair_reject(lib):
     wb = experts * n * 84
     # slotted: x holds one row per route (n_tokens*top_k*k), not per token
     assert lib.q2k_matmul_id_slotted(0x10000, n_tokens * k, 0x100000, wb, 0x3000000, 0x1000000,
-                                     n_tokens * top_k * n, ctypes.byref(p), None, None) == INVALID
+                                     n_tokens * top_k * n, ctypes.byref(p), None, None, 0,
+                                     None) == INVALID
     assert "n_tokens*top_k*k" in lib.q2k_last_error().decode()
     args = (0x10000, n_tokens * k, 0x100000, wb)
     # pair: missing second weight set, short second weight set, aliasing outputs
     assert lib.q2k_matmul_id_pair(*args, None, wb, 0x3000000, 0x1000000, 0x2000000,
-                                  n_tokens * top_k * n, ctypes.byref(p), None, None) == INVALID
+                                  n_tokens * top_k * n, ctypes.byref(p), None, None, 0, None) == INVALID
     assert lib.q2k_matmul_id_pair(*args, 0x200000, wb - 4, 0x3000000, 0x1000000, 0x2000000,
-                                  n_tokens * top_k * n, ctypes.byref(p), None, None) == INVALID
+                                  n_tokens * top_k * n, ctypes.byref(p), None, None, 0, None) == INVALID
     assert "w has" in lib.q2k_last_error().decode()
     assert lib.q2k_matmul_id_pair(*args, 0x200000, wb, 0x3000000, 0x1000000, 0x1000000 + 32,
-                                  n_tokens * top_k * n, ctypes.byref(p), None, None) == INVALID
+                                  n_tokens * top_k * n, ctypes.byref(p), None, None, 0, None) == INVALID
     assert "alias" in lib.q2k_last_error().decode()
     big = q2k.MatmulIdParams(16384, 2, n, k, experts, 10, n * 84)
     assert lib.q2k_matmul_id_pair(0x10000, 16384 * k, 0x100000, wb, 0x200000, wb, 0x3000000,
                                   0x1000000, 0x8000000, 32768 * n, ctypes.byref(big), None,
-                                  None) == INVALID
+                                  None, 0, None) == INVALID
     assert "32767" in lib.q2k_last_error().decode()
 
 
@@ -269,3 +270,17 @@ def test_matmul_ex_batch_checks_every_call_first(lib):
     assert lib.q2k_matmul_ex_batch(calls, 2, 0x3000008, 1024, None) == INVALID
     assert "aligned" in lib.q2k_last_error().decode()
     assert lib.q2k_matmul_ex_batch(None, 0, None, 0, None) == 0   # nothing to do
+
+
+def test_x_planes_scratch_size_and_checks(lib):
+    # k/64 slices x 49 words + k/16 x 8 bytes per row, rounded up to 256
+    assert lib.q2k_x_planes_bytes(4096, 3) == 3 * ((64 * 49 * 4 + 256 * 8 + 255) // 256 * 256)
+    assert lib.q2k_x_planes_bytes(16640, 1) == 0     # above the m = 1 kernel's k
+    assert lib.q2k_x_planes_bytes(255, 1) == 0
+    need = lib.q2k_x_planes_bytes(256, 3)
+    x, w, y = 0x10000, 0x100000, 0x1000000
+    args = (x, 3 * 256, w, 3 * 8 * 84, y, 3 * 8, 3, 1, 8, 256)
+    assert lib.q2k_matmul_batched_mv(*args, 0x2000000, need - 16, None) == INVALID
+    assert "scratch" in lib.q2k_last_error().decode()
+    assert lib.q2k_matmul_batched_mv(*args, 0x2000008, need, None) == INVALID
+    assert lib.q2k_matmul_batched_mv(*args, x, need, None) == INVALID    # over x

@@ -230,3 +230,24 @@ def test_matmul_id_pair_counts_bad_ids_per_product():
     torch.cuda.synchronize()
     assert int(count.item()) == 2
     assert (ya[1] == 0).all() and (yb[1] == 0).all()
+
+
+def test_x_planes_scratch_gives_the_same_bits():
+    """Batched and routed calls with x converted once per row (the default
+    scratch) and per CTA (scratch=None) give identical results."""
+    rng = np.random.default_rng(9)
+    batches, n, k = 4, 700, 4096
+    w = wl.random_blocks(rng, batches * n * (k // 256)).reshape(-1)
+    x = wl.random_activations(rng, batches, k)
+    wd, xd = dev(w), dev(x)
+    a = q2k.matmul_batched_mv(xd, wd, n, scratch="auto")
+    b = q2k.matmul_batched_mv(xd, wd, n)
+    tokens, top_k, experts, ne = 3, 4, 6, 512
+    we = wl.random_blocks(rng, experts * ne * (k // 256)).reshape(-1)
+    ids = rng.integers(0, experts, tokens * top_k).astype(np.uint32)
+    xt = dev(wl.random_activations(rng, tokens, k))
+    wed, idd = dev(we), dev(ids.view(np.int32))
+    c = q2k.matmul_id(xt, wed, idd, ne, experts, top_k)
+    d = q2k.matmul_id(xt, wed, idd, ne, experts, top_k, scratch=None)
+    torch.cuda.synchronize()
+    assert bits_equal(a, b) and bits_equal(c, d)
