@@ -366,7 +366,8 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     // routes uses w2 and y2); one problem: all strides 0.
     const int prob = blockIdx.y;
     if (pr.ids != nullptr) {
-        pdl_wait_prerequisites();  // the ids (and x) may come from the grid before this one
+        // the ids (and x) may come from the grid before this one
+        if (!independent) pdl_wait_prerequisites();
         const bool second = pr.second_from > 0 && prob >= pr.second_from;
         const int route = second ? prob - pr.second_from : prob;
         if (second) {
@@ -412,10 +413,12 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     const uint8_t* gsrc = w + static_cast<size_t>(r0) * row_bytes;
     const size_t chunk = static_cast<size_t>(rows) * row_bytes;
 
-    // Let the next grid in the stream start now: its prologue (barrier set-up,
-    // weight prefetch or copy) then overlaps this grid; it still waits for this
-    // grid to complete before it reads x or writes y.
-    pdl_allow_dependents();
+    // Let the next grid in the stream start: its prologue (barrier set-up,
+    // weight prefetch or copy) then overlaps this grid.  An independent call
+    // lets it start at once; a dependent one once its own dependency wait has
+    // returned (below), so that whatever starts after it finds the grids
+    // before this one complete.
+    if (independent) pdl_allow_dependents();
     const int nwarps = nthreads >> 5;
     const bool issuer = (tid & 31) == 0;
     if (tid == 0) {
@@ -449,7 +452,10 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
                              static_cast<uint32_t>(left < (size_t(1) << 20) ? left : (size_t(1) << 20)));
         }
     }
-    if (!independent) pdl_wait_prerequisites();
+    if (!independent) {
+        pdl_wait_prerequisites();
+        pdl_allow_dependents();
+    }
     __syncthreads();
     if (issuer && !const_weights)
         issue_weight_copies(smem_w, gsrc, bars, rows, row_bytes, delta, tid >> 5, nwarps);
