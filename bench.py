@@ -351,6 +351,39 @@ def bench_routed(torch, q2k, rw, steps, warmup, device):
             "unique_experts_per_launch": float(uniq), "path": "gemv per route (one launch)"}
 
 
+def bench_routed_tc(torch, q2k, rw, steps, warmup, device, peaks):
+    """mm_id on the tensor path (routes grouped per expert, bf16 MMAs): one
+    launch sequence (routing, x gather, GEMM) per step, fresh ids each step."""
+    rng = np.random.default_rng(rw.seed)
+    pool = torch.from_numpy(np.concatenate([wl.random_blocks(rng, rw.n * (rw.k // wl.QK_K))
+                                            for _ in range(rw.n_experts)])).to(device)
+    x = torch.from_numpy(wl.random_activations(rng, rw.n_tokens, rw.k)).to(device)
+    launches = 4
+    ids = [torch.from_numpy(wl.make_routed_ids(rw, i).view(np.int32)).to(device)
+           for i in range(launches)]
+    routes = rw.n_tokens * rw.top_k
+    ys = torch.empty((launches, routes, rw.n), dtype=torch.float32, device=device)
+    ws = torch.empty(q2k.matmul_id_workspace_bytes(rw.n_tokens, rw.top_k, rw.n, rw.k,
+                                                   rw.n_experts, path="tensor"),
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def step():
+        for i in range(launches):
+            q2k.matmul_id_ex(x, pool, ids[i], rw.n, rw.n_experts, rw.top_k, path="tensor",
+                             out=ys[i], check=False, workspace=ws)
+
+    g = capture(torch, stream, step)
+    ms = time_graph(torch, g, stream, steps, warmup)
+    us = ms * 1e3 / launches
+    tflops = 2.0 * routes * rw.n * rw.k / (us * 1e-6) / 1e12
+    return {"us_per_launch": us, "TFLOPs": tflops,
+            "frac_bf16_measured": tflops / peaks["bf16_tflops"],
+            "weight_GBps": rw.n_experts * rw.expert_bytes / (us * 1e-6) / 1e9,
+            "n_tokens": rw.n_tokens, "top_k": rw.top_k, "n": rw.n, "k": rw.k,
+            "n_experts": rw.n_experts, "path": "tensor (routes tiled per expert)"}
+
+
 def bench_gather(torch, q2k, w: wl.Workload, steps, warmup, device):
     inp = wl.make_inputs(w)
     table = torch.from_numpy(inp.table).to(device)
@@ -580,6 +613,8 @@ def run_ours(args):
         r = bench_routed(torch, q2k, wl.MOE_DECODE, max(3, steps // 4), 3, device)
         r["frac_hbm_measured"] = r["weight_GBps"] / peaks["hbm_gbs"]
         sec[wl.MOE_DECODE.name] = r
+        sec[wl.MOE_PREFILL.name] = bench_routed_tc(torch, q2k, wl.MOE_PREFILL, max(3, steps // 4),
+                                                   3, device, peaks)
         line["secondary"] = sec
         assert q2k.device_error() == 0
 

@@ -29,6 +29,7 @@ GGML_TYPE_Q2_K = 10
 PATH_AUTO, PATH_GEMV, PATH_TENSOR = 0, 1, 2
 FLAG_CONST_WEIGHTS = 1
 FLAG_INDEPENDENT = 2
+ID_SLOTTED = 1
 _PATHS = {"auto": PATH_AUTO, "gemv": PATH_GEMV, "tensor": PATH_TENSOR,
           PATH_AUTO: PATH_AUTO, PATH_GEMV: PATH_GEMV, PATH_TENSOR: PATH_TENSOR}
 
@@ -125,6 +126,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q2k_matmul_id_slotted.argtypes = lib.q2k_matmul_id.argtypes
         lib.q2k_matmul_id_pair.argtypes = [vp, sz, vp, sz, vp, sz, vp, vp, vp, sz,
                                            ctypes.POINTER(MatmulIdParams), vp, vp, sz, vp]
+        lib.q2k_matmul_id_ex.argtypes = [ctypes.c_int, ctypes.c_uint32, vp, sz, vp, sz, vp, vp, sz,
+                                         ctypes.POINTER(MatmulIdParams), vp, vp, sz, vp]
+        lib.q2k_matmul_id_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_uint32,
+                                                      ctypes.POINTER(MatmulIdParams)]
+        lib.q2k_matmul_id_workspace_bytes.restype = sz
         lib.q2k_x_planes_bytes.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
         lib.q2k_x_planes_bytes.restype = sz
         lib.q2k_gguf_open.argtypes = [ctypes.c_char_p, ctypes.POINTER(vp)]
@@ -533,6 +539,62 @@ def matmul_id(x, w, ids, n: int, n_experts: int, top_k: int, expert_stride: int 
     if n_bad:
         raise InvalidArgument(1, f"{n_bad} expert id(s) >= n_experts {n_experts}")
     return out
+
+
+def matmul_id_ex(x, w, ids, n: int, n_experts: int, top_k: int = 1, path="auto",
+                 slotted: bool = False, expert_stride: int | None = None, out=None,
+                 check: bool = True, workspace=None):
+    """``matmul_id`` (or, with ``slotted``, ``matmul_id_slotted``; then ``x`` is
+    ``[n_tokens, top_k, k]`` and ``top_k`` is taken from it) on a chosen path:
+    ``"gemv"`` (fp32, as ``matmul_id``), ``"tensor"`` (routes grouped per
+    expert and multiplied on the bf16 tensor cores) or ``"auto"`` (tensor above
+    32 tokens).  ``workspace``: a CUDA uint8 tensor of at least
+    ``matmul_id_workspace_bytes`` bytes, allocated here when None."""
+    torch = _torch()
+    _require_cuda(x, "x", torch.float32)
+    _require_cuda(w, "w", torch.uint8)
+    _require_cuda(ids, "ids", ids.dtype)
+    if ids.element_size() != 4 or ids.is_floating_point():
+        raise TypeError("ids must be a 32-bit integer tensor (read as uint32)")
+    if slotted:
+        n_tokens, top_k, k = x.shape
+        shape = (n_tokens, top_k, n)
+    else:
+        n_tokens, k = x.shape
+        shape = (n_tokens * top_k, n)
+    if expert_stride is None:
+        expert_stride = n * (k // QK_K) * BLOCK_BYTES
+    if out is None:
+        out = torch.empty(shape, dtype=torch.float32, device=x.device)
+    _require_cuda(out, "out", torch.float32)
+    bad = torch.zeros(1, dtype=torch.int32, device=x.device)
+    p = MatmulIdParams(n_tokens, top_k, n, k, n_experts, GGML_TYPE_Q2_K, expert_stride)
+    pcode = _PATHS[path]
+    flags = ID_SLOTTED if slotted else 0
+    lib = load()
+    if workspace is None:
+        nbytes = lib.q2k_matmul_id_workspace_bytes(pcode, flags, ctypes.byref(p))
+        if nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+    wp = workspace.data_ptr() if workspace is not None else None
+    wb = workspace.numel() if workspace is not None else 0
+    with _on_device(x):
+        _check(lib, lib.q2k_matmul_id_ex(pcode, flags, x.data_ptr(), x.numel(), w.data_ptr(),
+                                         w.numel(), ids.data_ptr(), out.data_ptr(), out.numel(),
+                                         ctypes.byref(p), bad.data_ptr(), wp, wb,
+                                         _stream_handle(x)))
+    return _routed_finish(bad, check, (out,), n_experts)
+
+
+def matmul_id_workspace_bytes(n_tokens: int, top_k: int, n: int, k: int, n_experts: int,
+                              path="auto", slotted: bool = False,
+                              expert_stride: int | None = None) -> int:
+    """Bytes of workspace ``matmul_id_ex`` takes on ``path`` (0: none or invalid)."""
+    if expert_stride is None:
+        expert_stride = n * (k // QK_K) * BLOCK_BYTES
+    p = MatmulIdParams(n_tokens, top_k, n, k, n_experts, GGML_TYPE_Q2_K, expert_stride)
+    return int(load().q2k_matmul_id_workspace_bytes(_PATHS[path], ID_SLOTTED if slotted else 0,
+                                                    ctypes.byref(p)))
 
 
 class GgufFile:

@@ -507,10 +507,18 @@ namespace {
 // (or per route when `slotted`); wb / yb are the second weight set and output
 // of a pair (NULL otherwise).  Every malformed argument is rejected before any
 // device work.
+// The pages' routed product takes its matrix-matrix (reduced-precision) path
+// above 32 tokens; at most 32 it runs a GEMV per route.
+q2k_path routed_auto_path(const q2k_matmul_id_params* p) {
+    return p->n_tokens > 32 && p->n_experts <= uint32_t(q2k::kRoutedMaxExperts) ? Q2K_PATH_TENSOR
+                                                                               : Q2K_PATH_GEMV;
+}
+
 q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void* wa, size_t wa_bytes,
                        const void* wb, size_t wb_bytes, const uint32_t* ids, float* ya, float* yb,
                        size_t y_elems, const q2k_matmul_id_params* p, uint32_t* bad_id_count,
-                       void* scratch, size_t scratch_bytes, q2k_stream_t stream, const char* what) {
+                       void* scratch, size_t scratch_bytes, q2k_stream_t stream, const char* what,
+                       q2k_path path = Q2K_PATH_GEMV) {
     g_last_error[0] = '\0';
     const bool pair = yb != nullptr || wb != nullptr;
     if (p == nullptr) return fail(Q2K_ERR_INVALID_ARGUMENT, "params is NULL");
@@ -569,6 +577,35 @@ q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void*
     }
     // x rows: tokens, or routes when slotted
     const size_t x_rows = slotted ? routes : size_t(p->n_tokens);
+    if (path == Q2K_PATH_AUTO) path = routed_auto_path(p);
+    if (path == Q2K_PATH_TENSOR) {
+        if (pair) return fail(Q2K_ERR_INVALID_ARGUMENT, "the paired product has no tensor-core path");
+        if (p->n_experts > uint32_t(q2k::kRoutedMaxExperts))
+            return fail(Q2K_ERR_INVALID_ARGUMENT, "tensor-core path supports n_experts <= %d",
+                        q2k::kRoutedMaxExperts);
+        const size_t need = q2k::gemm_tc_routed_workspace_bytes(int(routes), int(p->n_experts), int(p->k));
+        if (scratch == nullptr || scratch_bytes < need)
+            return fail(Q2K_ERR_INVALID_ARGUMENT, "workspace has %zu bytes, needs %zu",
+                        scratch == nullptr ? size_t(0) : scratch_bytes, need);
+        if (!aligned(scratch, 16)) return fail(Q2K_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+        if (overlaps(scratch, need, x, x_bytes) || overlaps(scratch, need, wa, wa_bytes) ||
+            overlaps(scratch, need, ya, y_bytes) || overlaps(scratch, need, ids, id_bytes) ||
+            (bad_id_count != nullptr && overlaps(scratch, need, bad_id_count, 4)))
+            return fail(Q2K_ERR_INVALID_ARGUMENT, "workspace must not alias x, w, ids or y");
+        DeviceInfo dev;
+        q2k_status st = current_device(&dev);
+        if (st != Q2K_OK) return st;
+        const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        cudaError_t e = cudaSuccess;
+        if (bad_id_count != nullptr) e = cudaMemsetAsync(bad_id_count, 0, 4, s);
+        if (e == cudaSuccess)
+            e = q2k::launch_gemm_tc_routed(x, static_cast<const uint8_t*>(wa),
+                                           static_cast<long long>(p->expert_stride), ids, ya,
+                                           int(routes), slotted ? 1 : int(p->top_k), int(p->n_experts),
+                                           int(p->n), int(p->k), bad_id_count, dev.device,
+                                           dev.sm_count, scratch, s);
+        return e == cudaSuccess ? Q2K_OK : cuda_fail(e, what);
+    }
     uint8_t* planes = nullptr;
     q2k_status st = check_planes_scratch(scratch, scratch_bytes, p->k, x_rows, x, x_bytes, wa,
                                          wa_bytes, ya, y_bytes, &planes);
@@ -629,6 +666,39 @@ q2k_status q2k_matmul_id_slotted(const float* x, size_t x_elems, const void* w, 
                                  void* scratch, size_t scratch_bytes, q2k_stream_t stream) {
     return routed_call(x, x_elems, true, w, w_bytes, nullptr, 0, ids, y, nullptr, y_elems, p,
                        bad_id_count, scratch, scratch_bytes, stream, "q2k_matmul_id_slotted launch");
+}
+
+size_t q2k_matmul_id_workspace_bytes(q2k_path path, uint32_t flags,
+                                     const q2k_matmul_id_params* p) {
+    if (p == nullptr || p->n_tokens == 0 || p->top_k == 0 || p->n == 0 || p->k == 0 ||
+        p->n_experts == 0 || p->k % Q2K_QK_K != 0 || p->k > INT_MAX || (flags & ~1u) != 0)
+        return 0;
+    const size_t routes = size_t(p->n_tokens) * p->top_k;
+    if (routes > 65535u) return 0;
+    if (path == Q2K_PATH_AUTO) path = routed_auto_path(p);
+    if (path == Q2K_PATH_TENSOR) {
+        if (p->n_experts > uint32_t(q2k::kRoutedMaxExperts)) return 0;
+        return q2k::gemm_tc_routed_workspace_bytes(int(routes), int(p->n_experts), int(p->k));
+    }
+    if (path != Q2K_PATH_GEMV) return 0;
+    return q2k_x_planes_bytes(p->k, uint32_t((flags & Q2K_ID_SLOTTED) ? routes : p->n_tokens));
+}
+
+q2k_status q2k_matmul_id_ex(q2k_path path, uint32_t flags, const float* x, size_t x_elems,
+                            const void* w, size_t w_bytes, const uint32_t* ids, float* y,
+                            size_t y_elems, const q2k_matmul_id_params* p, uint32_t* bad_id_count,
+                            void* workspace, size_t workspace_bytes, q2k_stream_t stream) {
+    if (path != Q2K_PATH_AUTO && path != Q2K_PATH_GEMV && path != Q2K_PATH_TENSOR) {
+        g_last_error[0] = '\0';
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "unknown path %d", static_cast<int>(path));
+    }
+    if ((flags & ~uint32_t(Q2K_ID_SLOTTED)) != 0) {
+        g_last_error[0] = '\0';
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "unknown flag bits 0x%x", flags);
+    }
+    return routed_call(x, x_elems, (flags & Q2K_ID_SLOTTED) != 0, w, w_bytes, nullptr, 0, ids, y,
+                       nullptr, y_elems, p, bad_id_count, workspace, workspace_bytes, stream,
+                       "q2k_matmul_id_ex launch", path);
 }
 
 q2k_status q2k_matmul_id_pair(const float* x, size_t x_elems, const void* w_a, size_t w_a_bytes,

@@ -26,6 +26,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstring>
 #include <mutex>
 
@@ -660,6 +661,17 @@ struct WtCfg {
     static_assert(!kSmall || kOffRaw >= kRows * kXRows * 4, "reduction slice");
 };
 
+// Routed mode of the weights-as-A kernel: x tile t's expert and routed rows
+// (tile_info[t] = {expert or -1, rows}), each x row's route (row_route[v], -1
+// for padding rows), the bytes between experts' weights and, for the TMA
+// view of the whole weight pool, the rows between them.
+struct WtRouted {
+    const int2* tile_info = nullptr;
+    const int* row_route = nullptr;
+    long long expert_stride = 0;
+    int expert_rows = 0;
+};
+
 // ---- thread-block cluster: barrier and distributed shared memory -----------
 
 // Every thread of every CTA in the cluster arrives (release) and waits
@@ -784,7 +796,7 @@ template <int kXRows, bool kTmaW>
 __global__ void __launch_bounds__(WtCfg<kXRows, kTmaW>::kThreads, 1)
 gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                const uint8_t* __restrict__ w, float* __restrict__ y, float* __restrict__ partial,
-               unsigned int* __restrict__ tile_count, int M, int N, int K,
+               unsigned int* __restrict__ tile_count, int M, int N, int K, WtRouted rt,
                const __grid_constant__ CUtensorMap tmap_w) {
     using C = WtCfg<kXRows, kTmaW>;
     extern __shared__ uint8_t smem_dyn[];
@@ -795,7 +807,19 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
     const int lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * C::kRows;
     const int m0 = blockIdx.y * kXRows;
-    const int nx = min(kXRows, (M - m0 + 15) & ~15);  // MMA N: this tile's x rows, padded to 16
+    // Routed mode: x tile blockIdx.y holds rows of one expert (tile_info: the
+    // expert, the tile's routed rows; -1: none, and the CTA leaves before any
+    // set-up); its weights are that expert's, its outputs go to their routes.
+    int tma_row0 = 0;  // the expert's first row in the TMA view of the weight pool
+    int tile_rows = M - m0;
+    if (rt.tile_info != nullptr) {
+        const int2 ti = __ldg(rt.tile_info + blockIdx.y);
+        if (ti.x < 0) return;
+        w += static_cast<size_t>(ti.x) * rt.expert_stride;
+        tma_row0 = ti.x * rt.expert_rows;
+        tile_rows = ti.y;
+    }
+    const int nx = min(kXRows, (tile_rows + 15) & ~15);  // MMA N: the tile's x rows, padded to 16
     const int blocks_per_row = K / kQK;
     const size_t row_bytes = static_cast<size_t>(blocks_per_row) * kBlockBytes;
     // K split (gridDim.z parts): this CTA's blocks [kb0, kb0 + n_blocks) of each
@@ -1043,7 +1067,10 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
                         const int m = m0 + c0 + q;
-                        if (m < M) out[static_cast<size_t>(m) * N + n] = __uint_as_float(v[q]);
+                        if (m >= M || c0 + q >= tile_rows) continue;
+                        // routed: x row m is route row_route[m] (-1: padding)
+                        const int r = rt.row_route != nullptr ? __ldg(rt.row_route + m) : m;
+                        if (r >= 0) out[static_cast<size_t>(r) * N + n] = __uint_as_float(v[q]);
                     }
                 }
             }
@@ -1185,8 +1212,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                 mbar_arrive_expect_tx(bar_raw + 8 * buf, C::kRawBytes);
                 // x: the 16-byte boundary at or below row block kb0 + b
                 // (84 (kb0 + b) - 4 ((kb0 + b) % 4))
-                tma_load_2d(raw0 + buf * C::kRawBytes, &tmap_w, (kBlockBytes * (kb0 + b)) & ~15, n0,
-                            bar_raw + 8 * buf);
+                tma_load_2d(raw0 + buf * C::kRawBytes, &tmap_w, (kBlockBytes * (kb0 + b)) & ~15,
+                            tma_row0 + n0, bar_raw + 8 * buf);
             }
             if (*abort_flag) {
                 // a copy may still be in flight: give it a bounded 50 us to land
@@ -1385,7 +1412,8 @@ bool make_weight_map(CUtensorMap* map, const uint8_t* w, int N, int K, int rows)
 template <int kXRows, bool kTmaW>
 cudaError_t launch_wt_kernel(const uint8_t* xa, const float* xf, const uint8_t* w, float* y,
                              float* partial, unsigned int* tile_count, int splits, int M, int N,
-                             int K, int device, const CUtensorMap& map, cudaStream_t stream) {
+                             int K, int device, const CUtensorMap& map, cudaStream_t stream,
+                             const WtRouted& rt = WtRouted{}) {
     using C = WtCfg<kXRows, kTmaW>;
     static bool attr_done[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
@@ -1415,7 +1443,7 @@ cudaError_t launch_wt_kernel(const uint8_t* xa, const float* xf, const uint8_t* 
         cfg.numAttrs = 2;
     }
     return cudaLaunchKernelEx(&cfg, gemm_wt_kernel<kXRows, kTmaW>, xa, xf, w, y, partial,
-                              tile_count, M, N, K, map);
+                              tile_count, M, N, K, rt, map);
 }
 
 template <int kXRows>
@@ -1548,6 +1576,179 @@ cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, in
         return launch_wt<256>(xa, nullptr, w, y, partial, tile_count, splits, M, N, K, device,
                               stream);
     return launch_wt<128>(xa, nullptr, w, y, partial, tile_count, splits, M, N, K, device, stream);
+}
+
+// ---- routed products on tensor cores (mul_mat_id with many routes) -----------
+//
+// Route r (token r / top_k, or slot r) multiplies its x row by expert ids[r]'s
+// weights.  The routes are grouped by expert into 128-row x tiles: expert e's
+// routes fill ceil(count_e / 128) tiles, its last one padded; the weights-as-A
+// kernel then runs one CTA per (weight tile, x tile) with the x tile's expert's
+// weights and writes each row to its route.  A route's result does not depend
+// on where in its tile it lands (each MMA column is a separate dot product),
+// so the order the routes are placed in does not matter.
+
+// Tiles a routed product can need: sum_e ceil(c_e / 128) <= routes / 128 + the
+// number of experts that have a route.
+int routed_tiles_max(int routes, int n_experts) {
+    return (routes + 127) / 128 + std::min(routes, n_experts);
+}
+
+// One CTA: count the routes per expert, scan to tile starts, and write each
+// x tile's {expert, rows} (-1: unused), each x row's route (-1: padding) and,
+// for a route whose id is out of range, a zero row of y and a count.
+__global__ void __launch_bounds__(1024)
+route_tiles_kernel(const uint32_t* __restrict__ ids, int routes, int n_experts, int tiles_max,
+                   int2* __restrict__ tile_info, int* __restrict__ row_route, float* __restrict__ y,
+                   int N, unsigned int* __restrict__ bad_ids) {
+    extern __shared__ int route_smem[];
+    int* cnt = route_smem;              // per expert: routes, then the placement cursor
+    int* start = route_smem + n_experts;  // per expert: first tile
+    __shared__ int warp_sum[32];
+    __shared__ int total_tiles;
+    const int tid = threadIdx.x;
+    const int nt = blockDim.x;
+    for (int e = tid; e < n_experts; e += nt) cnt[e] = 0;
+    __syncthreads();
+    for (int r = tid; r < routes; r += nt) {
+        const uint32_t e = ids[r];
+        if (e < static_cast<uint32_t>(n_experts)) {
+            atomicAdd(&cnt[e], 1);
+        } else {
+            if (bad_ids != nullptr) atomicAdd(bad_ids, 1u);
+            float* row = y + static_cast<size_t>(r) * N;
+            for (int n = 0; n < N; ++n) row[n] = 0.0f;
+        }
+    }
+    __syncthreads();
+    // exclusive scan of the tile counts: each thread a run of experts
+    const int per = (n_experts + nt - 1) / nt;
+    const int e0 = min(n_experts, tid * per), e1 = min(n_experts, e0 + per);
+    int mine = 0;
+    for (int e = e0; e < e1; ++e) mine += (cnt[e] + 127) >> 7;
+    const int lane = tid & 31, warp = tid >> 5;
+    int incl = mine;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = nt >> 5;
+        int v = lane < nw ? warp_sum[lane] : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int u = __shfl_up_sync(0xFFFFFFFFu, v, d);
+            if (lane >= d) v += u;
+        }
+        if (lane < nw) warp_sum[lane] = v;  // inclusive over warps
+        if (lane == nw - 1) total_tiles = v;
+    }
+    __syncthreads();
+    int t = incl - mine + (warp > 0 ? warp_sum[warp - 1] : 0);
+    for (int e = e0; e < e1; ++e) {
+        start[e] = t;
+        const int c = cnt[e];
+        for (int j = 0; j < (c + 127) >> 7; ++j)
+            tile_info[t + j] = make_int2(e, min(128, c - 128 * j));
+        // the last tile's padding rows
+        const int used = (c + 127) & ~127;
+        for (int v = c; v < used; ++v) row_route[128 * t + v] = -1;
+        t += (c + 127) >> 7;
+    }
+    for (int u = total_tiles + tid; u < tiles_max; u += nt) tile_info[u] = make_int2(-1, 0);
+    __syncthreads();
+    for (int e = tid; e < n_experts; e += nt) cnt[e] = 0;
+    __syncthreads();
+    for (int r = tid; r < routes; r += nt) {
+        const uint32_t e = ids[r];
+        if (e < static_cast<uint32_t>(n_experts))
+            row_route[128 * start[e] + atomicAdd(&cnt[e], 1)] = r;
+    }
+}
+
+// x rows by route into the bf16 tile image of the routed rows (x tile t =
+// rows 128 t .. 128 t + 127): row v holds x row row_route[v] / x_div, zeros
+// for padding; tiles no expert uses are left alone.  As x_to_bf16_tiles_kernel
+// it lets the GEMM after it start early.
+__global__ void __launch_bounds__(256)
+gather_x_tiles_kernel(const float* __restrict__ x, uint8_t* __restrict__ xa,
+                      const int2* __restrict__ tile_info, const int* __restrict__ row_route, int x_div,
+                      int K, size_t n_chunks) {
+    pdl_allow_dependents();
+    const int chunks_per_row = K >> 3;
+    const int stages = K / kKS;
+    for (size_t id = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; id < n_chunks;
+         id += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int v = static_cast<int>(id / chunks_per_row);
+        const int j = static_cast<int>(id - static_cast<size_t>(v) * chunks_per_row);
+        if (tile_info[v >> 7].x < 0) continue;
+        const int r = row_route[v];
+        uint4 packed = make_uint4(0u, 0u, 0u, 0u);
+        if (r >= 0) {
+            const float4* src =
+                reinterpret_cast<const float4*>(x + static_cast<size_t>(r / x_div) * K + 8 * j);
+            const float4 a = __ldg(src), b = __ldg(src + 1);
+            packed = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                                pack_bf16x2(b.z, b.w));
+        }
+        const size_t tile = static_cast<size_t>(v / kXSuperRows) * stages + (j >> 3);
+        *reinterpret_cast<uint4*>(xa + tile * kXSuperBytes + sw128_offset(v % kXSuperRows, j & 7)) =
+            packed;
+    }
+}
+
+// Workspace of a routed product: tile table, row routes, then the x image.
+static size_t routed_info_bytes(int tiles) { return (static_cast<size_t>(tiles) * 8 + 255) & ~size_t(255); }
+static size_t routed_rows_bytes(int tiles) { return static_cast<size_t>(tiles) * 128 * 4; }
+
+size_t gemm_tc_routed_workspace_bytes(int routes, int n_experts, int K) {
+    const int tiles = routed_tiles_max(routes, n_experts);
+    return routed_info_bytes(tiles) + routed_rows_bytes(tiles) + image_bytes(tiles * 128, K);
+}
+
+cudaError_t launch_gemm_tc_routed(const float* x, const uint8_t* w, long long expert_stride,
+                                  const uint32_t* ids, float* y, int routes, int x_div,
+                                  int n_experts, int N, int K, unsigned int* bad_ids, int device,
+                                  int sm_count, void* workspace, cudaStream_t stream) {
+    if (n_experts > kRoutedMaxExperts) return cudaErrorInvalidValue;
+    const int tiles = routed_tiles_max(routes, n_experts);
+    const int M = tiles * 128;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    int2* tile_info = reinterpret_cast<int2*>(base);
+    int* row_route = reinterpret_cast<int*>(base + routed_info_bytes(tiles));
+    uint8_t* xa = base + routed_info_bytes(tiles) + routed_rows_bytes(tiles);
+    route_tiles_kernel<<<1, 1024, 2 * n_experts * sizeof(int), stream>>>(
+        ids, routes, n_experts, tiles, tile_info, row_route, y, N, bad_ids);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t n_chunks = static_cast<size_t>(M) * (K / 8);
+    size_t blocks = (n_chunks + 255) / 256;
+    const size_t cap = static_cast<size_t>(sm_count) * 4;
+    if (blocks > cap) blocks = cap;
+    gather_x_tiles_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        x, xa, tile_info, row_route, x_div, K, n_chunks);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    WtRouted rt;
+    rt.tile_info = tile_info;
+    rt.row_route = row_route;
+    rt.expert_stride = expert_stride;
+    alignas(64) CUtensorMap map;
+    const long long row_bytes = static_cast<long long>(K / kQK) * kBlockBytes;
+    if (expert_stride % row_bytes == 0) {
+        const long long per = expert_stride / row_bytes;
+        const long long pool_rows = static_cast<long long>(n_experts - 1) * per + N;
+        rt.expert_rows = static_cast<int>(per);
+        if (pool_rows <= INT_MAX && make_weight_map(&map, w, static_cast<int>(pool_rows), K, 128))
+            return launch_wt_kernel<128, true>(xa, nullptr, w, y, nullptr, nullptr, 1, M, N, K,
+                                               device, map, stream, rt);
+    }
+    memset(&map, 0, sizeof(map));
+    return launch_wt_kernel<128, false>(xa, nullptr, w, y, nullptr, nullptr, 1, M, N, K, device,
+                                        map, stream, rt);
 }
 
 cudaError_t launch_gemm_tc_static(const float* x, const uint8_t* w, float* y, int M, int N, int K,

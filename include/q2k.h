@@ -298,6 +298,44 @@ q2k_status q2k_matmul_id_pair(const float *x, size_t x_elems, const void *w_a, s
                               uint32_t *bad_id_count, void *scratch, size_t scratch_bytes,
                               q2k_stream_t stream);
 
+/* Flag of q2k_matmul_id_ex: one x row per route (q2k_matmul_id_slotted). */
+#define Q2K_ID_SLOTTED 1u
+
+/* q2k_matmul_id_ex - q2k_matmul_id (or, with Q2K_ID_SLOTTED in `flags`,
+ * q2k_matmul_id_slotted) on a chosen path.  Page "tests/deepseek_q2_k.rs":
+ * fn run_expert, whose public routed product with more than 32 tokens (and the
+ * forced mm_id path) is held to 1e-2 instead of 2e-4: it multiplies many routes
+ * per expert as a matrix product.
+ *   Q2K_PATH_GEMV    as q2k_matmul_id; workspace = its scratch (NULL allowed)
+ *   Q2K_PATH_TENSOR  routes grouped per expert into 128-row tiles, each tile
+ *                    multiplied on the bf16 tensor cores with fp32 accumulation
+ *                    (error within 8e-3 * sum_k |x w| per element, as
+ *                    q2k_matmul_path's tensor path); needs a workspace of
+ *                    q2k_matmul_id_workspace_bytes(Q2K_PATH_TENSOR, ...) bytes,
+ *                    16-byte aligned, aliasing no other argument, and
+ *                    n_experts <= 4096.  Not a bit-for-bit match of the GEMV.
+ *   Q2K_PATH_AUTO    the tensor path when n_tokens > 32 (and n_experts <=
+ *                    4096), else the GEMV
+ * Other arguments, checks and bad-id handling as q2k_matmul_id: a bad id's
+ * route is a zero row and counted.  An unknown path or flag bit is
+ * Q2K_ERR_INVALID_ARGUMENT; so is a tensor-path call without a large enough
+ * workspace. */
+q2k_status q2k_matmul_id_ex(q2k_path path, uint32_t flags, const float *x, size_t x_elems,
+                            const void *w, size_t w_bytes, const uint32_t *ids, float *y,
+                            size_t y_elems, const q2k_matmul_id_params *params,
+                            uint32_t *bad_id_count, void *workspace, size_t workspace_bytes,
+                            q2k_stream_t stream);
+
+/* q2k_matmul_id_workspace_bytes - the workspace q2k_matmul_id_ex takes on
+ * `path` (AUTO resolved as there) for these params and flags: for the tensor
+ * path the routes' tile table and the bf16 image of their x rows, about
+ * (n_tokens*top_k + 128*min(n_experts, n_tokens*top_k)) * (2k + 4) bytes; for
+ * the GEMV its optional scratch (q2k_x_planes_bytes).  0 for invalid params,
+ * more than 65535 routes, or a tensor path with n_experts > 4096.  Geometry
+ * only: no device is touched. */
+size_t q2k_matmul_id_workspace_bytes(q2k_path path, uint32_t flags,
+                                     const q2k_matmul_id_params *params);
+
 /* q2k_matmul_workspace_bytes - device bytes of workspace q2k_matmul_ex can use
  * for this geometry and path (0: the path takes none).  The tensor-core path
  * stores x there as bf16 in the tile layout its shared memory uses,

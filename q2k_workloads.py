@@ -141,6 +141,8 @@ class RoutedWorkload:
 # Decode step of a DeepSeek-style MoE layer: one token, 8 of 64 experts of hidden
 # size 7168 and expert width 2048 (a 308 MB pool, larger than L2).
 MOE_DECODE = RoutedWorkload("moe_decode_top8", 5, 1, 8, 2048, 7168, 64)
+# Prefill of the same layer: 512 tokens, so about 64 routes per expert.
+MOE_PREFILL = RoutedWorkload("moe_prefill_top8", 6, 512, 8, 2048, 7168, 64)
 # Eight decode GEMVs of the 4096 x 4096 workload in one batched launch.
 BATCHED_DECODE_BATCHES = 8
 

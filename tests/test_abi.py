@@ -248,6 +248,45 @@ def test_matmul_id_slotted_and_pair_reject(lib):
     assert "32767" in lib.q2k_last_error().decode()
 
 
+def test_matmul_id_ex_workspace_and_rejections(lib):
+    """The routed product's tensor path: its workspace size (tile table, row
+    routes, x image of up to routes/128 + min(experts, routes) tiles) and the
+    checks made before any device work."""
+    n_tokens, top_k, n, k, experts = 64, 8, 2048, 7168, 64
+    p = q2k.MatmulIdParams(n_tokens, top_k, n, k, experts, 10, n * (k // 256) * 84)
+    tiles = 512 // 128 + 64
+    info = (tiles * 8 + 255) // 256 * 256
+    image = (tiles * 128 + 255) // 256 * 256 * k * 2
+    want = info + tiles * 128 * 4 + image
+    assert lib.q2k_matmul_id_workspace_bytes(q2k.PATH_TENSOR, 0, ctypes.byref(p)) == want
+    assert lib.q2k_matmul_id_workspace_bytes(q2k.PATH_AUTO, 0, ctypes.byref(p)) == want
+    # auto takes the GEMV at <= 32 tokens: its optional scratch is the x planes
+    small = q2k.MatmulIdParams(32, top_k, n, k, experts, 10, p.expert_stride)
+    assert (lib.q2k_matmul_id_workspace_bytes(q2k.PATH_AUTO, 0, ctypes.byref(small))
+            == lib.q2k_x_planes_bytes(k, 32))
+    assert (lib.q2k_matmul_id_workspace_bytes(q2k.PATH_GEMV, q2k.ID_SLOTTED, ctypes.byref(small))
+            == lib.q2k_x_planes_bytes(k, 32 * top_k))
+    many = q2k.MatmulIdParams(n_tokens, top_k, n, k, 4097, 10, p.expert_stride)
+    assert lib.q2k_matmul_id_workspace_bytes(q2k.PATH_TENSOR, 0, ctypes.byref(many)) == 0
+    assert lib.q2k_matmul_id_workspace_bytes(q2k.PATH_TENSOR, 2, ctypes.byref(p)) == 0
+    wb = experts * p.expert_stride
+    args = (0x10000, n_tokens * k, 0x10000000, wb, 0x1000000, 0x200000000, 512 * n, ctypes.byref(p),
+            None)
+    assert lib.q2k_matmul_id_ex(7, 0, *args, None, 0, None) == INVALID
+    assert "unknown path" in lib.q2k_last_error().decode()
+    assert lib.q2k_matmul_id_ex(q2k.PATH_TENSOR, 4, *args, None, 0, None) == INVALID
+    assert "flag" in lib.q2k_last_error().decode()
+    assert lib.q2k_matmul_id_ex(q2k.PATH_TENSOR, 0, *args, None, 0, None) == INVALID
+    assert "workspace" in lib.q2k_last_error().decode()
+    assert lib.q2k_matmul_id_ex(q2k.PATH_TENSOR, 0, *args, 0x300000000, want - 16, None) == INVALID
+    assert "workspace" in lib.q2k_last_error().decode()
+    assert lib.q2k_matmul_id_ex(q2k.PATH_TENSOR, 0, *args, 0x300000008, want, None) == INVALID
+    assert "aligned" in lib.q2k_last_error().decode()
+    # the workspace overlapping y
+    assert lib.q2k_matmul_id_ex(q2k.PATH_TENSOR, 0, *args, 0x200000000 + 4096, want, None) == INVALID
+    assert "alias" in lib.q2k_last_error().decode()
+
+
 def test_matmul_ex_batch_checks_every_call_first(lib):
     """A malformed call anywhere rejects the batch before any launch; its index is named."""
     calls = (q2k.MatmulCall * 2)()

@@ -251,3 +251,104 @@ def test_x_planes_scratch_gives_the_same_bits():
     d = q2k.matmul_id(xt, wed, idd, ne, experts, top_k, scratch=None)
     torch.cuda.synchronize()
     assert bits_equal(a, b) and bits_equal(c, d)
+
+
+# ------------------------------------------------------- mm_id on tensor cores
+
+TOL_TC = 8e-3   # bf16 operands, fp32 accumulation: as the dense tensor path
+
+
+def _tc_case(rng, tokens, top_k, experts, n, k, stride_pad=0, ids=None):
+    size = n * (k // 256) * 84
+    stride = size + stride_pad
+    w = np.zeros((experts - 1) * stride + size, dtype=np.uint8)
+    for e in range(experts):
+        w[e * stride:e * stride + size] = wl.random_blocks(rng, n * (k // 256)).reshape(-1)
+    x = wl.random_activations(rng, tokens, k)
+    if ids is None:
+        ids = rng.integers(0, experts, tokens * top_k).astype(np.uint32)
+    return w, x, ids, stride
+
+
+def test_matmul_id_tensor_page_case():
+    """Page fn run_expert(33, 6, 8) with force_mm: the matrix path, held to 1e-2."""
+    tokens, top_k, experts, n = 33, 6, 8, 8
+    w, x, ids, stride = _expert_case(tokens, top_k, experts, n)
+    wd, xd, idd = dev(w), dev(x), dev(ids.view(np.int32))
+    y = q2k.matmul_id_ex(xd, wd, idd, n, experts, top_k, path="tensor")
+    yref, s = oracle.matmul_id(x, w, ids, n, experts, stride, top_k)
+    got = y.cpu().numpy().astype(np.float64)
+    assert_close(got, yref, s, TOL_TC, "tensor run_expert(33, 6, 8)")
+    assert np.abs(got - yref).max() <= 1e-2   # the page's tolerance for the mm path
+    # auto takes the matrix path above 32 tokens
+    ya = q2k.matmul_id_ex(xd, wd, idd, n, experts, top_k)
+    torch.cuda.synchronize()
+    assert bits_equal(ya, y)
+
+
+@pytest.mark.parametrize("tokens,top_k,experts,n,k,pad", [
+    (80, 6, 8, 320, 1024, 0),       # ragged n (2.5 weight tiles), TMA weights
+    (70, 4, 16, 200, 512, 0),       # rows not a multiple of 1024 bytes: no TMA view
+    (48, 8, 6, 256, 2048, 2 * 84 * 8),  # stride a whole number of rows past the matrix
+    (40, 2, 5, 136, 1024, 20),      # stride off the row size: per-expert offsets, no TMA
+])
+def test_matmul_id_tensor_random(tokens, top_k, experts, n, k, pad):
+    rng = np.random.default_rng(tokens * 7 + k)
+    w, x, ids, stride = _tc_case(rng, tokens, top_k, experts, n, k, pad)
+    wd, xd, idd = dev(w), dev(x), dev(ids.view(np.int32))
+    y = q2k.matmul_id_ex(xd, wd, idd, n, experts, top_k, path="tensor", expert_stride=stride)
+    yref, s = oracle.matmul_id(x, w, ids, n, experts, stride, top_k, threads=ORACLE_THREADS)
+    assert_close(y.cpu().numpy().astype(np.float64), yref, s, TOL_TC,
+                 f"tensor mm_id {tokens}x{top_k} of {experts}, {n}x{k}")
+
+
+def test_matmul_id_tensor_skewed_routes():
+    """One expert takes 300 routes (three x tiles, the last ragged), several
+    take none, the rest one each: the tile table's edge cases."""
+    tokens, top_k, experts, n, k = 150, 2, 12, 256, 1024
+    ids = np.full(tokens * top_k, 3, dtype=np.uint32)
+    ids[::37] = 7
+    ids[5] = 11
+    ids[8] = 0
+    rng = np.random.default_rng(9)
+    w, x, ids, stride = _tc_case(rng, tokens, top_k, experts, n, k, ids=ids)
+    wd, xd, idd = dev(w), dev(x), dev(ids.view(np.int32))
+    y = q2k.matmul_id_ex(xd, wd, idd, n, experts, top_k, path="tensor")
+    yref, s = oracle.matmul_id(x, w, ids, n, experts, stride, top_k, threads=ORACLE_THREADS)
+    assert_close(y.cpu().numpy().astype(np.float64), yref, s, TOL_TC, "skewed tensor mm_id")
+
+
+def test_matmul_id_tensor_slotted_and_bad_ids():
+    tokens, top_k, experts, n, k = 40, 4, 6, 256, 1024
+    rng = np.random.default_rng(21)
+    w, _, ids, stride = _tc_case(rng, tokens, top_k, experts, n, k)
+    x = wl.random_activations(rng, tokens * top_k, k).reshape(tokens, top_k, k)
+    bad = ids.copy()
+    bad[3] = experts
+    bad[77] = 0xFFFFFFFF
+    wd, xd, idd = dev(w), dev(x), dev(bad.view(np.int32))
+    y, count = q2k.matmul_id_ex(xd, wd, idd, n, experts, path="tensor", slotted=True, check=False)
+    torch.cuda.synchronize()
+    assert int(count.item()) == 2
+    got = y.cpu().numpy().reshape(tokens * top_k, n)
+    assert (got[3] == 0).all() and (got[77] == 0).all()
+    yref, s = oracle.matmul_id(x.reshape(tokens * top_k, k), w, ids, n, experts, stride, 1,
+                               threads=ORACLE_THREADS)
+    good = [r for r in range(tokens * top_k) if r not in (3, 77)]
+    assert_close(got[good].astype(np.float64), yref[good], s[good], TOL_TC, "slotted tensor mm_id")
+
+
+def test_matmul_id_tensor_moe_prefill_sampled():
+    """The MoE layer's prefill shape (512 tokens, top-8 of 64 experts of
+    2048 x 7168): sampled routes against the oracle."""
+    tokens, top_k, experts, n, k = 512, 8, 64, 2048, 7168
+    rng = np.random.default_rng(31)
+    w, x, ids, stride = _tc_case(rng, tokens, top_k, experts, n, k)
+    wd, xd, idd = dev(w), dev(x), dev(ids.view(np.int32))
+    y = q2k.matmul_id_ex(xd, wd, idd, n, experts, top_k, path="tensor").cpu().numpy()
+    routes = rng.choice(tokens * top_k, 12, replace=False)
+    size = n * (k // 256) * 84
+    for r in routes.tolist():
+        e = int(ids[r])
+        yref, s = oracle.matmul(x[r // top_k:r // top_k + 1], w[e * stride:e * stride + size], n)
+        assert_close(y[r:r + 1].astype(np.float64), yref, s, TOL_TC, f"route {r}")
