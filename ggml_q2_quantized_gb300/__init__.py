@@ -128,6 +128,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                            ctypes.POINTER(MatmulIdParams), vp, vp, sz, vp]
         lib.q2k_matmul_id_ex.argtypes = [ctypes.c_int, ctypes.c_uint32, vp, sz, vp, sz, vp, vp, sz,
                                          ctypes.POINTER(MatmulIdParams), vp, vp, sz, vp]
+        lib.q2k_matmul_id_pair_ex.argtypes = [ctypes.c_int, vp, sz, vp, sz, vp, sz, vp, vp, vp, sz,
+                                              ctypes.POINTER(MatmulIdParams), vp, vp, sz, vp]
         lib.q2k_matmul_id_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_uint32,
                                                       ctypes.POINTER(MatmulIdParams)]
         lib.q2k_matmul_id_workspace_bytes.restype = sz
@@ -149,7 +151,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.q2k_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         for fn in ("q2k_dequantize", "q2k_embedding_gather", "q2k_matmul", "q2k_matmul_path",
                    "q2k_matmul_ex", "q2k_matmul_ex_batch", "q2k_matmul_batched_mv", "q2k_matmul_id",
-                   "q2k_matmul_id_slotted", "q2k_matmul_id_pair", "q2k_device_error",
+                   "q2k_matmul_id_slotted", "q2k_matmul_id_pair", "q2k_matmul_id_ex",
+                   "q2k_matmul_id_pair_ex", "q2k_device_error",
                    "q2k_selftest_wait_timeout", "q2k_gguf_open", "q2k_gguf_tensor_info",
                    "q2k_gguf_read_tensor"):
             getattr(lib, fn).restype = ctypes.c_int
@@ -476,9 +479,13 @@ def matmul_id_slotted(x, w, ids, n: int, n_experts: int, expert_stride: int | No
 
 
 def matmul_id_pair(x, w_a, w_b, ids, n: int, n_experts: int, top_k: int,
-                   expert_stride: int | None = None, check: bool = True, scratch="auto"):
+                   expert_stride: int | None = None, check: bool = True, scratch="auto",
+                   path=None, workspace=None):
     """Two routed products sharing ``x`` and ``ids`` (e.g. the gate and up
-    projections) in one launch; returns ``(y_a, y_b)`` as ``matmul_id`` would."""
+    projections) in one launch; returns ``(y_a, y_b)`` as ``matmul_id`` would.
+    ``path`` ("gemv", "tensor" or "auto", as ``matmul_id_ex``) goes through
+    ``q2k_matmul_id_pair_ex``; the tensor path routes and gathers x once for
+    both products.  ``workspace`` as in ``matmul_id_ex``."""
     torch = _torch()
     _require_cuda(x, "x", torch.float32)
     _require_cuda(w_a, "w_a", torch.uint8)
@@ -494,6 +501,21 @@ def matmul_id_pair(x, w_a, w_b, ids, n: int, n_experts: int, top_k: int,
     bad = torch.zeros(1, dtype=torch.int32, device=x.device)
     p = MatmulIdParams(n_tokens, top_k, n, k, n_experts, GGML_TYPE_Q2_K, expert_stride)
     lib = load()
+    if path is not None:
+        pcode = _PATHS[path]
+        if workspace is None:
+            nbytes = lib.q2k_matmul_id_workspace_bytes(pcode, 0, ctypes.byref(p))
+            if nbytes:
+                workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+        wp = workspace.data_ptr() if workspace is not None else None
+        wb = workspace.numel() if workspace is not None else 0
+        with _on_device(x):
+            _check(lib, lib.q2k_matmul_id_pair_ex(pcode, x.data_ptr(), x.numel(), w_a.data_ptr(),
+                                                  w_a.numel(), w_b.data_ptr(), w_b.numel(),
+                                                  ids.data_ptr(), y_a.data_ptr(), y_b.data_ptr(),
+                                                  y_a.numel(), ctypes.byref(p), bad.data_ptr(),
+                                                  wp, wb, _stream_handle(x)))
+        return _routed_finish(bad, check, (y_a, y_b), n_experts)
     sp, sb, _keep = _planes_scratch(lib, k, n_tokens, x.device, scratch)
     with _on_device(x):
         _check(lib, lib.q2k_matmul_id_pair(x.data_ptr(), x.numel(), w_a.data_ptr(), w_a.numel(),

@@ -579,7 +579,6 @@ q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void*
     const size_t x_rows = slotted ? routes : size_t(p->n_tokens);
     if (path == Q2K_PATH_AUTO) path = routed_auto_path(p);
     if (path == Q2K_PATH_TENSOR) {
-        if (pair) return fail(Q2K_ERR_INVALID_ARGUMENT, "the paired product has no tensor-core path");
         if (p->n_experts > uint32_t(q2k::kRoutedMaxExperts))
             return fail(Q2K_ERR_INVALID_ARGUMENT, "tensor-core path supports n_experts <= %d",
                         q2k::kRoutedMaxExperts);
@@ -590,6 +589,7 @@ q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void*
         if (!aligned(scratch, 16)) return fail(Q2K_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
         if (overlaps(scratch, need, x, x_bytes) || overlaps(scratch, need, wa, wa_bytes) ||
             overlaps(scratch, need, ya, y_bytes) || overlaps(scratch, need, ids, id_bytes) ||
+            (pair && (overlaps(scratch, need, wb, wb_bytes) || overlaps(scratch, need, yb, y_bytes))) ||
             (bad_id_count != nullptr && overlaps(scratch, need, bad_id_count, 4)))
             return fail(Q2K_ERR_INVALID_ARGUMENT, "workspace must not alias x, w, ids or y");
         DeviceInfo dev;
@@ -603,7 +603,9 @@ q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void*
                                            static_cast<long long>(p->expert_stride), ids, ya,
                                            int(routes), slotted ? 1 : int(p->top_k), int(p->n_experts),
                                            int(p->n), int(p->k), bad_id_count, dev.device,
-                                           dev.sm_count, scratch, s);
+                                           dev.sm_count, scratch, s,
+                                           pair ? static_cast<const uint8_t*>(wb) : nullptr,
+                                           pair ? yb : nullptr);
         return e == cudaSuccess ? Q2K_OK : cuda_fail(e, what);
     }
     uint8_t* planes = nullptr;
@@ -699,6 +701,21 @@ q2k_status q2k_matmul_id_ex(q2k_path path, uint32_t flags, const float* x, size_
     return routed_call(x, x_elems, (flags & Q2K_ID_SLOTTED) != 0, w, w_bytes, nullptr, 0, ids, y,
                        nullptr, y_elems, p, bad_id_count, workspace, workspace_bytes, stream,
                        "q2k_matmul_id_ex launch", path);
+}
+
+q2k_status q2k_matmul_id_pair_ex(q2k_path path, const float* x, size_t x_elems, const void* w_a,
+                                 size_t w_a_bytes, const void* w_b, size_t w_b_bytes,
+                                 const uint32_t* ids, float* y_a, float* y_b, size_t y_elems,
+                                 const q2k_matmul_id_params* p, uint32_t* bad_id_count,
+                                 void* workspace, size_t workspace_bytes, q2k_stream_t stream) {
+    g_last_error[0] = '\0';
+    if (path != Q2K_PATH_AUTO && path != Q2K_PATH_GEMV && path != Q2K_PATH_TENSOR)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "unknown path %d", static_cast<int>(path));
+    if (y_b == nullptr || w_b == nullptr)
+        return fail(Q2K_ERR_INVALID_ARGUMENT, "x, w, ids and y must be non-NULL");
+    return routed_call(x, x_elems, false, w_a, w_a_bytes, w_b, w_b_bytes, ids, y_a, y_b, y_elems, p,
+                       bad_id_count, workspace, workspace_bytes, stream,
+                       "q2k_matmul_id_pair_ex launch", path);
 }
 
 q2k_status q2k_matmul_id_pair(const float* x, size_t x_elems, const void* w_a, size_t w_a_bytes,

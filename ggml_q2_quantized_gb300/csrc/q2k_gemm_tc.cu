@@ -1596,11 +1596,12 @@ int routed_tiles_max(int routes, int n_experts) {
 
 // One CTA: count the routes per expert, scan to tile starts, and write each
 // x tile's {expert, rows} (-1: unused), each x row's route (-1: padding) and,
-// for a route whose id is out of range, a zero row of y and a count.
+// for a route whose id is out of range, a zero row of y (and of y2, when not
+// null) and a count (one per output).
 __global__ void __launch_bounds__(1024)
 route_tiles_kernel(const uint32_t* __restrict__ ids, int routes, int n_experts, int tiles_max,
                    int2* __restrict__ tile_info, int* __restrict__ row_route, float* __restrict__ y,
-                   int N, unsigned int* __restrict__ bad_ids) {
+                   float* __restrict__ y2, int N, unsigned int* __restrict__ bad_ids) {
     extern __shared__ int route_smem[];
     int* cnt = route_smem;              // per expert: routes, then the placement cursor
     int* start = route_smem + n_experts;  // per expert: first tile
@@ -1615,9 +1616,13 @@ route_tiles_kernel(const uint32_t* __restrict__ ids, int routes, int n_experts, 
         if (e < static_cast<uint32_t>(n_experts)) {
             atomicAdd(&cnt[e], 1);
         } else {
-            if (bad_ids != nullptr) atomicAdd(bad_ids, 1u);
+            if (bad_ids != nullptr) atomicAdd(bad_ids, y2 != nullptr ? 2u : 1u);
             float* row = y + static_cast<size_t>(r) * N;
             for (int n = 0; n < N; ++n) row[n] = 0.0f;
+            if (y2 != nullptr) {
+                row = y2 + static_cast<size_t>(r) * N;
+                for (int n = 0; n < N; ++n) row[n] = 0.0f;
+            }
         }
     }
     __syncthreads();
@@ -1712,7 +1717,8 @@ size_t gemm_tc_routed_workspace_bytes(int routes, int n_experts, int K) {
 cudaError_t launch_gemm_tc_routed(const float* x, const uint8_t* w, long long expert_stride,
                                   const uint32_t* ids, float* y, int routes, int x_div,
                                   int n_experts, int N, int K, unsigned int* bad_ids, int device,
-                                  int sm_count, void* workspace, cudaStream_t stream) {
+                                  int sm_count, void* workspace, cudaStream_t stream,
+                                  const uint8_t* w2, float* y2) {
     if (n_experts > kRoutedMaxExperts) return cudaErrorInvalidValue;
     const int tiles = routed_tiles_max(routes, n_experts);
     const int M = tiles * 128;
@@ -1721,7 +1727,7 @@ cudaError_t launch_gemm_tc_routed(const float* x, const uint8_t* w, long long ex
     int* row_route = reinterpret_cast<int*>(base + routed_info_bytes(tiles));
     uint8_t* xa = base + routed_info_bytes(tiles) + routed_rows_bytes(tiles);
     route_tiles_kernel<<<1, 1024, 2 * n_experts * sizeof(int), stream>>>(
-        ids, routes, n_experts, tiles, tile_info, row_route, y, N, bad_ids);
+        ids, routes, n_experts, tiles, tile_info, row_route, y, y2, N, bad_ids);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t n_chunks = static_cast<size_t>(M) * (K / 8);
@@ -1736,19 +1742,30 @@ cudaError_t launch_gemm_tc_routed(const float* x, const uint8_t* w, long long ex
     rt.tile_info = tile_info;
     rt.row_route = row_route;
     rt.expert_stride = expert_stride;
-    alignas(64) CUtensorMap map;
-    const long long row_bytes = static_cast<long long>(K / kQK) * kBlockBytes;
-    if (expert_stride % row_bytes == 0) {
-        const long long per = expert_stride / row_bytes;
-        const long long pool_rows = static_cast<long long>(n_experts - 1) * per + N;
-        rt.expert_rows = static_cast<int>(per);
-        if (pool_rows <= INT_MAX && make_weight_map(&map, w, static_cast<int>(pool_rows), K, 128))
-            return launch_wt_kernel<128, true>(xa, nullptr, w, y, nullptr, nullptr, 1, M, N, K,
-                                               device, map, stream, rt);
+    // one GEMM per weight pool over the same tiles and x image
+    for (int o = 0; o < (w2 != nullptr ? 2 : 1); ++o) {
+        const uint8_t* wo = o == 0 ? w : w2;
+        float* yo = o == 0 ? y : y2;
+        alignas(64) CUtensorMap map;
+        const long long row_bytes = static_cast<long long>(K / kQK) * kBlockBytes;
+        bool tma = false;
+        if (expert_stride % row_bytes == 0) {
+            const long long per = expert_stride / row_bytes;
+            const long long pool_rows = static_cast<long long>(n_experts - 1) * per + N;
+            rt.expert_rows = static_cast<int>(per);
+            tma = pool_rows <= INT_MAX && make_weight_map(&map, wo, static_cast<int>(pool_rows), K, 128);
+        }
+        if (tma) {
+            e = launch_wt_kernel<128, true>(xa, nullptr, wo, yo, nullptr, nullptr, 1, M, N, K,
+                                            device, map, stream, rt);
+        } else {
+            memset(&map, 0, sizeof(map));
+            e = launch_wt_kernel<128, false>(xa, nullptr, wo, yo, nullptr, nullptr, 1, M, N, K,
+                                             device, map, stream, rt);
+        }
+        if (e != cudaSuccess) return e;
     }
-    memset(&map, 0, sizeof(map));
-    return launch_wt_kernel<128, false>(xa, nullptr, w, y, nullptr, nullptr, 1, M, N, K, device,
-                                        map, stream, rt);
+    return cudaSuccess;
 }
 
 cudaError_t launch_gemm_tc_static(const float* x, const uint8_t* w, float* y, int M, int N, int K,

@@ -93,7 +93,8 @@ cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, in
 // Routed product on tensor cores: route r = 0..routes-1 multiplies x row
 // r / x_div by expert ids[r]'s weights (w + ids[r] * expert_stride, N rows)
 // into y row r; ids out of range give a zero row and a count in *bad_ids (if
-// not null).  The routes are grouped into 128-row x tiles per expert in a
+// not null).  With w2 and y2 (same layout) the second product reuses the
+// routing and the x image: one more GEMM, and a bad id counts once per output.  The routes are grouped into 128-row x tiles per expert in a
 // workspace of gemm_tc_routed_workspace_bytes bytes (16-byte aligned).
 // cudaErrorInvalidValue for more than kRoutedMaxExperts experts.
 constexpr int kRoutedMaxExperts = 4096;
@@ -101,7 +102,8 @@ size_t gemm_tc_routed_workspace_bytes(int routes, int n_experts, int K);
 cudaError_t launch_gemm_tc_routed(const float* x, const uint8_t* w, long long expert_stride,
                                   const uint32_t* ids, float* y, int routes, int x_div,
                                   int n_experts, int N, int K, unsigned int* bad_ids, int device,
-                                  int sm_count, void* workspace, cudaStream_t stream);
+                                  int sm_count, void* workspace, cudaStream_t stream,
+                                  const uint8_t* w2 = nullptr, float* y2 = nullptr);
 
 // Size of the library's own fixed scratch for the tensor-core path (the x tile
 // image), used by q2k_matmul_static_workspace.

@@ -326,6 +326,20 @@ q2k_status q2k_matmul_id_ex(q2k_path path, uint32_t flags, const float *x, size_
                             uint32_t *bad_id_count, void *workspace, size_t workspace_bytes,
                             q2k_stream_t stream);
 
+/* q2k_matmul_id_pair_ex - q2k_matmul_id_pair on a chosen path, as
+ * q2k_matmul_id_ex (page fn run_expert with force_mm runs the pair on its matrix
+ * path).  On the tensor path the routes are grouped and x gathered once, and one
+ * GEMM per weight set reads the shared tiles: y_a and y_b each within 8e-3 *
+ * sum_k |x w|, and bit-identical to two q2k_matmul_id_ex tensor calls.  The
+ * tensor path's workspace is q2k_matmul_id_workspace_bytes(Q2K_PATH_TENSOR, 0,
+ * params) bytes; on the GEMV path the workspace is q2k_matmul_id_pair's optional
+ * scratch.  A bad id is counted once per product. */
+q2k_status q2k_matmul_id_pair_ex(q2k_path path, const float *x, size_t x_elems, const void *w_a,
+                                 size_t w_a_bytes, const void *w_b, size_t w_b_bytes,
+                                 const uint32_t *ids, float *y_a, float *y_b, size_t y_elems,
+                                 const q2k_matmul_id_params *params, uint32_t *bad_id_count,
+                                 void *workspace, size_t workspace_bytes, q2k_stream_t stream);
+
 /* q2k_matmul_id_workspace_bytes - the workspace q2k_matmul_id_ex takes on
  * `path` (AUTO resolved as there) for these params and flags: for the tensor
  * path the routes' tile table and the bf16 image of their x rows, about

@@ -285,6 +285,18 @@ def test_matmul_id_ex_workspace_and_rejections(lib):
     # the workspace overlapping y
     assert lib.q2k_matmul_id_ex(q2k.PATH_TENSOR, 0, *args, 0x200000000 + 4096, want, None) == INVALID
     assert "alias" in lib.q2k_last_error().decode()
+    # the pair: unknown path, missing second set, workspace overlapping the second output
+    pair = (0x10000, n_tokens * k, 0x10000000, wb, 0x40000000, wb, 0x1000000, 0x200000000,
+            0x280000000, 512 * n, ctypes.byref(p), None)
+    assert lib.q2k_matmul_id_pair_ex(9, *pair, None, 0, None) == INVALID
+    assert "unknown path" in lib.q2k_last_error().decode()
+    assert lib.q2k_matmul_id_pair_ex(q2k.PATH_TENSOR, 0x10000, n_tokens * k, 0x10000000, wb, None,
+                                     wb, 0x1000000, 0x200000000, 0x280000000, 512 * n,
+                                     ctypes.byref(p), None, None, 0, None) == INVALID
+    assert lib.q2k_matmul_id_pair_ex(q2k.PATH_TENSOR, *pair, 0x280000000 + 64, want, None) == INVALID
+    assert "alias" in lib.q2k_last_error().decode()
+    assert lib.q2k_matmul_id_pair_ex(q2k.PATH_TENSOR, *pair, None, 0, None) == INVALID
+    assert "workspace" in lib.q2k_last_error().decode()
 
 
 def test_matmul_ex_batch_checks_every_call_first(lib):

@@ -356,3 +356,30 @@ def test_matmul_id_tensor_moe_prefill_sampled():
         e = int(ids[r])
         yref, s = oracle.matmul(x[r // top_k:r // top_k + 1], w[e * stride:e * stride + size], n)
         assert_close(y[r:r + 1].astype(np.float64), yref, s, TOL_TC, f"route {r}")
+
+
+def test_matmul_id_pair_tensor_shares_routing():
+    """Page fn run_expert with force_mm runs the pair on its matrix path: here
+    routing and the x gather run once and each weight set's GEMM reads the same
+    tiles, so each output equals its own tensor-path call bit for bit."""
+    tokens, top_k, experts, n, k = 48, 6, 8, 320, 1024
+    rng = np.random.default_rng(41)
+    wa, x, ids, stride = _tc_case(rng, tokens, top_k, experts, n, k)
+    wb, _, _, _ = _tc_case(rng, tokens, top_k, experts, n, k, ids=ids)
+    bad = ids.copy()
+    bad[10] = experts + 3
+    xd, idd = dev(x), dev(bad.view(np.int32))
+    wad, wbd = dev(wa), dev(wb)
+    ya, yb, count = q2k.matmul_id_pair(xd, wad, wbd, idd, n, experts, top_k, path="tensor",
+                                       check=False)
+    sa, ca = q2k.matmul_id_ex(xd, wad, idd, n, experts, top_k, path="tensor", check=False)
+    sb, cb = q2k.matmul_id_ex(xd, wbd, idd, n, experts, top_k, path="tensor", check=False)
+    torch.cuda.synchronize()
+    assert int(count.item()) == 2 and int(ca.item()) == 1 and int(cb.item()) == 1
+    assert bits_equal(ya, sa) and bits_equal(yb, sb)
+    good = [r for r in range(tokens * top_k) if r != 10]
+    for y, w in ((ya, wa), (yb, wb)):
+        got = y.cpu().numpy()
+        assert (got[10] == 0).all()
+        yref, s = oracle.matmul_id(x, w, ids, n, experts, stride, top_k, threads=ORACLE_THREADS)
+        assert_close(got[good].astype(np.float64), yref[good], s[good], TOL_TC, "pair tensor")
