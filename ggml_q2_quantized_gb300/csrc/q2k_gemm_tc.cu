@@ -1063,13 +1063,19 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                 // one K part alone goes to y; parts of a split go to their own
                 // slice of the partial buffer, summed in part order below
                 float* out = gridDim.z == 1 ? y : partial + static_cast<size_t>(blockIdx.z) * M * N;
-                if (n < N) {
+                if (n < N && rt.row_route == nullptr) {
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
                         const int m = m0 + c0 + q;
-                        if (m >= M || c0 + q >= tile_rows) continue;
-                        // routed: x row m is route row_route[m] (-1: padding)
-                        const int r = rt.row_route != nullptr ? __ldg(rt.row_route + m) : m;
+                        if (m < M) out[static_cast<size_t>(m) * N + n] = __uint_as_float(v[q]);
+                    }
+                } else if (n < N) {
+                    // routed: x row m is route row_route[m] (-1: padding)
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int m = m0 + c0 + q;
+                        if (c0 + q >= tile_rows) continue;
+                        const int r = __ldg(rt.row_route + m);
                         if (r >= 0) out[static_cast<size_t>(r) * N + n] = __uint_as_float(v[q]);
                     }
                 }
