@@ -383,3 +383,23 @@ def test_matmul_id_pair_tensor_shares_routing():
         assert (got[10] == 0).all()
         yref, s = oracle.matmul_id(x, w, ids, n, experts, stride, top_k, threads=ORACLE_THREADS)
         assert_close(got[good].astype(np.float64), yref[good], s[good], TOL_TC, "pair tensor")
+
+
+@pytest.mark.parametrize("experts,tokens,top_k", [(4096, 40, 2), (1, 70, 1), (3, 33, 3)])
+def test_matmul_id_tensor_expert_counts(experts, tokens, top_k):
+    """The routing kernel's scan at its limits: 4096 experts (4 per scan thread,
+    most empty), a single expert (every route in one expert's tiles), and auto
+    at 33 tokens (the first count the matrix path takes)."""
+    n, k = 8 if experts > 8 else 136, 256 if experts > 8 else 1024
+    rng = np.random.default_rng(experts + tokens)
+    w, x, ids, stride = _tc_case(rng, tokens, top_k, experts, n, k)
+    if experts == 4096:
+        ids = rng.choice(experts, tokens * top_k, replace=False).astype(np.uint32)
+    wd, xd, idd = dev(w), dev(x), dev(ids.view(np.int32))
+    y = q2k.matmul_id_ex(xd, wd, idd, n, experts, top_k, path="auto")
+    yt = q2k.matmul_id_ex(xd, wd, idd, n, experts, top_k, path="tensor")
+    torch.cuda.synchronize()
+    assert bits_equal(y, yt)   # more than 32 tokens: auto is the tensor path
+    yref, s = oracle.matmul_id(x, w, ids, n, experts, stride, top_k, threads=ORACLE_THREADS)
+    assert_close(y.cpu().numpy().astype(np.float64), yref, s, TOL_TC,
+                 f"tensor mm_id, {experts} experts")
