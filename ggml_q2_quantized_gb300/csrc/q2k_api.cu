@@ -325,9 +325,15 @@ q2k_status plan_batch(const q2k_matmul_call* calls, size_t count, BatchPlan* bp)
                                         c.w_bytes, c.y, c.y_elems, &c.params, c.workspace,
                                         c.workspace_bytes, &bp->path[i], &bp->ws[i]);
         if (st != Q2K_OK) {
-            char msg[512];
-            snprintf(msg, sizeof msg, "call %zu: %s", i, g_last_error);
-            snprintf(g_last_error, sizeof g_last_error, "%s", msg);
+            // prefix the message with the call's index (a long message loses its tail)
+            char msg[sizeof g_last_error];
+            const int head = snprintf(msg, sizeof msg, "call %zu: ", i);
+            if (head > 0 && static_cast<size_t>(head) < sizeof msg) {
+                const size_t room = sizeof msg - static_cast<size_t>(head) - 1;
+                strncpy(msg + head, g_last_error, room);
+                msg[sizeof msg - 1] = '\0';
+                memcpy(g_last_error, msg, sizeof msg);
+            }
             return st;
         }
         if (bp->path[i] == Q2K_PATH_GEMV && q2k::gemv_shares_planes(int(c.params.m), int(c.params.k))) {

@@ -203,7 +203,7 @@ __device__ __forceinline__ void decode_word(uint32_t word, uint32_t lo, uint32_t
                                             uint32_t& p0, uint32_t& p1) {
     // byte i of t2 = 2 q_i for the four lanes of this word at shift 2J
     uint32_t t2;
-    if (J == 0)
+    if constexpr (J == 0)
         t2 = (word * 2u) & 0x06060606u;
     else
         t2 = (word >> (2 * J - 1)) & 0x06060606u;
