@@ -461,13 +461,17 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
         issue_weight_copies(smem_w, gsrc, bars, rows, row_bytes, delta, tid >> 5, nwarps);
     // x -> integer planes, once per CTA, while the weights stream in
     if (xplanes == nullptr) convert_x(x, planes, run_sum, run_inv, n_runs, tid, nthreads);
-    // With the copies issued before the dependency wait they have (nearly)
-    // landed by now: one thread waits for all of them, and the barrier below
-    // publishes that, so the row loop needs no barrier polls of its own.
+    // A dependent call's copies, issued before its dependency wait, have
+    // (nearly) landed by now: one thread waits for all of them, and the
+    // barrier below publishes that, so the row loop needs no barrier polls of
+    // its own.  An independent call's copies were issued just now: its row
+    // loop waits for each piece of rows as it needs it instead, and starts on
+    // the first rows while the rest are in flight.
+    const bool wait_all = const_weights && !independent;
     bool all_ok = true;
     if (xplanes != nullptr && tid == 0)
         all_ok = mbar_wait_backoff(planes_bar, 0, abort_flag, &g_gemv_error, kErrTimeoutGemv, 64);
-    if (const_weights && tid == 0) {
+    if (wait_all && tid == 0) {
         for (int p = 0; p < n_pieces; ++p)
             all_ok = all_ok && mbar_wait_backoff(bars + 8 * p, 0, abort_flag, &g_gemv_error,
                                                  kErrTimeoutGemv, 64);
@@ -485,7 +489,7 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     const int lane = tid & 31;
     const int wig = sl >> 5;  // warp index within the group
     const uint8_t* my_col = smem_w + b * kBlockBytes;
-    const int waited = const_weights ? n_pieces - 1 : -1;
+    const int waited = wait_all ? n_pieces - 1 : -1;
     const bool ok = !(const_weights && *abort_flag);
     dot_rows(my_col, row_bytes, rows, g, groups, lane, wig, warps_per_group, active, h, seg, ssel, s,
              red, bars, 0u, waited, abort_flag, ok);
