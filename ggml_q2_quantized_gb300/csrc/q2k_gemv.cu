@@ -299,12 +299,14 @@ __device__ __forceinline__ void load_slice_planes(const uint32_t* planes, const 
 }
 
 // Rows [0, rows) of a weight chunk in shared memory (this thread's slice of
-// row r at my_col + r row_bytes) against the slice planes s: group g takes rows
-// g, g + groups, ... eight at a time, and each row's total over the group's
-// warps goes to red[row * warps_per_group + warp in group].  Piece p (rows
-// 4p .. 4p + 3) is waited for, once, before its rows are read: from piece
-// waited + 1 on, with the parity of bit p of `parity`.  Returns false once a
-// wait gave up (the rows after it count as zero).
+// row r at my_col + r row_bytes) against the slice planes s: group g takes the
+// blocks of eight consecutive rows g, g + groups, ... (rows 8 g .. 8 g + 7,
+// then 8 (g + groups) ..), and each row's total over the group's warps goes to
+// red[row * warps_per_group + warp in group].  The pieces (rows 4p .. 4p + 3)
+// a block reads are waited for before its rows are read, unless all pieces up
+// to `waited` are known to have landed; each piece barrier completes once, so
+// waiting on it again returns at once.  Returns false once a wait gave up (the
+// rows after it count as zero).
 __device__ __forceinline__ bool dot_rows(const uint8_t* my_col, size_t row_bytes, int rows, int g,
                                          int groups, int lane, int wig, int warps_per_group,
                                          bool active, int h, int seg, uint32_t ssel,
@@ -312,25 +314,24 @@ __device__ __forceinline__ bool dot_rows(const uint8_t* my_col, size_t row_bytes
                                          uint32_t parity, int waited, volatile int* abort_flag,
                                          bool ok) {
     constexpr int kLoad = 2 * kRowBatch;  // rows loaded and decoded together
-    for (int base = g; base < rows; base += groups * kLoad) {
-        // Make sure every piece this batch touches has landed, then issue all
-        // shared-memory loads of the batch before any arithmetic.
-        const int last = min(rows - 1, base + (kLoad - 1) * groups);
-        for (int pw = waited + 1; pw <= last / kPieceRows; ++pw)
+    for (int base = g * kLoad; base < rows; base += groups * kLoad) {
+        // Make sure the pieces of this block have landed, then issue all
+        // shared-memory loads of the block before any arithmetic.
+        const int last = min(rows - 1, base + kLoad - 1);
+        for (int pw = max(waited + 1, base / kPieceRows); pw <= last / kPieceRows; ++pw)
             ok = ok && mbar_wait_backoff(bars + 8 * pw, (parity >> pw) & 1u, abort_flag,
                                          &g_gemv_error, kErrTimeoutGemv, 64);
-        waited = max(waited, last / kPieceRows);
         RowWords rw[kLoad];
 #pragma unroll
         for (int u = 0; u < kLoad; ++u) {
-            const int lr = min(base + u * groups, last);
+            const int lr = min(base + u, last);
             rw[u] = load_row_words(my_col + static_cast<size_t>(lr) * row_bytes, h, seg, ssel);
         }
         float part[kLoad];
 #pragma unroll
         for (int u = 0; u < kLoad; ++u) {
             const float v = slice_dot(rw[u], s);
-            part[u] = (active && ok && base + u * groups < rows) ? v : 0.f;
+            part[u] = (active && ok && base + u < rows) ? v : 0.f;
         }
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
@@ -339,7 +340,7 @@ __device__ __forceinline__ bool dot_rows(const uint8_t* my_col, size_t row_bytes
             for (int u = 0; u < kRowBatch; ++u) p4[u] = part[hb * kRowBatch + u];
             int which;
             const float tot = transpose_reduce4(p4, lane, &which);
-            const int lr = base + (hb * kRowBatch + which) * groups;
+            const int lr = base + hb * kRowBatch + which;
             if ((lane & 7) == 0 && lr < rows) red[lr * warps_per_group + wig] = tot;
         }
     }
