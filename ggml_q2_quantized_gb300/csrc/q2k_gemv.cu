@@ -5,11 +5,11 @@
 //
 // Two kernels:
 //
-// gemv_m1_kernel (m = 1, k <= 16384, 16-byte aligned W): one CTA owns a
+// gemv_m1_kernel (m = 1, k <= 16384, 4-byte aligned W): one CTA owns a
 //   contiguous chunk of weight rows.  Its bytes are prefetched into L2 before
 //   the kernel waits on the previous grid (programmatic dependent launch; an L2
 //   prefetch is coherent, so this is safe even if that grid wrote W), then
-//   copied into shared memory by bulk asynchronous copies, four rows per
+//   copied into shared memory by bulk asynchronous copies, eight rows per
 //   mbarrier so decoding starts as soon as the first rows land.  Every thread
 //   owns one 64-weight slice of K - one (block, half, segment): 16 quant bytes
 //   read at the four shifts - and keeps the slice of x in registers for all
@@ -38,7 +38,11 @@ __device__ unsigned int g_gemv_error;
 namespace {
 
 constexpr int kGemvWarps = 8;
-constexpr int kPieceRows = 4;      // rows per bulk copy / mbarrier
+// Rows per bulk copy and mbarrier: one block of the row loop (8 rows), so a
+// block waits for exactly one piece.  Piece starts are 8 rows = 672 k/256
+// bytes apart, a multiple of 16, so every piece keeps the chunk's offset from
+// a 16-byte boundary (as CTA chunks do, being a multiple of 4 rows apart).
+constexpr int kPieceRows = 8;
 constexpr int kM1MaxSlices = 256;  // k <= 16384
 // Threads per CTA of the m = 1 kernel.  A dependent call runs alone once its
 // predecessor completes, so it takes more threads per CTA (shorter critical
@@ -302,7 +306,7 @@ __device__ __forceinline__ void load_slice_planes(const uint32_t* planes, const 
 // row r at my_col + r row_bytes) against the slice planes s: group g takes the
 // blocks of eight consecutive rows g, g + groups, ... (rows 8 g .. 8 g + 7,
 // then 8 (g + groups) ..), and each row's total over the group's warps goes to
-// red[row * warps_per_group + warp in group].  The pieces (rows 4p .. 4p + 3)
+// red[row * warps_per_group + warp in group].  The pieces (rows 8p .. 8p + 7)
 // a block reads are waited for before its rows are read, unless all pieces up
 // to `waited` are known to have landed; each piece barrier completes once, so
 // waiting on it again returns at once.  Returns false once a wait gave up (the
