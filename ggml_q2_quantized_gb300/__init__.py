@@ -340,12 +340,18 @@ class MatmulBatch:
     separate ``matmul`` calls; m = 1 calls reading one x convert it once).  The
     tensors stay bound: update their contents in place between runs.  ``outs``
     lists the output tensors in call order.
+
+    ``graph=True``: the first ``run()`` enqueues the calls and captures them
+    into a CUDA graph; later runs replay it on the current stream, one launch
+    from the host for the whole list (the same kernels and bits).
     """
 
-    def __init__(self, calls):
+    def __init__(self, calls, graph: bool = False):
         torch = _torch()
         calls = list(calls)
         self._lib = load()
+        self._use_graph = bool(graph)
+        self._graph = None
         self._arr = (MatmulCall * max(1, len(calls)))()
         self._keep = []
         self.outs = []
@@ -392,14 +398,35 @@ class MatmulBatch:
         self._scratch = (torch.empty(need, dtype=torch.uint8, device=calls[0]["x"].device)
                          if need else None)
 
-    def run(self):
-        if self._count == 0:
-            return self.outs
+    def _enqueue(self):
         with _on_device(self._keep[0][0]):
             sp = self._scratch
             _check(self._lib, self._lib.q2k_matmul_ex_batch(
                 self._arr, self._count, sp.data_ptr() if sp is not None else None,
                 sp.numel() if sp is not None else 0, _stream_handle(self._keep[0][0])))
+
+    def run(self):
+        if self._count == 0:
+            return self.outs
+        if not self._use_graph:
+            self._enqueue()
+            return self.outs
+        if self._graph is not None:
+            with _on_device(self._keep[0][0]):
+                self._graph.replay()
+            return self.outs
+        torch = _torch()
+        self._enqueue()  # this run; the graph serves the next ones
+        dev = self._keep[0][0].device
+        with _on_device(self._keep[0][0]):
+            cur = torch.cuda.current_stream(dev)
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(cur)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                self._enqueue()
+            cur.wait_stream(side)
+        self._graph = g
         return self.outs
 
 

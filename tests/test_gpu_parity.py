@@ -475,3 +475,29 @@ def test_bounded_wait_times_out_and_reports_without_fault():
     y = q2k.matmul(dev(x), dev(w), 256)
     yref, s = oracle.matmul(x, w, 256)
     assert_close(y.cpu().numpy().astype(np.float64), yref, s, TOL_GEMV, "after time-out")
+
+
+def test_matmul_batch_graph_replays_the_same_bits():
+    """MatmulBatch(graph=True): the first run enqueues and captures, later runs
+    replay the graph; every run gives the bits of the plain batch."""
+    rng = np.random.default_rng(77)
+    k, n = 1024, 384
+    x = dev(wl.random_activations(rng, 1, k))
+    ws = [dev(wl.random_blocks(rng, n * (k // 256)).reshape(-1)) for _ in range(3)]
+    plain = q2k.MatmulBatch([dict(x=x, w=w, n=n, independent=True) for w in ws])
+    graphed = q2k.MatmulBatch([dict(x=x, w=w, n=n, independent=True) for w in ws], graph=True)
+    want = [o.clone() for o in plain.run()]
+    for _ in range(3):
+        for o in graphed.outs:
+            o.fill_(float("nan"))
+        got = graphed.run()
+        torch.cuda.synchronize()
+        for a, b in zip(got, want):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    # contents updated in place are picked up by the replay
+    x.mul_(2.0)
+    want2 = [o.clone() for o in plain.run()]
+    got2 = graphed.run()
+    torch.cuda.synchronize()
+    for a, b in zip(got2, want2):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
