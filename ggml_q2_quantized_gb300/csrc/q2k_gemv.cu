@@ -50,6 +50,13 @@ constexpr int kM1MaxSlices = 256;  // k <= 16384
 // (up to four at 116 registers a thread).
 constexpr int kM1ThreadsDependent = 256;
 constexpr int kM1ThreadsIndependent = 128;
+// Independent calls with more than 128 slices (k > 8192): one CTA's chunk and
+// x planes fill an SM's shared memory, so the CTA takes two groups of warps
+// over the slices (twice the warps to hide latencies with).
+inline int m1_independent_threads(int K) {
+    const int slices = K / 64;
+    return slices > 128 ? 2 * ((slices + 31) / 32 * 32) : kM1ThreadsIndependent;
+}
 
 // ------------------------------------------------------------------ m = 1
 
@@ -351,7 +358,7 @@ __device__ __forceinline__ bool dot_rows(const uint8_t* my_col, size_t row_bytes
     return ok;
 }
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(512, 1)
 gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
                int N, int K, int rows_per_cta, int slices_pad, int groups, uint32_t flags,
                GemvProblems pr, const uint8_t* __restrict__ xplanes, uint32_t xplanes_stride) {
@@ -717,7 +724,7 @@ cudaError_t launch_gemv_problems(const float* x, const uint8_t* w, float* y, int
     // problem.  (Only the K slicing decides the arithmetic of a row, so the
     // plan never changes a result bit.)
     const bool small_ctas = (flags & kGemvIndependent) != 0 || n_problems > 1;
-    const int threads = small_ctas ? kM1ThreadsIndependent : kM1ThreadsDependent;
+    const int threads = small_ctas ? m1_independent_threads(K) : kM1ThreadsDependent;
     if (M == 1 && plan_m1(N, K, sm_count, threads, small_ctas, &plan))
         return launch_m1(x, w, y, N, K, plan, device, flags, pr, n_problems, xplanes,
                          xplanes_stride, stream);
