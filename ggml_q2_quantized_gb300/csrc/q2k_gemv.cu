@@ -358,7 +358,10 @@ __device__ __forceinline__ bool dot_rows(const uint8_t* my_col, size_t row_bytes
     return ok;
 }
 
-__global__ void __launch_bounds__(512, 1)
+// kMaxThreads: 256 for every plan but the two-group CTAs of large k (512); the
+// smaller bound leaves the compiler more registers a thread.
+template <int kMaxThreads>
+__global__ void __launch_bounds__(kMaxThreads, 1)
 gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
                int N, int K, int rows_per_cta, int slices_pad, int groups, uint32_t flags,
                GemvProblems pr, const uint8_t* __restrict__ xplanes, uint32_t xplanes_stride) {
@@ -579,9 +582,12 @@ cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, 
     static bool smem_set[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!smem_set[device]) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel,
+        cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel<256>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              227 * 1024);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemv_m1_kernel<512>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         smem_set[device] = true;
     }
@@ -595,8 +601,11 @@ cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_m1_kernel, x, w, y, N, K, p.rows_per_cta, p.slices_pad,
-                              p.groups, flags, pr, xplanes, xplanes_stride);
+    if (p.threads > 256)
+        return cudaLaunchKernelEx(&cfg, gemv_m1_kernel<512>, x, w, y, N, K, p.rows_per_cta,
+                                  p.slices_pad, p.groups, flags, pr, xplanes, xplanes_stride);
+    return cudaLaunchKernelEx(&cfg, gemv_m1_kernel<256>, x, w, y, N, K, p.rows_per_cta,
+                              p.slices_pad, p.groups, flags, pr, xplanes, xplanes_stride);
 }
 
 // ------------------------------------------------------------------ general m
