@@ -335,3 +335,18 @@ def test_x_planes_scratch_size_and_checks(lib):
     assert "scratch" in lib.q2k_last_error().decode()
     assert lib.q2k_matmul_batched_mv(*args, 0x2000008, need, None) == INVALID
     assert lib.q2k_matmul_batched_mv(*args, x, need, None) == INVALID    # over x
+
+
+def test_python_matmul_id_workspace_bytes_matches_the_library(lib):
+    """The binding's workspace query is the library's (geometry only, no device)."""
+    for n_tokens, top_k, n, k, experts in [(512, 8, 2048, 7168, 64), (33, 6, 8, 256, 8),
+                                           (40, 2, 136, 1024, 4096)]:
+        p = q2k.MatmulIdParams(n_tokens, top_k, n, k, experts, 10, n * (k // 256) * 84)
+        for path in ("auto", "gemv", "tensor"):
+            for slotted in (False, True):
+                code = {"auto": q2k.PATH_AUTO, "gemv": q2k.PATH_GEMV, "tensor": q2k.PATH_TENSOR}[path]
+                want = lib.q2k_matmul_id_workspace_bytes(code, q2k.ID_SLOTTED if slotted else 0,
+                                                         ctypes.byref(p))
+                got = q2k.matmul_id_workspace_bytes(n_tokens, top_k, n, k, experts, path=path,
+                                                    slotted=slotted)
+                assert got == want
