@@ -216,7 +216,7 @@ def capture(torch, stream, fn):
 
 
 def bench_matmul(torch, q2k, w: wl.Workload, steps, warmup, l2_bytes, device, with_e2e=False,
-                 path="auto", independent=False):
+                 path="auto", independent=False, workspace="auto"):
     """Time a stack of distinct weight matrices of workload ``w`` (one launch each),
     all applied to the same x (independent projections when ``independent``)."""
     inp = wl.make_inputs(w, with_gather=False)
@@ -231,7 +231,8 @@ def bench_matmul(torch, q2k, w: wl.Workload, steps, warmup, l2_bytes, device, wi
             q2k.matmul(x, ws[l], w.n, out=ys[l], path=path, independent=independent)
 
     batch_all = q2k.MatmulBatch([dict(x=x, w=ws[l], n=w.n, out=ys[l], path=path,
-                                      independent=independent) for l in range(layers)])
+                                      independent=independent, workspace=workspace)
+                                 for l in range(layers)])
     g = capture(torch, stream, batch_all.run)
     ms = time_graph(torch, g, stream, steps, warmup)
     res = {"layers": layers, "ms_per_step": ms, "us_per_call": ms * 1e3 / layers,
@@ -432,6 +433,20 @@ def cpu_baseline(w: wl.Workload, budget_s: float = 12.0):
 
 # --------------------------------------------------------------------------- arms
 
+def headline_parity(w: wl.Workload, inp, y) -> dict:
+    """The headline launch's y (layer 0: the workload's seeded matrix and x)
+    against the oracle, |y - y_ref| / S per output (part of the CPU-baseline
+    leg, the one place besides the tests that runs the oracle)."""
+    import oracle
+    yref, s = oracle.matmul(inp.x, inp.w, w.n, threads=os.cpu_count() or 1)
+    err = np.abs(y.astype(np.float64) - yref)
+    tol = 1e-5 if w.m <= 8 else 8e-3
+    ratio = np.where(s > 0, err / np.maximum(s, 1e-300), 0.0)
+    return {"max_err_over_S": float(ratio.max()), "tolerance_over_S": tol,
+            "within_tolerance": bool((err <= tol * s).all()),
+            "outputs": int(y.size), "reference": "CPU oracle (f64 sum of the page's f32 weights)"}
+
+
 def run_reference(args):
     world, rank, _ = dist_setup()
     w = wl.by_name(args.workload)
@@ -511,22 +526,42 @@ def run_ours(args):
     for _ in range(warmup):
         graph.replay()
     barrier()
+    # The timed region: `steps` steps, timed with CUDA events on the replay
+    # stream, repeated back to back until the repeats cover >= 1 s (so the
+    # clock sampler sees the load); the median repeat is reported.
+    probe_s = torch.cuda.Event(enable_timing=True)
+    probe_e = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        probe_s.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        probe_e.record(stream)
+    probe_e.synchronize()
+    repeats = max(1, min(2000, math.ceil(1000.0 / max(probe_s.elapsed_time(probe_e), 1e-3))))
+    if world > 1:
+        t = torch.tensor([repeats], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        repeats = int(t.item())
+    barrier()
     with ClockSampler(device.index) as clk:
         barrier()
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(repeats)]
         with torch.cuda.stream(stream):
-            start.record(stream)
-            for _ in range(steps):
-                graph.replay()
-            end.record(stream)
-        end.synchronize()
+            for start, end in evs:
+                start.record(stream)
+                for _ in range(steps):
+                    graph.replay()
+                end.record(stream)
+        evs[-1][1].synchronize()
         barrier()
-    ms = start.elapsed_time(end) / steps
+    per_repeat = [a.elapsed_time(b) / steps for a, b in evs]
+    ms = statistics.median(per_repeat)
     if world > 1:
         t = torch.tensor([ms], device=device)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
+    y_check = ys[0].cpu().numpy()   # layer 0: the workload's own matrix and x
     assert q2k.device_error() == 0
     bytes_per_step = layers * w.weight_bytes
     value = world * bytes_per_step / (ms * 1e-3) / 1e9
@@ -546,7 +581,10 @@ def run_ours(args):
                    "l2_policy": f"inputs larger than L2: {layers} distinct weight matrices "
                                 f"({bytes_per_step / 2**20:.0f} MiB) per step vs "
                                 f"{l2_bytes / 2**20:.0f} MiB L2",
-                   "timing": "CUDA graph of the step's launches, CUDA events on the replay stream",
+                   "timing": (f"CUDA graph of the step's launches, CUDA events on the replay "
+                              f"stream; {repeats} back-to-back repeats of the {steps} timed steps, "
+                              f"median repeat reported (spread {min(per_repeat):.4f}-"
+                              f"{max(per_repeat):.4f} ms per step)"),
                    "calls": ("independent projections of one x (Q2K_FLAG_INDEPENDENT) enqueued as "
                              "one q2k.MatmulBatch: x converted once per step" if indep
                              else "one launch per matrix"),
@@ -558,7 +596,7 @@ def run_ours(args):
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
                      "algorithmic_bytes_per_launch": algo_bytes,
-                     "kernel": "q2k gemv_kernel<1>" if w.m == 1 else f"q2k {kernel_key}",
+                     "kernel": "q2k gemv_m1_kernel" if w.m == 1 else f"q2k {kernel_key}",
                      "frac_of_nominal_8TBps": achieved / 8000.0},
     }
     if traffic_note:
@@ -599,6 +637,16 @@ def run_ours(args):
                 entry["frac_bf16_measured"] = entry["TFLOPs"] / peaks["bf16_tflops"]
                 entry["frac_bf16_nominal_2250"] = entry["TFLOPs"] / 2250.0
             sec[name] = entry
+        # the M=512 workload through the plain q2k_matmul call (no workspace: the
+        # tensor-core kernel converts x itself)
+        sw = wl.by_name("prefill_m512")
+        r = bench_matmul(torch, q2k, sw, max(3, steps // 4), 3, l2_bytes, device, workspace=None)
+        us = r["us_per_call"]
+        sec["prefill_m512_plain_c_call"] = {
+            "us_per_call": us, "TFLOPs": sw.flops / (us * 1e-6) / 1e12,
+            "frac_bf16_measured": sw.flops / (us * 1e-6) / 1e12 / peaks["bf16_tflops"],
+            "m": sw.m, "n": sw.n, "k": sw.k, "path": "tensor, no workspace (q2k_matmul)",
+            "matrices_per_step": r["layers"]}
         # the M=16 workload through the fp32 GEMV path as well (forced)
         sw = wl.by_name("spec_verify_m16")
         r = bench_matmul(torch, q2k, sw, max(3, steps // 4), 3, l2_bytes, device, path="gemv")
@@ -627,6 +675,7 @@ def run_ours(args):
 
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
+        line["parity"] = headline_parity(w, inp, y_check)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -12,6 +12,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "q2k.h"
@@ -79,6 +80,90 @@ q2k_status current_device(DeviceInfo* info) {
                     dev, cc_cache[dev] / 10, cc_cache[dev] % 10);
     info->device = dev;
     info->sm_count = sm_cache[dev];
+    return Q2K_OK;
+}
+
+// ---- bad ids reported as a status (bad_id_count == NULL) --------------------
+//
+// The pages' gather and routed calls fail with an error for an id out of
+// range.  Ids live on the device here, so the kernel counts them; a caller
+// that passes no counter of its own gets the count in one of these words,
+// read back (4 bytes) and waited for before the call returns
+// Q2K_ERR_BAD_ID or Q2K_OK.  Each call in flight holds its own word.
+constexpr int kStatusWords = 64;
+__device__ unsigned int g_status_words[kStatusWords];
+
+struct StatusWords {
+    std::mutex mu;
+    unsigned int* base[64] = {};  // device address of g_status_words, per device
+    uint64_t used[64] = {};       // words held by calls in flight, per device
+};
+
+StatusWords& status_words() {
+    static StatusWords s;
+    return s;
+}
+
+// A free status word on `device` (current), zeroed on `stream`.
+q2k_status acquire_status_word(int device, cudaStream_t stream, unsigned int** word, int* slot) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone)
+        return fail(Q2K_ERR_INVALID_ARGUMENT,
+                    "bad_id_count is required while the stream is being captured (without it the "
+                    "call waits for its own result)");
+    StatusWords& s = status_words();
+    {
+        std::lock_guard<std::mutex> lk(s.mu);
+        if (s.base[device] == nullptr) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_status_words);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status words)");
+            s.base[device] = static_cast<unsigned int*>(p);
+        }
+        *slot = -1;
+        for (int i = 0; i < kStatusWords; ++i)
+            if (((s.used[device] >> i) & 1u) == 0) {
+                s.used[device] |= uint64_t(1) << i;
+                *slot = i;
+                break;
+            }
+        if (*slot < 0)
+            return fail(Q2K_ERR_INVALID_ARGUMENT,
+                        "more than %d calls without bad_id_count in flight on device %d",
+                        kStatusWords, device);
+        *word = s.base[device] + *slot;
+    }
+    e = cudaMemsetAsync(*word, 0, 4, stream);
+    if (e != cudaSuccess) {
+        std::lock_guard<std::mutex> lk(s.mu);
+        s.used[device] &= ~(uint64_t(1) << *slot);
+        return cuda_fail(e, "clearing the bad-id status word");
+    }
+    return Q2K_OK;
+}
+
+// Read the word back after the call's kernels (waits for `stream`), free it,
+// and turn a nonzero count into Q2K_ERR_BAD_ID.  `launched` is the launch
+// status: on failure the word is freed once the stream has drained.
+q2k_status finish_status_word(int device, int slot, unsigned int* word, cudaStream_t stream,
+                              cudaError_t launched, const char* what, const char* limit_name,
+                              uint32_t limit) {
+    unsigned int count = 0;
+    cudaError_t e = launched;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&count, word, 4, cudaMemcpyDeviceToHost, stream);
+    const cudaError_t sync = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) e = sync;
+    {
+        StatusWords& s = status_words();
+        std::lock_guard<std::mutex> lk(s.mu);
+        s.used[device] &= ~(uint64_t(1) << slot);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    if (count != 0)
+        return fail(Q2K_ERR_BAD_ID, "%u id(s) out of range (>= %s = %u); their rows are zeros",
+                    count, limit_name, limit);
     return Q2K_OK;
 }
 
@@ -207,9 +292,19 @@ q2k_status q2k_embedding_gather(const void* table, size_t table_bytes, const uin
     DeviceInfo dev;
     q2k_status st = current_device(&dev);
     if (st != Q2K_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned int* word = nullptr;
+    int slot = -1;
+    if (bad_id_count == nullptr) {
+        st = acquire_status_word(dev.device, s, &word, &slot);
+        if (st != Q2K_OK) return st;
+    }
     cudaError_t e = q2k::launch_gather(static_cast<const uint8_t*>(table), ids, out, p->vocab_size,
-                                       p->embed_dim, p->n_tokens, bad_id_count, dev.sm_count,
-                                       reinterpret_cast<cudaStream_t>(stream));
+                                       p->embed_dim, p->n_tokens,
+                                       bad_id_count != nullptr ? bad_id_count : word, dev.sm_count, s);
+    if (word != nullptr)
+        return finish_status_word(dev.device, slot, word, s, e, "q2k_embedding_gather",
+                                  "vocab_size", p->vocab_size);
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, "q2k_embedding_gather launch");
 }
 
@@ -602,16 +697,26 @@ q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void*
         q2k_status st = current_device(&dev);
         if (st != Q2K_OK) return st;
         const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        unsigned int* word = nullptr;
+        int slot = -1;
         cudaError_t e = cudaSuccess;
-        if (bad_id_count != nullptr) e = cudaMemsetAsync(bad_id_count, 0, 4, s);
+        if (bad_id_count != nullptr) {
+            e = cudaMemsetAsync(bad_id_count, 0, 4, s);
+        } else {
+            st = acquire_status_word(dev.device, s, &word, &slot);
+            if (st != Q2K_OK) return st;
+        }
         if (e == cudaSuccess)
             e = q2k::launch_gemm_tc_routed(x, static_cast<const uint8_t*>(wa),
                                            static_cast<long long>(p->expert_stride), ids, ya,
                                            int(routes), slotted ? 1 : int(p->top_k), int(p->n_experts),
-                                           int(p->n), int(p->k), bad_id_count, dev.device,
+                                           int(p->n), int(p->k),
+                                           bad_id_count != nullptr ? bad_id_count : word, dev.device,
                                            dev.sm_count, scratch, s,
                                            pair ? static_cast<const uint8_t*>(wb) : nullptr,
                                            pair ? yb : nullptr);
+        if (word != nullptr)
+            return finish_status_word(dev.device, slot, word, s, e, what, "n_experts", p->n_experts);
         return e == cudaSuccess ? Q2K_OK : cuda_fail(e, what);
     }
     uint8_t* planes = nullptr;
@@ -629,15 +734,22 @@ q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void*
     if (st != Q2K_OK) return st;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
-    if (bad_id_count != nullptr) e = cudaMemsetAsync(bad_id_count, 0, 4, s);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing bad_id_count");
+    unsigned int* word = nullptr;
+    int slot = -1;
+    if (bad_id_count != nullptr) {
+        e = cudaMemsetAsync(bad_id_count, 0, 4, s);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing bad_id_count");
+    } else {
+        st = acquire_status_word(dev.device, s, &word, &slot);
+        if (st != Q2K_OK) return st;
+    }
     q2k::GemvProblems pr;
     pr.w_stride = static_cast<long long>(p->expert_stride);
     pr.y_stride = static_cast<long long>(p->n);
     pr.ids = ids;
     pr.n_experts = p->n_experts;
     pr.top_k = slotted ? 1u : p->top_k;  // x row of route r: r / top_k, or r itself
-    pr.bad_ids = bad_id_count;
+    pr.bad_ids = bad_id_count != nullptr ? bad_id_count : word;
     if (pair) {
         pr.second_from = static_cast<int>(routes);
         pr.w2 = static_cast<const uint8_t*>(wb);
@@ -648,6 +760,8 @@ q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void*
         e = q2k::launch_gemv_problems(x, static_cast<const uint8_t*>(wa), ya, 1, int(p->n), int(p->k),
                                       dev.device, dev.sm_count, 0u, pr, int(pair ? 2 * routes : routes),
                                       s, planes, planes ? uint32_t(q2k::gemv_planes_stride(int(p->k))) : 0u);
+    if (word != nullptr)
+        return finish_status_word(dev.device, slot, word, s, e, what, "n_experts", p->n_experts);
     return e == cudaSuccess ? Q2K_OK : cuda_fail(e, what);
 }
 

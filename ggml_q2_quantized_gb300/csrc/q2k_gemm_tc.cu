@@ -1779,16 +1779,23 @@ cudaError_t launch_gemm_tc_static(const float* x, const uint8_t* w, float* y, in
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (gemm_tc_workspace_bytes(M, N, K) > kStaticWorkspaceBytes) return cudaErrorInvalidValue;
     // In host code the array's name is only a stand-in: its device address is
-    // looked up once per device, with that device current (the caller's).
-    static std::once_flag once[64];
+    // looked up per device, with that device current (the caller's), and kept
+    // once a lookup has succeeded; a failed lookup is retried by the next call.
+    static std::mutex mu;
     static void* addr[64] = {};
-    static cudaError_t status[64] = {};
-    std::call_once(once[device], [device]() {
-        status[device] = cudaGetSymbolAddress(&addr[device], g_static_x_image);
-    });
-    if (status[device] != cudaSuccess) return status[device];
-    if (addr[device] == nullptr) return cudaErrorInvalidSymbol;
-    return launch_gemm_tc(x, w, y, M, N, K, device, sm_count, addr[device], stream);
+    void* image = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (addr[device] == nullptr) {
+            void* p = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&p, g_static_x_image);
+            if (e != cudaSuccess) return e;
+            if (p == nullptr) return cudaErrorInvalidSymbol;
+            addr[device] = p;
+        }
+        image = addr[device];
+    }
+    return launch_gemm_tc(x, w, y, M, N, K, device, sm_count, image, stream);
 }
 
 cudaError_t read_and_clear_tc_error(uint32_t* out, cudaStream_t stream) {

@@ -3,7 +3,11 @@
 // mlx-native page "tests/deepseek_q2_k.rs", fn run_dense: the decode path the
 // pages test at m <= 8 with an f32 tolerance (2e-4 absolute at n = 8, k = 256).
 //
-// Two kernels:
+// Both kernels form every weight exactly as the page's f32 decode does
+// (dl*q - ml with one rounding, the value fn reference_dequant returns) and
+// multiply-accumulate it with x in fp32 along accumulation chains of bounded
+// length L, so |y - sum_k x w| <= L 2^-24 sum_k |x w| (+ the f32 underflow
+// range) for every finite x and W: no rounding of x, no factored dl / ml terms.
 //
 // gemv_m1_kernel (m = 1, k <= 16384, 4-byte aligned W): one CTA owns a
 //   contiguous chunk of weight rows.  Its bytes are prefetched into L2 before
@@ -12,24 +16,54 @@
 //   copied into shared memory by bulk asynchronous copies, eight rows per
 //   mbarrier so decoding starts as soon as the first rows land.  Every thread
 //   owns one 64-weight slice of K - one (block, half, segment): 16 quant bytes
-//   read at the four shifts - and keeps the slice of x in registers for all
-//   rows of the chunk.  Per row it forms the four 16-weight sums
-//   S_j = sum_l x_l q_l and adds dl_j S_j - ml_j X_j (X_j = sum_l x_l, fixed per
-//   thread).  Partial sums meet in a fixed-order butterfly of warp shuffles and
-//   a fixed-order sum over warps, so results are bit-reproducible.
-//   kVariant selects how S_j is formed:
-//     0  q to float through a byte permute into the bits of 1 + q/4, then the
-//        bias removed exactly (packed f32 add) and packed f32 FMAs;
-//     1  q to float by integer conversion, packed f32 FMAs;
-//     2  exact integer dot products (dp4a) of q with three byte planes of x
-//        scaled to 23-bit integers per slice (|x| max -> 2^21..2^22).
+//   read at the four shifts - and keeps that slice of x in registers (scaled by
+//   a power of two) for all rows of the chunk.  Per row and slice:
+//     - the 2-bit code of (lane, shift) is masked in place out of its quant word
+//       and read as the bits of a float: q 2^(s - 149), s = its bit position
+//       (a subnormal, or the smallest normals, exact);
+//     - one packed fp32 FMA per two weights gives w 2^-42 = fl(q 2^(s-149) *
+//       dl 2^(107 - s) - ml 2^-42): the product is exact, so this is the
+//       page's dl*q - ml rounded once, scaled by 2^-42 (no overflow: dl < 2^20);
+//     - one packed FMA per two weights accumulates x 2^t * w 2^-42, and the
+//       slice's sum is scaled back by 2^(42 - t).
+//   Slice sums meet in a fixed-order butterfly of warp shuffles and a
+//   fixed-order sum over warps, so results are bit-reproducible and do not
+//   depend on the launch plan.
 //
 // gemv_rows_kernel (any m <= 8 per launch slice, any k): one warp per weight
-//   row, eight lanes per 84-byte block, x read through the read-only cache.
+//   row, eight lanes per 84-byte block, x read through the read-only cache;
+//   per-block sums added in a fixed three-level hierarchy (bounded chains).
 #include <cuda_runtime.h>
 
 #include "q2k_device.cuh"
 #include "q2k_internal.h"
+
+// Tuning knobs (compile-time; ROWS and MINB change no bits, ACCS changes the
+// order of a slice's sum and so its rounding, within the same bound):
+//   Q2K_GEMV_ROWS  rows decoded together and reduced by one transposed butterfly (2 or 4)
+//   Q2K_GEMV_ACCS  independent accumulator pairs per row and slice (1, 2 or 4)
+//   Q2K_GEMV_MINB  CTAs per SM the 128-thread plan is compiled for (register cap)
+#ifndef Q2K_GEMV_ROWS
+#define Q2K_GEMV_ROWS 4
+#endif
+#ifndef Q2K_GEMV_ACCS
+#define Q2K_GEMV_ACCS 1
+#endif
+#ifndef Q2K_GEMV_MINB
+#define Q2K_GEMV_MINB 4
+#endif
+//   Q2K_GEMV_W2 / Q2K_GEMV_DOT2  form the weights / the dot with packed (1) or
+//                  scalar (0) fp32 FMAs (same arithmetic, same bits)
+#ifndef Q2K_GEMV_W2
+#define Q2K_GEMV_W2 0
+#endif
+#ifndef Q2K_GEMV_DOT2
+#define Q2K_GEMV_DOT2 1
+#endif
+//   Q2K_GEMV_DEP_THREADS  threads per CTA of dependent calls (256 or 512)
+#ifndef Q2K_GEMV_DEP_THREADS
+#define Q2K_GEMV_DEP_THREADS 256
+#endif
 
 namespace q2k {
 
@@ -46,12 +80,11 @@ constexpr int kPieceRows = 8;
 constexpr int kM1MaxSlices = 256;  // k <= 16384
 // Threads per CTA of the m = 1 kernel.  A dependent call runs alone once its
 // predecessor completes, so it takes more threads per CTA (shorter critical
-// path); independent calls overlap, so smaller CTAs let more calls share an SM
-// (up to four at 116 registers a thread).
-constexpr int kM1ThreadsDependent = 256;
+// path); independent calls overlap, so smaller CTAs let more calls share an SM.
+constexpr int kM1ThreadsDependent = Q2K_GEMV_DEP_THREADS;
 constexpr int kM1ThreadsIndependent = 128;
-// Independent calls with more than 128 slices (k > 8192): one CTA's chunk and
-// x planes fill an SM's shared memory, so the CTA takes two groups of warps
+// Independent calls with more than 128 slices (k > 8192): one CTA's chunk
+// fills much of an SM's shared memory, so the CTA takes two groups of warps
 // over the slices (twice the warps to hide latencies with).
 inline int m1_independent_threads(int K) {
     const int slices = K / 64;
@@ -60,106 +93,81 @@ inline int m1_independent_threads(int K) {
 
 // ------------------------------------------------------------------ m = 1
 
-constexpr int kRowBatch = 4;  // rows reduced together by one transposed butterfly
+constexpr int kRowBatch = Q2K_GEMV_ROWS;
+static_assert(kRowBatch == 2 || kRowBatch == 4, "Q2K_GEMV_ROWS must be 2 or 4");
+constexpr int kAccs = Q2K_GEMV_ACCS;
+static_assert(kAccs == 1 || kAccs == 2 || kAccs == 4, "Q2K_GEMV_ACCS must be 1, 2 or 4");
+constexpr int kWScaleLog2 = 42;  // the row loop forms w 2^-42
 
-// x as integers: each 16-weight run r (k = 16 r .. 16 r + 15, one (half,
-// shift, segment) of a block) is scaled by 2^e_r so that its largest |x| lies
-// in [2^18, 2^19), rounded to nearest (relative error <= 2^-19 of the run's
-// largest |x|), and split into byte planes x_int = p2 * 65536 + p1 * 256 + p0
-// (p2 signed, p1/p0 unsigned).  19 bits keep every integer product of the
-// dot below 2^31 (16 * 12 * 15 * 2^19 < 2^31), so the scale multiplies stay
-// in integers.  The plane words of a run are 4 consecutive weights each.
-// Also kept per run: the f32 sum of its 16 x (for the -ml term) and 2^-e_r.
-struct RunPlanes {
-    uint32_t p0[4], p1[4], p2[4];
+// One thread's 64-weight slice of x (block b, half h, segment seg: weights
+// k = 256 b + 128 h + 32 j + 16 seg + l, l = 0..15, j = 0..3), scaled by 2^t.
+// Pair P = ((i * 2 + src) * 2 + a) * 2 + jp holds lane l = 4 i + 2 src + a at
+// shifts j = 2 jp and 2 jp + 1 - the order in which slice_dot reads the
+// lanes out of quant word i (src 1: the word shifted down by 16).
+// t = min(42, 252 - biased exponent of the slice's largest |x|): every scaled
+// |x| stays below 2^126, and the products x 2^t * w 2^-42 are x w scaled by
+// 2^(t - 42), exactly 1 unless some |x| of the slice is 2^84 or more.
+struct SliceX {
+    float2 v[32];
+    float rescale;  // 2^(42 - t): back from the slice's scale to x w
 };
 
-// Shared-memory home of the planes: the 4 runs of slice sl (its 48 words,
-// run j's planes at 12 j) start at word kSlicePitch * sl; the odd pitch puts
-// the 32 slices a warp reads at once in 32 different banks.
-constexpr int kSlicePitch = 49;
+constexpr size_t kSliceXBytes = 64 * 4;  // the 64 scaled x of a slice, in pair order
 
-__device__ __forceinline__ void convert_run(const float* __restrict__ xr, uint32_t* planes,
-                                            float* run_sum, float* run_inv) {
-    float v[16];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float4 t = __ldg(reinterpret_cast<const float4*>(xr + 4 * q));
-        v[4 * q] = t.x;
-        v[4 * q + 1] = t.y;
-        v[4 * q + 2] = t.z;
-        v[4 * q + 3] = t.w;
-    }
-    float mx = 0.f, sum = 0.f;
-#pragma unroll
-    for (int l = 0; l < 16; ++l) {
-        mx = fmaxf(mx, fabsf(v[l]));
-        sum += v[l];
-    }
-    // e = 18 - floor(log2 max|x|), kept within the normal range; for max|x| = 0
-    // (or a subnormal max) any e gives zeros, so e = 0 then.
-    const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu);  // biased exponent
-    int e = (ex == 0 || ex == 255) ? 0 : 145 - ex;                            // 18 - (ex - 127)
-    e = max(-126, min(126, e));
-    const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);   // 2^e, exact
-    RunPlanes pl;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t b0 = 0, b1 = 0, b2 = 0;
-#pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) {
-            // |x 2^e| < 2^19: adding 1.5 * 2^23 rounds it to an integer (nearest,
-            // ties to even) held in the low mantissa bits.
-            const float biased = fmaf(v[4 * q + e4], up, 12582912.f);
-            const uint32_t xi = __float_as_uint(biased) - 0x4B400000u;  // two's complement
-            b0 |= (xi & 0xFFu) << (8 * e4);
-            b1 |= ((xi >> 8) & 0xFFu) << (8 * e4);
-            b2 |= ((xi >> 16) & 0xFFu) << (8 * e4);
-        }
-        pl.p0[q] = b0;
-        pl.p1[q] = b1;
-        pl.p2[q] = b2;
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        planes[q] = pl.p0[q];
-        planes[4 + q] = pl.p1[q];
-        planes[8 + q] = pl.p2[q];
-    }
-    *run_sum = sum;
-    *run_inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
-}
-
-struct SlicePlanes {
-    RunPlanes r[4];  // shift j = 0..3
-    float inv[4];    // 2^-e of the run, times 1/4 for odd j (see slice_dot)
-    // The four run sums X_j as integers with one scale 2^eX for the slice
-    // (largest |X_j| in [2^21, 2^22)), byte j of each word = run j's byte.
-    uint32_t xq0, xq1, xq2;
-    float xinv;      // 2^-eX
-};
-
-// X_j -> the slice's integer byte planes (same rounding as convert_run).
-__device__ __forceinline__ void quantize_run_sums(const float (&X)[4], SlicePlanes& s) {
+__device__ __forceinline__ void scale_slice(const float (&v)[4][16], SliceX& s) {
     float mx = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(X[j]));
-    const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu);
-    int e = (ex == 0 || ex == 255) ? 0 : 148 - ex;  // 21 - (ex - 127)
-    e = max(-126, min(126, e));
-    const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
-    uint32_t b0 = 0, b1 = 0, b2 = 0;
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t xi = __float_as_uint(fmaf(X[j], up, 12582912.f)) - 0x4B400000u;
-        b0 |= (xi & 0xFFu) << (8 * j);
-        b1 |= ((xi >> 8) & 0xFFu) << (8 * j);
-        b2 |= ((xi >> 16) & 0xFFu) << (8 * j);
+        for (int l = 0; l < 16; ++l) mx = fmaxf(mx, fabsf(v[j][l]));
+    const int eb = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu);
+    const int t = min(kWScaleLog2, 252 - eb);
+    const float up = __uint_as_float(static_cast<uint32_t>(127 + t) << 23);  // 2^t, exact
+    s.rescale = __uint_as_float(static_cast<uint32_t>(127 + kWScaleLog2 - t) << 23);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int src = 0; src < 2; ++src)
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int jp = 0; jp < 2; ++jp) {
+                    const int l = 4 * i + 2 * src + a;
+                    s.v[((i * 2 + src) * 2 + a) * 2 + jp] =
+                        make_float2(v[2 * jp][l] * up, v[2 * jp + 1][l] * up);
+                }
+}
+
+// The slice of x row `x` (K floats, 16-byte aligned) for (b, h, seg).
+__device__ __forceinline__ void load_slice_x(const float* __restrict__ x, int b, int h, int seg,
+                                             SliceX& s) {
+    const float* base = x + 256 * b + 128 * h + 16 * seg;
+    float v[4][16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 t = __ldg(reinterpret_cast<const float4*>(base + 32 * j + 4 * q));
+            v[j][4 * q] = t.x;
+            v[j][4 * q + 1] = t.y;
+            v[j][4 * q + 2] = t.z;
+            v[j][4 * q + 3] = t.w;
+        }
+    scale_slice(v, s);
+}
+
+// Prepared x (prep_x_kernel): slice sl's pairs at sl * 256 bytes, the rescale
+// factors of all S slices after the S slices.
+__device__ __forceinline__ void load_slice_prepared(const uint8_t* __restrict__ xp, int S, int sl,
+                                                    SliceX& s) {
+    const float4* p = reinterpret_cast<const float4*>(xp + static_cast<size_t>(sl) * kSliceXBytes);
+#pragma unroll
+    for (int v = 0; v < 16; ++v) {
+        const float4 t = __ldg(p + v);
+        s.v[2 * v] = make_float2(t.x, t.y);
+        s.v[2 * v + 1] = make_float2(t.z, t.w);
     }
-    s.xq0 = b0;
-    s.xq1 = b1;
-    s.xq2 = b2;
-    s.xinv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    s.rescale = __ldg(reinterpret_cast<const float*>(xp + static_cast<size_t>(S) * kSliceXBytes) + sl);
 }
 
 // The 7 words of one weight row a thread needs: its 16 quant bytes, the four
@@ -181,63 +189,109 @@ __device__ __forceinline__ RowWords load_row_words(const uint8_t* __restrict__ r
     return r;
 }
 
-// Partial dot product of one weight row with this thread's 64-weight slice:
-// d sum_j sc_j 2^-e_j S_j - dmin sum_j m_j X_j with S_j = sum_l q_l x_int_l.
-// The 2-bit codes of shift j sit at bits 2 j of each quant byte; the odd
-// shifts are masked in place (the code times 4, no shift needed) and s.inv
-// carries the compensating 1/4.  sc_j S_j is formed in integers (below 2^31,
-// see convert_run) and the min term is one integer dot of the four 4-bit
-// mins with the slice's quantized run sums.
-__device__ __forceinline__ float slice_dot(const RowWords& r, const SlicePlanes& s) {
-    const uint32_t lo = r.sc4 & 0x0F0F0F0Fu;
-    const uint32_t hi = (r.sc4 >> 4) & 0x0F0F0F0Fu;
-    uint32_t q4[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) q4[i] = r.q[i] >> 4;
-    float acc = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t mask = (j & 1) ? 0x0C0C0C0Cu : 0x03030303u;
-        int a2 = 0;
-        unsigned a1 = 0, a0 = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t t = (j < 2 ? r.q[i] : q4[i]) & mask;
-            a2 = __dp4a(static_cast<int>(s.r[j].p2[i]), static_cast<int>(t), a2);
-            a1 = __dp4a(s.r[j].p1[i], t, a1);
-            a0 = __dp4a(s.r[j].p0[i], t, a0);
-        }
-        const int sint = a2 * 65536 + static_cast<int>(a1 * 256u + a0);
-        const int sc = static_cast<int>(__byte_perm(lo, 0u, static_cast<uint32_t>(j) | 0x4440u));
-        acc = fmaf(static_cast<float>(sint * sc), s.inv[j], acc);
-    }
-    int m2 = __dp4a(static_cast<int>(s.xq2), static_cast<int>(hi), 0);
-    unsigned m1 = __dp4a(s.xq1, hi, 0u), m0 = __dp4a(s.xq0, hi, 0u);
-    const int mint = m2 * 65536 + static_cast<int>(m1 * 256u + m0);
-    const float d = f16_bits_to_float(r.dd);
-    const float dmin = f16_bits_to_float(r.dd >> 16);
-    return fmaf(d, acc, -(dmin * (static_cast<float>(mint) * s.xinv)));
+__device__ __forceinline__ float2 bits2(uint32_t a, uint32_t b) {
+    return make_float2(__uint_as_float(a), __uint_as_float(b));
 }
 
-// Sum v[0..kRowBatch) over the 32 lanes; afterwards lane L holds the total of
-// row (L >> 3) & (kRowBatch - 1) ... in a fixed order (deterministic).
-// Returns the row index this lane's value belongs to via *row.
-__device__ __forceinline__ float transpose_reduce4(float (&v)[kRowBatch], int lane, int* row) {
-    // xor 16: split rows {0,1} / {2,3}
+// Dot product of one weight row with this thread's slice of x.
+//
+// Scale byte j of the slice (sc4 byte j): sc_j = low nibble, m_j = high
+// nibble.  A 4-bit field at bit position p is made an exact float by OR-ing
+// it into the mantissa of 2^E and subtracting 2^E (the field times 2^(E+p-23));
+// E is picked per field to give sc_j 4^-j and m_j.  Then, exactly:
+//   M[a][jp] = {dl_j 2^(107 - 8a - 2j)} for j = 2 jp, 2 jp + 1 (d 2^107 or d 2^99 times sc_j 4^-j),
+//   A[jp]    = {-ml_j 2^-42}.
+// Quant word i holds lanes 4 i .. 4 i + 3 in its bytes; lanes 4 i + 2, 4 i + 3
+// are read from the word shifted down by 16, so lane 4 i + 2 src + a has its
+// code of shift j at bit s = 8 a + 2 j.  u & (3 << s), read as a float, is
+// q 2^(s - 149); times M it is dl q 2^-42 exactly, and the FMA with A rounds
+// dl q - ml once.
+__device__ __forceinline__ float slice_dot(const RowWords& r, const SliceX& s) {
+    const uint32_t sc = r.sc4;
+    const uint32_t sh = sc >> 16;  // scale bytes 2, 3 in the low half
+    const float2 scA = fadd2(bits2((sc & 0xFu) | 0x4B000000u, (sc & 0xF00u) | 0x46000000u),
+                             make_float2(-0x1p23f, -0x1p13f));  // {sc_0, sc_1 / 4}
+    const float2 scB = fadd2(bits2((sh & 0xFu) | 0x49000000u, (sh & 0xF00u) | 0x44000000u),
+                             make_float2(-0x1p19f, -0x1p9f));   // {sc_2 / 16, sc_3 / 64}
+    const float2 mA = fadd2(bits2((sc & 0xF0u) | 0x49000000u, (sc & 0xF000u) | 0x45000000u),
+                            make_float2(-0x1p19f, -0x1p11f));   // {m_0, m_1}
+    const float2 mB = fadd2(bits2((sh & 0xF0u) | 0x49000000u, (sh & 0xF000u) | 0x45000000u),
+                            make_float2(-0x1p19f, -0x1p11f));   // {m_2, m_3}
+    // {d 2^107, -dmin 2^-42}
+    const float2 dn = fmul2(make_float2(f16_bits_to_float(r.dd), f16_bits_to_float(r.dd >> 16)),
+                            make_float2(0x1p107f, -0x1p-42f));
+    const float2 D0 = make_float2(dn.x, dn.x), NM = make_float2(dn.y, dn.y);
+    const float2 M00 = fmul2(scA, D0), M01 = fmul2(scB, D0);
+    const float2 M10 = fmul2(M00, make_float2(0x1p-8f, 0x1p-8f));  // lanes a = 1: codes 8 bits up
+    const float2 M11 = fmul2(M01, make_float2(0x1p-8f, 0x1p-8f));
+    const float2 A0 = fmul2(mA, NM), A1 = fmul2(mB, NM);
+    float2 acc[kAccs];
+#pragma unroll
+    for (int c = 0; c < kAccs; ++c) acc[c] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t qw = r.q[i];
+        const uint32_t qh = qw >> 16;
+#pragma unroll
+        for (int src = 0; src < 2; ++src) {
+            const uint32_t u = src ? qh : qw;
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int jp = 0; jp < 2; ++jp) {
+                    const int s0 = 8 * a + 4 * jp;
+                    const float2 g = bits2(u & (3u << s0), u & (3u << (s0 + 2)));
+                    const float2 M = a ? (jp ? M11 : M10) : (jp ? M01 : M00);
+                    const float2 A = jp ? A1 : A0;
+#if Q2K_GEMV_W2
+                    const float2 w = ffma2(g, M, A);
+#else
+                    const float2 w = make_float2(fmaf(g.x, M.x, A.x), fmaf(g.y, M.y, A.y));
+#endif
+                    const float2 xv = s.v[((i * 2 + src) * 2 + a) * 2 + jp];
+#if Q2K_GEMV_DOT2
+                    acc[i % kAccs] = ffma2(xv, w, acc[i % kAccs]);
+#else
+                    acc[i % kAccs] = make_float2(fmaf(xv.x, w.x, acc[i % kAccs].x),
+                                                 fmaf(xv.y, w.y, acc[i % kAccs].y));
+#endif
+                }
+        }
+    }
+#pragma unroll
+    for (int c = 1; c < kAccs; ++c) acc[0] = fadd2(acc[0], acc[c]);
+    return (acc[0].x + acc[0].y) * s.rescale;
+}
+
+// Sum v[0..kRowBatch) over the 32 lanes in a fixed order (deterministic);
+// afterwards the lanes of row_of_lane(lane) hold that row's total.
+__device__ __forceinline__ int row_of_lane(int lane) {
+    return kRowBatch == 4 ? ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1) : (lane >> 4) & 1;
+}
+
+__device__ __forceinline__ float transpose_reduce(float (&v)[kRowBatch], int lane) {
     const bool up16 = (lane & 16) != 0;
-    float a0 = up16 ? v[2] : v[0], a1 = up16 ? v[3] : v[1];
-    float s0 = up16 ? v[0] : v[2], s1 = up16 ? v[1] : v[3];
-    a0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 16);
-    a1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 16);
-    // xor 8: split the remaining pair
-    const bool up8 = (lane & 8) != 0;
-    float b = up8 ? a1 : a0;
-    const float t = up8 ? a0 : a1;
-    b += __shfl_xor_sync(0xFFFFFFFFu, t, 8);
+    float b;
+    if constexpr (kRowBatch == 4) {
+        // xor 16: split rows {0,1} / {2,3}
+        float a0 = up16 ? v[2] : v[0], a1 = up16 ? v[3] : v[1];
+        const float s0 = up16 ? v[0] : v[2], s1 = up16 ? v[1] : v[3];
+        a0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 16);
+        a1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 16);
+        // xor 8: split the remaining pair
+        const bool up8 = (lane & 8) != 0;
+        b = up8 ? a1 : a0;
+        const float t = up8 ? a0 : a1;
+        b += __shfl_xor_sync(0xFFFFFFFFu, t, 8);
+    } else {
+        b = up16 ? v[1] : v[0];
+        const float t = up16 ? v[0] : v[1];
+        b += __shfl_xor_sync(0xFFFFFFFFu, t, 16);
+        b += __shfl_xor_sync(0xFFFFFFFFu, b, 8);
+    }
     b += __shfl_xor_sync(0xFFFFFFFFu, b, 4);
     b += __shfl_xor_sync(0xFFFFFFFFu, b, 2);
     b += __shfl_xor_sync(0xFFFFFFFFu, b, 1);
-    *row = (up16 ? 2 : 0) + (up8 ? 1 : 0);
     return b;
 }
 
@@ -273,106 +327,67 @@ __device__ __forceinline__ void issue_weight_copies(uint8_t* smem_w, const uint8
     }
 }
 
-// x (K floats) -> the run planes, run sums and run scales in shared memory,
-// spread over the CTA's threads.
-__device__ __forceinline__ void convert_x(const float* __restrict__ x, uint32_t* planes,
-                                          float* run_sum, float* run_inv, int n_runs, int tid,
-                                          int nthreads) {
-    for (int r = tid; r < n_runs; r += nthreads) {
-        // run r = (block, half, shift j, segment): slice 4 block + 2 half + segment
-        const int slr = ((r >> 4) << 2) | (((r >> 3) & 1) << 1) | (r & 1);
-        convert_run(x + 16 * r, planes + slr * kSlicePitch + 12 * ((r >> 1) & 3), &run_sum[r],
-                    &run_inv[r]);
-    }
-}
-
-// This thread's slice (block b, half h, segment seg) of the converted x, into
-// registers: the planes of its four runs, their scales and quantized sums.
-__device__ __forceinline__ void load_slice_planes(const uint32_t* planes, const float* run_sum,
-                                                  const float* run_inv, int sl, bool active, int b,
-                                                  int h, int seg, SlicePlanes& s) {
-    float X[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        // run of (block b, half h, shift j, segment seg)
-        const int run = active ? 16 * b + 8 * h + 2 * j + seg : 0;
-        const uint32_t* pj = planes + (active ? sl : 0) * kSlicePitch + 12 * j;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            s.r[j].p0[q] = pj[q];
-            s.r[j].p1[q] = pj[4 + q];
-            s.r[j].p2[q] = pj[8 + q];
-        }
-        X[j] = active ? run_sum[run] : 0.f;
-        s.inv[j] = active ? run_inv[run] * ((j & 1) ? 0.25f : 1.f) : 0.f;
-    }
-    quantize_run_sums(X, s);
-}
-
 // Rows [0, rows) of a weight chunk in shared memory (this thread's slice of
-// row r at my_col + r row_bytes) against the slice planes s: group g takes the
+// row r at my_col + r row_bytes) against the slice of x: group g takes the
 // blocks of eight consecutive rows g, g + groups, ... (rows 8 g .. 8 g + 7,
-// then 8 (g + groups) ..), and each row's total over the group's warps goes to
-// red[row * warps_per_group + warp in group].  The pieces (rows 8p .. 8p + 7)
-// a block reads are waited for before its rows are read, unless all pieces up
-// to `waited` are known to have landed; each piece barrier completes once, so
-// waiting on it again returns at once.  Returns false once a wait gave up (the
-// rows after it count as zero).
-__device__ __forceinline__ bool dot_rows(const uint8_t* my_col, size_t row_bytes, int rows, int g,
-                                         int groups, int lane, int wig, int warps_per_group,
-                                         bool active, int h, int seg, uint32_t ssel,
-                                         const SlicePlanes& s, float* red, uint32_t bars,
-                                         uint32_t parity, int waited, volatile int* abort_flag,
+// then 8 (g + groups) ..), kRowBatch rows at a time, and each row's total over
+// the group's warps goes to red[row * warps_per_group + warp in group].  The
+// piece (rows 8p .. 8p + 7) a block reads is waited for before its rows are
+// read, unless all pieces up to `waited` are known to have landed; each piece
+// barrier completes once, so waiting on it again returns at once.  Rows past
+// `rows` in the last block are read from the chunk's shared memory (sized for
+// whole blocks of eight rows) and their sums dropped.  kB: blocks per row when
+// known at compile time (the row stride then folds into the loads), else 0.
+// Returns false once a wait gave up (the rows after it count as zero).
+template <int kB>
+__device__ __forceinline__ bool dot_rows(const uint8_t* my_col, int B, int rows, int g, int groups,
+                                         int lane, int wig, int warps_per_group, bool active, int h,
+                                         int seg, uint32_t ssel, const SliceX& s, float* red,
+                                         uint32_t bars, int waited, volatile int* abort_flag,
                                          bool ok) {
-    constexpr int kLoad = 2 * kRowBatch;  // rows loaded and decoded together
-    for (int base = g * kLoad; base < rows; base += groups * kLoad) {
-        // Make sure the pieces of this block have landed, then issue all
-        // shared-memory loads of the block before any arithmetic.
-        const int last = min(rows - 1, base + kLoad - 1);
-        for (int pw = max(waited + 1, base / kPieceRows); pw <= last / kPieceRows; ++pw)
-            ok = ok && mbar_wait_backoff(bars + 8 * pw, (parity >> pw) & 1u, abort_flag,
-                                         &g_gemv_error, kErrTimeoutGemv, 64);
-        RowWords rw[kLoad];
+    const int row_bytes = (kB ? kB : B) * kBlockBytes;
+    for (int base = g * kPieceRows; base < rows; base += groups * kPieceRows) {
+        const int piece = base / kPieceRows;
+        if (piece > waited)
+            ok = ok && mbar_wait_backoff(bars + 8 * piece, 0u, abort_flag, &g_gemv_error,
+                                         kErrTimeoutGemv, 64);
+        const bool live = active && ok;
+        const uint8_t* rp = my_col + base * row_bytes;
+#pragma unroll 1
+        for (int rb = base; rb < min(rows, base + kPieceRows); rb += kRowBatch, rp += kRowBatch * row_bytes) {
+            // issue all shared-memory loads of the rows before any arithmetic
+            RowWords rw[kRowBatch];
 #pragma unroll
-        for (int u = 0; u < kLoad; ++u) {
-            const int lr = min(base + u, last);
-            rw[u] = load_row_words(my_col + static_cast<size_t>(lr) * row_bytes, h, seg, ssel);
-        }
-        float part[kLoad];
+            for (int u = 0; u < kRowBatch; ++u) rw[u] = load_row_words(rp + u * row_bytes, h, seg, ssel);
+            float part[kRowBatch];
 #pragma unroll
-        for (int u = 0; u < kLoad; ++u) {
-            const float v = slice_dot(rw[u], s);
-            part[u] = (active && ok && base + u < rows) ? v : 0.f;
-        }
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-            float p4[kRowBatch];
-#pragma unroll
-            for (int u = 0; u < kRowBatch; ++u) p4[u] = part[hb * kRowBatch + u];
-            int which;
-            const float tot = transpose_reduce4(p4, lane, &which);
-            const int lr = base + hb * kRowBatch + which;
-            if ((lane & 7) == 0 && lr < rows) red[lr * warps_per_group + wig] = tot;
+            for (int u = 0; u < kRowBatch; ++u) {
+                const float v = slice_dot(rw[u], s);
+                part[u] = live ? v : 0.f;
+            }
+            const float tot = transpose_reduce(part, lane);
+            const int lr = rb + row_of_lane(lane);
+            if ((lane & (32 / kRowBatch - 1)) == 0 && lr < rows) red[lr * warps_per_group + wig] = tot;
         }
     }
     return ok;
 }
 
-// kMaxThreads: 256 for every plan but the two-group CTAs of large k (512); the
-// smaller bound leaves the compiler more registers a thread.
-template <int kMaxThreads>
-__global__ void __launch_bounds__(kMaxThreads, 1)
+// kMaxThreads: 128 for the independent plan of k <= 8192, 256 for dependent
+// calls, 512 for the two-group CTAs of large k; kMinBlocks caps the registers
+// so that as many CTAs share an SM.
+template <int kMaxThreads, int kMinBlocks, int kB>
+__global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
 gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
                int N, int K, int rows_per_cta, int slices_pad, int groups, uint32_t flags,
-               GemvProblems pr, const uint8_t* __restrict__ xplanes, uint32_t xplanes_stride) {
+               GemvProblems pr, const uint8_t* __restrict__ xprep, uint32_t xprep_stride) {
     const bool independent = (flags & kGemvIndependent) != 0;
     const bool const_weights = independent || (flags & kGemvConstWeights) != 0;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
     const int nthreads = blockDim.x;
-    const int B = K >> 8;
-    const int S = K >> 6;
-    const int n_runs = K >> 4;
+    const int B = kB ? kB : K >> 8;
+    const int S = 4 * B;
     const size_t row_bytes = static_cast<size_t>(B) * kBlockBytes;
     const int r0 = blockIdx.x * rows_per_cta;
     const int rows = min(rows_per_cta, N - r0);
@@ -399,32 +414,27 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
         }
         x += static_cast<size_t>(route / pr.top_k) * K;
         w += static_cast<size_t>(e) * pr.w_stride;
-        if (xplanes != nullptr) xplanes += static_cast<size_t>(route / pr.top_k) * xplanes_stride;
+        if (xprep != nullptr) xprep += static_cast<size_t>(route / pr.top_k) * xprep_stride;
     } else {
         x += static_cast<size_t>(prob) * pr.x_stride;
         w += static_cast<size_t>(prob) * pr.w_stride;
         y += static_cast<size_t>(prob) * pr.y_stride;
-        if (xplanes != nullptr) xplanes += static_cast<size_t>(prob) * xplanes_stride;
+        if (xprep != nullptr) xprep += static_cast<size_t>(prob) * xprep_stride;
     }
     const uint32_t delta = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(w) & 15u);
     const int n_pieces = (rows + kPieceRows - 1) / kPieceRows;
     const int max_pieces = (rows_per_cta + kPieceRows - 1) / kPieceRows;
     const int warps_per_group = slices_pad >> 5;
-    // shared layout: W chunk (at offset delta) | run planes | run sums | run
-    // scales | red | bars | flag
-    const size_t w_smem = (static_cast<size_t>(rows_per_cta) * row_bytes + 31) & ~size_t(15);
+    // shared layout: W chunk (at offset delta, room for whole blocks of eight
+    // rows) | red | bars | flag
+    const int rows_alloc = (rows_per_cta + kPieceRows - 1) / kPieceRows * kPieceRows;
+    const size_t w_smem = (static_cast<size_t>(rows_alloc) * row_bytes + 31) & ~size_t(15);
     uint8_t* smem_w = smem + delta;
-    uint32_t* planes = reinterpret_cast<uint32_t*>(smem + w_smem);
-    float* run_sum = reinterpret_cast<float*>(planes + (n_runs >> 2) * kSlicePitch);
-    float* run_inv = run_sum + n_runs;
-    float* red = run_inv + n_runs;
-    const size_t red_end = w_smem + static_cast<size_t>(n_runs >> 2) * kSlicePitch * 4 +
-                           static_cast<size_t>(n_runs) * 8 +
-                           static_cast<size_t>(rows_per_cta) * warps_per_group * 4;
+    float* red = reinterpret_cast<float*>(smem + w_smem);
+    const size_t red_end = w_smem + static_cast<size_t>(rows_per_cta) * warps_per_group * 4;
     const size_t bar_off = (red_end + 7) & ~size_t(7);
     const uint32_t bars = smem_u32(smem + bar_off);
-    const uint32_t planes_bar = bars + 8 * max_pieces;  // x planes copied in (xplanes)
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + bar_off + 8 * (max_pieces + 1));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + bar_off + 8 * max_pieces);
     const uint8_t* gsrc = w + static_cast<size_t>(r0) * row_bytes;
     const size_t chunk = static_cast<size_t>(rows) * row_bytes;
 
@@ -438,20 +448,10 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
     const bool issuer = (tid & 31) == 0;
     if (tid == 0) {
         for (int p = 0; p < n_pieces; ++p) mbar_init(bars + 8 * p, 1);
-        mbar_init(planes_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    // x converted once for several calls (prep_x_planes_kernel, a grid that
-    // completed before this one started): one bulk copy of its planes, run
-    // sums and run scales, laid out as convert_x lays them out here
-    const uint32_t planes_bytes = static_cast<uint32_t>(
-        static_cast<size_t>(n_runs >> 2) * kSlicePitch * 4 + static_cast<size_t>(n_runs) * 8);
-    if (xplanes != nullptr && tid == 0) {
-        mbar_arrive_expect_tx(planes_bar, planes_bytes);
-        bulk_copy_g2s(smem_u32(planes), xplanes, planes_bytes, planes_bar);
-    }
     if (const_weights) {
         // The caller guarantees the grids that may still run do not write W,
         // so the weight copies may start before the dependency wait.
@@ -467,47 +467,56 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
                              static_cast<uint32_t>(left < (size_t(1) << 20) ? left : (size_t(1) << 20)));
         }
     }
-    if (!independent) {
+    const int g = tid / slices_pad;
+    const int sl = tid - g * slices_pad;
+    const bool active = sl < S;
+    // inactive slice lanes (S not a multiple of 32) read block 0 and discard it
+    const int b = active ? sl >> 2 : 0, h = (sl >> 1) & 1, seg = sl & 1;
+    SliceX sx;
+    if (independent) {
+        // x is not written by any grid that may still run: read it now
+        if (active) {
+            if (xprep != nullptr) load_slice_prepared(xprep, S, sl, sx);
+            else load_slice_x(x, b, h, seg, sx);
+        }
+    } else {
         pdl_wait_prerequisites();
         pdl_allow_dependents();
+        __syncthreads();
+        if (issuer && !const_weights)
+            issue_weight_copies(smem_w, gsrc, bars, rows, row_bytes, delta, tid >> 5, nwarps);
+        if (active) {
+            if (xprep != nullptr) load_slice_prepared(xprep, S, sl, sx);
+            else load_slice_x(x, b, h, seg, sx);
+        }
     }
-    __syncthreads();
-    if (issuer && !const_weights)
-        issue_weight_copies(smem_w, gsrc, bars, rows, row_bytes, delta, tid >> 5, nwarps);
-    // x -> integer planes, once per CTA, while the weights stream in
-    if (xplanes == nullptr) convert_x(x, planes, run_sum, run_inv, n_runs, tid, nthreads);
+    if (!active) {
+#pragma unroll
+        for (int v = 0; v < 32; ++v) sx.v[v] = make_float2(0.f, 0.f);
+        sx.rescale = 0.f;
+    }
     // A dependent call's copies, issued before its dependency wait, have
     // (nearly) landed by now: one thread waits for all of them, and the
     // barrier below publishes that, so the row loop needs no barrier polls of
-    // its own.  An independent call's copies were issued just now: its row
-    // loop waits for each piece of rows as it needs it instead, and starts on
-    // the first rows while the rest are in flight.
+    // its own.  Other calls' row loops wait for each piece of rows as they
+    // need it instead, and start on the first rows while the rest are in flight.
     const bool wait_all = const_weights && !independent;
     bool all_ok = true;
-    if (xplanes != nullptr && tid == 0)
-        all_ok = mbar_wait_backoff(planes_bar, 0, abort_flag, &g_gemv_error, kErrTimeoutGemv, 64);
     if (wait_all && tid == 0) {
         for (int p = 0; p < n_pieces; ++p)
             all_ok = all_ok && mbar_wait_backoff(bars + 8 * p, 0, abort_flag, &g_gemv_error,
                                                  kErrTimeoutGemv, 64);
     }
-    __syncthreads();
+    if (wait_all) __syncthreads();
 
-    const int g = tid / slices_pad;
-    const int sl = tid - g * slices_pad;
-    const bool active = sl < S;
-    const int b = sl >> 2, h = (sl >> 1) & 1, seg = sl & 1;
     const uint32_t ssel = seg | ((seg + 2) << 4) | ((seg + 4) << 8) | ((seg + 6) << 12);
-    SlicePlanes s;
-    load_slice_planes(planes, run_sum, run_inv, sl, active, b, h, seg, s);
-
     const int lane = tid & 31;
     const int wig = sl >> 5;  // warp index within the group
     const uint8_t* my_col = smem_w + b * kBlockBytes;
     const int waited = wait_all ? n_pieces - 1 : -1;
-    const bool ok = !(const_weights && *abort_flag);
-    dot_rows(my_col, row_bytes, rows, g, groups, lane, wig, warps_per_group, active, h, seg, ssel, s,
-             red, bars, 0u, waited, abort_flag, ok);
+    const bool ok = !(wait_all && *abort_flag);
+    dot_rows<kB>(my_col, B, rows, g, groups, lane, wig, warps_per_group, active, h, seg, ssel, sx,
+                 red, bars, waited, abort_flag, ok);
     __syncthreads();
     for (int lr = tid; lr < rows; lr += nthreads) {
         float v = 0.f;
@@ -519,8 +528,6 @@ gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float
         volatile int no_abort = 0;
         for (int p = 0; p < n_pieces; ++p)
             mbar_wait_bounded(bars + 8 * p, 0, &no_abort, &g_gemv_error, kErrTimeoutGemv);
-        if (xplanes != nullptr)
-            mbar_wait_bounded(planes_bar, 0, &no_abort, &g_gemv_error, kErrTimeoutGemv);
     }
     // Independent calls finish only after the grid before them, so work
     // enqueued later on the stream sees every earlier call complete.  One CTA
@@ -536,12 +543,10 @@ struct M1Plan {
 
 size_t m1_smem(int rows, int K, int slices_pad) {
     const size_t row_bytes = static_cast<size_t>(K / 256) * kBlockBytes;
-    const int n_runs = K / 16;
     const int pieces = (rows + kPieceRows - 1) / kPieceRows;
-    const size_t w_smem = (static_cast<size_t>(rows) * row_bytes + 31) & ~size_t(15);
-    const size_t red_end = w_smem + static_cast<size_t>(n_runs / 4) * kSlicePitch * 4 +
-                           static_cast<size_t>(n_runs) * 8 + static_cast<size_t>(rows) * (slices_pad / 32) * 4;
-    return ((red_end + 7) & ~size_t(7)) + 8 * (pieces + 1) + 16;
+    const size_t w_smem = (static_cast<size_t>(pieces * kPieceRows) * row_bytes + 31) & ~size_t(15);
+    const size_t red_end = w_smem + static_cast<size_t>(rows) * (slices_pad / 32) * 4;
+    return ((red_end + 7) & ~size_t(7)) + 8 * pieces + 16;
 }
 
 bool plan_m1(int N, int K, int sm_count, int threads, bool whole_batches, M1Plan* p) {
@@ -553,10 +558,9 @@ bool plan_m1(int N, int K, int sm_count, int threads, bool whole_batches, M1Plan
     // Rows per CTA a multiple of what one pass of the row loop covers (groups x
     // 8 rows) when asked: the loop then never decodes a row twice at the end.
     // Independent calls share the SMs, so fewer CTAs than SMs costs nothing there.
-    const int quantum = whole_batches ? groups * 2 * kRowBatch : 1;
+    const int quantum = whole_batches ? groups * kPieceRows : 1;
     // Independent calls overlap on the SMs: their CTAs are kept to 72 KB of
-    // shared memory (three share an SM) when 32 rows still fit there, so that
-    // the x conversion every CTA repeats stays a small share of its work;
+    // shared memory (three share an SM) when 32 rows still fit there;
     // otherwise, and for dependent calls, the largest chunk that fits is taken.
     size_t cap = size_t(200) * 1024;
     if (whole_batches && m1_smem(32, K, slices_pad) <= size_t(72) * 1024) cap = size_t(72) * 1024;
@@ -576,21 +580,41 @@ bool plan_m1(int N, int K, int sm_count, int threads, bool whole_batches, M1Plan
     return p->smem <= 227 * 1024;
 }
 
-cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, const M1Plan& p,
-                      int device, uint32_t flags, const GemvProblems& pr, int n_problems,
-                      const uint8_t* xplanes, uint32_t xplanes_stride, cudaStream_t stream) {
+template <int kT, int kMinB, int kB>
+cudaError_t launch_m1_as(const cudaLaunchConfig_t& cfg, int device, const float* x,
+                         const uint8_t* w, float* y, int N, int K, const M1Plan& p, uint32_t flags,
+                         const GemvProblems& pr, const uint8_t* xprep, uint32_t xprep_stride) {
     static bool smem_set[64] = {};
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (!smem_set[device]) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel<256>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             227 * 1024);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_m1_kernel<512>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        const cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel<kT, kMinB, kB>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   227 * 1024);
         if (e != cudaSuccess) return e;
         smem_set[device] = true;
     }
+    return cudaLaunchKernelEx(&cfg, gemv_m1_kernel<kT, kMinB, kB>, x, w, y, N, K, p.rows_per_cta,
+                              p.slices_pad, p.groups, flags, pr, xprep, xprep_stride);
+}
+
+// The row stride is compiled in for the common K (2048, 4096, 7168, 14336).
+template <int kT, int kMinB>
+cudaError_t launch_m1_threads(const cudaLaunchConfig_t& cfg, int device, const float* x,
+                              const uint8_t* w, float* y, int N, int K, const M1Plan& p,
+                              uint32_t flags, const GemvProblems& pr, const uint8_t* xprep,
+                              uint32_t xprep_stride) {
+    switch (K / 256) {
+        case 8: return launch_m1_as<kT, kMinB, 8>(cfg, device, x, w, y, N, K, p, flags, pr, xprep, xprep_stride);
+        case 16: return launch_m1_as<kT, kMinB, 16>(cfg, device, x, w, y, N, K, p, flags, pr, xprep, xprep_stride);
+        case 28: return launch_m1_as<kT, kMinB, 28>(cfg, device, x, w, y, N, K, p, flags, pr, xprep, xprep_stride);
+        case 56: return launch_m1_as<kT, kMinB, 56>(cfg, device, x, w, y, N, K, p, flags, pr, xprep, xprep_stride);
+        default: return launch_m1_as<kT, kMinB, 0>(cfg, device, x, w, y, N, K, p, flags, pr, xprep, xprep_stride);
+    }
+}
+
+cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, const M1Plan& p,
+                      int device, uint32_t flags, const GemvProblems& pr, int n_problems,
+                      const uint8_t* xprep, uint32_t xprep_stride, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.ctas, n_problems);
     cfg.blockDim = dim3(p.threads);
@@ -602,13 +626,49 @@ cudaError_t launch_m1(const float* x, const uint8_t* w, float* y, int N, int K, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (p.threads > 256)
-        return cudaLaunchKernelEx(&cfg, gemv_m1_kernel<512>, x, w, y, N, K, p.rows_per_cta,
-                                  p.slices_pad, p.groups, flags, pr, xplanes, xplanes_stride);
-    return cudaLaunchKernelEx(&cfg, gemv_m1_kernel<256>, x, w, y, N, K, p.rows_per_cta,
-                              p.slices_pad, p.groups, flags, pr, xplanes, xplanes_stride);
+        return launch_m1_threads<512, 1>(cfg, device, x, w, y, N, K, p, flags, pr, xprep, xprep_stride);
+    if (p.threads > 128)
+        return launch_m1_threads<256, 1>(cfg, device, x, w, y, N, K, p, flags, pr, xprep, xprep_stride);
+    return launch_m1_threads<128, Q2K_GEMV_MINB>(cfg, device, x, w, y, N, K, p, flags, pr, xprep,
+                                                 xprep_stride);
 }
 
 // ------------------------------------------------------------------ general m
+
+// Running sum of per-block values with a bounded accumulation chain: blocks
+// are summed 16 at a time, those sums 16 at a time, and those into the total,
+// so a value passes through at most 16 + 16 + ceil(nb / 256) additions for nb
+// blocks, in a fixed order (counts are uniform across the lanes of a warp).
+template <int MT>
+struct BlockSum {
+    float l0[MT], l1[MT], tot[MT];
+    int c0 = 0, c1 = 0;
+    __device__ __forceinline__ BlockSum() {
+#pragma unroll
+        for (int mm = 0; mm < MT; ++mm) l0[mm] = l1[mm] = tot[mm] = 0.f;
+    }
+    __device__ __forceinline__ void add(const float (&blk)[MT]) {
+#pragma unroll
+        for (int mm = 0; mm < MT; ++mm) l0[mm] += blk[mm];
+        if (++c0 == 16) {
+            c0 = 0;
+#pragma unroll
+            for (int mm = 0; mm < MT; ++mm) {
+                l1[mm] += l0[mm];
+                l0[mm] = 0.f;
+            }
+            if (++c1 == 16) {
+                c1 = 0;
+#pragma unroll
+                for (int mm = 0; mm < MT; ++mm) {
+                    tot[mm] += l1[mm];
+                    l1[mm] = 0.f;
+                }
+            }
+        }
+    }
+    __device__ __forceinline__ float total(int mm) const { return tot[mm] + (l1[mm] + l0[mm]); }
+};
 
 template <int MT>
 __global__ void __launch_bounds__(kGemvWarps * 32)
@@ -653,10 +713,7 @@ gemv_rows_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, flo
     // Select scale bytes seg, seg+2, seg+4, seg+6 of the 8 bytes at 8*half.
     const uint32_t ssel = seg | ((seg + 2) << 4) | ((seg + 4) << 8) | ((seg + 6) << 12);
 
-    float acc[MT];
-#pragma unroll
-    for (int mm = 0; mm < MT; ++mm) acc[mm] = 0.f;
-
+    BlockSum<MT> sum;
     for (int b = lane >> 3; b < B; b += 4) {
         const uint8_t* blk = row + static_cast<size_t>(b) * kBlockBytes;
         const uint32_t q0 = ldg_stream_u32(blk + qoff);
@@ -668,6 +725,9 @@ gemv_rows_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, flo
         const float d = f16_bits_to_float(dd);
         const float dmin = f16_bits_to_float(dd >> 16);
         const float* xb = x + static_cast<size_t>(m0) * K + b * kQK + 128 * half + 16 * seg + l0;
+        float acc[MT];
+#pragma unroll
+        for (int mm = 0; mm < MT; ++mm) acc[mm] = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint32_t sc = (sc4 >> (8 * j)) & 0xFFu;
@@ -698,18 +758,20 @@ gemv_rows_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, flo
                 }
             }
         }
+        sum.add(acc);  // this lane's 32 weights of block b
     }
+    float tot[MT];
 #pragma unroll
     for (int mm = 0; mm < MT; ++mm) {
-        float v = acc[mm];
+        float v = sum.total(mm);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-        acc[mm] = v;
+        tot[mm] = v;
     }
     if (lane == 0) {
 #pragma unroll
         for (int mm = 0; mm < MT; ++mm)
-            if (mm < mcount) y[static_cast<size_t>(m0 + mm) * N + n] = acc[mm];
+            if (mm < mcount) y[static_cast<size_t>(m0 + mm) * N + n] = tot[mm];
     }
 }
 
@@ -759,33 +821,37 @@ cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N
 bool gemv_shares_planes(int M, int K) { return M == 1 && K / 64 <= kM1MaxSlices; }
 
 size_t gemv_planes_bytes(int K) {
-    return static_cast<size_t>(K / 64) * kSlicePitch * 4 + static_cast<size_t>(K / 16) * 8;
+    return static_cast<size_t>(K / 64) * (kSliceXBytes + 4);
 }
 
 size_t gemv_planes_stride(int K) { return (gemv_planes_bytes(K) + 255) & ~size_t(255); }
 
-// x (one row) -> the integer planes, run sums and run scales in the layout the
-// m = 1 kernel keeps in shared memory, for several of its calls to copy.  It
-// never lets the next grid start early, so every later grid sees it complete.
+// x (one row per blockIdx.y) -> the m = 1 kernel's per-slice form (the scaled
+// x of each 64-weight slice in the order its row loop reads them, then the
+// slices' rescale factors), for several of its calls to load instead of
+// converting x themselves: the same values, so the same bits.  It never lets
+// the next grid start early, so every later grid sees it complete.
 __global__ void __launch_bounds__(128)
-prep_x_planes_kernel(const float* __restrict__ x, int K, uint8_t* __restrict__ dst,
-                     size_t stride) {
-    // x row blockIdx.y -> planes at dst + blockIdx.y stride
-    const int n_runs = K >> 4;
+prep_x_kernel(const float* __restrict__ x, int K, uint8_t* __restrict__ dst, size_t stride) {
+    const int S = K >> 6;
     x += static_cast<size_t>(blockIdx.y) * K;
     dst += static_cast<size_t>(blockIdx.y) * stride;
-    uint32_t* planes = reinterpret_cast<uint32_t*>(dst);
-    float* run_sum = reinterpret_cast<float*>(planes + (n_runs >> 2) * kSlicePitch);
-    float* run_inv = run_sum + n_runs;
-    convert_x(x, planes, run_sum, run_inv, n_runs, blockIdx.x * blockDim.x + threadIdx.x,
-              gridDim.x * blockDim.x);
+    for (int sl = blockIdx.x * blockDim.x + threadIdx.x; sl < S; sl += gridDim.x * blockDim.x) {
+        SliceX s;
+        load_slice_x(x, sl >> 2, (sl >> 1) & 1, sl & 1, s);
+        float4* p = reinterpret_cast<float4*>(dst + static_cast<size_t>(sl) * kSliceXBytes);
+#pragma unroll
+        for (int v = 0; v < 16; ++v)
+            p[v] = make_float4(s.v[2 * v].x, s.v[2 * v].y, s.v[2 * v + 1].x, s.v[2 * v + 1].y);
+        reinterpret_cast<float*>(dst + static_cast<size_t>(S) * kSliceXBytes)[sl] = s.rescale;
+    }
 }
 
 cudaError_t launch_prep_x_planes(const float* x, int K, uint8_t* dst, cudaStream_t stream,
                                  int rows) {
-    const int n_runs = K / 16;
-    prep_x_planes_kernel<<<dim3((n_runs + 127) / 128, rows), 128, 0, stream>>>(
-        x, K, dst, gemv_planes_stride(K));
+    const int S = K / 64;
+    prep_x_kernel<<<dim3((S + 127) / 128, rows), 128, 0, stream>>>(x, K, dst,
+                                                                  gemv_planes_stride(K));
     return cudaGetLastError();
 }
 

@@ -46,7 +46,7 @@ typedef struct CUstream_st *q2k_stream_t;
 typedef enum q2k_status {
     Q2K_OK = 0,
     Q2K_ERR_INVALID_ARGUMENT = 1, /* the pages' MlxError::InvalidArgument */
-    Q2K_ERR_BAD_ID = 2,           /* reserved: gather reports bad ids through bad_id_count */
+    Q2K_ERR_BAD_ID = 2,           /* an id out of range (gather, routed calls without bad_id_count) */
     Q2K_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed */
     Q2K_ERR_TIMEOUT = 4,          /* a kernel gave up waiting (see q2k_device_error) */
     Q2K_ERR_NO_DEVICE = 5,        /* no sm_103 device is current */
@@ -121,10 +121,19 @@ q2k_status q2k_dequantize(const void *blocks, size_t blocks_bytes,
  *               16-byte aligned
  *   bad_id_count  device u32 or NULL.  The pages reject an id >= vocab_size.
  *               Ids live on the device here, so the check runs in the kernel:
- *               a row with a bad id is written as zeros and, when bad_id_count
- *               is not NULL, the number of bad ids is stored there (the call
- *               zeroes it first, stream-ordered).  Read it after the stream
- *               completes; nonzero means the pages' error.
+ *               a row with a bad id is written as zeros and the bad ids are
+ *               counted.
+ *                 NULL: the call counts them in a word of its own, reads it
+ *                 back (4 bytes) and waits for `stream` to finish, then
+ *                 returns Q2K_ERR_BAD_ID if any id was out of range (the
+ *                 pages' error), else Q2K_OK.  This form synchronises, so it
+ *                 is refused (Q2K_ERR_INVALID_ARGUMENT) while `stream` is
+ *                 being captured; at most 64 such calls may be in flight per
+ *                 device at once (from concurrent host threads).
+ *                 Not NULL: the count is stored there (the call zeroes it
+ *                 first, stream-ordered) and the call returns without
+ *                 waiting; read it after the stream completes, nonzero means
+ *                 the pages' error.
  * Decoded values are bit-identical to q2k_dequantize of the same rows. */
 q2k_status q2k_embedding_gather(const void *table, size_t table_bytes,
                                 const uint32_t *ids, float *out, size_t out_elems,
@@ -191,8 +200,10 @@ q2k_status q2k_matmul_batched_mv(const float *x, size_t x_elems, const void *w, 
                                  q2k_stream_t stream);
 
 /* q2k_x_planes_bytes - device bytes of scratch the batched and routed calls
- * use to convert x to its integer form once per x row (rows rows of k)
- * instead of once per CTA: k/64 * 196 + k/2 bytes per row, rounded up to 256.
+ * use to bring x into the m = 1 GEMV's per-slice form once per x row (rows
+ * rows of k) instead of once per CTA: each 64-weight slice of x scaled by a
+ * power of two, in the order the kernel reads it, plus one scale factor per
+ * slice - k/64 * 260 bytes per row, rounded up to 256.
  * 0 when k is not a positive multiple of 256 or above 16384 (no such
  * sharing).  Those calls take such a scratch as their `scratch` argument:
  * NULL (or smaller) keeps the conversion per CTA; results are the same bits
@@ -213,9 +224,12 @@ size_t q2k_x_planes_bytes(uint32_t k, uint32_t rows);
  *           16-byte aligned; fully overwritten, must not alias x, w or ids
  *   bad_id_count  device u32 or NULL.  Ids live on the device, so they are
  *           checked in the kernel: a route whose id is >= n_experts gets a
- *           zero row and, when bad_id_count is not NULL, is counted there
- *           (the call zeroes it first, stream-ordered).  Read it after the
- *           stream completes; nonzero means the pages' error.
+ *           zero row and is counted.  With NULL the call waits for its own
+ *           count and returns Q2K_ERR_BAD_ID if it is nonzero (synchronising;
+ *           refused during stream capture; as q2k_embedding_gather); with a
+ *           device word the count is stored there (zeroed first,
+ *           stream-ordered) and the call returns without waiting: nonzero
+ *           after the stream completes means the pages' error.
  * Every route runs the fp32 GEMV (error within 1e-5 * sum_k |x w|; the pages
  * allow 2e-4 absolute, 1e-2 for their reduced-precision path); each route's
  * row is bit-identical to q2k_matmul(m = 1) of its token and expert.
@@ -403,7 +417,7 @@ typedef struct q2k_matmul_call {
  *   scratch  device, NULL or at least q2k_matmul_batch_scratch_bytes(calls,
  *            count) bytes, 16-byte aligned, not overlapping any call's
  *            buffers.  With it, m = 1 calls on the fp32 GEMV path (k <= 16384)
- *            that read the same x row convert x to their integer form once,
+ *            that read the same x row bring x into the GEMV's per-slice form once,
  *            into the scratch, instead of once per CTA of every call (the
  *            same values: same bits).  A call of the batch that writes that
  *            row ends the sharing.  Without it (or smaller) every call
@@ -429,7 +443,8 @@ size_t q2k_matmul_batch_scratch_bytes(const q2k_matmul_call *calls, size_t count
  *   k = 7168); larger geometries are rejected with Q2K_ERR_INVALID_ARGUMENT.
  *   Nothing is allocated by the call.  The first call on a device looks up the
  *   array's device address (with that device current); make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is kept once found; a lookup that
+ *   fails returns Q2K_ERR_CUDA and is tried again by the next call.
  *   All calls share the one array: calls whose work may overlap on the GPU
  *   (different streams, different host threads without ordering) race on it
  *   and give wrong results; serialise them, e.g. on one stream.  Leftovers

@@ -312,20 +312,20 @@ def test_matmul_ex_batch_checks_every_call_first(lib):
     assert "call 1:" in lib.q2k_last_error().decode()
     assert lib.q2k_matmul_batch_scratch_bytes(calls, 2) == 0
     calls[1].params = q2k.MatmulParams(1, 8, 256, 10)
-    # two m = 1 calls on one x: one slot of x planes (K/64 slices x 49 words + K/16 x 8 bytes)
-    assert lib.q2k_matmul_batch_scratch_bytes(calls, 2) == (4 * 49 * 4 + 16 * 8 + 255) // 256 * 256
+    # two m = 1 calls on one x: one slot of prepared x (K/64 slices x (64 floats + 1 scale))
+    assert lib.q2k_matmul_batch_scratch_bytes(calls, 2) == (4 * 260 + 255) // 256 * 256
     calls[0].flags = 8
     assert lib.q2k_matmul_ex_batch(calls, 2, None, 0, None) == INVALID
     assert "call 0:" in lib.q2k_last_error().decode()
     calls[0].flags = 0
-    assert lib.q2k_matmul_ex_batch(calls, 2, 0x3000008, 1024, None) == INVALID
+    assert lib.q2k_matmul_ex_batch(calls, 2, 0x3000008, 2048, None) == INVALID
     assert "aligned" in lib.q2k_last_error().decode()
     assert lib.q2k_matmul_ex_batch(None, 0, None, 0, None) == 0   # nothing to do
 
 
 def test_x_planes_scratch_size_and_checks(lib):
-    # k/64 slices x 49 words + k/16 x 8 bytes per row, rounded up to 256
-    assert lib.q2k_x_planes_bytes(4096, 3) == 3 * ((64 * 49 * 4 + 256 * 8 + 255) // 256 * 256)
+    # k/64 slices x (64 scaled floats + 1 scale factor) per row, rounded up to 256
+    assert lib.q2k_x_planes_bytes(4096, 3) == 3 * ((64 * 260 + 255) // 256 * 256)
     assert lib.q2k_x_planes_bytes(16640, 1) == 0     # above the m = 1 kernel's k
     assert lib.q2k_x_planes_bytes(255, 1) == 0
     need = lib.q2k_x_planes_bytes(256, 3)

@@ -101,6 +101,51 @@ def test_dequantize_special_scales_bit_exact():
     assert np.array_equal(out.view(np.uint32), oracle.dequantize(flat).view(np.uint32))
 
 
+def _same_or_both_nan(a, b):
+    """Bit-equal, except that any NaN matches any NaN (payloads are not specified)."""
+    a, b = a.reshape(-1), b.reshape(-1)
+    nan = np.isnan(a)
+    return np.array_equal(nan, np.isnan(b)) and np.array_equal(a[~nan].view(np.uint32),
+                                                               b[~nan].view(np.uint32))
+
+
+# d or dmin = +Inf, -Inf or NaN (binary16 0x7C00, 0xFC00, 0x7E00), beside finite ones
+NONFINITE_SCALES = [(0x7C00, 0x3C00), (0x3C00, 0x7C00), (0xFC00, 0x2E66), (0x2E66, 0xFC00),
+                    (0x7E00, 0x3C00), (0x3C00, 0x7E00), (0x7C00, 0x7C00), (0x7C00, 0xFC00),
+                    (0x0000, 0x7C00), (0x7C00, 0x0000), (0x7E00, 0x7E00)]
+
+
+def _nonfinite_blocks(seed):
+    rng = np.random.default_rng(seed)
+    blocks = wl.random_blocks(rng, 2 * len(NONFINITE_SCALES)).reshape(-1, 84)
+    for i, (d, dm) in enumerate(NONFINITE_SCALES):
+        blocks[2 * i, 80:82] = [d & 0xFF, d >> 8]
+        blocks[2 * i, 82:84] = [dm & 0xFF, dm >> 8]
+    blocks[1::4, 0:16] = 0x00          # sc = m = 0 beside an infinite scale: inf * 0
+    blocks[2::4, 16:80] = 0x00         # q = 0 everywhere
+    return blocks
+
+
+def test_dequantize_nonfinite_scales_match_oracle():
+    """Blocks whose d or dmin is +-Inf or NaN decode as the page's f32 loop
+    does (IEEE: inf * 0 = NaN, inf - inf = NaN); NaNs compared as NaN."""
+    flat = _nonfinite_blocks(41).reshape(-1)
+    out = q2k.dequantize(dev(flat)).cpu().numpy()
+    want = oracle.dequantize(flat)
+    assert np.isnan(want).any() and np.isinf(want).any()
+    assert _same_or_both_nan(out, want)
+
+
+def test_gather_nonfinite_scales_match_oracle():
+    blocks = _nonfinite_blocks(42)
+    vocab = blocks.shape[0] // 2   # rows of 512 (two blocks)
+    table = blocks.reshape(-1)
+    ids = np.array([0, vocab - 1, 3, 3, 1], dtype=np.uint32)
+    out = q2k.embedding_gather(dev(table), dev(ids.astype(np.int32)), 512).cpu().numpy()
+    want = oracle.gather(table, vocab, 512, ids)
+    assert _same_or_both_nan(out, want)
+
+
 def test_dequantize_rejects_malformed_on_device():
     b = dev(wl.page_block(1))
     with pytest.raises(q2k.InvalidArgument):
