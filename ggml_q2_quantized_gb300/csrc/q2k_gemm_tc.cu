@@ -42,6 +42,12 @@ __device__ unsigned int g_tc_error;
 // Every GPU that loads the library keeps these bytes until the process exits.
 static __device__ __align__(256) uint8_t g_static_x_image[kStaticWorkspaceBytes];
 
+// The plain calls' own scratch (q2k_matmul / q2k_matmul_path / q2k_matmul_ex
+// without a workspace): the same x tile image, so that a caller who passes no
+// workspace still gets the weights-as-A kernel.  Calls that use it are
+// serialised on the GPU by an event per device (see launch_gemm_tc_plain).
+static __device__ __align__(256) uint8_t g_plain_x_image[kPlainScratchBytes];
+
 namespace {
 
 constexpr int kBM = 128;                 // x rows per tile (MMA M)
@@ -1796,6 +1802,39 @@ cudaError_t launch_gemm_tc_static(const float* x, const uint8_t* w, float* y, in
         image = addr[device];
     }
     return launch_gemm_tc(x, w, y, M, N, K, device, sm_count, image, stream);
+}
+
+cudaError_t launch_gemm_tc_plain(const float* x, const uint8_t* w, float* y, int M, int N, int K,
+                                 int device, int sm_count, cudaStream_t stream) {
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    const size_t need = gemm_tc_workspace_bytes(M, N, K);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) return e;
+    // No image needed (small m), too large, or inside a capture (where a wait
+    // on another stream's event is not allowed): the GEMM converts x itself.
+    if (need == 0 || need > kPlainScratchBytes || cs != cudaStreamCaptureStatusNone)
+        return launch_gemm_tc(x, w, y, M, N, K, device, sm_count, nullptr, stream);
+    static std::mutex mu;
+    static void* addr[64] = {};
+    static cudaEvent_t done[64] = {};
+    std::lock_guard<std::mutex> lk(mu);
+    if (addr[device] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_plain_x_image);
+        if (e != cudaSuccess) return e;
+        if (p == nullptr) return cudaErrorInvalidSymbol;
+        if (done[device] == nullptr) {
+            e = cudaEventCreateWithFlags(&done[device], cudaEventDisableTiming);
+            if (e != cudaSuccess) return e;
+        }
+        addr[device] = p;
+    }
+    // the previous call through this scratch (any stream) finishes first
+    e = cudaStreamWaitEvent(stream, done[device], 0);
+    if (e == cudaSuccess) e = launch_gemm_tc(x, w, y, M, N, K, device, sm_count, addr[device], stream);
+    if (e == cudaSuccess) e = cudaEventRecord(done[device], stream);
+    return e;
 }
 
 cudaError_t read_and_clear_tc_error(uint32_t* out, cudaStream_t stream) {

@@ -64,6 +64,18 @@
 #ifndef Q2K_GEMV_DEP_THREADS
 #define Q2K_GEMV_DEP_THREADS 256
 #endif
+//   Q2K_GEMV_PIECE_ROWS  weight rows per bulk copy and barrier (4 or 8)
+#ifndef Q2K_GEMV_PIECE_ROWS
+#define Q2K_GEMV_PIECE_ROWS 8
+#endif
+//   Q2K_GEMV_BIGK_GROUPS, Q2K_GEMV_BIGK_CAP_KB  independent calls with k > 8192:
+//                  groups of warps per CTA (1 or 2) and the CTA's shared-memory cap
+#ifndef Q2K_GEMV_BIGK_GROUPS
+#define Q2K_GEMV_BIGK_GROUPS 2
+#endif
+#ifndef Q2K_GEMV_BIGK_CAP_KB
+#define Q2K_GEMV_BIGK_CAP_KB 200
+#endif
 
 namespace q2k {
 
@@ -72,11 +84,12 @@ __device__ unsigned int g_gemv_error;
 namespace {
 
 constexpr int kGemvWarps = 8;
-// Rows per bulk copy and mbarrier: one block of the row loop (8 rows), so a
-// block waits for exactly one piece.  Piece starts are 8 rows = 672 k/256
-// bytes apart, a multiple of 16, so every piece keeps the chunk's offset from
-// a 16-byte boundary (as CTA chunks do, being a multiple of 4 rows apart).
-constexpr int kPieceRows = 8;
+// Rows per bulk copy and mbarrier: one block of the row loop, so a block waits
+// for exactly one piece.  Piece starts are 4 or 8 rows = 336 k/256 or 672 k/256
+// bytes apart, multiples of 16, so every piece keeps the chunk's offset from a
+// 16-byte boundary (as CTA chunks do, being a multiple of 4 rows apart).
+constexpr int kPieceRows = Q2K_GEMV_PIECE_ROWS;
+static_assert(kPieceRows == 4 || kPieceRows == 8, "Q2K_GEMV_PIECE_ROWS must be 4 or 8");
 constexpr int kM1MaxSlices = 256;  // k <= 16384
 // Threads per CTA of the m = 1 kernel.  A dependent call runs alone once its
 // predecessor completes, so it takes more threads per CTA (shorter critical
@@ -88,7 +101,7 @@ constexpr int kM1ThreadsIndependent = 128;
 // over the slices (twice the warps to hide latencies with).
 inline int m1_independent_threads(int K) {
     const int slices = K / 64;
-    return slices > 128 ? 2 * ((slices + 31) / 32 * 32) : kM1ThreadsIndependent;
+    return slices > 128 ? Q2K_GEMV_BIGK_GROUPS * ((slices + 31) / 32 * 32) : kM1ThreadsIndependent;
 }
 
 // ------------------------------------------------------------------ m = 1
@@ -563,7 +576,9 @@ bool plan_m1(int N, int K, int sm_count, int threads, bool whole_batches, M1Plan
     // shared memory (three share an SM) when 32 rows still fit there;
     // otherwise, and for dependent calls, the largest chunk that fits is taken.
     size_t cap = size_t(200) * 1024;
-    if (whole_batches && m1_smem(32, K, slices_pad) <= size_t(72) * 1024) cap = size_t(72) * 1024;
+    if (whole_batches)
+        cap = m1_smem(32, K, slices_pad) <= size_t(72) * 1024 ? size_t(72) * 1024
+                                                              : size_t(Q2K_GEMV_BIGK_CAP_KB) * 1024;
     int rows = 0;
     for (int waves = 1;; ++waves) {
         rows = (N + sm_count * waves - 1) / (sm_count * waves);

@@ -116,6 +116,16 @@ constexpr size_t kStaticWorkspaceBytes = size_t(8) << 20;
 cudaError_t launch_gemm_tc_static(const float* x, const uint8_t* w, float* y, int M, int N, int K,
                                   int device, int sm_count, cudaStream_t stream);
 
+// The plain calls' scratch: the tensor-core path of a call without a
+// workspace keeps its x tile image here when it fits (32 MiB: e.g. m <= 2048
+// at k = 7168, m <= 1024 at k = 14336).  Such calls wait for the previous one through it
+// (an event per device), so calls on different streams never share it at the
+// same time; inside a stream capture, or when the image does not fit, the
+// GEMM converts x itself (launch_gemm_tc without a workspace).
+constexpr size_t kPlainScratchBytes = size_t(32) << 20;
+cudaError_t launch_gemm_tc_plain(const float* x, const uint8_t* w, float* y, int M, int N, int K,
+                                 int device, int sm_count, cudaStream_t stream);
+
 // Read and clear the tensor-core kernels' device error word (synchronises `stream`).
 cudaError_t read_and_clear_tc_error(uint32_t* out, cudaStream_t stream);
 

@@ -147,11 +147,16 @@ q2k_status q2k_embedding_gather(const void *table, size_t table_bytes,
  *   w           device, w_bytes = n * k/256 * 84, 4-byte aligned
  *   y           device f32 [m, n] row-major, y_elems = m*n, 16-byte aligned;
  *               fully overwritten
- * Path: m <= 8 runs the fp32 GEMV (error within 1e-5 * sum_k |x w| per
- * output); m > 8 runs the bf16 tensor-core GEMM (x and W rounded to bf16,
- * fp32 accumulation; error within 8e-3 * sum_k |x w|), mirroring the pages'
- * switch of tolerance at rows > 8.  Repeated calls on the same inputs give
- * bit-identical y (no floating-point atomics). */
+ * Path: m <= 8 runs the fp32 GEMV: each weight is formed exactly as the
+ * page's f32 decode (dl*q - ml rounded once) and multiplied into fp32 sums in
+ * which a product passes through at most L roundings - L = 46 for m = 1 with
+ * k <= 16384, L = 71 + k/262144 otherwise - so the error is at most
+ * L * 2^-24 * sum_k |x w|: within the 1e-5 tolerance for k <= 2^24, for every
+ * finite x whose products x w stay in the f32 normal range.  m > 8 runs the bf16 tensor-core GEMM (x and W rounded to
+ * bf16, fp32 accumulation; error within 8e-3 * sum_k |x w|), mirroring the
+ * pages' switch of tolerance at rows > 8; without a workspace it uses the
+ * library's scratch as described at q2k_matmul_ex.  Repeated calls on the
+ * same inputs give bit-identical y (no floating-point atomics). */
 q2k_status q2k_matmul(const float *x, size_t x_elems, const void *w, size_t w_bytes,
                       float *y, size_t y_elems, const q2k_matmul_params *params,
                       q2k_stream_t stream);
@@ -381,8 +386,17 @@ size_t q2k_matmul_workspace_bytes(const q2k_matmul_params *params, q2k_path path
  *                    path) bytes, 16-byte aligned, not overlapping x, w or y.
  *                    Its contents on entry do not matter and are clobbered.
  *                    With it the tensor-core path converts x once in a prepass
- *                    and streams it into the GEMM by bulk copies (faster for
- *                    large m); without it the GEMM converts x itself.
+ *                    and streams it into the GEMM by bulk copies.  Without it
+ *                    (and in q2k_matmul / q2k_matmul_path) the library uses a
+ *                    scratch of its own, 32 MiB per device, for the same
+ *                    kernel when the x image fits (e.g. m <= 2048 at k = 7168,
+ *                    m <= 1024 at k = 14336): same bits as with a workspace.
+ *                    Such calls take turns on the GPU (each waits, through an
+ *                    event, for the previous one to finish with the scratch),
+ *                    so calls on different streams do not overlap there.
+ *                    Inside a stream capture, or when the image does not fit,
+ *                    the GEMM converts x itself instead (within the same
+ *                    tolerance, not the same bits).
  *   workspace_bytes  its size (ignored when workspace is NULL).
  * Same arguments, sizes, errors and tolerances otherwise.  Calls on different
  * streams must not share a workspace while both may run. */

@@ -442,24 +442,75 @@ def test_const_weights_flag_same_bits(n, k):
     assert_close(b.cpu().numpy().astype(np.float64), yref, s, TOL_GEMV, f"const n={n} k={k}")
 
 
+def _captured_call(xd, wd, n):
+    """q2k.matmul without a workspace enqueued inside a CUDA graph capture:
+    the library then runs the GEMM that converts x itself (no scratch)."""
+    s = torch.cuda.Stream()
+    out = torch.empty((xd.shape[0], n), dtype=torch.float32, device="cuda")
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        q2k.matmul(xd, wd, n, path="tensor", workspace=None, out=out)
+    g.replay()
+    torch.cuda.synchronize()
+    return out
+
+
 @pytest.mark.parametrize("m,n,k", [(9, 8, 256), (130, 10000, 256), (300, 1000, 512), (16, 4096, 1024)])
 def test_tensor_workspace_and_in_kernel_conversion_agree(m, n, k):
     """With a workspace x is converted by the prepass and the weights-as-A
-    kernel runs; without, the GEMM converts x itself with x as the A operand.
-    Both round x and the weights to bf16 the same way; the MMAs differ in
-    orientation, so only the fp32 accumulation order may differ."""
+    kernel runs; a plain call without one uses the library's own scratch for
+    the same kernel (bit-identical); inside a graph capture the GEMM converts
+    x itself with x as the A operand.  All round x and the weights to bf16 the
+    same way; the MMAs differ in orientation, so only the fp32 accumulation
+    order may differ."""
     x, w = wl.make_matmul_inputs(3000 + m + n, m, n, k)
     xd, wd = dev(x), dev(w)
-    a = q2k.matmul(xd, wd, n, path="tensor", workspace=None)
+    a = _captured_call(xd, wd, n)
     b = q2k.matmul(xd, wd, n, path="tensor")
+    c = q2k.matmul(xd, wd, n, path="tensor", workspace=None)
     torch.cuda.synchronize()
     yref, s = oracle.matmul(x, w, n, threads=ORACLE_THREADS)
     ya = a.cpu().numpy().astype(np.float64)
     yb = b.cpu().numpy().astype(np.float64)
-    assert_close(ya, yref, s, TOL_TC, f"no-ws m={m} n={n} k={k}")
+    yc = c.cpu().numpy().astype(np.float64)
+    assert_close(ya, yref, s, TOL_TC, f"in-kernel x m={m} n={n} k={k}")
     assert_close(yb, yref, s, TOL_TC, f"ws m={m} n={n} k={k}")
+    assert np.array_equal(yb, yc), "the plain call's scratch runs the workspace kernel: same bits"
     # same bf16 operands, fp32 sums of k exact products in two orders
     assert np.all(np.abs(ya - yb) <= 1e-5 * s + 1e-30)
+
+
+def test_plain_calls_on_two_streams_share_the_scratch_safely():
+    """Plain (no-workspace) tensor calls on two streams at once: the library's
+    scratch is handed from one to the next on the GPU, so both are correct."""
+    m, n, k = 300, 2048, 2048
+    x1, w1 = wl.make_matmul_inputs(4101, m, n, k)
+    x2, w2 = wl.make_matmul_inputs(4102, m, n, k)
+    d = [(dev(x1), dev(w1)), (dev(x2), dev(w2))]
+    want = [q2k.matmul(xd, wd, n, path="tensor") for xd, wd in d]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [[], []]
+    torch.cuda.synchronize()
+    for rep in range(6):
+        for i, st in enumerate(streams):
+            with torch.cuda.stream(st):
+                outs[i].append(q2k.matmul(d[i][0], d[i][1], n, path="tensor", workspace=None))
+    torch.cuda.synchronize()
+    for i in range(2):
+        for y in outs[i]:
+            assert torch.equal(y, want[i])
+
+
+def test_plain_call_beyond_the_scratch_converts_x_in_kernel():
+    """An x image larger than the library's 32 MiB scratch (m = 4096, k = 4096:
+    32 MiB + padding) falls back to the GEMM that converts x itself."""
+    m, n, k = 4224, 136, 4096
+    x, w = wl.make_matmul_inputs(4103, m, n, k)
+    y = q2k.matmul(dev(x), dev(w), n, path="tensor", workspace=None)
+    torch.cuda.synchronize()
+    yref, s = oracle.matmul(x, w, n, threads=ORACLE_THREADS)
+    assert_close(y.cpu().numpy().astype(np.float64), yref, s, TOL_TC, "beyond scratch")
 
 
 @pytest.mark.parametrize("n,k", [(4096, 4096), (333, 4096), (14336, 4096), (77, 14336)])
