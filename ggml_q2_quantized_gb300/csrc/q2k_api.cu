@@ -198,23 +198,15 @@ q2k_status check_matmul(const float* x, size_t x_elems, const void* w, size_t w_
     return Q2K_OK;
 }
 
-// An optional scratch for x converted once per x row (rows rows of k): NULL,
-// or at least q2k_x_planes_bytes(k, rows) bytes, 16-byte aligned, not
-// overlapping the call's buffers.  *planes is the scratch when it will be
-// used (k small enough for the m = 1 kernel), else NULL.
+// The batched and routed calls' optional scratch argument: accepted for ABI
+// compatibility and not used (their kernels convert x per thread; see
+// q2k_x_planes_bytes).
 q2k_status check_planes_scratch(void* scratch, size_t scratch_bytes, uint32_t k, size_t rows,
                                 const void* x, size_t x_bytes, const void* w, size_t w_bytes,
                                 const void* y, size_t y_bytes, uint8_t** planes) {
+    (void)scratch, (void)scratch_bytes, (void)k, (void)rows, (void)x, (void)x_bytes, (void)w;
+    (void)w_bytes, (void)y, (void)y_bytes;
     *planes = nullptr;
-    if (scratch == nullptr || !q2k::gemv_shares_planes(1, int(k))) return Q2K_OK;
-    const size_t need = q2k::gemv_planes_stride(int(k)) * rows;
-    if (scratch_bytes < need)
-        return fail(Q2K_ERR_INVALID_ARGUMENT, "scratch has %zu bytes, needs %zu", scratch_bytes, need);
-    if (!aligned(scratch, 16)) return fail(Q2K_ERR_INVALID_ARGUMENT, "scratch must be 16-byte aligned");
-    if (overlaps(scratch, need, x, x_bytes) || overlaps(scratch, need, w, w_bytes) ||
-        overlaps(scratch, need, y, y_bytes))
-        return fail(Q2K_ERR_INVALID_ARGUMENT, "scratch must not alias x, w or y");
-    *planes = static_cast<uint8_t*>(scratch);
     return Q2K_OK;
 }
 
@@ -595,7 +587,6 @@ q2k_status q2k_matmul_batched_mv(const float* x, size_t x_elems, const void* w, 
     pr.w_stride = static_cast<long long>(per_w);
     pr.y_stride = static_cast<long long>(n);
     cudaError_t e = cudaSuccess;
-    if (planes != nullptr) e = q2k::launch_prep_x_planes(x, int(k), planes, s, int(batches));
     if (e == cudaSuccess)
         e = q2k::launch_gemv_problems(x, static_cast<const uint8_t*>(w), y, 1, int(n), int(k),
                                       dev.device, dev.sm_count, 0u, pr, int(batches), s, planes,
@@ -758,7 +749,6 @@ q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void*
         pr.w2 = static_cast<const uint8_t*>(wb);
         pr.y2 = yb;
     }
-    if (planes != nullptr) e = q2k::launch_prep_x_planes(x, int(p->k), planes, s, int(x_rows));
     if (e == cudaSuccess)
         e = q2k::launch_gemv_problems(x, static_cast<const uint8_t*>(wa), ya, 1, int(p->n), int(p->k),
                                       dev.device, dev.sm_count, 0u, pr, int(pair ? 2 * routes : routes),
@@ -773,8 +763,12 @@ q2k_status routed_call(const float* x, size_t x_elems, bool slotted, const void*
 extern "C" {
 
 size_t q2k_x_planes_bytes(uint32_t k, uint32_t rows) {
-    if (k == 0 || k % Q2K_QK_K != 0 || k > INT_MAX || !q2k::gemv_shares_planes(1, int(k))) return 0;
-    return q2k::gemv_planes_stride(int(k)) * rows;
+    // The batched and routed GEMV launches bring x into their per-slice form
+    // per thread (a few instructions per CTA); a separate prepare launch, and
+    // the wait behind it, cost more than it saved.  They take no scratch.
+    (void)k;
+    (void)rows;
+    return 0;
 }
 
 q2k_status q2k_matmul_id(const float* x, size_t x_elems, const void* w, size_t w_bytes,

@@ -198,22 +198,17 @@ enum {
  * Each batch's y is bit-identical to q2k_matmul(m = 1) of that batch's x and W
  * alone (the same kernel and arithmetic run per batch): fp32, error within
  * 1e-5 * sum_k |x w|.  batches <= 65535.
- *   scratch  NULL or q2k_x_planes_bytes(k, batches) bytes (see there). */
+ *   scratch  not used (see q2k_x_planes_bytes). */
 q2k_status q2k_matmul_batched_mv(const float *x, size_t x_elems, const void *w, size_t w_bytes,
                                  float *y, size_t y_elems, uint32_t batches, uint32_t m,
                                  uint32_t n, uint32_t k, void *scratch, size_t scratch_bytes,
                                  q2k_stream_t stream);
 
 /* q2k_x_planes_bytes - device bytes of scratch the batched and routed calls
- * use to bring x into the m = 1 GEMV's per-slice form once per x row (rows
- * rows of k) instead of once per CTA: each 64-weight slice of x scaled by a
- * power of two, in the order the kernel reads it, plus one scale factor per
- * slice - k/64 * 260 bytes per row, rounded up to 256.
- * 0 when k is not a positive multiple of 256 or above 16384 (no such
- * sharing).  Those calls take such a scratch as their `scratch` argument:
- * NULL (or smaller) keeps the conversion per CTA; results are the same bits
- * either way.  It must be 16-byte aligned and overlap none of the call's
- * buffers. */
+ * take: 0.  Their kernels bring x into the GEMV's per-slice form per thread
+ * (a few instructions per CTA), which costs less than a separate launch and
+ * the wait behind it.  The `scratch` arguments of those calls are accepted
+ * for compatibility and not used (any value, NULL included). */
 size_t q2k_x_planes_bytes(uint32_t k, uint32_t rows);
 
 /* q2k_matmul_id - the expert-routed product of a mixture-of-experts layer:
@@ -239,9 +234,7 @@ size_t q2k_x_planes_bytes(uint32_t k, uint32_t rows);
  * allow 2e-4 absolute, 1e-2 for their reduced-precision path); each route's
  * row is bit-identical to q2k_matmul(m = 1) of its token and expert.
  * n_tokens * top_k <= 65535.
- *   scratch  NULL or q2k_x_planes_bytes(k, n_tokens) bytes (n_tokens * top_k
- *            for the slotted call): each x row converted once for all its
- *            routes (see q2k_x_planes_bytes). */
+ *   scratch  not used (see q2k_x_planes_bytes). */
 q2k_status q2k_matmul_id(const float *x, size_t x_elems, const void *w, size_t w_bytes,
                          const uint32_t *ids, float *y, size_t y_elems,
                          const q2k_matmul_id_params *params, uint32_t *bad_id_count,

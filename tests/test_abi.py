@@ -323,18 +323,16 @@ def test_matmul_ex_batch_checks_every_call_first(lib):
     assert lib.q2k_matmul_ex_batch(None, 0, None, 0, None) == 0   # nothing to do
 
 
-def test_x_planes_scratch_size_and_checks(lib):
-    # k/64 slices x (64 scaled floats + 1 scale factor) per row, rounded up to 256
-    assert lib.q2k_x_planes_bytes(4096, 3) == 3 * ((64 * 260 + 255) // 256 * 256)
-    assert lib.q2k_x_planes_bytes(16640, 1) == 0     # above the m = 1 kernel's k
-    assert lib.q2k_x_planes_bytes(255, 1) == 0
-    need = lib.q2k_x_planes_bytes(256, 3)
+def test_x_planes_scratch_is_not_needed(lib):
+    # the batched and routed GEMV launches convert x per thread: no scratch
+    for k in (256, 4096, 16384, 16640):
+        assert lib.q2k_x_planes_bytes(k, 3) == 0
+    # a scratch argument is accepted and ignored: the call gets past every
+    # argument check (it then fails only for want of a device here)
     x, w, y = 0x10000, 0x100000, 0x1000000
     args = (x, 3 * 256, w, 3 * 8 * 84, y, 3 * 8, 3, 1, 8, 256)
-    assert lib.q2k_matmul_batched_mv(*args, 0x2000000, need - 16, None) == INVALID
-    assert "scratch" in lib.q2k_last_error().decode()
-    assert lib.q2k_matmul_batched_mv(*args, 0x2000008, need, None) == INVALID
-    assert lib.q2k_matmul_batched_mv(*args, x, need, None) == INVALID    # over x
+    st = lib.q2k_matmul_batched_mv(*args, 0x2000008, 16, None)
+    assert st != INVALID, lib.q2k_last_error().decode()
 
 
 def test_python_matmul_id_workspace_bytes_matches_the_library(lib):
