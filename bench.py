@@ -677,8 +677,11 @@ def run_ours(args):
         sec = {}
         for name in ("ffn_pair", "ffn_pair_down", "spec_verify_m16", "prefill_m512"):
             sw = wl.by_name(name)
+            # the step's calls are projections of one x, each with its own W
+            # and y (Q2K_FLAG_INDEPENDENT: used by the GEMV and by the
+            # small-m tensor path, ignored at M = 512)
             r = bench_matmul(torch, q2k, sw, max(3, steps // 4), 3, l2_bytes, device,
-                             independent=sw.m == 1)
+                             independent=True)
             us = r["us_per_call"]
             entry = {"us_per_call": us, "weight_GBps": sw.weight_bytes / (us * 1e-6) / 1e9,
                      "TFLOPs": sw.flops / (us * 1e-6) / 1e12, "m": sw.m, "n": sw.n, "k": sw.k,

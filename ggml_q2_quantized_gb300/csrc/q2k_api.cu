@@ -359,10 +359,13 @@ cudaError_t launch_matmul_ex(q2k_path path, uint32_t flags, const float* x, cons
                                 ((flags & Q2K_FLAG_CONST_WEIGHTS) ? q2k::kGemvConstWeights : 0u) |
                                     ((flags & Q2K_FLAG_INDEPENDENT) ? q2k::kGemvIndependent : 0u),
                                 s);
+    const uint32_t kf = ((flags & Q2K_FLAG_CONST_WEIGHTS) ? q2k::kGemvConstWeights : 0u) |
+                        ((flags & Q2K_FLAG_INDEPENDENT) ? q2k::kGemvIndependent : 0u);
     if (ws == nullptr)
         return q2k::launch_gemm_tc_plain(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device,
-                                         dev.sm_count, s);
-    return q2k::launch_gemm_tc(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count, ws, s);
+                                         dev.sm_count, s, kf);
+    return q2k::launch_gemm_tc(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count, ws,
+                               s, kf);
 }
 
 }  // namespace

@@ -676,6 +676,11 @@ struct WtRouted {
     const int* row_route = nullptr;
     long long expert_stride = 0;
     int expert_rows = 0;
+    // small m: kGemvConstWeights (no grid that may still run writes W: the
+    // weight copies start before the dependency wait) and kGemvIndependent (it
+    // touches neither x, W nor y: nothing waits for it but CTA (0, 0, 0),
+    // before it exits, so calls still complete in stream order)
+    uint32_t flags = 0;
 };
 
 // ---- thread-block cluster: barrier and distributed shared memory -----------
@@ -899,7 +904,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
         // A columns of K-steps seg and 2 + seg, stage 0
         const uint32_t a_col0 = tmem_base + t_lane + C::kColA + 8u * seg;
         if constexpr (C::kSmall) {
-            pdl_wait_prerequisites();  // x (and W) may be written by the grid before this one
+            // x (and W) may be written by the grid before this one
+            if (!(rt.flags & kGemvIndependent)) pdl_wait_prerequisites();
             // x rows m0 .. m0 + nx - 1 over the CTA's K stages -> bf16, stage i
             // at kOffX + i kXStage in the swizzled K-major layout the MMA reads
             // (rows past M as zeros).  One 16-byte chunk (8 K-elements) per
@@ -1213,7 +1219,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
         if (kTmaW && lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w))
                          : "memory");
-            if constexpr (C::kSmall) pdl_wait_prerequisites();  // W may be written by it
+            if (C::kSmall && !(rt.flags & (kGemvConstWeights | kGemvIndependent)))
+                pdl_wait_prerequisites();  // W may be written by it
             const uint32_t raw0 = sbase + C::kOffRaw;
             for (int b = 0; b < n_blocks; ++b) {
                 const int buf = b % C::kRaw;
@@ -1315,6 +1322,11 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                      "r"(C::kTmemCols)
                      : "memory");
     }
+    // An independent call completes only after the grid before it, so work
+    // enqueued later on the stream sees every earlier call complete.
+    if (C::kSmall && (rt.flags & kGemvIndependent) && threadIdx.x == 0 && blockIdx.x == 0 &&
+        blockIdx.y == 0 && blockIdx.z == 0)
+        pdl_wait_prerequisites();
 }
 
 // x (f32 [M, K]) -> bf16 in the tile image the GEMM copies into shared memory:
@@ -1461,14 +1473,16 @@ cudaError_t launch_wt_kernel(const uint8_t* xa, const float* xf, const uint8_t* 
 template <int kXRows>
 cudaError_t launch_wt(const uint8_t* xa, const float* xf, const uint8_t* w, float* y,
                       float* partial, unsigned int* tile_count, int splits, int M, int N, int K,
-                      int device, cudaStream_t stream) {
+                      int device, cudaStream_t stream, uint32_t flags = 0) {
     alignas(64) CUtensorMap map;
+    WtRouted rt;
+    rt.flags = flags;
     if (make_weight_map(&map, w, N, K, 128))
         return launch_wt_kernel<kXRows, true>(xa, xf, w, y, partial, tile_count, splits, M, N, K,
-                                              device, map, stream);
+                                              device, map, stream, rt);
     memset(&map, 0, sizeof(map));
     return launch_wt_kernel<kXRows, false>(xa, xf, w, y, partial, tile_count, splits, M, N, K,
-                                           device, map, stream);
+                                           device, map, stream, rt);
 }
 
 // K parts of the weights-as-A kernel: with fewer than 64 weight tiles (small m
@@ -1553,12 +1567,13 @@ size_t gemm_tc_workspace_bytes(int M, int N, int K) {
 }
 
 cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, int N, int K,
-                           int device, int sm_count, void* workspace, cudaStream_t stream) {
+                           int device, int sm_count, void* workspace, cudaStream_t stream,
+                           uint32_t flags) {
     if (const int parts = small_splits(M, N, K)) {
         switch (small_xrows(M)) {
-            case 16: return launch_wt<16>(nullptr, x, w, y, nullptr, nullptr, parts, M, N, K, device, stream);
-            case 32: return launch_wt<32>(nullptr, x, w, y, nullptr, nullptr, parts, M, N, K, device, stream);
-            default: return launch_wt<64>(nullptr, x, w, y, nullptr, nullptr, parts, M, N, K, device, stream);
+            case 16: return launch_wt<16>(nullptr, x, w, y, nullptr, nullptr, parts, M, N, K, device, stream, flags);
+            case 32: return launch_wt<32>(nullptr, x, w, y, nullptr, nullptr, parts, M, N, K, device, stream, flags);
+            default: return launch_wt<64>(nullptr, x, w, y, nullptr, nullptr, parts, M, N, K, device, stream, flags);
         }
     }
     const int bn = choose_bn(M, N, sm_count);
@@ -1805,7 +1820,7 @@ cudaError_t launch_gemm_tc_static(const float* x, const uint8_t* w, float* y, in
 }
 
 cudaError_t launch_gemm_tc_plain(const float* x, const uint8_t* w, float* y, int M, int N, int K,
-                                 int device, int sm_count, cudaStream_t stream) {
+                                 int device, int sm_count, cudaStream_t stream, uint32_t flags) {
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     const size_t need = gemm_tc_workspace_bytes(M, N, K);
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -1814,7 +1829,7 @@ cudaError_t launch_gemm_tc_plain(const float* x, const uint8_t* w, float* y, int
     // No image needed (small m), too large, or inside a capture (where a wait
     // on another stream's event is not allowed): the GEMM converts x itself.
     if (need == 0 || need > kPlainScratchBytes || cs != cudaStreamCaptureStatusNone)
-        return launch_gemm_tc(x, w, y, M, N, K, device, sm_count, nullptr, stream);
+        return launch_gemm_tc(x, w, y, M, N, K, device, sm_count, nullptr, stream, flags);
     static std::mutex mu;
     static void* addr[64] = {};
     static cudaEvent_t done[64] = {};
@@ -1832,7 +1847,7 @@ cudaError_t launch_gemm_tc_plain(const float* x, const uint8_t* w, float* y, int
     }
     // the previous call through this scratch (any stream) finishes first
     e = cudaStreamWaitEvent(stream, done[device], 0);
-    if (e == cudaSuccess) e = launch_gemm_tc(x, w, y, M, N, K, device, sm_count, addr[device], stream);
+    if (e == cudaSuccess) e = launch_gemm_tc(x, w, y, M, N, K, device, sm_count, addr[device], stream, flags);
     if (e == cudaSuccess) e = cudaEventRecord(done[device], stream);
     return e;
 }

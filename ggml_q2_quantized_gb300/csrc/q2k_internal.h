@@ -87,8 +87,13 @@ size_t gemm_tc_workspace_bytes(int M, int N, int K);
 // workspace of gemm_tc_workspace_bytes(M, N, K) bytes (16-byte aligned), x is first
 // converted to the bf16 tile image there and the GEMM copies A stages in bulk;
 // with workspace == nullptr the GEMM converts x itself.
+// flags (the small-m mode, m <= 64, only; see GemvProblems' kGemv* above):
+// kGemvConstWeights lets the weight copies start before the dependency wait;
+// kGemvIndependent also reads x and writes y without waiting for the grid
+// before, which then only CTA (0, 0, 0) waits for, before it exits.
 cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, int N, int K,
-                           int device, int sm_count, void* workspace, cudaStream_t stream);
+                           int device, int sm_count, void* workspace, cudaStream_t stream,
+                           uint32_t flags = 0);
 
 // Routed product on tensor cores: route r = 0..routes-1 multiplies x row
 // r / x_div by expert ids[r]'s weights (w + ids[r] * expert_stride, N rows)
@@ -124,7 +129,7 @@ cudaError_t launch_gemm_tc_static(const float* x, const uint8_t* w, float* y, in
 // GEMM converts x itself (launch_gemm_tc without a workspace).
 constexpr size_t kPlainScratchBytes = size_t(32) << 20;
 cudaError_t launch_gemm_tc_plain(const float* x, const uint8_t* w, float* y, int M, int N, int K,
-                                 int device, int sm_count, cudaStream_t stream);
+                                 int device, int sm_count, cudaStream_t stream, uint32_t flags = 0);
 
 // Read and clear the tensor-core kernels' device error word (synchronises `stream`).
 cudaError_t read_and_clear_tc_error(uint32_t* out, cudaStream_t stream);

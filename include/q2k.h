@@ -181,7 +181,11 @@ enum {
      * y, enqueued back to back).  The m = 1 GEMV then reads x and writes y
      * without waiting for the kernel before it, so consecutive calls overlap;
      * it still waits for that kernel before it finishes, so calls complete in
-     * stream order.  Implies Q2K_FLAG_CONST_WEIGHTS.  Other paths ignore it. */
+     * stream order.  Implies Q2K_FLAG_CONST_WEIGHTS.
+     * Both flags also apply to the tensor-core path for m <= 64 (whose GEMM
+     * converts x itself): its weight copies (CONST_WEIGHTS), and its x
+     * conversion and y stores (INDEPENDENT), start before the wait for the
+     * kernel before.  The other paths ignore them. */
     Q2K_FLAG_INDEPENDENT = 2
 };
 

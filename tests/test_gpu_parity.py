@@ -363,15 +363,36 @@ def test_tensor_spec_verify_workload_full():
     print(f"{w.name}: max |y - y_ref| / S = {ratio:.3e}")
 
 
-@pytest.mark.parametrize("m,n,k", [(512, 7168, 7168), (512, 8192, 1024)])
-def test_tensor_large_sampled_rows(m, n, k):
-    """Full-size prefill (and the 256-row tile width) on sampled weight rows."""
-    seed = 4 if (m, n, k) == (512, 7168, 7168) else 77
-    if (m, n, k) == (512, 7168, 7168):
-        inp = wl.make_inputs(wl.WORKLOADS[4])
-        x, w = inp.x, inp.w
-    else:
-        x, w = wl.make_matmul_inputs(seed, m, n, k)
+def test_tensor_prefill_workload_full_every_path():
+    """The prefill workload (M=512, N=K=7168) in full, every one of its 3.7 M
+    outputs against the oracle: with a workspace (the binding's default), as
+    the plain C call q2k_matmul makes it (the library's own scratch), and
+    enqueued inside a graph capture (the GEMM converts x itself)."""
+    w_ = wl.WORKLOADS[4]
+    inp = wl.make_inputs(w_)
+    x, w = inp.x, inp.w
+    yref, s = oracle.matmul(x, w, w_.n, threads=ORACLE_THREADS)
+    xd, wd = dev(x), dev(w)
+    lib = q2k.load()
+    y_plain = torch.full((w_.m, w_.n), float("nan"), device="cuda")
+    p = q2k.MatmulParams(w_.m, w_.n, w_.k, 10)
+    st = lib.q2k_matmul(xd.data_ptr(), xd.numel(), wd.data_ptr(), wd.numel(), y_plain.data_ptr(),
+                        y_plain.numel(), ctypes.byref(p), torch.cuda.current_stream().cuda_stream)
+    assert st == 0, lib.q2k_last_error().decode()
+    results = {"workspace": q2k.matmul(xd, wd, w_.n, path="auto"), "plain C call": y_plain,
+               "in-kernel x (capture)": _captured_call(xd, wd, w_.n)}
+    torch.cuda.synchronize()
+    for name, y in results.items():
+        ratio = assert_close(y.cpu().numpy().astype(np.float64), yref, s, TOL_TC,
+                             f"prefill 512x7168x7168 {name}")
+        print(f"prefill {name}: max |y - y_ref| / S = {ratio:.3e}")
+    assert torch.equal(results["workspace"], results["plain C call"])
+
+
+def test_tensor_256_row_tiles_sampled_rows():
+    """The 256-row tile width at a long N (8192) and short K on sampled weight rows."""
+    m, n, k, seed = 512, 8192, 1024, 77
+    x, w = wl.make_matmul_inputs(seed, m, n, k)
     y = run_matmul(x, w, n, "auto")
     rng = np.random.default_rng(seed)
     rows = np.unique(np.concatenate([rng.choice(n, 40, replace=False), [0, n - 1]]))
@@ -550,6 +571,36 @@ def test_independent_calls_complete_in_order_before_a_dependent_one():
             assert_close(got[:, i * n:(i + 1) * n], yref, s, TOL_GEMV, f"projection {i}")
         zref, s = oracle.matmul(got.astype(np.float32), w_next, 256, threads=ORACLE_THREADS)
         assert_close(z.cpu().numpy().astype(np.float64), zref, s, TOL_GEMV, f"consumer rep {rep}")
+
+
+@pytest.mark.parametrize("m", [16, 40])
+def test_tensor_small_m_flags_same_bits_and_order(m):
+    """The small-m tensor path honours Q2K_FLAG_CONST_WEIGHTS and _INDEPENDENT
+    (its weight copies, x conversion and y stores start before the wait for
+    the kernel before): the same bits as without, and independent calls still
+    finish before a dependent consumer of their outputs runs."""
+    n_proj, n, k = 5, 1024, 4096
+    x = wl.make_matmul_inputs(601 + m, m, 1, k)[0]
+    ws = [wl.make_matmul_inputs(610 + i, m, n, k)[1] for i in range(n_proj)]
+    w_next = wl.make_matmul_inputs(630, 1, 512, n)[1]
+    xd = dev(x)
+    wds = [dev(w) for w in ws]
+    wnd = dev(w_next)
+    base = [q2k.matmul(xd, wd, n, path="tensor") for wd in wds]
+    # projection i writes rows i m .. i m + m - 1 of `stack`, which the
+    # consumer then reads as its x
+    stack = torch.empty((n_proj * m, n), device="cuda")
+    for rep in range(3):
+        stack.fill_(float("nan"))
+        for i in range(n_proj):
+            q2k.matmul(xd, wds[i], n, out=stack[i * m:(i + 1) * m], path="tensor",
+                       independent=(rep != 1), const_weights=(rep == 1))
+        z = q2k.matmul(stack, wnd, 512, path="tensor")
+        torch.cuda.synchronize()
+        for i in range(n_proj):
+            assert torch.equal(stack[i * m:(i + 1) * m], base[i]), f"projection {i}, rep {rep}"
+        zref, s = oracle.matmul(stack.cpu().numpy(), w_next, 512, threads=ORACLE_THREADS)
+        assert_close(z.cpu().numpy().astype(np.float64), zref, s, TOL_TC, f"consumer rep {rep}")
 
 
 def test_bounded_wait_times_out_and_reports_without_fault():
