@@ -611,6 +611,12 @@ constexpr int kMaxKParts = 8;
 // converted to bf16 by the kernel itself and stays in shared memory, in this
 // many bytes.
 constexpr int kSmallXBytes = 160 * 1024;
+#ifndef Q2K_TC_SMALL_ACC
+#define Q2K_TC_SMALL_ACC 1
+#endif
+#ifndef Q2K_TC_SMALL_STAGES
+#define Q2K_TC_SMALL_STAGES 8
+#endif
 
 template <int kXRows, bool kTmaW>
 struct WtCfg {
@@ -634,7 +640,20 @@ struct WtCfg {
     // x barriers: a full / empty pair per ring stage; small m has one "all of
     // x converted" barrier (one arrival per decoder warp)
     static constexpr int kXBars = kSmall ? 1 : kXStages;
-    static constexpr int kAStages = 8;                      // decoded stages in TMEM
+    // Accumulators.  A narrow MMA (16 to 64 x rows) costs about the same
+    // whatever its N, and a run of them into one accumulator issues back to
+    // back; rotating over several costs more per MMA, so small m keeps one
+    // unless Q2K_TC_SMALL_ACC says otherwise.
+    static constexpr int kAcc = kSmall ? Q2K_TC_SMALL_ACC : 1;
+    static constexpr uint32_t kColA = kXRows * kAcc;        // A ring after the accumulators
+    static constexpr int kTmemCols = 512;
+    // Decoded stages in TMEM (32 columns each).  The decoders' TMEM stores
+    // and the narrow MMAs reading A from TMEM slow each other down; a ring of
+    // 8 (Q2K_TC_SMALL_STAGES) keeps the decoders at most two blocks ahead and
+    // measured faster than deeper rings (12, 15) or shallower ones (4, 6).
+    static constexpr int kAStages =
+        kSmall ? std::min(Q2K_TC_SMALL_STAGES, static_cast<int>((kTmemCols - kColA) / 32)) : 8;
+    static_assert(kAStages >= 4, "a block's four stages must fit in TMEM at once");
     // Raw weight slabs: the decoders take a block into registers as soon as it
     // lands, so two slabs keep the next block's copy a whole block ahead.  A
     // small-m CTA has few blocks and little else to hide their latency behind:
@@ -645,13 +664,6 @@ struct WtCfg {
     // starts at the 16-byte boundary at or below the block).
     static constexpr int kRawPitch = kTmaW ? kTmaBoxBytes : kBlockBytes;
     static constexpr int kRawBytes = kRows * kRawPitch;
-    // Accumulators.  Consecutive MMAs into one accumulator wait for each other;
-    // a narrow MMA (16 to 64 x rows) is over long before that latency, so small
-    // m rotates its MMAs over several accumulators (summed in the epilogue,
-    // in order) to keep the tensor pipe busy.
-    static constexpr int kAcc = kSmall ? (kXRows <= 32 ? 8 : 4) : 1;
-    static constexpr uint32_t kColA = kXRows * kAcc;        // A ring after the accumulators
-    static constexpr int kTmemCols = 512;
     static constexpr int kOffX = 0;
     static constexpr int kOffRaw = kXStages * kXStage;
     // bars: x_full[kXBars], x_empty[kXBars], a_full[kAStages], a_empty[kAStages],
@@ -858,26 +870,29 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
         // now, read x and W and write y only after waiting for it.
         pdl_allow_dependents();
     }
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kXBars; ++s) {
+    if (warp == 0) {
+        // the barriers are set up by the lanes of warp 0 in parallel
+        for (int s = lane; s < C::kXBars; s += 32) {
             // producer's expect-tx arrival + the copy's bytes; small m: one
             // arrival per decoder warp once its share of x is converted
             mbar_init(bar_xfull + 8 * s, C::kSmall ? C::kDecWarps : 1);
             mbar_init(bar_xempty + 8 * s, 1);  // MMA commit
         }
-        for (int s = 0; s < C::kAStages; ++s) {
+        for (int s = lane; s < C::kAStages; s += 32) {
             mbar_init(bar_afull + 8 * s, C::kGroupWarps);  // one arrival per warp of its group
             mbar_init(bar_aempty + 8 * s, 1);            // MMA commit
         }
-        for (int r = 0; r < C::kRaw; ++r) {
+        for (int r = lane; r < C::kRaw; r += 32) {
             // TMA: the producer's expect-tx arrival + the box bytes; else one
             // arrival per decoder warp once its cp.async groups landed
             mbar_init(bar_raw + 8 * r, kTmaW ? 1 : C::kDecWarps);
             mbar_init(bar_rawempty + 8 * r, C::kDecWarps);  // decoders done reading (kTmaW)
         }
-        mbar_init(bar_accum, 1);
-        mbar_init(bar_drain, 1);
-        *abort_flag = 0;
+        if (lane == 0) {
+            mbar_init(bar_accum, 1);
+            mbar_init(bar_drain, 1);
+            *abort_flag = 0;
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == C::kMmaWarp) {
@@ -1177,7 +1192,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                         mma_bf16_tmem_a(d, a_s + 8u * kk, xdesc + 2u * kk, idesc,
                                         g >= C::kAcc ? 1u : 0u);
                     }
-                    mma_commit(bar_aempty + 8 * sa);
+                    // only a stage the decoders refill needs its release
+                    if (i + C::kAStages < n_iters) mma_commit(bar_aempty + 8 * sa);
                     if (!C::kSmall) mma_commit(bar_xempty + 8 * sx);
                 }
             }
