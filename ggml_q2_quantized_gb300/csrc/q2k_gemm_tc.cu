@@ -980,8 +980,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
             const int buf = b % C::kRaw;
             uint32_t mine;
             if constexpr (kTmaW) {
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait_lean(bar_raw + 8 * buf, (b / C::kRaw) & 1,
-                                                            abort_flag, err, kErrTimeoutEmpty, 64))) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_raw + 8 * buf, (b / C::kRaw) & 1,
+                                                               abort_flag, err, kErrTimeoutEmpty))) {
                     ok = false;
                     break;
                 }
@@ -990,8 +990,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                 cp_async_wait_group<C::kRaw - 2>();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_raw + 8 * buf);
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait_lean(bar_raw + 8 * buf, (b / C::kRaw) & 1,
-                                                            abort_flag, err, kErrTimeoutEmpty, 64))) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_raw + 8 * buf, (b / C::kRaw) & 1,
+                                                               abort_flag, err, kErrTimeoutEmpty))) {
                     ok = false;
                     break;
                 }
@@ -1037,8 +1037,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                 }
                 if (i >= C::kAStages &&
                     !__all_sync(0xFFFFFFFFu,
-                                mbar_wait_lean(bar_aempty + 8 * s, ((i / C::kAStages) - 1) & 1,
-                                               abort_flag, err, kErrTimeoutEmpty, 64))) {
+                                mbar_wait_bounded(bar_aempty + 8 * s, ((i / C::kAStages) - 1) & 1,
+                                                  abort_flag, err, kErrTimeoutEmpty))) {
                     ok = false;
                     break;
                 }
@@ -1213,17 +1213,17 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
     } else if (warp == C::kWaitWarp) {
         // ---------------- stage waiter: hands filled stages to the MMA warp ----------------
         if (C::kSmall && lane == 0)  // all of x, once
-            mbar_wait_lean(bar_xfull, 0, abort_flag, err, kErrTimeoutFull, 32);
+            mbar_wait_bounded(bar_xfull, 0, abort_flag, err, kErrTimeoutFull);
         for (int i0 = 0; i0 < n_iters; i0 += C::kPair) {
             if (lane == 0 && !*abort_flag) {
 #pragma unroll
                 for (int u = 0; u < C::kPair; ++u) {
                     const int i = i0 + u;
                     if ((!C::kSmall &&
-                         !mbar_wait_lean(bar_xfull + 8 * (i % C::kXStages), (i / C::kXStages) & 1,
-                                         abort_flag, err, kErrTimeoutFull, 32)) ||
-                        !mbar_wait_lean(bar_afull + 8 * (i % C::kAStages), (i / C::kAStages) & 1,
-                                        abort_flag, err, kErrTimeoutFull, 32))
+                         !mbar_wait_bounded(bar_xfull + 8 * (i % C::kXStages), (i / C::kXStages) & 1,
+                                            abort_flag, err, kErrTimeoutFull)) ||
+                        !mbar_wait_bounded(bar_afull + 8 * (i % C::kAStages), (i / C::kAStages) & 1,
+                                           abort_flag, err, kErrTimeoutFull))
                         break;
                 }
             }
@@ -1241,8 +1241,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
             for (int b = 0; b < n_blocks; ++b) {
                 const int buf = b % C::kRaw;
                 if (b >= C::kRaw &&
-                    !mbar_wait_lean(bar_rawempty + 8 * buf, ((b / C::kRaw) - 1) & 1, abort_flag,
-                                    err, kErrTimeoutEmpty, 128))
+                    !mbar_wait_bounded(bar_rawempty + 8 * buf, ((b / C::kRaw) - 1) & 1, abort_flag,
+                                       err, kErrTimeoutEmpty))
                     break;
                 mbar_arrive_expect_tx(bar_raw + 8 * buf, C::kRawBytes);
                 // x: the 16-byte boundary at or below row block kb0 + b
@@ -1275,8 +1275,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
             for (int i = warp - C::kXWarp0; i < n_iters; i += 2) {
                 const int s = i % C::kXStages;
                 if (i >= C::kXStages &&
-                    !mbar_wait_lean(bar_xempty + 8 * s, ((i / C::kXStages) - 1) & 1, abort_flag,
-                                    err, kErrTimeoutEmpty, 128))
+                    !mbar_wait_bounded(bar_xempty + 8 * s, ((i / C::kXStages) - 1) & 1, abort_flag,
+                                       err, kErrTimeoutEmpty))
                     break;
                 mbar_arrive_expect_tx(bar_xfull + 8 * s, bytes);
                 bulk_copy_g2s(sbase + C::kOffX + s * C::kXStage,
