@@ -617,6 +617,9 @@ constexpr int kSmallXBytes = 160 * 1024;
 #ifndef Q2K_TC_SMALL_STAGES
 #define Q2K_TC_SMALL_STAGES 8
 #endif
+#ifndef Q2K_TC_SMALL_HANDOVER
+#define Q2K_TC_SMALL_HANDOVER 4
+#endif
 
 template <int kXRows, bool kTmaW>
 struct WtCfg {
@@ -634,7 +637,10 @@ struct WtCfg {
     static constexpr int kWWarp = kDecWarps + 2;
     static constexpr int kXWarp0 = kDecWarps + 3;
     static constexpr int kThreads = 32 * (kDecWarps + 5);
-    static constexpr int kPair = 2;                         // K stages per MMA hand-over
+    // K stages per MMA hand-over: a hand-over (the waiter's named barrier)
+    // costs about as much as one narrow MMA, so small m takes a whole block
+    // (four stages) at a time
+    static constexpr int kPair = kSmall ? Q2K_TC_SMALL_HANDOVER : 2;
     static constexpr int kXStage = kXRows * kKS * 2;        // bytes of one x stage
     static constexpr int kXStages = kSmall ? kSmallXBytes / kXStage : (kXRows == 256 ? 6 : 8);
     // x barriers: a full / empty pair per ring stage; small m has one "all of
@@ -653,7 +659,8 @@ struct WtCfg {
     // measured faster than deeper rings (12, 15) or shallower ones (4, 6).
     static constexpr int kAStages =
         kSmall ? std::min(Q2K_TC_SMALL_STAGES, static_cast<int>((kTmemCols - kColA) / 32)) : 8;
-    static_assert(kAStages >= 4, "a block's four stages must fit in TMEM at once");
+    static_assert(kAStages >= 4 && kAStages % 2 == 0,
+                  "a block's four stages fit in TMEM at once; small m releases stages in pairs");
     // Raw weight slabs: the decoders take a block into registers as soon as it
     // lands, so two slabs keep the next block's copy a whole block ahead.  A
     // small-m CTA has few blocks and little else to hide their latency behind:
@@ -1035,9 +1042,12 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_afull + 8 * (prev % C::kAStages));
                 }
+                // (small m releases stages in pairs: the release of stage
+                // i | 1 covers stage i too)
+                const int rel = (C::kSmall ? (i | 1) : i) % C::kAStages;
                 if (i >= C::kAStages &&
                     !__all_sync(0xFFFFFFFFu,
-                                mbar_wait_bounded(bar_aempty + 8 * s, ((i / C::kAStages) - 1) & 1,
+                                mbar_wait_bounded(bar_aempty + 8 * rel, ((i / C::kAStages) - 1) & 1,
                                                   abort_flag, err, kErrTimeoutEmpty))) {
                     ok = false;
                     break;
@@ -1192,8 +1202,13 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                         mma_bf16_tmem_a(d, a_s + 8u * kk, xdesc + 2u * kk, idesc,
                                         g >= C::kAcc ? 1u : 0u);
                     }
-                    // only a stage the decoders refill needs its release
-                    if (i + C::kAStages < n_iters) mma_commit(bar_aempty + 8 * sa);
+                    // a stage is released only when the decoders refill it;
+                    // small m releases them in pairs, after the second one's
+                    // MMAs (a commit covers every MMA before it), since each
+                    // commit costs about as much as a narrow MMA
+                    if (C::kSmall ? ((i & 1) && i - 1 + C::kAStages < n_iters)
+                                  : i + C::kAStages < n_iters)
+                        mma_commit(bar_aempty + 8 * sa);
                     if (!C::kSmall) mma_commit(bar_xempty + 8 * sx);
                 }
             }
