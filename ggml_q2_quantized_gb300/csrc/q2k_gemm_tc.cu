@@ -1326,7 +1326,15 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
 #pragma unroll
                 for (int p = 0; p < kMaxKParts; ++p)
                     src[p] = cluster_map_shared(red, static_cast<uint32_t>(p < parts ? p : 0));
-                for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += C::kDecThreads) {
+                // this thread's sums wait in registers until the second
+                // barrier (a release arrival would otherwise wait for their
+                // global stores); at most 128 * 64 / 2 / 512 of them
+                constexpr int kPer = C::kRows * kXRows / 2 / C::kDecThreads;
+                float sums[kPer];
+#pragma unroll
+                for (int j = 0; j < kPer; ++j) {
+                    const int e = e0 + static_cast<int>(threadIdx.x) + j * C::kDecThreads;
+                    if (e >= e1) break;
                     float v[kMaxKParts];
 #pragma unroll
                     for (int p = 0; p < kMaxKParts; ++p)
@@ -1335,13 +1343,22 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
 #pragma unroll
                     for (int p = 1; p < kMaxKParts; ++p)
                         if (p < parts) sum += v[p];
+                    sums[j] = sum;
+                }
+                __syncwarp();
+                cluster_sync_all();
+#pragma unroll
+                for (int j = 0; j < kPer; ++j) {
+                    const int e = e0 + static_cast<int>(threadIdx.x) + j * C::kDecThreads;
+                    if (e >= e1) break;
                     const int nn = n0 + (e & (C::kRows - 1));
                     const int mm = m0 + e / C::kRows;
-                    if (nn < N && mm < M) y[static_cast<size_t>(mm) * N + nn] = sum;
+                    if (nn < N && mm < M) y[static_cast<size_t>(mm) * N + nn] = sums[j];
                 }
+            } else {
+                __syncwarp();
+                cluster_sync_all();
             }
-            __syncwarp();
-            cluster_sync_all();
         }
     }
 
