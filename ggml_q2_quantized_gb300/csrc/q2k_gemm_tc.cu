@@ -620,6 +620,9 @@ constexpr int kSmallXBytes = 160 * 1024;
 #ifndef Q2K_TC_SMALL_HANDOVER
 #define Q2K_TC_SMALL_HANDOVER 4
 #endif
+#ifndef Q2K_TC_SMALL_FIRST_BOX_ALONE
+#define Q2K_TC_SMALL_FIRST_BOX_ALONE 1
+#endif
 
 template <int kXRows, bool kTmaW>
 struct WtCfg {
@@ -721,9 +724,14 @@ __device__ __forceinline__ uint32_t cluster_map_shared(uint32_t saddr, uint32_t 
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+// Four consecutive floats of (another CTA's) shared memory in the cluster
+// (16-byte aligned).
+__device__ __forceinline__ float4 ld_shared_cluster_v4f(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
     return v;
 }
 
@@ -1259,6 +1267,13 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                     !mbar_wait_bounded(bar_rawempty + 8 * buf, ((b / C::kRaw) - 1) & 1, abort_flag,
                                        err, kErrTimeoutEmpty))
                     break;
+                // Small m: every CTA of the grid asks for its first block at
+                // once; the rest follow when that one has landed, so the
+                // first blocks are not queued behind the others in DRAM and
+                // decoding starts earlier.
+                if (C::kSmall && Q2K_TC_SMALL_FIRST_BOX_ALONE && b == 1 &&
+                    !mbar_wait_bounded(bar_raw, 0, abort_flag, err, kErrTimeoutFull))
+                    break;
                 mbar_arrive_expect_tx(bar_raw + 8 * buf, C::kRawBytes);
                 // x: the 16-byte boundary at or below row block kb0 + b
                 // (84 (kb0 + b) - 4 ((kb0 + b) % 4))
@@ -1318,9 +1333,11 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
             if (warp < C::kDecWarps) {
                 const int parts = static_cast<int>(gridDim.z);
                 const int rank = static_cast<int>(cluster_cta_rank());
-                const int total = C::kRows * nx;
-                const int e0 = rank * total / parts;
-                const int e1 = (rank + 1) * total / parts;
+                // part `rank` sums quads (4 consecutive elements, 16 bytes)
+                // [q0, q1) of the tile's 32 nx quads
+                const int quads = C::kRows * nx / 4;
+                const int q0 = rank * quads / parts;
+                const int q1 = (rank + 1) * quads / parts;
                 const uint32_t red = sbase + C::kOffX;
                 uint32_t src[kMaxKParts];
 #pragma unroll
@@ -1328,32 +1345,45 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                     src[p] = cluster_map_shared(red, static_cast<uint32_t>(p < parts ? p : 0));
                 // this thread's sums wait in registers until the second
                 // barrier (a release arrival would otherwise wait for their
-                // global stores); at most 128 * 64 / 2 / 512 of them
-                constexpr int kPer = C::kRows * kXRows / 2 / C::kDecThreads;
-                float sums[kPer];
+                // global stores): at most ceil(32 * 64 / 2 / 512) quads
+                constexpr int kPer = (C::kRows * kXRows / 4 / 2 + C::kDecThreads - 1) / C::kDecThreads;
+                float4 sums[kPer];
 #pragma unroll
                 for (int j = 0; j < kPer; ++j) {
-                    const int e = e0 + static_cast<int>(threadIdx.x) + j * C::kDecThreads;
-                    if (e >= e1) break;
-                    float v[kMaxKParts];
+                    const int q = q0 + static_cast<int>(threadIdx.x) + j * C::kDecThreads;
+                    if (q >= q1) break;
+                    float4 v[kMaxKParts];
 #pragma unroll
                     for (int p = 0; p < kMaxKParts; ++p)
-                        v[p] = p < parts ? ld_shared_cluster_f32(src[p] + 4u * e) : 0.f;
-                    float sum = v[0];
+                        v[p] = p < parts ? ld_shared_cluster_v4f(src[p] + 16u * q)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4 sum = v[0];
 #pragma unroll
-                    for (int p = 1; p < kMaxKParts; ++p)
-                        if (p < parts) sum += v[p];
+                    for (int p = 1; p < kMaxKParts; ++p) {
+                        if (p < parts) {
+                            sum.x += v[p].x;
+                            sum.y += v[p].y;
+                            sum.z += v[p].z;
+                            sum.w += v[p].w;
+                        }
+                    }
                     sums[j] = sum;
                 }
                 __syncwarp();
                 cluster_sync_all();
 #pragma unroll
                 for (int j = 0; j < kPer; ++j) {
-                    const int e = e0 + static_cast<int>(threadIdx.x) + j * C::kDecThreads;
-                    if (e >= e1) break;
-                    const int nn = n0 + (e & (C::kRows - 1));
-                    const int mm = m0 + e / C::kRows;
-                    if (nn < N && mm < M) y[static_cast<size_t>(mm) * N + nn] = sums[j];
+                    const int q = q0 + static_cast<int>(threadIdx.x) + j * C::kDecThreads;
+                    if (q >= q1) break;
+                    // elements 4 q .. 4 q + 3: weight rows n0 + (4 q % 128) + 0..3 of x row m
+                    const int nn = n0 + ((4 * q) & (C::kRows - 1));
+                    const int mm = m0 + 4 * q / C::kRows;
+                    if (mm >= M) continue;
+                    float* out = y + static_cast<size_t>(mm) * N + nn;
+                    if (nn < N) out[0] = sums[j].x;
+                    if (nn + 1 < N) out[1] = sums[j].y;
+                    if (nn + 2 < N) out[2] = sums[j].z;
+                    if (nn + 3 < N) out[3] = sums[j].w;
                 }
             } else {
                 __syncwarp();
