@@ -611,8 +611,11 @@ constexpr int kMaxKParts = 8;
 // converted to bf16 by the kernel itself and stays in shared memory, in this
 // many bytes.
 constexpr int kSmallXBytes = 160 * 1024;
+#ifndef Q2K_TC_SMALL_ISSUERS
+#define Q2K_TC_SMALL_ISSUERS 2
+#endif
 #ifndef Q2K_TC_SMALL_ACC
-#define Q2K_TC_SMALL_ACC 1
+#define Q2K_TC_SMALL_ACC (Q2K_TC_SMALL_ISSUERS)
 #endif
 #ifndef Q2K_TC_SMALL_STAGES
 #define Q2K_TC_SMALL_STAGES 8
@@ -654,6 +657,12 @@ struct WtCfg {
     // back; rotating over several costs more per MMA, so small m keeps one
     // unless Q2K_TC_SMALL_ACC says otherwise.
     static constexpr int kAcc = kSmall ? Q2K_TC_SMALL_ACC : 1;
+    // Threads issuing MMAs.  One thread issues narrow MMAs at about half the
+    // rate the tensor core takes them, so small m has two: the MMA warp the
+    // even stages of a hand-over into accumulator 0, the waiter the odd ones
+    // into accumulator 1.
+    static constexpr int kIssuers = kSmall ? Q2K_TC_SMALL_ISSUERS : 1;
+    static_assert(kIssuers == 1 || (kIssuers == 2 && kAcc == 2 && kPair % 2 == 0), "MMA issuers");
     static constexpr uint32_t kColA = kXRows * kAcc;        // A ring after the accumulators
     static constexpr int kTmemCols = 512;
     // Decoded stages in TMEM (32 columns each).  The decoders' TMEM stores
@@ -895,7 +904,7 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
         }
         for (int s = lane; s < C::kAStages; s += 32) {
             mbar_init(bar_afull + 8 * s, C::kGroupWarps);  // one arrival per warp of its group
-            mbar_init(bar_aempty + 8 * s, 1);            // MMA commit
+            mbar_init(bar_aempty + 8 * s, C::kIssuers);  // MMA commit(s)
         }
         for (int r = lane; r < C::kRaw; r += 32) {
             // TMA: the producer's expect-tx arrival + the box bytes; else one
@@ -904,8 +913,8 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
             mbar_init(bar_rawempty + 8 * r, C::kDecWarps);  // decoders done reading (kTmaW)
         }
         if (lane == 0) {
-            mbar_init(bar_accum, 1);
-            mbar_init(bar_drain, 1);
+            mbar_init(bar_accum, C::kIssuers);
+            mbar_init(bar_drain, C::kIssuers);
             *abort_flag = 0;
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1196,6 +1205,7 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                 tc_fence_after();
 #pragma unroll
                 for (int u = 0; u < C::kPair; ++u) {
+                    if (C::kIssuers > 1 && (u & 1)) continue;  // the waiter's stages
                     const int i = i0 + u;
                     const int sx = i % C::kXStages;
                     const int sa = i % C::kAStages;
@@ -1203,20 +1213,23 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                     const uint32_t a_s = a_base0 + 32u * sa;
 #pragma unroll
                     for (int kk = 0; kk < kKS / 16; ++kk) {
-                        // MMA g = 4 i + kk goes to accumulator g % kAcc; the
-                        // first one into each starts it from zero
-                        const int g = 4 * i + kk;
-                        const uint32_t d = tmem_base + static_cast<uint32_t>((g % C::kAcc) * kXRows);
+                        // MMA g = 4 i + kk goes to accumulator g % kAcc (with
+                        // two issuers: accumulator 0, stage i / 2 of this
+                        // thread's); the first one into each starts it from zero
+                        const int g = C::kIssuers > 1 ? 4 * (i >> 1) + kk : 4 * i + kk;
+                        const uint32_t d =
+                            tmem_base + static_cast<uint32_t>((C::kIssuers > 1 ? 0 : g % C::kAcc) * kXRows);
                         mma_bf16_tmem_a(d, a_s + 8u * kk, xdesc + 2u * kk, idesc,
-                                        g >= C::kAcc ? 1u : 0u);
+                                        g >= (C::kIssuers > 1 ? 1 : C::kAcc) ? 1u : 0u);
                     }
                     // a stage is released only when the decoders refill it;
                     // small m releases them in pairs, after the second one's
-                    // MMAs (a commit covers every MMA before it), since each
-                    // commit costs about as much as a narrow MMA
-                    if (C::kSmall ? ((i & 1) && i - 1 + C::kAStages < n_iters)
+                    // MMAs (a commit covers every MMA of its thread before
+                    // it; with two issuers each commits its stage of the
+                    // pair), since each commit costs about as much as a narrow MMA
+                    if (C::kSmall ? ((C::kIssuers > 1 || (i & 1)) && (i & ~1) + C::kAStages < n_iters)
                                   : i + C::kAStages < n_iters)
-                        mma_commit(bar_aempty + 8 * sa);
+                        mma_commit(bar_aempty + 8 * ((C::kSmall ? (i | 1) : i) % C::kAStages));
                     if (!C::kSmall) mma_commit(bar_xempty + 8 * sx);
                 }
             }
@@ -1252,6 +1265,42 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
             }
             __syncwarp();
             asm volatile("bar.sync 1, 64;" ::: "memory");
+            if constexpr (C::kIssuers > 1) {
+                // second issuer: the odd stages of the hand-over, into
+                // accumulator 1 (the epilogue adds the accumulators in order)
+                if (lane == 0 && !*abort_flag) {
+                    tc_fence_after();
+                    const uint32_t idesc = make_idesc(kBM, nx);
+                    const uint64_t xdesc0 = sw128_desc(sbase + C::kOffX);
+                    const uint32_t a_base0 = tmem_base + C::kColA;
+#pragma unroll
+                    for (int u = 1; u < C::kPair; u += 2) {
+                        const int i = i0 + u;
+                        const int sx = i % C::kXStages;
+                        const int sa = i % C::kAStages;
+                        const uint64_t xdesc = xdesc0 + static_cast<uint64_t>(sx * (C::kXStage >> 4));
+                        const uint32_t a_s = a_base0 + 32u * sa;
+#pragma unroll
+                        for (int kk = 0; kk < kKS / 16; ++kk)
+                            mma_bf16_tmem_a(tmem_base + static_cast<uint32_t>(kXRows), a_s + 8u * kk,
+                                            xdesc + 2u * kk, idesc, (i > 1 || kk > 0) ? 1u : 0u);
+                        if ((i & ~1) + C::kAStages < n_iters) mma_commit(bar_aempty + 8 * sa);
+                    }
+                }
+                __syncwarp();
+            }
+        }
+        if constexpr (C::kIssuers > 1) {
+            if (lane == 0) {
+                if (!*abort_flag) {
+                    mma_commit(bar_accum);
+                } else {
+                    mma_commit(bar_drain);
+                    volatile int no_abort = 0;
+                    mbar_wait_bounded(bar_drain, 0, &no_abort, err, kErrTimeoutDrain);
+                }
+            }
+            __syncwarp();
         }
     } else if (warp == C::kWWarp) {
         // ---------------- raw weight blocks: one TMA box per block ----------------
