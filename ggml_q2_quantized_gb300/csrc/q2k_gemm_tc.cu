@@ -614,6 +614,9 @@ constexpr int kSmallXBytes = 160 * 1024;
 #ifndef Q2K_TC_SMALL_ISSUERS
 #define Q2K_TC_SMALL_ISSUERS 2
 #endif
+#ifndef Q2K_TC_X128_ISSUERS
+#define Q2K_TC_X128_ISSUERS 2
+#endif
 #ifndef Q2K_TC_SMALL_ACC
 #define Q2K_TC_SMALL_ACC (Q2K_TC_SMALL_ISSUERS)
 #endif
@@ -656,12 +659,14 @@ struct WtCfg {
     // whatever its N, and a run of them into one accumulator issues back to
     // back; rotating over several costs more per MMA, so small m keeps one
     // unless Q2K_TC_SMALL_ACC says otherwise.
-    static constexpr int kAcc = kSmall ? Q2K_TC_SMALL_ACC : 1;
     // Threads issuing MMAs.  One thread issues narrow MMAs at about half the
-    // rate the tensor core takes them, so small m has two: the MMA warp the
-    // even stages of a hand-over into accumulator 0, the waiter the odd ones
-    // into accumulator 1.
-    static constexpr int kIssuers = kSmall ? Q2K_TC_SMALL_ISSUERS : 1;
+    // rate the tensor core takes them, so small m (and 128-row x tiles, whose
+    // accumulators leave room for a second) has two: the MMA warp the even
+    // stages of a hand-over into accumulator 0, the waiter the odd ones into
+    // accumulator 1.
+    static constexpr int kIssuers =
+        kSmall ? Q2K_TC_SMALL_ISSUERS : (kXRows == 128 ? Q2K_TC_X128_ISSUERS : 1);
+    static constexpr int kAcc = kSmall ? Q2K_TC_SMALL_ACC : kIssuers;
     static_assert(kIssuers == 1 || (kIssuers == 2 && kAcc == 2 && kPair % 2 == 0), "MMA issuers");
     static constexpr uint32_t kColA = kXRows * kAcc;        // A ring after the accumulators
     static constexpr int kTmemCols = 512;
@@ -904,7 +909,9 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
         }
         for (int s = lane; s < C::kAStages; s += 32) {
             mbar_init(bar_afull + 8 * s, C::kGroupWarps);  // one arrival per warp of its group
-            mbar_init(bar_aempty + 8 * s, C::kIssuers);  // MMA commit(s)
+            // MMA commit(s): small m releases stages in pairs, one commit
+            // from each issuer
+            mbar_init(bar_aempty + 8 * s, C::kSmall ? C::kIssuers : 1);
         }
         for (int r = lane; r < C::kRaw; r += 32) {
             // TMA: the producer's expect-tx arrival + the box bytes; else one
@@ -1284,7 +1291,9 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                         for (int kk = 0; kk < kKS / 16; ++kk)
                             mma_bf16_tmem_a(tmem_base + static_cast<uint32_t>(kXRows), a_s + 8u * kk,
                                             xdesc + 2u * kk, idesc, (i > 1 || kk > 0) ? 1u : 0u);
-                        if ((i & ~1) + C::kAStages < n_iters) mma_commit(bar_aempty + 8 * sa);
+                        if (C::kSmall ? (i & ~1) + C::kAStages < n_iters : i + C::kAStages < n_iters)
+                            mma_commit(bar_aempty + 8 * sa);
+                        if (!C::kSmall) mma_commit(bar_xempty + 8 * sx);
                     }
                 }
                 __syncwarp();
