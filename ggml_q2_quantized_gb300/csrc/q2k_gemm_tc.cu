@@ -617,6 +617,12 @@ constexpr int kSmallXBytes = 160 * 1024;
 #ifndef Q2K_TC_X128_ISSUERS
 #define Q2K_TC_X128_ISSUERS 2
 #endif
+#ifndef Q2K_TC_X128_HANDOVER
+#define Q2K_TC_X128_HANDOVER 4
+#endif
+#ifndef Q2K_TC_X256_HANDOVER
+#define Q2K_TC_X256_HANDOVER 2
+#endif
 #ifndef Q2K_TC_SMALL_ACC
 #define Q2K_TC_SMALL_ACC (Q2K_TC_SMALL_ISSUERS)
 #endif
@@ -649,7 +655,8 @@ struct WtCfg {
     // K stages per MMA hand-over: a hand-over (the waiter's named barrier)
     // costs about as much as one narrow MMA, so small m takes a whole block
     // (four stages) at a time
-    static constexpr int kPair = kSmall ? Q2K_TC_SMALL_HANDOVER : 2;
+    static constexpr int kPair =
+        kSmall ? Q2K_TC_SMALL_HANDOVER : (kXRows == 128 ? Q2K_TC_X128_HANDOVER : Q2K_TC_X256_HANDOVER);
     static constexpr int kXStage = kXRows * kKS * 2;        // bytes of one x stage
     static constexpr int kXStages = kSmall ? kSmallXBytes / kXStage : (kXRows == 256 ? 6 : 8);
     // x barriers: a full / empty pair per ring stage; small m has one "all of
