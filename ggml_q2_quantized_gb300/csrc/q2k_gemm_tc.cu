@@ -623,6 +623,9 @@ constexpr int kSmallXBytes = 160 * 1024;
 #ifndef Q2K_TC_X256_HANDOVER
 #define Q2K_TC_X256_HANDOVER 2
 #endif
+#ifndef Q2K_TC_X128_PAIR_RELEASE
+#define Q2K_TC_X128_PAIR_RELEASE 1
+#endif
 #ifndef Q2K_TC_SMALL_ACC
 #define Q2K_TC_SMALL_ACC (Q2K_TC_SMALL_ISSUERS)
 #endif
@@ -685,6 +688,12 @@ struct WtCfg {
         kSmall ? std::min(Q2K_TC_SMALL_STAGES, static_cast<int>((kTmemCols - kColA) / 32)) : 8;
     static_assert(kAStages >= 4 && kAStages % 2 == 0,
                   "a block's four stages fit in TMEM at once; small m releases stages in pairs");
+    // Stages released to the producers in pairs (one commit per issuer per
+    // pair) instead of one by one; with an x ring as deep as the A ring
+    // (128-row tiles), one release serves both the x and the A stage.  Each
+    // commit costs about as much as a narrow MMA.
+    static constexpr bool kPairRelease =
+        kSmall || (kXRows == 128 && Q2K_TC_X128_PAIR_RELEASE && kXStages == kAStages);
     // Raw weight slabs: the decoders take a block into registers as soon as it
     // lands, so two slabs keep the next block's copy a whole block ahead.  A
     // small-m CTA has few blocks and little else to hide their latency behind:
@@ -918,7 +927,7 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
             mbar_init(bar_afull + 8 * s, C::kGroupWarps);  // one arrival per warp of its group
             // MMA commit(s): small m releases stages in pairs, one commit
             // from each issuer
-            mbar_init(bar_aempty + 8 * s, C::kSmall ? C::kIssuers : 1);
+            mbar_init(bar_aempty + 8 * s, C::kPairRelease ? C::kIssuers : 1);
         }
         for (int r = lane; r < C::kRaw; r += 32) {
             // TMA: the producer's expect-tx arrival + the box bytes; else one
@@ -1075,7 +1084,7 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                 }
                 // (small m releases stages in pairs: the release of stage
                 // i | 1 covers stage i too)
-                const int rel = (C::kSmall ? (i | 1) : i) % C::kAStages;
+                const int rel = (C::kPairRelease ? (i | 1) : i) % C::kAStages;
                 if (i >= C::kAStages &&
                     !__all_sync(0xFFFFFFFFu,
                                 mbar_wait_bounded(bar_aempty + 8 * rel, ((i / C::kAStages) - 1) & 1,
@@ -1241,10 +1250,10 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                     // MMAs (a commit covers every MMA of its thread before
                     // it; with two issuers each commits its stage of the
                     // pair), since each commit costs about as much as a narrow MMA
-                    if (C::kSmall ? ((C::kIssuers > 1 || (i & 1)) && (i & ~1) + C::kAStages < n_iters)
+                    if (C::kPairRelease ? ((C::kIssuers > 1 || (i & 1)) && (i & ~1) + C::kAStages < n_iters)
                                   : i + C::kAStages < n_iters)
-                        mma_commit(bar_aempty + 8 * ((C::kSmall ? (i | 1) : i) % C::kAStages));
-                    if (!C::kSmall) mma_commit(bar_xempty + 8 * sx);
+                        mma_commit(bar_aempty + 8 * ((C::kPairRelease ? (i | 1) : i) % C::kAStages));
+                    if (!C::kSmall && !C::kPairRelease) mma_commit(bar_xempty + 8 * sx);
                 }
             }
             __syncwarp();
@@ -1298,9 +1307,9 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                         for (int kk = 0; kk < kKS / 16; ++kk)
                             mma_bf16_tmem_a(tmem_base + static_cast<uint32_t>(kXRows), a_s + 8u * kk,
                                             xdesc + 2u * kk, idesc, (i > 1 || kk > 0) ? 1u : 0u);
-                        if (C::kSmall ? (i & ~1) + C::kAStages < n_iters : i + C::kAStages < n_iters)
+                        if (C::kPairRelease ? (i & ~1) + C::kAStages < n_iters : i + C::kAStages < n_iters)
                             mma_commit(bar_aempty + 8 * sa);
-                        if (!C::kSmall) mma_commit(bar_xempty + 8 * sx);
+                        if (!C::kSmall && !C::kPairRelease) mma_commit(bar_xempty + 8 * sx);
                     }
                 }
                 __syncwarp();
@@ -1370,7 +1379,9 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
             for (int i = warp - C::kXWarp0; i < n_iters; i += 2) {
                 const int s = i % C::kXStages;
                 if (i >= C::kXStages &&
-                    !mbar_wait_bounded(bar_xempty + 8 * s, ((i / C::kXStages) - 1) & 1, abort_flag,
+                    !mbar_wait_bounded(C::kPairRelease ? bar_aempty + 8 * ((i | 1) % C::kAStages)
+                                                       : bar_xempty + 8 * s,
+                                       ((i / C::kXStages) - 1) & 1, abort_flag,
                                        err, kErrTimeoutEmpty))
                     break;
                 mbar_arrive_expect_tx(bar_xfull + 8 * s, bytes);
