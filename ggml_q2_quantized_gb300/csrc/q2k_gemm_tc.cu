@@ -1073,15 +1073,6 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                 uint32_t o0[8], o1[8];
                 if (cp == 0) wt_decode_half_stage<0>(qh, sh, d, dmin, o0, o1);
                 else wt_decode_half_stage<1>(qh, sh, d, dmin, o0, o1);
-                // This warp's previous stage (i - 1, or i - 3 across a block):
-                // its TMEM stores had this decode to land; publish it now.
-                if (b > 0 || cp > 0) {
-                    const int prev = cp > 0 ? i - 1 : i - 3;
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_afull + 8 * (prev % C::kAStages));
-                }
                 // (small m releases stages in pairs: the release of stage
                 // i | 1 covers stage i too)
                 const int rel = (C::kPairRelease ? (i | 1) : i) % C::kAStages;
@@ -1096,14 +1087,13 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                 const uint32_t a_col = a_col0 + 32u * s;
                 tmem_st8(a_col, o0);
                 tmem_st8(a_col + 16u, o1);
+                // published as soon as its stores have landed (waiting here
+                // measured faster than deferring it past the next decode)
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_afull + 8 * s);
             }
-        }
-        if (ok) {
-            // publish this warp's last stage
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_afull + 8 * ((n_iters - 3 + 2 * half) % C::kAStages));
         }
         if constexpr (!kTmaW) cp_async_wait_all();  // no copy may land after this CTA is gone
 
