@@ -678,8 +678,9 @@ def run_ours(args):
         for name in ("ffn_pair", "ffn_pair_down", "spec_verify_m16", "prefill_m512"):
             sw = wl.by_name(name)
             # the step's calls are projections of one x, each with its own W
-            # and y (Q2K_FLAG_INDEPENDENT: used by the GEMV and by the
-            # small-m tensor path, ignored at M = 512)
+            # and y (Q2K_FLAG_INDEPENDENT: the GEMV and the small-m tensor
+            # path fetch their inputs before the dependency wait; at M = 512
+            # the batch converts x once and the GEMMs overlap)
             r = bench_matmul(torch, q2k, sw, max(3, steps // 4), 3, l2_bytes, device,
                              independent=True)
             us = r["us_per_call"]

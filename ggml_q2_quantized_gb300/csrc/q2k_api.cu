@@ -352,7 +352,7 @@ q2k_status check_matmul_ex(q2k_path path, uint32_t flags, const float* x, size_t
 // Enqueue one checked call.
 cudaError_t launch_matmul_ex(q2k_path path, uint32_t flags, const float* x, const void* w, float* y,
                              const q2k_matmul_params* p, void* ws, const DeviceInfo& dev,
-                             cudaStream_t s) {
+                             cudaStream_t s, bool image_ready = false) {
     const uint8_t* wb = static_cast<const uint8_t*>(w);
     if (path == Q2K_PATH_GEMV)
         return q2k::launch_gemv(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count,
@@ -365,7 +365,7 @@ cudaError_t launch_matmul_ex(q2k_path path, uint32_t flags, const float* x, cons
         return q2k::launch_gemm_tc_plain(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device,
                                          dev.sm_count, s, kf);
     return q2k::launch_gemm_tc(x, wb, y, int(p->m), int(p->n), int(p->k), dev.device, dev.sm_count, ws,
-                               s, kf);
+                               s, kf | (image_ready ? q2k::kImageReady : 0u));
 }
 
 }  // namespace
@@ -496,6 +496,19 @@ q2k_status q2k_matmul_ex_batch(const q2k_matmul_call* calls, size_t count, void*
     for (size_t i = 0; i < count; ++i) {
         const q2k_matmul_call& c = calls[i];
         cudaError_t e = cudaSuccess;
+        // A tensor call right after one with the same x, m and k in the same
+        // workspace finds x's image there already: when it is independent
+        // (nothing still running writes its x, W or y, the call before
+        // included), it skips the conversion and may run beside that call.
+        bool image_ready = false;
+        if (i > 0 && bp.path[i] == Q2K_PATH_TENSOR && bp.ws[i] != nullptr &&
+            (c.flags & Q2K_FLAG_INDEPENDENT)) {
+            const q2k_matmul_call& q = calls[i - 1];
+            image_ready = bp.path[i - 1] == Q2K_PATH_TENSOR && bp.ws[i - 1] == bp.ws[i] &&
+                          q.x == c.x && q.params.m == c.params.m && q.params.k == c.params.k &&
+                          q2k::gemm_tc_image_reusable(int(q.params.m), int(q.params.n), int(q.params.k)) &&
+                          q2k::gemm_tc_image_reusable(int(c.params.m), int(c.params.n), int(c.params.k));
+        }
         const int g = bp.group[i];
         if (share && g >= 0 && bp.slot[g] != SIZE_MAX) {
             uint8_t* planes = static_cast<uint8_t*>(scratch) + bp.slot[g];
@@ -510,7 +523,8 @@ q2k_status q2k_matmul_ex_batch(const q2k_matmul_call* calls, size_t count, void*
                                          ((c.flags & Q2K_FLAG_INDEPENDENT) ? q2k::kGemvIndependent : 0u),
                                      s, planes);
         } else {
-            e = launch_matmul_ex(bp.path[i], c.flags, c.x, c.w, c.y, &c.params, bp.ws[i], dev, s);
+            e = launch_matmul_ex(bp.path[i], c.flags, c.x, c.w, c.y, &c.params, bp.ws[i], dev, s,
+                                 image_ready);
         }
         if (e != cudaSuccess) {
             char what[64];

@@ -1365,7 +1365,13 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                                  static_cast<size_t>(m0 % kXSuperRows) * (kKS * 2);
             const uint32_t bytes = kXRows == kXSuperRows ? static_cast<uint32_t>(kXSuperBytes)
                                                          : static_cast<uint32_t>(nx) * (kKS * 2);
-            pdl_wait_prerequisites();  // the image is written by the grid before this one
+            // The image is written by the grid before this one, unless it is
+            // ready from an earlier call (kImageReady): wait for it, then let
+            // the next grid start on the SMs this one leaves free (every
+            // later grid of the library waits before it reads what this one
+            // writes, or is independent of it).
+            if (!(rt.flags & kImageReady)) pdl_wait_prerequisites();
+            pdl_allow_dependents();
             for (int i = warp - C::kXWarp0; i < n_iters; i += 2) {
                 const int s = i % C::kXStages;
                 if (i >= C::kXStages &&
@@ -1466,10 +1472,11 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                      "r"(C::kTmemCols)
                      : "memory");
     }
-    // An independent call completes only after the grid before it, so work
-    // enqueued later on the stream sees every earlier call complete.
-    if (C::kSmall && (rt.flags & kGemvIndependent) && threadIdx.x == 0 && blockIdx.x == 0 &&
-        blockIdx.y == 0 && blockIdx.z == 0)
+    // An independent call (or one on a ready image, which never waited)
+    // completes only after the grid before it, so work enqueued later on the
+    // stream sees every earlier call complete.
+    if (((C::kSmall && (rt.flags & kGemvIndependent)) || (!C::kSmall && (rt.flags & kImageReady))) &&
+        threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
         pdl_wait_prerequisites();
 }
 
@@ -1710,6 +1717,10 @@ size_t gemm_tc_workspace_bytes(int M, int N, int K) {
     return img + parts_bytes(M, N, splits) + tiles * 4;
 }
 
+bool gemm_tc_image_reusable(int M, int N, int K) {
+    return small_splits(M, N, K) == 0 && wt_splits(M, N, K) == 1;
+}
+
 cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, int N, int K,
                            int device, int sm_count, void* workspace, cudaStream_t stream,
                            uint32_t flags) {
@@ -1734,19 +1745,25 @@ cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, in
         tile_count = reinterpret_cast<unsigned int*>(p + parts_bytes(M, N, splits));
         n_tiles = ((N + 127) / 128) * ((M + 127) / 128);
     }
-    // only x's own rows: the image's padding rows are never read into a kept output
-    const size_t n_chunks = static_cast<size_t>(M) * (K / 8);
-    size_t blocks = (n_chunks + 255) / 256;
-    const size_t cap = static_cast<size_t>(sm_count) * 4;
-    if (blocks > cap) blocks = cap;
-    x_to_bf16_tiles_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, xa, M, K, n_chunks,
-                                                                             tile_count, n_tiles);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    // kImageReady (one K part only): the workspace already holds this x's
+    // image from the call before, which is still in the stream
+    const uint32_t wt_flags = splits == 1 ? (flags & kImageReady) : 0u;
+    if (!wt_flags) {
+        // only x's own rows: the image's padding rows are never read into a kept output
+        const size_t n_chunks = static_cast<size_t>(M) * (K / 8);
+        size_t blocks = (n_chunks + 255) / 256;
+        const size_t cap = static_cast<size_t>(sm_count) * 4;
+        if (blocks > cap) blocks = cap;
+        x_to_bf16_tiles_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            x, xa, M, K, n_chunks, tile_count, n_tiles);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     if (choose_wt_xrows(M, N, sm_count) == 256)
         return launch_wt<256>(xa, nullptr, w, y, partial, tile_count, splits, M, N, K, device,
-                              stream);
-    return launch_wt<128>(xa, nullptr, w, y, partial, tile_count, splits, M, N, K, device, stream);
+                              stream, wt_flags);
+    return launch_wt<128>(xa, nullptr, w, y, partial, tile_count, splits, M, N, K, device, stream,
+                          wt_flags);
 }
 
 // ---- routed products on tensor cores (mul_mat_id with many routes) -----------

@@ -27,6 +27,11 @@ cudaError_t launch_gather(const uint8_t* table, const uint32_t* ids, float* out,
 //                      grid before it only at its very end (completion order).
 constexpr uint32_t kGemvConstWeights = 1u;
 constexpr uint32_t kGemvIndependent = 2u;
+// tensor path with a workspace, one K part (gemm_tc_image_reusable): the
+// workspace already holds this x's bf16 image, written for an earlier call
+// that is still in the stream; the GEMM skips the prepass and its wait, may
+// overlap the call before it, and completes after it
+constexpr uint32_t kImageReady = 4u;
 cudaError_t launch_gemv(const float* x, const uint8_t* w, float* y, int M, int N, int K,
                         int device, int sm_count, uint32_t flags, cudaStream_t stream,
                         const uint8_t* xplanes = nullptr);
@@ -94,6 +99,9 @@ size_t gemm_tc_workspace_bytes(int M, int N, int K);
 cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, int N, int K,
                            int device, int sm_count, void* workspace, cudaStream_t stream,
                            uint32_t flags = 0);
+// The geometry keeps its x image in the workspace for a whole call (no small-m
+// in-kernel conversion, one K part), so kImageReady may reuse it.
+bool gemm_tc_image_reusable(int M, int N, int K);
 
 // Routed product on tensor cores: route r = 0..routes-1 multiplies x row
 // r / x_div by expert ids[r]'s weights (w + ids[r] * expert_stride, N rows)

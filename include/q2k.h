@@ -185,7 +185,9 @@ enum {
      * Both flags also apply to the tensor-core path for m <= 64 (whose GEMM
      * converts x itself): its weight copies (CONST_WEIGHTS), and its x
      * conversion and y stores (INDEPENDENT), start before the wait for the
-     * kernel before.  The other paths ignore them. */
+     * kernel before.  In q2k_matmul_ex_batch, INDEPENDENT also lets a
+     * tensor-path call reuse the x image of the call before it (same x, m, k
+     * and workspace) and run beside it.  The other paths ignore them. */
     Q2K_FLAG_INDEPENDENT = 2
 };
 
@@ -432,7 +434,13 @@ typedef struct q2k_matmul_call {
  *            into the scratch, instead of once per CTA of every call (the
  *            same values: same bits).  A call of the batch that writes that
  *            row ends the sharing.  Without it (or smaller) every call
- *            converts x itself. */
+ *            converts x itself.
+ * A tensor-path call with Q2K_FLAG_INDEPENDENT right after a tensor-path call
+ * with the same x pointer, m, k and workspace (and, for both, the workspace
+ * layout of one K part: m > 64 and no K split) finds x's bf16 image in that
+ * workspace already: it skips the conversion and, independent of the call
+ * before it by the flag's promise, may run beside that call on the SMs it
+ * leaves free; it still completes after it.  Same bits as the separate call. */
 q2k_status q2k_matmul_ex_batch(const q2k_matmul_call *calls, size_t count, void *scratch,
                                size_t scratch_bytes, q2k_stream_t stream);
 

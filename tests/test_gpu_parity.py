@@ -285,6 +285,38 @@ def test_tensor_small_m_sampled_rows(m, n, k):
     assert_close(y[:, rows], yref, s, TOL_TC, f"m={m} n={n} k={k} sampled")
 
 
+def test_matmul_batch_shared_image_independent_calls():
+    """Consecutive independent tensor calls on one x (same m, k, workspace) in a
+    batch: the later ones reuse the x image the first one converted and may run
+    beside each other.  Each output is bit-identical to its own call and within
+    the tensor path's bound of the oracle; 256- and 128-row x tiles, a ragged
+    last weight tile, and a call on another x in between (which converts anew)."""
+    for m, k, ns in ((512, 1024, (1024, 640, 1000, 1024)), (200, 768, (4096, 333, 4096))):
+        x, _ = wl.make_matmul_inputs(3400 + m, m, 16, k)
+        xd = dev(x)
+        ws_list, calls, ref, refs_np = [], [], [], []
+        for i, n in enumerate(ns):
+            _, w = wl.make_matmul_inputs(3500 + m + i, m, n, k)
+            wd = dev(w)
+            calls.append(dict(x=xd, w=wd, n=n, path="tensor", independent=True))
+            ref.append(q2k.matmul(xd, wd, n, path="tensor", independent=True))
+            refs_np.append((w, n))
+        # a call on another x between two calls on xd: the one after it converts again
+        x2, w2 = wl.make_matmul_inputs(3600 + m, m, 256, k)
+        calls.insert(2, dict(x=dev(x2), w=dev(w2), n=256, path="tensor", independent=True))
+        ref.insert(2, q2k.matmul(dev(x2), dev(w2), 256, path="tensor", independent=True))
+        torch.cuda.synchronize()
+        for run in range(2):
+            outs = q2k.MatmulBatch(calls).run()
+            torch.cuda.synchronize()
+            for i, (a, b) in enumerate(zip(outs, ref)):
+                assert torch.equal(a.view(torch.int32), b.view(torch.int32)), f"m={m} call {i} run {run}"
+        rows = np.arange(0, 16)
+        for (w, n), y in zip(refs_np, [o for j, o in enumerate(outs) if j != 2]):
+            yref, s_ = oracle.matmul_rows(x, w, n, rows[rows < n], threads=ORACLE_THREADS)
+            assert_close(y.cpu().numpy()[:, rows[rows < n]], yref, s_, TOL_TC, f"m={m} n={n} sampled")
+
+
 def test_matmul_batch_equals_separate_calls():
     """q2k_matmul_ex_batch (MatmulBatch): GEMV and tensor calls of several
     geometries, the tensor ones sharing a workspace, bit-identical to separate
