@@ -60,15 +60,11 @@
 #ifndef Q2K_GEMV_DOT2
 #define Q2K_GEMV_DOT2 1
 #endif
-//   Q2K_GEMV_DEP_THREADS  threads per CTA of dependent calls (256 or 512)
-#ifndef Q2K_GEMV_DEP_THREADS
-#define Q2K_GEMV_DEP_THREADS 256
-#endif
 //   Q2K_GEMV_PIECE_ROWS  weight rows per bulk copy and barrier (4 or 8)
 #ifndef Q2K_GEMV_PIECE_ROWS
 #define Q2K_GEMV_PIECE_ROWS 8
 #endif
-//   Q2K_GEMV_BIGK_GROUPS, Q2K_GEMV_BIGK_CAP_KB  independent calls with k > 8192:
+//   Q2K_GEMV_BIGK_GROUPS, Q2K_GEMV_BIGK_CAP_KB  calls with k > 8192:
 //                  groups of warps per CTA (1 or 2) and the CTA's shared-memory cap
 #ifndef Q2K_GEMV_BIGK_GROUPS
 #define Q2K_GEMV_BIGK_GROUPS 2
@@ -91,17 +87,14 @@ constexpr int kGemvWarps = 8;
 constexpr int kPieceRows = Q2K_GEMV_PIECE_ROWS;
 static_assert(kPieceRows == 4 || kPieceRows == 8, "Q2K_GEMV_PIECE_ROWS must be 4 or 8");
 constexpr int kM1MaxSlices = 256;  // k <= 16384
-// Threads per CTA of the m = 1 kernel.  A dependent call runs alone once its
-// predecessor completes, so it takes more threads per CTA (shorter critical
-// path); independent calls overlap, so smaller CTAs let more calls share an SM.
-constexpr int kM1ThreadsDependent = Q2K_GEMV_DEP_THREADS;
-constexpr int kM1ThreadsIndependent = 128;
-// Independent calls with more than 128 slices (k > 8192): one CTA's chunk
-// fills much of an SM's shared memory, so the CTA takes two groups of warps
-// over the slices (twice the warps to hide latencies with).
-inline int m1_independent_threads(int K) {
+// Threads per CTA of the m = 1 kernel: 128 (small CTAs, several per SM).
+// With more than 128 slices (k > 8192) one CTA's chunk fills much of an SM's
+// shared memory, so the CTA takes two groups of warps over the slices (twice
+// the warps to hide latencies with).
+constexpr int kM1Threads = 128;
+inline int m1_threads(int K) {
     const int slices = K / 64;
-    return slices > 128 ? Q2K_GEMV_BIGK_GROUPS * ((slices + 31) / 32 * 32) : kM1ThreadsIndependent;
+    return slices > 128 ? Q2K_GEMV_BIGK_GROUPS * ((slices + 31) / 32 * 32) : kM1Threads;
 }
 
 // ------------------------------------------------------------------ m = 1
@@ -386,9 +379,8 @@ __device__ __forceinline__ bool dot_rows(const uint8_t* my_col, int B, int rows,
     return ok;
 }
 
-// kMaxThreads: 128 for the independent plan of k <= 8192, 256 for dependent
-// calls, 512 for the two-group CTAs of large k; kMinBlocks caps the registers
-// so that as many CTAs share an SM.
+// kMaxThreads: 128 for k <= 8192, 256 or 512 for the one- or two-group CTAs
+// of larger k; kMinBlocks caps the registers so that as many CTAs share an SM.
 template <int kMaxThreads, int kMinBlocks, int kB>
 __global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
 gemv_m1_kernel(const float* __restrict__ x, const uint8_t* __restrict__ w, float* __restrict__ y,
@@ -562,23 +554,21 @@ size_t m1_smem(int rows, int K, int slices_pad) {
     return ((red_end + 7) & ~size_t(7)) + 8 * pieces + 16;
 }
 
-bool plan_m1(int N, int K, int sm_count, int threads, bool whole_batches, M1Plan* p) {
+bool plan_m1(int N, int K, int sm_count, int threads, M1Plan* p) {
     const int B = K / 256;
     const int S = K / 64;
     if (S > kM1MaxSlices) return false;
     const int slices_pad = (S + 31) / 32 * 32;
     const int groups = slices_pad >= threads ? 1 : threads / slices_pad;
     // Rows per CTA a multiple of what one pass of the row loop covers (groups x
-    // 8 rows) when asked: the loop then never decodes a row twice at the end.
-    // Independent calls share the SMs, so fewer CTAs than SMs costs nothing there.
-    const int quantum = whole_batches ? groups * kPieceRows : 1;
-    // Independent calls overlap on the SMs: their CTAs are kept to 72 KB of
-    // shared memory (three share an SM) when 32 rows still fit there;
-    // otherwise, and for dependent calls, the largest chunk that fits is taken.
-    size_t cap = size_t(200) * 1024;
-    if (whole_batches)
-        cap = m1_smem(32, K, slices_pad) <= size_t(72) * 1024 ? size_t(72) * 1024
-                                                              : size_t(Q2K_GEMV_BIGK_CAP_KB) * 1024;
+    // 8 rows): the loop then never decodes a row twice at the end.  Calls
+    // share the SMs, so fewer CTAs than SMs costs nothing.
+    const int quantum = groups * kPieceRows;
+    // CTAs are kept to 72 KB of shared memory (three share an SM) when 32
+    // rows still fit there; otherwise to Q2K_GEMV_BIGK_CAP_KB.
+    const size_t cap = m1_smem(32, K, slices_pad) <= size_t(72) * 1024
+                           ? size_t(72) * 1024
+                           : size_t(Q2K_GEMV_BIGK_CAP_KB) * 1024;
     int rows = 0;
     for (int waves = 1;; ++waves) {
         rows = (N + sm_count * waves - 1) / (sm_count * waves);
@@ -805,13 +795,14 @@ cudaError_t launch_gemv_problems(const float* x, const uint8_t* w, float* y, int
                                  const GemvProblems& pr, int n_problems, cudaStream_t stream,
                                  const uint8_t* xplanes, uint32_t xplanes_stride) {
     M1Plan plan;
-    // Several problems in one grid overlap on the SMs like independent calls
-    // do, so they take the same small CTAs of whole row batches, planned per
-    // problem.  (Only the K slicing decides the arithmetic of a row, so the
-    // plan never changes a result bit.)
-    const bool small_ctas = (flags & kGemvIndependent) != 0 || n_problems > 1;
-    const int threads = small_ctas ? m1_independent_threads(K) : kM1ThreadsDependent;
-    if (M == 1 && plan_m1(N, K, sm_count, threads, small_ctas, &plan))
+    // Every call takes small CTAs of whole row batches (several share an SM),
+    // planned per problem: independent calls and the problems of one grid
+    // overlap on the SMs, and a dependent call's short critical path after
+    // its wait is better served by more, smaller CTAs than by one large CTA
+    // per SM (5.6 vs 5.9 us per call in a chain of 4096^2 calls).  (Only the
+    // K slicing decides the arithmetic of a row, so the plan never changes a
+    // result bit.)
+    if (M == 1 && plan_m1(N, K, sm_count, m1_threads(K), &plan))
         return launch_m1(x, w, y, N, K, plan, device, flags, pr, n_problems, xplanes,
                          xplanes_stride, stream);
     switch (M < 8 ? M : 8) {
