@@ -337,7 +337,10 @@ class MatmulBatch:
     geometry, shared by its calls).  Everything is checked and packed once;
     ``run()`` enqueues all calls in order on the current stream of the first
     call's device with ``q2k_matmul_ex_batch`` (results bit-identical to
-    separate ``matmul`` calls; m = 1 calls reading one x convert it once).  The
+    separate ``matmul`` calls; m = 1 calls reading one x convert it once),
+    except that independent tensor-path calls with m <= 64 on one x, enough
+    of them to fill the GPU, share persistent grids over all of k (the tensor
+    path's bound, deterministic, other bits than a separate call).  The
     tensors stay bound: update their contents in place between runs.  ``outs``
     lists the output tensors in call order.
 
@@ -393,7 +396,8 @@ class MatmulBatch:
             self._keep.append((x, w, out, ws))
             self.outs.append(out)
         self._count = len(calls)
-        # scratch for the x rows several m = 1 calls share (converted once)
+        # scratch for x converted once: the rows several m = 1 calls share, and
+        # the bf16 image of each run of independent small-m tensor calls
         need = self._lib.q2k_matmul_batch_scratch_bytes(self._arr, self._count) if calls else 0
         self._scratch = (torch.empty(need, dtype=torch.uint8, device=calls[0]["x"].device)
                          if need else None)

@@ -401,8 +401,23 @@ struct BatchPlan {
     std::vector<void*> ws;
     std::vector<int> group;          // per call: its group or -1
     std::vector<size_t> slot;        // per group: scratch offset (SIZE_MAX: alone, no slot)
+    std::vector<int> run;            // per call: the length of the run it starts, else 0
+    std::vector<size_t> run_slot;    // per call starting a run: its x image's scratch offset
     size_t scratch = 0;
 };
+
+// Independent tensor-path calls with m <= 64 (the small-m mode) that follow
+// one another on the same x (same pointer, m and k) form a run when their
+// weight tiles are enough to give every SM several: the run converts x once
+// and runs as persistent grids (q2k::launch_gemm_tc_multi) instead of one
+// launch per call.  A call whose output overlaps x ends the run before it.
+constexpr int kMultiMinTiles = 128;
+
+bool multi_member(const q2k_matmul_call& c, q2k_path path) {
+    return path == Q2K_PATH_TENSOR && (c.flags & Q2K_FLAG_INDEPENDENT) &&
+           q2k::gemm_tc_multi_eligible(int(c.params.m), int(c.params.k), c.w) &&
+           !overlaps(c.y, c.y_elems * 4, c.x, size_t(c.params.m) * c.params.k * 4);
+}
 
 q2k_status plan_batch(const q2k_matmul_call* calls, size_t count, BatchPlan* bp) {
     bp->path.resize(count);
@@ -454,6 +469,29 @@ q2k_status plan_batch(const q2k_matmul_call* calls, size_t count, BatchPlan* bp)
             bp->slot[g] = bp->scratch;
             bp->scratch += (q2k::gemv_planes_bytes(int(ks[g])) + 255) & ~size_t(255);
         }
+    bp->run.assign(count, 0);
+    bp->run_slot.assign(count, SIZE_MAX);
+    for (size_t i = 0; i < count;) {
+        const q2k_matmul_call& c = calls[i];
+        if (!multi_member(c, bp->path[i])) {
+            ++i;
+            continue;
+        }
+        size_t j = i;
+        long tiles = 0;
+        while (j < count && multi_member(calls[j], bp->path[j]) && calls[j].x == c.x &&
+               calls[j].params.m == c.params.m && calls[j].params.k == c.params.k) {
+            tiles += (calls[j].params.n + 127) / 128;
+            ++j;
+        }
+        if (j - i >= 2 && tiles >= kMultiMinTiles) {
+            bp->run[i] = static_cast<int>(j - i);
+            bp->run_slot[i] = bp->scratch;
+            bp->scratch += (q2k::gemm_tc_multi_scratch_bytes(int(c.params.m), int(c.params.k)) + 255) &
+                           ~size_t(255);
+        }
+        i = j;
+    }
     return Q2K_OK;
 }
 
@@ -493,9 +531,30 @@ q2k_status q2k_matmul_ex_batch(const q2k_matmul_call* calls, size_t count, void*
     if (st != Q2K_OK) return st;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     std::vector<char> prepared(bp.slot.size(), 0);
+    std::vector<q2k::MultiCall> multi;
     for (size_t i = 0; i < count; ++i) {
         const q2k_matmul_call& c = calls[i];
         cudaError_t e = cudaSuccess;
+        if (share && bp.run[i] > 0) {
+            // a run of independent small-m calls on one x: persistent grids
+            const size_t len = static_cast<size_t>(bp.run[i]);
+            multi.clear();
+            for (size_t j = i; j < i + len; ++j)
+                multi.push_back({static_cast<const uint8_t*>(calls[j].w), calls[j].y,
+                                 int(calls[j].params.n)});
+            e = q2k::launch_gemm_tc_multi(c.x, int(c.params.m), int(c.params.k), multi.data(),
+                                          static_cast<int>(len),
+                                          static_cast<uint8_t*>(scratch) + bp.run_slot[i], dev.device,
+                                          dev.sm_count, s);
+            if (e != cudaSuccess) {
+                char what[80];
+                snprintf(what, sizeof what, "q2k_matmul_ex_batch launch of calls %zu..%zu", i,
+                         i + len - 1);
+                return cuda_fail(e, what);
+            }
+            i += len - 1;
+            continue;
+        }
         // A tensor call right after one with the same x, m and k in the same
         // workspace finds x's image there already: when it is independent
         // (nothing still running writes its x, W or y, the call before

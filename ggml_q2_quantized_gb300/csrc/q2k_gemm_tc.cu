@@ -1766,6 +1766,513 @@ cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, in
                           wt_flags);
 }
 
+// ---- independent small-m products of one x in one persistent grid -----------
+//
+// Several products y_c = x W_c^T of the same x (m <= 64 rows) whose calls are
+// independent of one another: one CTA per SM walks a sequence of 128-row
+// weight tiles (tile t of all the calls' tiles: blockIdx.x, + gridDim.x, ...),
+// each over all of K.  The decoders run on from one tile's blocks into the
+// next; the two MMA issuers write tile j into accumulator pair j % 2, so the
+// epilogue warps read tile j out of TMEM while tile j + 1 is multiplied.  No
+// K split and no per-tile start-up: a call's tiles cost decode time only.
+
+namespace {
+
+#ifndef Q2K_TC_MULTI_STAGES
+#define Q2K_TC_MULTI_STAGES 8
+#endif
+#ifndef Q2K_TC_MULTI_RAW
+#define Q2K_TC_MULTI_RAW 4
+#endif
+#ifndef Q2K_TC_MULTI_XRES_KB
+#define Q2K_TC_MULTI_XRES_KB 160
+#endif
+// calls per launch (the tensor maps travel in the kernel parameters)
+constexpr int kMultiMaxCalls = 32;
+// x stays resident for the whole grid when all its K stages fit this many
+// bytes of shared memory; otherwise it cycles through a ring as deep as the
+// decoded-weight ring
+constexpr int kMultiXResident = Q2K_TC_MULTI_XRES_KB * 1024;
+
+struct WtMultiCalls {
+    CUtensorMap maps[kMultiMaxCalls];  // call c's weights, 128-row x 112-byte boxes
+    float* y[kMultiMaxCalls];
+    int n[kMultiMaxCalls];
+    int tile0[kMultiMaxCalls + 1];     // call c's tiles: [tile0[c], tile0[c + 1])
+    int count;
+};
+
+template <int kXRows>
+struct MultiCfg {
+    static constexpr int kRows = 128;
+    static constexpr int kDecWarps = 16;   // as in the weights-as-A kernel
+    static constexpr int kGroupWarps = 8;
+    static constexpr int kDecThreads = 32 * kDecWarps;
+    static constexpr int kMmaWarp = kDecWarps;
+    static constexpr int kWaitWarp = kDecWarps + 1;
+    static constexpr int kWWarp = kDecWarps + 2;
+    static constexpr int kXWarp = kDecWarps + 3;
+    static constexpr int kEpiWarp0 = kDecWarps + 4;  // four warps: lane quarters 0..3
+    static constexpr int kThreads = 32 * (kDecWarps + 8);
+    static_assert(kEpiWarp0 % 4 == 0, "epilogue warp w reads TMEM lane quarter w % 4");
+    static constexpr int kPair = 4;        // stages per hand-over: one block
+    static constexpr int kXStage = kXRows * kKS * 2;
+    static constexpr uint32_t kColPair = 2 * kXRows;  // a tile's two accumulators
+    static constexpr uint32_t kColA = 2 * kColPair;   // after both pairs
+    static constexpr int kTmemCols = 512;
+    // decoded-weight ring (and x ring): as deep as asked and TMEM holds, even
+    // (stages are released in pairs)
+    static constexpr int kStages =
+        std::min(Q2K_TC_MULTI_STAGES, static_cast<int>((kTmemCols - kColA) / 32)) & ~1;
+    static_assert(kStages >= 8, "two blocks of stages in flight");
+    static_assert(kColA + 32u * kStages <= static_cast<uint32_t>(kTmemCols), "TMEM");
+    static constexpr int kRaw = Q2K_TC_MULTI_RAW;
+    static constexpr int kRawBytes = kRows * kTmaBoxBytes;
+    // bars: x_full[kStages], a_full[kStages], a_empty[kStages], raw_full[kRaw],
+    //       raw_empty[kRaw], acc_full[2], acc_empty[2], drain
+    static constexpr int kNumBars = 3 * kStages + 2 * kRaw + 5;
+    static_assert(kRawBytes % 1024 == 0 && kXStage % 1024 == 0, "TMA / swizzle alignment");
+};
+
+// x bytes of shared memory: all K stages, or the ring
+template <int kXRows>
+__host__ __device__ inline int multi_x_bytes(int K) {
+    using C = MultiCfg<kXRows>;
+    const int all = (K / kKS) * C::kXStage;
+    return all <= kMultiXResident ? all : C::kStages * C::kXStage;
+}
+template <int kXRows>
+__host__ __device__ inline int multi_smem_bytes(int K) {
+    using C = MultiCfg<kXRows>;
+    return multi_x_bytes<kXRows>(K) + C::kRaw * C::kRawBytes + 8 * C::kNumBars + 16 + 1024;
+}
+
+template <int kXRows>
+constexpr int multi_smem_max() {
+    using C = MultiCfg<kXRows>;
+    return (kMultiXResident > C::kStages * C::kXStage ? kMultiXResident : C::kStages * C::kXStage) +
+           C::kRaw * C::kRawBytes + 8 * C::kNumBars + 16 + 1024;
+}
+static_assert(multi_smem_max<16>() <= 232448 && multi_smem_max<64>() <= 232448, "shared memory");
+
+__device__ __forceinline__ int multi_call_of(const WtMultiCalls& calls, int tile) {
+    int c = 0;
+    while (c + 1 < calls.count && tile >= calls.tile0[c + 1]) ++c;
+    return c;
+}
+
+// MMA issuers of the persistent kernel.  The waiter (kWaiter) waits for a
+// block's four stages (and, before a tile's first block, for its accumulator
+// pair to be read out) and meets the MMA warp at named barrier 1; then the MMA
+// warp issues the even stages into accumulator 0 of the pair, the waiter the
+// odd ones into accumulator 1.  Both pass the barrier once per block of every
+// tile, whatever happens, so neither can be left waiting there.  Each issuer
+// is its own instantiation: the issue loop's stage arithmetic stays at
+// compile time (a runtime issuer choice measured slower).
+template <int kXRows, bool kWaiter>
+__device__ __forceinline__ void multi_issue(int lane, uint32_t tmem_base, uint32_t sbase, int nx,
+                                            int n_iters, int my_tiles, int all_iters, bool resident,
+                                            uint32_t bar_xfull, uint32_t bar_afull,
+                                            uint32_t bar_aempty, uint32_t bar_accfull,
+                                            uint32_t bar_accempty, uint32_t bar_drain,
+                                            volatile int* abort_flag, unsigned int* err) {
+    using C = MultiCfg<kXRows>;
+    const uint32_t idesc = make_idesc(kBM, nx);
+    const uint64_t xdesc0 = sw128_desc(sbase);
+    const uint32_t a_base0 = tmem_base + C::kColA;
+    int G0 = 0;
+    for (int j = 0; j < my_tiles; ++j) {
+        const uint32_t acc = tmem_base + static_cast<uint32_t>(j & 1) * C::kColPair +
+                             (kWaiter ? static_cast<uint32_t>(kXRows) : 0u);
+        for (int i0 = 0; i0 < n_iters; i0 += C::kPair, G0 += C::kPair) {
+            if (kWaiter && lane == 0 && !*abort_flag) {
+                bool ok = true;
+                if (resident && G0 == 0)
+                    ok = mbar_wait_bounded(bar_xfull, 0, abort_flag, err, kErrTimeoutFull);
+                if (ok && i0 == 0 && j >= 2)
+                    ok = mbar_wait_bounded(bar_accempty + 8 * (j & 1), ((j >> 1) - 1) & 1,
+                                           abort_flag, err, kErrTimeoutAccum);
+#pragma unroll
+                for (int u = 0; u < C::kPair; ++u) {
+                    const int G = G0 + u;
+                    const int s = G % C::kStages;
+                    const uint32_t par = (G / C::kStages) & 1;
+                    if (ok && !resident)
+                        ok = mbar_wait_bounded(bar_xfull + 8 * s, par, abort_flag, err, kErrTimeoutFull);
+                    if (ok)
+                        ok = mbar_wait_bounded(bar_afull + 8 * s, par, abort_flag, err, kErrTimeoutFull);
+                }
+            }
+            __syncwarp();
+            asm volatile("bar.sync 1, 64;" ::: "memory");
+            if (lane == 0 && !*abort_flag) {
+                tc_fence_after();
+#pragma unroll
+                for (int u = kWaiter ? 1 : 0; u < C::kPair; u += 2) {
+                    const int G = G0 + u;
+                    const int i = i0 + u;
+                    const int sx = resident ? i : G % C::kStages;
+                    const uint64_t xdesc = xdesc0 + static_cast<uint64_t>(sx * (C::kXStage >> 4));
+                    const uint32_t a_s = a_base0 + 32u * static_cast<uint32_t>(G % C::kStages);
+#pragma unroll
+                    for (int kk = 0; kk < kKS / 16; ++kk)
+                        mma_bf16_tmem_a(acc, a_s + 8u * kk, xdesc + 2u * kk, idesc,
+                                        (i > 1 || kk > 0) ? 1u : 0u);
+                    // both issuers release the pair (G & ~1, G | 1) once its
+                    // MMAs are done, when a later stage reuses it
+                    if ((G & ~1) + C::kStages < all_iters)
+                        mma_commit(bar_aempty + 8 * ((G | 1) % C::kStages));
+                }
+                if (i0 + C::kPair == n_iters) mma_commit(bar_accfull + 8 * (j & 1));
+            }
+            __syncwarp();
+        }
+    }
+    if (lane == 0 && *abort_flag) {
+        // no MMA may still write TMEM when it is freed
+        mma_commit(bar_drain);
+        volatile int no_abort = 0;
+        mbar_wait_bounded(bar_drain, 0, &no_abort, err, kErrTimeoutDrain);
+    }
+    __syncwarp();
+}
+
+template <int kXRows>
+__global__ void __launch_bounds__(MultiCfg<kXRows>::kThreads, 1)
+gemm_wt_multi_kernel(const uint8_t* __restrict__ xa, int M, int K, uint32_t flags,
+                     const __grid_constant__ WtMultiCalls calls) {
+    using C = MultiCfg<kXRows>;
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nx = min(kXRows, (M + 15) & ~15);  // MMA N
+    const int nb = K / kQK;                      // blocks per weight row
+    const int n_iters = 4 * nb;                  // 64-K stages per tile
+    const int total_tiles = calls.tile0[calls.count];
+    const int my_tiles =
+        static_cast<int>(blockIdx.x) < total_tiles
+            ? (total_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+            : 0;
+    const int all_iters = my_tiles * n_iters;  // this CTA's stages, all tiles
+    const int x_bytes = multi_x_bytes<kXRows>(K);
+    const bool resident = x_bytes == (K / kKS) * C::kXStage;
+    const uint32_t off_raw = static_cast<uint32_t>(x_bytes);
+    const uint32_t raw0 = sbase + off_raw;
+
+    const uint32_t bar_xfull = raw0 + C::kRaw * C::kRawBytes;
+    const uint32_t bar_afull = bar_xfull + 8 * C::kStages;
+    const uint32_t bar_aempty = bar_afull + 8 * C::kStages;
+    const uint32_t bar_raw = bar_aempty + 8 * C::kStages;
+    const uint32_t bar_rawempty = bar_raw + 8 * C::kRaw;
+    const uint32_t bar_accfull = bar_rawempty + 8 * C::kRaw;
+    const uint32_t bar_accempty = bar_accfull + 16;
+    const uint32_t bar_drain = bar_accempty + 16;
+    uint8_t* misc = smem + off_raw + C::kRaw * C::kRawBytes + 8 * C::kNumBars;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+    unsigned int* err = &g_tc_error;
+
+    if (warp == 0) {
+        for (int s = lane; s < C::kStages; s += 32) {
+            mbar_init(bar_xfull + 8 * s, 1);               // the producer's expect-tx arrival
+            mbar_init(bar_afull + 8 * s, C::kGroupWarps);  // one arrival per warp of its group
+            mbar_init(bar_aempty + 8 * s, 2);              // a stage pair: one commit per issuer
+        }
+        for (int r = lane; r < C::kRaw; r += 32) {
+            mbar_init(bar_raw + 8 * r, 1);
+            mbar_init(bar_rawempty + 8 * r, C::kDecWarps);
+        }
+        if (lane < 2) {
+            mbar_init(bar_accfull + 8 * lane, 2);   // one commit per issuer
+            mbar_init(bar_accempty + 8 * lane, 4);  // one arrival per epilogue warp
+        }
+        if (lane == 0) {
+            mbar_init(bar_drain, 2);
+            *abort_flag = 0;
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == C::kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(C::kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+    if (warp < C::kDecWarps) {
+        // ---------------- weight decoders: every block of every tile, in order ----------------
+        const int quarter = warp & 3;
+        const int seg = (warp >> 2) & 1;
+        const int half = warp >> 3;
+        const int row = 32 * quarter + lane;
+        const uint32_t a_col0 =
+            tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + C::kColA + 8u * seg;
+        const int all_blocks = my_tiles * nb;
+        for (int B = 0, b = 0; B < all_blocks; ++B, b = b + 1 == nb ? 0 : b + 1) {
+            // B: block counted over all tiles; b: the same block within its row
+            const int buf = B % C::kRaw;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_raw + 8 * buf, (B / C::kRaw) & 1,
+                                                           abort_flag, err, kErrTimeoutFull)))
+                break;
+            const uint32_t mine = raw0 + buf * C::kRawBytes + row * kTmaBoxBytes + 4 * (b & 3);
+            uint32_t sh[2], qh[4];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) sh[q] = ld_shared_u32(mine + 8 * half + 4 * q) >> (8 * seg);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                qh[e] = ld_shared_u32(mine + 16 + 32 * half + 16 * seg + 4 * e);
+            const uint32_t dd = ld_shared_u32(mine + 80);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_rawempty + 8 * buf);
+            const float d = f16_bits_to_float(dd);
+            const float dmin = f16_bits_to_float(dd >> 16);
+            bool ok = true;
+#pragma unroll
+            for (int cp = 0; cp < 2; ++cp) {
+                const int G = 4 * B + 2 * half + cp;  // stage, counted over all tiles
+                const int s = G % C::kStages;
+                uint32_t o0[8], o1[8];
+                if (cp == 0) wt_decode_half_stage<0>(qh, sh, d, dmin, o0, o1);
+                else wt_decode_half_stage<1>(qh, sh, d, dmin, o0, o1);
+                // the slot's last pair (stages G - 8, G - 7) released by both issuers
+                if (G >= C::kStages &&
+                    !__all_sync(0xFFFFFFFFu,
+                                mbar_wait_bounded(bar_aempty + 8 * ((G | 1) % C::kStages),
+                                                  ((G / C::kStages) - 1) & 1, abort_flag, err,
+                                                  kErrTimeoutEmpty))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_col = a_col0 + 32u * s;
+                tmem_st8(a_col, o0);
+                tmem_st8(a_col + 16u, o1);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_afull + 8 * s);
+            }
+            if (!ok) break;
+        }
+    } else if (warp == C::kMmaWarp) {
+        multi_issue<kXRows, false>(lane, tmem_base, sbase, nx, n_iters, my_tiles, all_iters, resident,
+                                   bar_xfull, bar_afull, bar_aempty, bar_accfull, bar_accempty,
+                                   bar_drain, abort_flag, err);
+    } else if (warp == C::kWaitWarp) {
+        multi_issue<kXRows, true>(lane, tmem_base, sbase, nx, n_iters, my_tiles, all_iters, resident,
+                                  bar_xfull, bar_afull, bar_aempty, bar_accfull, bar_accempty,
+                                  bar_drain, abort_flag, err);
+    } else if (warp == C::kWWarp) {
+        // ---------------- raw weight blocks: one TMA box each ----------------
+        if (lane == 0) {
+            for (int c = 0; c < calls.count; ++c)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&calls.maps[c]))
+                             : "memory");
+            // the calls are independent: no grid that may still run writes W
+            int B = 0;
+            bool ok = true;
+            for (int j = 0; j < my_tiles && ok; ++j) {
+                const int tile = static_cast<int>(blockIdx.x) + j * static_cast<int>(gridDim.x);
+                const int c = multi_call_of(calls, tile);
+                const int n0 = (tile - calls.tile0[c]) * C::kRows;
+                for (int b = 0; b < nb; ++b, ++B) {
+                    const int buf = B % C::kRaw;
+                    if (B >= C::kRaw &&
+                        !mbar_wait_bounded(bar_rawempty + 8 * buf, ((B / C::kRaw) - 1) & 1,
+                                           abort_flag, err, kErrTimeoutEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar_raw + 8 * buf, C::kRawBytes);
+                    // rows past the call's N read as zeros (they decode to 0)
+                    tma_load_2d(raw0 + buf * C::kRawBytes, &calls.maps[c], (kBlockBytes * b) & ~15,
+                                n0, bar_raw + 8 * buf);
+                }
+            }
+            if (*abort_flag) {
+                // a copy may still be in flight: give it a bounded 50 us to land
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 50000ull) __nanosleep(1000);
+            }
+        }
+        __syncwarp();
+    } else if (warp == C::kXWarp) {
+        // ---------------- x stages from the image ----------------
+        if (lane == 0) {
+            // the image is written by the grid before this one, unless an
+            // earlier grid of the same x already waited for it (kImageReady);
+            // later grids may start once every CTA is past this point
+            if (!(flags & kImageReady)) pdl_wait_prerequisites();
+            pdl_allow_dependents();
+            const uint32_t bytes = static_cast<uint32_t>(nx) * (kKS * 2);
+            if (resident) {
+                if (my_tiles > 0) {
+                    mbar_arrive_expect_tx(bar_xfull, bytes * static_cast<uint32_t>(n_iters));
+                    for (int i = 0; i < n_iters; ++i)
+                        bulk_copy_g2s(sbase + i * C::kXStage, xa + static_cast<size_t>(i) * kXSuperBytes,
+                                      bytes, bar_xfull);
+                }
+            } else {
+                for (int G = 0, i = 0; G < all_iters; ++G, i = i + 1 == n_iters ? 0 : i + 1) {
+                    const int s = G % C::kStages;
+                    if (G >= C::kStages &&
+                        !mbar_wait_bounded(bar_aempty + 8 * ((G | 1) % C::kStages),
+                                           ((G / C::kStages) - 1) & 1, abort_flag, err,
+                                           kErrTimeoutEmpty))
+                        break;
+                    mbar_arrive_expect_tx(bar_xfull + 8 * s, bytes);
+                    bulk_copy_g2s(sbase + s * C::kXStage,
+                                  xa + static_cast<size_t>(i) * kXSuperBytes, bytes,
+                                  bar_xfull + 8 * s);
+                }
+            }
+            if (*abort_flag) {
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 50000ull) __nanosleep(1000);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: accumulator pair -> y, tile by tile ----------------
+        const int quarter = warp & 3;
+        const int row = 32 * quarter + lane;
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
+        for (int j = 0; j < my_tiles; ++j) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_backoff(bar_accfull + 8 * (j & 1), (j >> 1) & 1,
+                                                           abort_flag, err, kErrTimeoutAccum, 512)))
+                break;
+            tc_fence_after();
+            const int tile = static_cast<int>(blockIdx.x) + j * static_cast<int>(gridDim.x);
+            const int c = multi_call_of(calls, tile);
+            const int N = calls.n[c];
+            const int n = (tile - calls.tile0[c]) * C::kRows + row;
+            float* yc = calls.y[c];
+            const uint32_t t_row = t_lane + static_cast<uint32_t>(j & 1) * C::kColPair;
+#pragma unroll 1
+            for (int c0 = 0; c0 < nx; c0 += 16) {
+                uint32_t v[16], u[16];
+                tmem_ld16(t_row + c0, v);
+                tmem_ld16(t_row + static_cast<uint32_t>(kXRows) + c0, u);
+                if (n < N) {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int m = c0 + q;
+                        // the two accumulators added in order (even stages + odd stages)
+                        if (m < M)
+                            yc[static_cast<size_t>(m) * N + n] =
+                                __uint_as_float(v[q]) + __uint_as_float(u[q]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_accempty + 8 * (j & 1));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == C::kMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(C::kTmemCols)
+                     : "memory");
+    }
+    // the calls complete only after the grid before them (stream order)
+    if (threadIdx.x == 0 && blockIdx.x == 0) pdl_wait_prerequisites();
+}
+
+template <int kXRows>
+cudaError_t launch_multi_chunk(const uint8_t* xa, int M, int K, uint32_t flags,
+                               const WtMultiCalls& calls, int sm_count, int device,
+                               cudaStream_t stream) {
+    using C = MultiCfg<kXRows>;
+    static bool attr_done[64] = {};
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    const int smem = multi_smem_bytes<kXRows>(K);
+    if (!attr_done[device]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_wt_multi_kernel<kXRows>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             multi_smem_max<kXRows>());
+        if (e != cudaSuccess) return e;
+        attr_done[device] = true;
+    }
+    const int tiles = calls.tile0[calls.count];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(std::min(tiles, sm_count)));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_wt_multi_kernel<kXRows>, xa, M, K, flags, calls);
+}
+
+}  // namespace
+
+bool gemm_tc_multi_eligible(int M, int K, const void* w) {
+    return M > 0 && small_xrows(M) > 0 && K > 0 && K % (4 * kQK) == 0 &&
+           (reinterpret_cast<uintptr_t>(w) & 15) == 0 && tensor_map_encoder() != nullptr;
+}
+
+size_t gemm_tc_multi_scratch_bytes(int M, int K) { return image_bytes(M, K); }
+
+cudaError_t launch_gemm_tc_multi(const float* x, int M, int K, const MultiCall* mc, int count,
+                                 void* scratch, int device, int sm_count, cudaStream_t stream) {
+    if (count <= 0) return cudaSuccess;
+    uint8_t* xa = static_cast<uint8_t*>(scratch);
+    {
+        const size_t n_chunks = static_cast<size_t>(M) * (K / 8);
+        size_t blocks = (n_chunks + 255) / 256;
+        const size_t cap = static_cast<size_t>(sm_count) * 4;
+        if (blocks > cap) blocks = cap;
+        x_to_bf16_tiles_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            x, xa, M, K, n_chunks, nullptr, 0);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // chunks of at most kMultiMaxCalls calls, as even as possible
+    const int n_launch = (count + kMultiMaxCalls - 1) / kMultiMaxCalls;
+    int first = 0;
+    for (int l = 0; l < n_launch; ++l) {
+        const int cnt = (count - first) / (n_launch - l);
+        WtMultiCalls calls;
+        memset(&calls, 0, sizeof calls);
+        calls.count = cnt;
+        int tiles = 0;
+        for (int c = 0; c < cnt; ++c) {
+            const MultiCall& q = mc[first + c];
+            if (!make_weight_map(&calls.maps[c], q.w, q.n, K, 128)) return cudaErrorNotSupported;
+            calls.y[c] = q.y;
+            calls.n[c] = q.n;
+            calls.tile0[c] = tiles;
+            tiles += (q.n + 127) / 128;
+        }
+        calls.tile0[cnt] = tiles;
+        const uint32_t flags = l > 0 ? kImageReady : 0u;
+        cudaError_t e;
+        switch (small_xrows(M)) {
+            case 16: e = launch_multi_chunk<16>(xa, M, K, flags, calls, sm_count, device, stream); break;
+            case 32: e = launch_multi_chunk<32>(xa, M, K, flags, calls, sm_count, device, stream); break;
+            default: e = launch_multi_chunk<64>(xa, M, K, flags, calls, sm_count, device, stream); break;
+        }
+        if (e != cudaSuccess) return e;
+        first += cnt;
+    }
+    return cudaSuccess;
+}
+
 // ---- routed products on tensor cores (mul_mat_id with many routes) -----------
 //
 // Route r (token r / top_k, or slot r) multiplies its x row by expert ids[r]'s

@@ -103,6 +103,22 @@ cudaError_t launch_gemm_tc(const float* x, const uint8_t* w, float* y, int M, in
 // in-kernel conversion, one K part), so kImageReady may reuse it.
 bool gemm_tc_image_reusable(int M, int N, int K);
 
+// Independent products y_c = x W_c^T of one x (M <= 64 rows) in persistent
+// weights-as-A grids: x converted once into `scratch`
+// (gemm_tc_multi_scratch_bytes, 16-byte aligned), then one grid per at most 32
+// calls, each CTA walking 128-row weight tiles of all of K (no K split).
+// Each W must be 16-byte aligned and K a multiple of 1024
+// (gemm_tc_multi_eligible).  No call may read or write another's output.
+struct MultiCall {
+    const uint8_t* w;
+    float* y;
+    int n;
+};
+bool gemm_tc_multi_eligible(int M, int K, const void* w);
+size_t gemm_tc_multi_scratch_bytes(int M, int K);
+cudaError_t launch_gemm_tc_multi(const float* x, int M, int K, const MultiCall* calls, int count,
+                                 void* scratch, int device, int sm_count, cudaStream_t stream);
+
 // Routed product on tensor cores: route r = 0..routes-1 multiplies x row
 // r / x_div by expert ids[r]'s weights (w + ids[r] * expert_stride, N rows)
 // into y row r; ids out of range give a zero row and a count in *bad_ids (if

@@ -187,7 +187,8 @@ enum {
      * conversion and y stores (INDEPENDENT), start before the wait for the
      * kernel before.  In q2k_matmul_ex_batch, INDEPENDENT also lets a
      * tensor-path call reuse the x image of the call before it (same x, m, k
-     * and workspace) and run beside it.  The other paths ignore them. */
+     * and workspace) and run beside it, and lets consecutive small-m calls on
+     * one x share persistent grids.  The other paths ignore them. */
     Q2K_FLAG_INDEPENDENT = 2
 };
 
@@ -424,9 +425,10 @@ typedef struct q2k_matmul_call {
  * decode step: the host cost per call falls from a binding's argument handling
  * to the launch itself).  Every call is checked first; the first malformed
  * one returns its q2k_matmul_ex error (the message names its index) and
- * nothing is launched.  Results are those of the separate calls, bit for bit.
- * Calls may share a workspace (they run in stream order).  `calls` is host
- * memory, read during the call only.
+ * nothing is launched.  Results are those of the separate calls, bit for bit,
+ * except in the runs of independent small-m calls described below (same
+ * tolerance, still deterministic).  Calls may share a workspace (they run in
+ * stream order).  `calls` is host memory, read during the call only.
  *   scratch  device, NULL or at least q2k_matmul_batch_scratch_bytes(calls,
  *            count) bytes, 16-byte aligned, not overlapping any call's
  *            buffers.  With it, m = 1 calls on the fp32 GEMV path (k <= 16384)
@@ -434,13 +436,24 @@ typedef struct q2k_matmul_call {
  *            into the scratch, instead of once per CTA of every call (the
  *            same values: same bits).  A call of the batch that writes that
  *            row ends the sharing.  Without it (or smaller) every call
- *            converts x itself.
+ *            converts x itself, and no run (below) is formed.
  * A tensor-path call with Q2K_FLAG_INDEPENDENT right after a tensor-path call
  * with the same x pointer, m, k and workspace (and, for both, the workspace
  * layout of one K part: m > 64 and no K split) finds x's bf16 image in that
  * workspace already: it skips the conversion and, independent of the call
  * before it by the flag's promise, may run beside that call on the SMs it
- * leaves free; it still completes after it.  Same bits as the separate call. */
+ * leaves free; it still completes after it.  Same bits as the separate call.
+ * Tensor-path calls with Q2K_FLAG_INDEPENDENT and m <= 64 that follow one
+ * another with the same x pointer, m and k (k a multiple of 1024, each W
+ * 16-byte aligned, no call's y overlapping x) form a run when they have at
+ * least 128 tiles of 128 weight rows between them and there is scratch: x is
+ * converted to bf16 once, into the scratch, and the run's calls share
+ * persistent grids (one per at most 32 calls) in which each CTA takes one
+ * tile after another over all of k, instead of one launch per call with k
+ * split into parts.  Each output is then a single fp32 accumulation over k
+ * (the even and the odd 64-k stages in two sums, added in that order): within
+ * the tensor path's 8e-3 * sum_k |x w| bound, and the same bits on every run,
+ * though not the bits of the separate call. */
 q2k_status q2k_matmul_ex_batch(const q2k_matmul_call *calls, size_t count, void *scratch,
                                size_t scratch_bytes, q2k_stream_t stream);
 

@@ -317,6 +317,70 @@ def test_matmul_batch_shared_image_independent_calls():
             assert_close(y.cpu().numpy()[:, rows[rows < n]], yref, s_, TOL_TC, f"m={m} n={n} sampled")
 
 
+def test_matmul_batch_small_m_runs_persistent():
+    """Independent small-m tensor calls on one x in a batch, enough tiles to
+    fill the GPU: the run shares persistent grids over all of k (x converted
+    once into the batch scratch).  Every output within the tensor path's bound
+    of the oracle on sampled weight rows (tile edges and the ragged last tile
+    included), and bit-identical on a second run.  Cases: x resident in shared
+    memory (m = 16, k = 4096) with a ragged call; the x ring (m = 40, k = 2048,
+    and m = 16, k = 14336); m = 5 forced onto the tensor path; more than 32
+    calls (two grids, the second on the ready image); a call on another x in
+    the middle splits the run."""
+    cases = [
+        (16, 4096, [4096] * 4 + [1000], {}),
+        (40, 2048, [4096] * 4 + [333], {}),
+        (16, 14336, [4096] * 4, {}),
+        (5, 1024, [2048] * 10, dict(path="tensor")),
+        (24, 1024, [512] * 36 + [200], {}),
+    ]
+    for ci, (m, k, ns, kw) in enumerate(cases):
+        x, _ = wl.make_matmul_inputs(4100 + ci, m, 16, k)
+        xd = dev(x)
+        calls, ws_np = [], []
+        for i, n in enumerate(ns):
+            _, w = wl.make_matmul_inputs(4200 + 50 * ci + i, m, n, k)
+            calls.append(dict(x=xd, w=dev(w), n=n, independent=True, **kw))
+            ws_np.append((w, n))
+        batch = q2k.MatmulBatch(calls)
+        assert batch._scratch is not None, f"case {ci}: no run formed"
+        outs = [o.clone() for o in batch.run()]
+        torch.cuda.synchronize()
+        for o in batch.outs:
+            o.fill_(float("nan"))
+        again = batch.run()
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(zip(again, outs)):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32)), f"case {ci} call {i} rerun"
+        rng = np.random.default_rng(4300 + ci)
+        for i, ((w, n), y) in enumerate(zip(ws_np, outs)):
+            if len(ns) > 8 and i % 7 and i != len(ns) - 1:
+                continue   # a sample of the many calls
+            pick = rng.choice(n, min(n, 24), replace=False)
+            rows = np.unique(np.concatenate([pick, [0, min(127, n - 1), min(128, n - 1), n - 1]]))
+            yref, s_ = oracle.matmul_rows(x, w, n, rows, threads=ORACLE_THREADS)
+            assert_close(y.cpu().numpy()[:, rows], yref, s_, TOL_TC, f"case {ci} (m={m} k={k}) call {i}")
+    # a call on another x splits the run: both parts still correct
+    m, k = 16, 1024
+    x, _ = wl.make_matmul_inputs(4400, m, 16, k)
+    x2, w2 = wl.make_matmul_inputs(4401, m, 256, k)
+    xd = dev(x)
+    calls, ws_np = [], []
+    for i in range(12):
+        _, w = wl.make_matmul_inputs(4402 + i, m, 2048, k)
+        calls.append(dict(x=xd, w=dev(w), n=2048, independent=True))
+        ws_np.append(w)
+    calls.insert(9, dict(x=dev(x2), w=dev(w2), n=256, independent=True))
+    outs = q2k.MatmulBatch(calls).run()
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 127, 128, 1000, 2047])
+    yref2, s2 = oracle.matmul_rows(x2, w2, 256, np.array([0, 100, 255]), threads=ORACLE_THREADS)
+    assert_close(outs[9].cpu().numpy()[:, [0, 100, 255]], yref2, s2, TOL_TC, "the call between runs")
+    for j, y in enumerate(outs[:9] + outs[10:]):
+        yref, s_ = oracle.matmul_rows(x, ws_np[j], 2048, rows, threads=ORACLE_THREADS)
+        assert_close(y.cpu().numpy()[:, rows], yref, s_, TOL_TC, f"split run call {j}")
+
+
 def test_matmul_batch_equals_separate_calls():
     """q2k_matmul_ex_batch (MatmulBatch): GEMV and tensor calls of several
     geometries, the tensor ones sharing a workspace, bit-identical to separate
