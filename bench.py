@@ -64,6 +64,9 @@ def parse_args():
     ap.add_argument("--workload", default="decode_gemv_4096")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dependent", action="store_true",
+                    help="time the workload's matrices as dependent calls (each may read what "
+                         "the one before wrote) instead of independent projections of one x")
     return ap.parse_args()
 
 
@@ -178,6 +181,24 @@ def dist_setup():
 
 def layers_for(weight_bytes: int, l2_bytes: int) -> int:
     return max(2, math.ceil(3 * l2_bytes / weight_bytes))
+
+
+def batch_launches(m: int, n: int, k: int, layers: int, independent: bool) -> int:
+    """Kernel launches of one q2k.MatmulBatch step of ``layers`` calls of one
+    geometry on one x, as q2k_matmul_ex_batch enqueues them (with its scratch
+    and per-geometry workspaces)."""
+    if m <= 8:
+        # fp32 GEMV, one launch per call; m = 1 calls on one x convert it once
+        return layers + (1 if m == 1 and k // 64 <= 256 and layers >= 2 else 0)
+    tiles = (n + 127) // 128
+    if m <= 64:
+        if independent and k % 1024 == 0 and layers >= 2 and tiles * layers >= 128:
+            return 1 + -(-layers // 32)   # x image once, persistent grids of <= 32 calls
+        return layers                     # small-m GEMM converts x itself
+    splits = 1 if m > 128 or tiles >= 64 else 2
+    if independent and splits == 1:
+        return layers + 1                 # later calls reuse the first call's x image
+    return 2 * layers                     # x image prepass + GEMM per call
 
 
 def stack_of_weights(w: wl.Workload, layers: int, first: np.ndarray):
@@ -541,12 +562,14 @@ def run_ours(args):
     ys = torch.empty((layers, w.m, w.n), dtype=torch.float32, device=device)
     stream = torch.cuda.Stream(device)
 
-    indep = w.m == 1
-    # the step's calls packed once: q2k_matmul_ex_batch enqueues them, and the
-    # m = 1 calls (all on this x) convert x once into the batch's scratch
+    indep = not args.dependent
+    # the step's calls packed once: q2k_matmul_ex_batch enqueues them; as
+    # independent projections of this x, x is converted once into the batch's
+    # scratch (m = 1: the GEMV's form; m <= 64: the bf16 image that persistent
+    # tensor grids share; m > 64: the workspace image later calls reuse)
     batch = q2k.MatmulBatch([dict(x=x, w=ws[l], n=w.n, out=ys[l], independent=indep)
                              for l in range(layers)])
-    launches_per_step = layers + (1 if batch._scratch is not None else 0)
+    launches_per_step = batch_launches(w.m, w.n, w.k, layers, indep)
 
     def step():
         batch.run()
@@ -616,7 +639,7 @@ def run_ours(args):
                               f"{max(per_repeat):.4f} ms per step)"),
                    "calls": ("independent projections of one x (Q2K_FLAG_INDEPENDENT) enqueued as "
                              "one q2k.MatmulBatch: x converted once per step" if indep
-                             else "one launch per matrix"),
+                             else "dependent calls, one launch per matrix, as one q2k.MatmulBatch"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "us_per_call": launch_us,
         "gpu_launches": steps * launches_per_step,

@@ -1781,6 +1781,9 @@ namespace {
 #ifndef Q2K_TC_MULTI_STAGES
 #define Q2K_TC_MULTI_STAGES 8
 #endif
+#ifndef Q2K_TC_MULTI_HANDOVER
+#define Q2K_TC_MULTI_HANDOVER 4
+#endif
 #ifndef Q2K_TC_MULTI_RAW
 #define Q2K_TC_MULTI_RAW 4
 #endif
@@ -1815,7 +1818,8 @@ struct MultiCfg {
     static constexpr int kEpiWarp0 = kDecWarps + 4;  // four warps: lane quarters 0..3
     static constexpr int kThreads = 32 * (kDecWarps + 8);
     static_assert(kEpiWarp0 % 4 == 0, "epilogue warp w reads TMEM lane quarter w % 4");
-    static constexpr int kPair = 4;        // stages per hand-over: one block
+    static constexpr int kPair = Q2K_TC_MULTI_HANDOVER;  // stages per hand-over (4: one block)
+    static_assert(kPair == 2 || kPair == 4 || kPair == 8, "a whole number of hand-overs per tile");
     static constexpr int kXStage = kXRows * kKS * 2;
     static constexpr uint32_t kColPair = 2 * kXRows;  // a tile's two accumulators
     static constexpr uint32_t kColA = 2 * kColPair;   // after both pairs
