@@ -87,6 +87,9 @@ constexpr int kGemvWarps = 8;
 constexpr int kPieceRows = Q2K_GEMV_PIECE_ROWS;
 static_assert(kPieceRows == 4 || kPieceRows == 8, "Q2K_GEMV_PIECE_ROWS must be 4 or 8");
 constexpr int kM1MaxSlices = 256;  // k <= 16384
+#ifndef Q2K_GEMV_DEP_WAVES
+#define Q2K_GEMV_DEP_WAVES 3
+#endif
 // Threads per CTA of the m = 1 kernel: 128 (small CTAs, several per SM).
 // With more than 128 slices (k > 8192) one CTA's chunk fills much of an SM's
 // shared memory, so the CTA takes two groups of warps over the slices (twice
@@ -554,7 +557,7 @@ size_t m1_smem(int rows, int K, int slices_pad) {
     return ((red_end + 7) & ~size_t(7)) + 8 * pieces + 16;
 }
 
-bool plan_m1(int N, int K, int sm_count, int threads, M1Plan* p) {
+bool plan_m1(int N, int K, int sm_count, int threads, M1Plan* p, int min_waves = 1) {
     const int B = K / 256;
     const int S = K / 64;
     if (S > kM1MaxSlices) return false;
@@ -570,7 +573,7 @@ bool plan_m1(int N, int K, int sm_count, int threads, M1Plan* p) {
                            ? size_t(72) * 1024
                            : size_t(Q2K_GEMV_BIGK_CAP_KB) * 1024;
     int rows = 0;
-    for (int waves = 1;; ++waves) {
+    for (int waves = min_waves;; ++waves) {
         rows = (N + sm_count * waves - 1) / (sm_count * waves);
         rows = (rows + quantum - 1) / quantum * quantum;
         if (B % 4) rows = (rows + 3) / 4 * 4;  // chunk starts stay 16-byte aligned
@@ -799,10 +802,19 @@ cudaError_t launch_gemv_problems(const float* x, const uint8_t* w, float* y, int
     // planned per problem: independent calls and the problems of one grid
     // overlap on the SMs, and a dependent call's short critical path after
     // its wait is better served by more, smaller CTAs than by one large CTA
-    // per SM (5.6 vs 5.9 us per call in a chain of 4096^2 calls).  (Only the
-    // K slicing decides the arithmetic of a row, so the plan never changes a
-    // result bit.)
-    if (M == 1 && plan_m1(N, K, sm_count, m1_threads(K), &plan))
+    // per SM.  (Only the K slicing decides the arithmetic of a row, so the
+    // plan never changes a result bit.)
+    // A lone dependent call has the GPU to itself: with 128-thread CTAs (k <=
+    // 8192) its rows are spread over Q2K_GEMV_DEP_WAVES CTAs per SM, fewer
+    // rows per thread on its critical path (a chain of 4096^2 calls 5.65 ->
+    // 5.30 us per call, 14336 x 4096 14.7 against 15.7 us).  The two-group
+    // CTAs of larger k measured slower that way (4096 x 14336: 18.4 against
+    // 15.0 us), so they keep one wave.
+    const int min_waves = (flags & kGemvIndependent) || n_problems > 1 ||
+                                  m1_threads(K) != kM1Threads
+                              ? 1
+                              : Q2K_GEMV_DEP_WAVES;
+    if (M == 1 && plan_m1(N, K, sm_count, m1_threads(K), &plan, min_waves))
         return launch_m1(x, w, y, N, K, plan, device, flags, pr, n_problems, xplanes,
                          xplanes_stride, stream);
     switch (M < 8 ? M : 8) {
