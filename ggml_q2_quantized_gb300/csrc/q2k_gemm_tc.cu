@@ -2294,13 +2294,15 @@ int routed_tiles_max(int routes, int n_experts) {
 }
 
 // One CTA: count the routes per expert, scan to tile starts, and write each
-// x tile's {expert, rows} (-1: unused), each x row's route (-1: padding) and,
-// for a route whose id is out of range, a zero row of y (and of y2, when not
-// null) and a count (one per output).
+// x tile's {expert, rows} (-1: unused), each x row's route (-1: padding), each
+// route's x row (-1: id out of range) and, for a route whose id is out of
+// range, a zero row of y (and of y2, when not null) and a count (one per
+// output).
 __global__ void __launch_bounds__(1024)
 route_tiles_kernel(const uint32_t* __restrict__ ids, int routes, int n_experts, int tiles_max,
-                   int2* __restrict__ tile_info, int* __restrict__ row_route, float* __restrict__ y,
-                   float* __restrict__ y2, int N, unsigned int* __restrict__ bad_ids) {
+                   int2* __restrict__ tile_info, int* __restrict__ row_route,
+                   int* __restrict__ route_row, float* __restrict__ y, float* __restrict__ y2, int N,
+                   unsigned int* __restrict__ bad_ids) {
     extern __shared__ int route_smem[];
     int* cnt = route_smem;              // per expert: routes, then the placement cursor
     int* start = route_smem + n_experts;  // per expert: first tile
@@ -2368,49 +2370,55 @@ route_tiles_kernel(const uint32_t* __restrict__ ids, int routes, int n_experts, 
     __syncthreads();
     for (int r = tid; r < routes; r += nt) {
         const uint32_t e = ids[r];
-        if (e < static_cast<uint32_t>(n_experts))
-            row_route[128 * start[e] + atomicAdd(&cnt[e], 1)] = r;
+        int v = -1;
+        if (e < static_cast<uint32_t>(n_experts)) {
+            v = 128 * start[e] + atomicAdd(&cnt[e], 1);
+            row_route[v] = r;
+        }
+        route_row[r] = v;
     }
 }
 
 // x rows by route into the bf16 tile image of the routed rows (x tile t =
-// rows 128 t .. 128 t + 127): row v holds x row row_route[v] / x_div, zeros
-// for padding; tiles no expert uses are left alone.  As x_to_bf16_tiles_kernel
-// it lets the GEMM after it start early.
+// rows 128 t .. 128 t + 127): route r's row route_row[r] gets x row r / x_div.
+// Only the routes' rows are written: a tile's padding rows feed only
+// accumulator columns that the GEMM's epilogue drops (each MMA column is its
+// own dot product), and tiles no expert uses are never read.  One thread
+// converts one 8-element chunk; consecutive threads take consecutive chunks
+// of a route's row.  As x_to_bf16_tiles_kernel it lets the GEMM after it
+// start early.
 __global__ void __launch_bounds__(256)
 gather_x_tiles_kernel(const float* __restrict__ x, uint8_t* __restrict__ xa,
-                      const int2* __restrict__ tile_info, const int* __restrict__ row_route, int x_div,
-                      int K, size_t n_chunks) {
+                      const int* __restrict__ route_row, int x_div, int K, size_t n_chunks) {
     pdl_allow_dependents();
     const int chunks_per_row = K >> 3;
     const int stages = K / kKS;
     for (size_t id = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; id < n_chunks;
          id += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const int v = static_cast<int>(id / chunks_per_row);
-        const int j = static_cast<int>(id - static_cast<size_t>(v) * chunks_per_row);
-        if (tile_info[v >> 7].x < 0) continue;
-        const int r = row_route[v];
-        uint4 packed = make_uint4(0u, 0u, 0u, 0u);
-        if (r >= 0) {
-            const float4* src =
-                reinterpret_cast<const float4*>(x + static_cast<size_t>(r / x_div) * K + 8 * j);
-            const float4 a = __ldg(src), b = __ldg(src + 1);
-            packed = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
-                                pack_bf16x2(b.z, b.w));
-        }
+        const int r = static_cast<int>(id / chunks_per_row);
+        const int j = static_cast<int>(id - static_cast<size_t>(r) * chunks_per_row);
+        const int v = route_row[r];
+        if (v < 0) continue;  // an id out of range: no row
+        const float4* src = reinterpret_cast<const float4*>(x + static_cast<size_t>(r / x_div) * K + 8 * j);
+        const float4 a = __ldg(src), b = __ldg(src + 1);
+        const uint4 packed = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
+                                        pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
         const size_t tile = static_cast<size_t>(v / kXSuperRows) * stages + (j >> 3);
         *reinterpret_cast<uint4*>(xa + tile * kXSuperBytes + sw128_offset(v % kXSuperRows, j & 7)) =
             packed;
     }
 }
 
-// Workspace of a routed product: tile table, row routes, then the x image.
+// Workspace of a routed product: tile table, row routes, route rows, then the
+// x image.
 static size_t routed_info_bytes(int tiles) { return (static_cast<size_t>(tiles) * 8 + 255) & ~size_t(255); }
 static size_t routed_rows_bytes(int tiles) { return static_cast<size_t>(tiles) * 128 * 4; }
+static size_t routed_route_bytes(int routes) { return (static_cast<size_t>(routes) * 4 + 255) & ~size_t(255); }
 
 size_t gemm_tc_routed_workspace_bytes(int routes, int n_experts, int K) {
     const int tiles = routed_tiles_max(routes, n_experts);
-    return routed_info_bytes(tiles) + routed_rows_bytes(tiles) + image_bytes(tiles * 128, K);
+    return routed_info_bytes(tiles) + routed_rows_bytes(tiles) + routed_route_bytes(routes) +
+           image_bytes(tiles * 128, K);
 }
 
 cudaError_t launch_gemm_tc_routed(const float* x, const uint8_t* w, long long expert_stride,
@@ -2424,17 +2432,18 @@ cudaError_t launch_gemm_tc_routed(const float* x, const uint8_t* w, long long ex
     uint8_t* base = static_cast<uint8_t*>(workspace);
     int2* tile_info = reinterpret_cast<int2*>(base);
     int* row_route = reinterpret_cast<int*>(base + routed_info_bytes(tiles));
-    uint8_t* xa = base + routed_info_bytes(tiles) + routed_rows_bytes(tiles);
+    int* route_row = reinterpret_cast<int*>(base + routed_info_bytes(tiles) + routed_rows_bytes(tiles));
+    uint8_t* xa = base + routed_info_bytes(tiles) + routed_rows_bytes(tiles) + routed_route_bytes(routes);
     route_tiles_kernel<<<1, 1024, 2 * n_experts * sizeof(int), stream>>>(
-        ids, routes, n_experts, tiles, tile_info, row_route, y, y2, N, bad_ids);
+        ids, routes, n_experts, tiles, tile_info, row_route, route_row, y, y2, N, bad_ids);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const size_t n_chunks = static_cast<size_t>(M) * (K / 8);
+    const size_t n_chunks = static_cast<size_t>(routes) * (K / 8);
     size_t blocks = (n_chunks + 255) / 256;
     const size_t cap = static_cast<size_t>(sm_count) * 4;
     if (blocks > cap) blocks = cap;
     gather_x_tiles_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        x, xa, tile_info, row_route, x_div, K, n_chunks);
+        x, xa, route_row, x_div, K, n_chunks);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     WtRouted rt;

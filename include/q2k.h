@@ -362,7 +362,8 @@ q2k_status q2k_matmul_id_pair_ex(q2k_path path, const float *x, size_t x_elems, 
 /* q2k_matmul_id_workspace_bytes - the workspace q2k_matmul_id_ex takes on
  * `path` (AUTO resolved as there) for these params and flags: for the tensor
  * path the routes' tile table and the bf16 image of their x rows, about
- * (n_tokens*top_k + 128*min(n_experts, n_tokens*top_k)) * (2k + 4) bytes; for
+ * (n_tokens*top_k + 128*min(n_experts, n_tokens*top_k)) * (2k + 4) bytes plus
+ * 4 per route; for
  * the GEMV its optional scratch (q2k_x_planes_bytes).  0 for invalid params,
  * more than 65535 routes, or a tensor path with n_experts > 4096.  Geometry
  * only: no device is touched. */

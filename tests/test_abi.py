@@ -250,14 +250,16 @@ def test_matmul_id_slotted_and_pair_reject(lib):
 
 def test_matmul_id_ex_workspace_and_rejections(lib):
     """The routed product's tensor path: its workspace size (tile table, row
-    routes, x image of up to routes/128 + min(experts, routes) tiles) and the
-    checks made before any device work."""
+    routes, each route's row, x image of up to routes/128 + min(experts, routes)
+    tiles) and the checks made before any device work."""
     n_tokens, top_k, n, k, experts = 64, 8, 2048, 7168, 64
     p = q2k.MatmulIdParams(n_tokens, top_k, n, k, experts, 10, n * (k // 256) * 84)
-    tiles = 512 // 128 + 64
+    routes = n_tokens * top_k
+    tiles = routes // 128 + 64
     info = (tiles * 8 + 255) // 256 * 256
+    route_rows = (routes * 4 + 255) // 256 * 256
     image = (tiles * 128 + 255) // 256 * 256 * k * 2
-    want = info + tiles * 128 * 4 + image
+    want = info + tiles * 128 * 4 + route_rows + image
     assert lib.q2k_matmul_id_workspace_bytes(q2k.PATH_TENSOR, 0, ctypes.byref(p)) == want
     assert lib.q2k_matmul_id_workspace_bytes(q2k.PATH_AUTO, 0, ctypes.byref(p)) == want
     # auto takes the GEMV at <= 32 tokens: its optional scratch is the x planes
