@@ -720,9 +720,10 @@ struct WtCfg {
 };
 
 // Routed mode of the weights-as-A kernel: x tile t's expert and routed rows
-// (tile_info[t] = {expert or -1, rows}), each x row's route (row_route[v], -1
-// for padding rows), the bytes between experts' weights and, for the TMA
-// view of the whole weight pool, the rows between them.
+// (tile_info[t] = {expert or -1, rows}), the route of each of those rows
+// (row_route[128 t + i], i < rows; padding rows have none), the bytes between
+// experts' weights and, for the TMA view of the whole weight pool, the rows
+// between them.
 struct WtRouted {
     const int2* tile_info = nullptr;
     const int* row_route = nullptr;
@@ -1137,7 +1138,7 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
                         if (m < M) out[static_cast<size_t>(m) * N + n] = __uint_as_float(v[q]);
                     }
                 } else if (n < N) {
-                    // routed: x row m is route row_route[m] (-1: padding)
+                    // routed: x row m < tile_rows is route row_route[m]
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
                         const int m = m0 + c0 + q;
@@ -2294,10 +2295,10 @@ int routed_tiles_max(int routes, int n_experts) {
 }
 
 // One CTA: count the routes per expert, scan to tile starts, and write each
-// x tile's {expert, rows} (-1: unused), each x row's route (-1: padding), each
-// route's x row (-1: id out of range) and, for a route whose id is out of
-// range, a zero row of y (and of y2, when not null) and a count (one per
-// output).
+// x tile's {expert, rows} (-1: unused), the route of each of a tile's first
+// `rows` x rows, each route's x row (-1: id out of range) and, for a route
+// whose id is out of range, a zero row of y (and of y2, when not null) and a
+// count (one per output).
 __global__ void __launch_bounds__(1024)
 route_tiles_kernel(const uint32_t* __restrict__ ids, int routes, int n_experts, int tiles_max,
                    int2* __restrict__ tile_info, int* __restrict__ row_route,
@@ -2359,9 +2360,8 @@ route_tiles_kernel(const uint32_t* __restrict__ ids, int routes, int n_experts, 
         const int c = cnt[e];
         for (int j = 0; j < (c + 127) >> 7; ++j)
             tile_info[t + j] = make_int2(e, min(128, c - 128 * j));
-        // the last tile's padding rows
-        const int used = (c + 127) & ~127;
-        for (int v = c; v < used; ++v) row_route[128 * t + v] = -1;
+        // (the last tile's padding rows get no route: the GEMM reads only a
+        // tile's first tile_info.y rows of row_route)
         t += (c + 127) >> 7;
     }
     for (int u = total_tiles + tid; u < tiles_max; u += nt) tile_info[u] = make_int2(-1, 0);
