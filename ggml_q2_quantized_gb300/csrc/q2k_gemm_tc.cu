@@ -1486,19 +1486,26 @@ gemm_wt_kernel(const uint8_t* __restrict__ xa, const float* __restrict__ xf,
 // rows 256 t .. 256 t + 255 (zeros past M) x K 64 s .. 64 s + 63 in the
 // 128-byte-swizzled K-major layout (8-row groups 1024 bytes apart).  One
 // thread writes one 16-byte chunk.
-__device__ __forceinline__ void x_chunk_to_image(const float* __restrict__ x, uint8_t* __restrict__ xa,
-                                                 int M, int K, size_t id) {
+__device__ __forceinline__ void x_chunk_load(const float* __restrict__ x, int M, int K, size_t id,
+                                             float4& lo, float4& hi) {
+    const int chunks_per_row = K >> 3;
+    const int m = static_cast<int>(id / chunks_per_row);
+    const int j = static_cast<int>(id - static_cast<size_t>(m) * chunks_per_row);
+    lo = hi = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (m < M) {
+        const float4* src = reinterpret_cast<const float4*>(x + static_cast<size_t>(m) * K + 8 * j);
+        lo = __ldg(src);
+        hi = __ldg(src + 1);
+    }
+}
+__device__ __forceinline__ void x_chunk_store(uint8_t* __restrict__ xa, int K, size_t id,
+                                              const float4& lo, const float4& hi) {
     const int chunks_per_row = K >> 3;
     const int stages = K / kKS;
     const int m = static_cast<int>(id / chunks_per_row);
     const int j = static_cast<int>(id - static_cast<size_t>(m) * chunks_per_row);
-    uint4 packed = make_uint4(0u, 0u, 0u, 0u);
-    if (m < M) {
-        const float4* src = reinterpret_cast<const float4*>(x + static_cast<size_t>(m) * K + 8 * j);
-        const float4 a = __ldg(src), b = __ldg(src + 1);
-        packed = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
-                            pack_bf16x2(b.z, b.w));
-    }
+    const uint4 packed = make_uint4(pack_bf16x2(lo.x, lo.y), pack_bf16x2(lo.z, lo.w),
+                                    pack_bf16x2(hi.x, hi.y), pack_bf16x2(hi.z, hi.w));
     const size_t tile = static_cast<size_t>(m / kXSuperRows) * stages + (j >> 3);
     *reinterpret_cast<uint4*>(xa + tile * kXSuperBytes + sw128_offset(m % kXSuperRows, j & 7)) =
         packed;
@@ -1507,7 +1514,8 @@ __device__ __forceinline__ void x_chunk_to_image(const float* __restrict__ x, ui
 // The GEMM after this kernel is launched as its programmatic dependent: it may
 // start (TMEM, barriers, weight decode) as soon as every block here has begun,
 // and waits for this grid to finish only before it copies the image.  Few
-// blocks per SM leave room for it.
+// blocks per SM leave room for it.  Each thread converts four chunks per
+// pass, all their loads issued before any store.
 __global__ void __launch_bounds__(256)
 x_to_bf16_tiles_kernel(const float* __restrict__ x, uint8_t* __restrict__ xa, int M, int K,
                        size_t n_chunks, unsigned int* __restrict__ tile_count, int n_tiles) {
@@ -1516,12 +1524,17 @@ x_to_bf16_tiles_kernel(const float* __restrict__ x, uint8_t* __restrict__ xa, in
     for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < n_tiles; t += gridDim.x * blockDim.x)
         tile_count[t] = 0u;
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-    size_t id = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    for (; id + stride < n_chunks; id += 2 * stride) {
-        x_chunk_to_image(x, xa, M, K, id);
-        x_chunk_to_image(x, xa, M, K, id + stride);
+    constexpr int kPer = 4;
+    for (size_t base = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < n_chunks;
+         base += kPer * stride) {
+        float4 lo[kPer], hi[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u)
+            if (base + u * stride < n_chunks) x_chunk_load(x, M, K, base + u * stride, lo[u], hi[u]);
+#pragma unroll
+        for (int u = 0; u < kPer; ++u)
+            if (base + u * stride < n_chunks) x_chunk_store(xa, K, base + u * stride, lo[u], hi[u]);
     }
-    if (id < n_chunks) x_chunk_to_image(x, xa, M, K, id);
 }
 
 template <int BN, bool kBulkA>
