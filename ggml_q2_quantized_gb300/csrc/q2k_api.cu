@@ -532,10 +532,12 @@ q2k_status q2k_matmul_ex_batch(const q2k_matmul_call* calls, size_t count, void*
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     std::vector<char> prepared(bp.slot.size(), 0);
     std::vector<q2k::MultiCall> multi;
+    // (without the tensor-map encoder a run's calls go one by one)
+    const bool runs = share && q2k::gemm_tc_multi_available();
     for (size_t i = 0; i < count; ++i) {
         const q2k_matmul_call& c = calls[i];
         cudaError_t e = cudaSuccess;
-        if (share && bp.run[i] > 0) {
+        if (runs && bp.run[i] > 0) {
             // a run of independent small-m calls on one x: persistent grids
             const size_t len = static_cast<size_t>(bp.run[i]);
             multi.clear();

@@ -2241,8 +2241,10 @@ cudaError_t launch_multi_chunk(const uint8_t* xa, int M, int K, uint32_t flags,
 
 bool gemm_tc_multi_eligible(int M, int K, const void* w) {
     return M > 0 && small_xrows(M) > 0 && K > 0 && K % (4 * kQK) == 0 &&
-           (reinterpret_cast<uintptr_t>(w) & 15) == 0 && tensor_map_encoder() != nullptr;
+           (reinterpret_cast<uintptr_t>(w) & 15) == 0;
 }
+
+bool gemm_tc_multi_available() { return tensor_map_encoder() != nullptr; }
 
 size_t gemm_tc_multi_scratch_bytes(int M, int K) { return image_bytes(M, K); }
 

@@ -108,13 +108,16 @@ bool gemm_tc_image_reusable(int M, int N, int K);
 // (gemm_tc_multi_scratch_bytes, 16-byte aligned), then one grid per at most 32
 // calls, each CTA walking 128-row weight tiles of all of K (no K split).
 // Each W must be 16-byte aligned and K a multiple of 1024
-// (gemm_tc_multi_eligible).  No call may read or write another's output.
+// (gemm_tc_multi_eligible, geometry only); the grids need the driver's
+// tensor-map encoder (gemm_tc_multi_available).  No call may read or write
+// another's output.
 struct MultiCall {
     const uint8_t* w;
     float* y;
     int n;
 };
 bool gemm_tc_multi_eligible(int M, int K, const void* w);
+bool gemm_tc_multi_available();
 size_t gemm_tc_multi_scratch_bytes(int M, int K);
 cudaError_t launch_gemm_tc_multi(const float* x, int M, int K, const MultiCall* calls, int count,
                                  void* scratch, int device, int sm_count, cudaStream_t stream);

@@ -325,6 +325,46 @@ def test_matmul_ex_batch_checks_every_call_first(lib):
     assert lib.q2k_matmul_ex_batch(None, 0, None, 0, None) == 0   # nothing to do
 
 
+def test_matmul_batch_plans_small_m_runs(lib):
+    """The batch's runs of independent small-m tensor calls on one x (planned on
+    the host, geometry only): each run gets one slot of the scratch for x's
+    bf16 image (ceil(m / 256) * 256 * k * 2 bytes) when its calls have at least
+    128 weight tiles of 128 rows between them; dependent calls, too few tiles,
+    k not a multiple of 1024, a W that is not 16-byte aligned and a call on
+    another x (which may overwrite the runs' x) all end or prevent a run."""
+    m, n, k = 16, 4096, 4096
+    wbytes = n * (k // 256) * 84
+    image = 256 * k * 2
+
+    def calls_for(count, flags=2, kk=k, nn=n, x=0x10000, w_off=0):
+        arr = (q2k.MatmulCall * count)()
+        for i, c in enumerate(arr):
+            c.x, c.x_elems = x, m * kk
+            c.w, c.w_bytes = 0x100000000 + i * 0x1000000 + w_off, nn * (kk // 256) * 84
+            c.y, c.y_elems = 0x800000000 + i * 0x1000000, m * nn
+            c.params = q2k.MatmulParams(m, nn, kk, 10)
+            c.path, c.flags = q2k.PATH_TENSOR, flags
+        return arr
+
+    assert lib.q2k_matmul_batch_scratch_bytes(calls_for(6), 6) == image      # 192 tiles: one run
+    assert lib.q2k_matmul_batch_scratch_bytes(calls_for(4), 4) == image      # 128 tiles
+    assert lib.q2k_matmul_batch_scratch_bytes(calls_for(3), 3) == 0          # 96 tiles
+    assert lib.q2k_matmul_batch_scratch_bytes(calls_for(6, flags=0), 6) == 0  # dependent
+    assert lib.q2k_matmul_batch_scratch_bytes(calls_for(6, kk=2816), 6) == 0  # k % 1024 != 0
+    assert lib.q2k_matmul_batch_scratch_bytes(calls_for(6, w_off=4), 6) == 0  # W 4-byte aligned
+    assert lib.q2k_matmul_batch_scratch_bytes(calls_for(2, nn=8192), 2) == image  # 2 x 64 tiles
+    # a call on another x between two runs: two slots
+    arr = calls_for(9)
+    arr[4].x = 0x20000
+    assert lib.q2k_matmul_batch_scratch_bytes(arr, 9) == 2 * image
+    # a call on another x that overwrites the runs' x: the same split
+    arr = calls_for(9)
+    arr[4].x, arr[4].y = 0x40000000, 0x10000
+    assert lib.q2k_matmul_batch_scratch_bytes(arr, 9) == 2 * image
+    # ... while the calls themselves stay as given
+    assert arr[0].w_bytes == wbytes
+
+
 def test_x_planes_scratch_is_not_needed(lib):
     # the batched and routed GEMV launches convert x per thread: no scratch
     for k in (256, 4096, 16384, 16640):
