@@ -365,6 +365,37 @@ def test_matmul_batch_plans_small_m_runs(lib):
     assert arr[0].w_bytes == wbytes
 
 
+def test_bench_launch_count_follows_the_batch_plan(lib):
+    """bench.py counts a step's kernel launches from the batch's plan; for the
+    workloads it times, its count agrees with the plan the library makes
+    (a scratch slot per shared x conversion or small-m run)."""
+    import bench
+
+    def scratch(m, n, k, layers, flags):
+        arr = (q2k.MatmulCall * layers)()
+        for i, c in enumerate(arr):
+            c.x, c.x_elems = 0x10000, m * k
+            c.w, c.w_bytes = 0x100000000 + i * 0x4000000, n * (k // 256) * 84
+            c.y, c.y_elems = 0x2000000000 + i * 0x4000000, m * n
+            c.params = q2k.MatmulParams(m, n, k, 10)
+            c.path, c.flags = q2k.PATH_AUTO, flags
+        return lib.q2k_matmul_batch_scratch_bytes(arr, layers)
+
+    # decode GEMV, 74 independent calls on one x: one x preparation + 74 GEMVs
+    assert scratch(1, 4096, 4096, 74, 2) > 0
+    assert bench.batch_launches(1, 4096, 4096, 74, True) == 75
+    # spec-verify, 74 independent m = 16 calls: one run -> image + 3 grids
+    assert scratch(16, 4096, 4096, 74, 2) == 256 * 4096 * 2
+    assert bench.batch_launches(16, 4096, 4096, 74, True) == 1 + 3
+    # the same calls dependent: no run, one small-m launch each
+    assert scratch(16, 4096, 4096, 74, 0) == 0
+    assert bench.batch_launches(16, 4096, 4096, 74, False) == 74
+    # prefill (m = 512): no batch scratch; the first call's prepass, then GEMMs
+    assert scratch(512, 7168, 7168, 4, 2) == 0
+    assert bench.batch_launches(512, 7168, 7168, 4, True) == 5
+    assert bench.batch_launches(512, 7168, 7168, 4, False) == 8
+
+
 def test_x_planes_scratch_is_not_needed(lib):
     # the batched and routed GEMV launches convert x per thread: no scratch
     for k in (256, 4096, 16384, 16640):
