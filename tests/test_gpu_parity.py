@@ -381,6 +381,31 @@ def test_matmul_batch_small_m_runs_persistent():
         assert_close(y.cpu().numpy()[:, rows], yref, s_, TOL_TC, f"split run call {j}")
 
 
+def test_spec_verify_workload_full_in_a_persistent_batch():
+    """The spec-verify workload (M=16, N=K=4096) as the bench times it: one of
+    many independent projections of one x in a batch, so its call runs in a
+    persistent grid.  The workload's own matrix is call 35 of 40 (the second
+    grid, on the ready x image); all of its 65536 outputs against the oracle,
+    and a sample of call 0's."""
+    w_ = wl.WORKLOADS[3]
+    inp = wl.make_inputs(w_, with_gather=False)
+    rng = np.random.default_rng(4500)
+    mats = [wl.random_blocks(rng, w_.n * (w_.k // 256)).reshape(-1) for _ in range(39)]
+    mats.insert(35, inp.w)
+    xd = dev(inp.x)
+    batch = q2k.MatmulBatch([dict(x=xd, w=dev(m), n=w_.n, independent=True) for m in mats])
+    assert batch._scratch is not None
+    outs = batch.run()
+    torch.cuda.synchronize()
+    yref, s_ = oracle.matmul(inp.x, inp.w, w_.n, threads=ORACLE_THREADS)
+    ratio = assert_close(outs[35].cpu().numpy().astype(np.float64), yref, s_, TOL_TC,
+                         "spec-verify in a persistent batch")
+    print(f"spec-verify in a persistent batch: max |y - y_ref| / S = {ratio:.3e}")
+    rows = np.array([0, 1, 127, 128, 2049, 4095])
+    yref0, s0 = oracle.matmul_rows(inp.x, mats[0], w_.n, rows, threads=ORACLE_THREADS)
+    assert_close(outs[0].cpu().numpy()[:, rows], yref0, s0, TOL_TC, "call 0 of the batch")
+
+
 def test_matmul_batch_equals_separate_calls():
     """q2k_matmul_ex_batch (MatmulBatch): GEMV and tensor calls of several
     geometries, the tensor ones sharing a workspace, bit-identical to separate
