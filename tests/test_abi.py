@@ -322,6 +322,11 @@ def test_matmul_ex_batch_checks_every_call_first(lib):
     calls[0].flags = 0
     assert lib.q2k_matmul_ex_batch(calls, 2, 0x3000008, 2048, None) == INVALID
     assert "aligned" in lib.q2k_last_error().decode()
+    # a scratch overlapping a call's output (or its x) is rejected before any launch
+    assert lib.q2k_matmul_ex_batch(calls, 2, 0x1000000 + 4096, 2048, None) == INVALID
+    assert "scratch must not alias call 1" in lib.q2k_last_error().decode()
+    assert lib.q2k_matmul_ex_batch(calls, 2, 0x10000, 2048, None) == INVALID
+    assert "scratch must not alias call 0" in lib.q2k_last_error().decode()
     assert lib.q2k_matmul_ex_batch(None, 0, None, 0, None) == 0   # nothing to do
 
 
